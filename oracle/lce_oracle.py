@@ -1,0 +1,202 @@
+"""fp64 CPU oracle for the fused chunked linear + cross-entropy loss.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports, calls or links
+this file; only the tests, the smoke check and the benchmark's CPU-baseline leg
+do. It shares no code, table or helper with the CUDA path.
+
+What it computes is the plain definition of linear projection + softmax
+cross-entropy with the mean over non-ignored rows, because the pages claim the
+fused method reaches exactly that result ("Unsloth Architecture: Manual Triton
+Backpropagation, Fused Cross-Entropy, and 80% VRAM Cut", pillar 4 "Zero
+Approximation Loss"). So the oracle materialises the logits (in row blocks,
+to bound host memory; the blocking changes no arithmetic) and follows the steps
+in the order the pages state them:
+
+  1. Z = H W^T  -- the LM-head projection ("Arquitectura interna de Unsloth y
+     optimizacion en Triton", section 3 "Fused Cross Entropy"; "Unsloth
+     Architecture ...", section "The Un-Fused Cross-Entropy Logit Disaster").
+  2. lse_i = m_i + log sum_j exp(Z_ij - m_i), m_i = max_j Z_ij -- subtract the
+     row maximum, then log-sum-exp (same section 3 of the Spanish page).
+  3. L_i = lse_i - Z_{i,y_i}; loss = sum over valid rows / N_valid
+     ("Unsloth Architecture ...", pillar 1 "Fused Chunked Cross-Entropy Loss").
+  4. dL/dZ_ij = (softmax(Z)_ij - 1[j = y_i]) * dloss / N_valid, zero rows for
+     ignored samples (section 3 of the Spanish page; pillar 1).
+  5. dH = G W and dW = G^T H -- backpropagation into both the hidden states and
+     the vocabulary projection (section 3 of the Spanish page).
+
+Readings where the pages are silent (each is listed in the design doc too):
+  * ignore_index rows (y == ignore_index) are dropped from the mean; the
+    normaliser is N_valid (the pages divide by the token count, which is the
+    same when nothing is ignored).
+  * labels outside [0, V) that are not ignore_index are treated as ignored
+    and reported through the returned ``n_bad``.
+  * N_valid == 0 gives loss 0 and zero gradients.
+  * the loss uses lse - z_y exactly, with no clamp of p.
+  * dloss is a scalar upstream gradient multiplying G.
+
+Pins: tests/test_oracle.py checks this module against closed forms (W = 0),
+invariants (row sums of G, column sums of dW, shift invariance, ignored rows),
+central finite differences, scipy's logsumexp and torch's cross_entropy in fp64.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+IGNORE_INDEX = -100
+
+
+def as_f64(a) -> np.ndarray:
+    """Upcast a torch tensor (any float dtype, incl. bf16) or array to fp64 numpy."""
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu")
+        if not a.is_floating_point():
+            return a.numpy()
+        import torch  # only for the dtype conversion of bf16 tensors
+        return a.to(torch.float64).numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+def as_labels(y) -> np.ndarray:
+    """Labels as an int64 numpy vector (accepts torch tensors, lists, arrays)."""
+    if hasattr(y, "detach"):
+        y = y.detach().to("cpu").numpy()
+    return np.asarray(y).astype(np.int64)
+
+
+def valid_rows(y: np.ndarray, V: int, ignore_index: int = IGNORE_INDEX):
+    """Rows that take part in the loss, and the count of out-of-range labels."""
+    y = as_labels(y)
+    in_range = (y >= 0) & (y < V)
+    bad = (~in_range) & (y != ignore_index)
+    return in_range & (y != ignore_index), int(bad.sum())
+
+
+def logits(H: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """Step 1: Z = H W^T in fp64."""
+    return H @ W.T
+
+
+def row_logsumexp(Z: np.ndarray) -> np.ndarray:
+    """Step 2: per-row log-sum-exp with the row maximum subtracted first."""
+    m = Z.max(axis=1)
+    return m + np.log(np.exp(Z - m[:, None]).sum(axis=1))
+
+
+def _block_iter(n: int, block: int):
+    for s in range(0, n, block):
+        yield s, min(s + block, n)
+
+
+def _block_rows(V: int) -> int:
+    # keep a block of fp64 logits near 256 MB
+    return max(1, min(4096, (256 << 20) // (8 * max(V, 1))))
+
+
+def forward(H, W, y, ignore_index: int = IGNORE_INDEX):
+    """Loss and per-row lse (steps 1-3). Returns (loss, lse[N], n_valid, n_bad)."""
+    H = as_f64(H)
+    W = as_f64(W)
+    y = as_labels(y)
+    N, V = H.shape[0], W.shape[0]
+    valid, n_bad = valid_rows(y, V, ignore_index)
+    n_valid = int(valid.sum())
+    lse = np.empty(N, dtype=np.float64)
+    total = 0.0
+    for s, e in _block_iter(N, _block_rows(V)):
+        Z = logits(H[s:e], W)
+        lse[s:e] = row_logsumexp(Z)
+        v = valid[s:e]
+        idx = np.nonzero(v)[0]
+        total += float(np.sum(lse[s:e][idx] - Z[idx, y[s:e][idx]]))
+    loss = total / n_valid if n_valid else 0.0
+    return loss, lse, n_valid, n_bad
+
+
+def forward_backward(H, W, y, ignore_index: int = IGNORE_INDEX, dloss: float = 1.0):
+    """Steps 1-5. Returns dict(loss, lse[N], dH[N,D], dW[V,D], n_valid, n_bad), fp64."""
+    H = as_f64(H)
+    W = as_f64(W)
+    y = as_labels(y)
+    N, D = H.shape
+    V = W.shape[0]
+    valid, n_bad = valid_rows(y, V, ignore_index)
+    n_valid = int(valid.sum())
+    scale = (dloss / n_valid) if n_valid else 0.0
+    lse = np.empty(N, dtype=np.float64)
+    dH = np.zeros((N, D), dtype=np.float64)
+    dW = np.zeros((V, D), dtype=np.float64)
+    total = 0.0
+    for s, e in _block_iter(N, _block_rows(V)):
+        Z = logits(H[s:e], W)
+        lse_b = row_logsumexp(Z)
+        lse[s:e] = lse_b
+        v = valid[s:e]
+        idx = np.nonzero(v)[0]
+        yb = y[s:e]
+        total += float(np.sum(lse_b[idx] - Z[idx, yb[idx]]))
+        # step 4: G = (softmax - onehot) * dloss / N_valid, ignored rows zero
+        G = np.exp(Z - lse_b[:, None])
+        G[idx, yb[idx]] -= 1.0
+        G *= scale
+        G[~v] = 0.0
+        # step 5
+        dH[s:e] = G @ W
+        dW += G.T @ H[s:e]
+    loss = total / n_valid if n_valid else 0.0
+    return dict(loss=loss, lse=lse, dH=dH, dW=dW, n_valid=n_valid, n_bad=n_bad)
+
+
+# ---------------------------------------------------------------------------
+# Sampled outputs for workloads too large to materialise on the host in a test.
+# Each one is the same definition restricted to the requested rows / columns.
+# ---------------------------------------------------------------------------
+
+def rows_lse_and_target(H, W, y, rows, ignore_index: int = IGNORE_INDEX):
+    """lse_i and z_{i,y_i} (nan when row i is not valid) for the selected rows."""
+    H = as_f64(H)
+    W = as_f64(W)
+    y = as_labels(y)
+    rows = np.asarray(rows, dtype=np.int64)
+    Z = logits(H[rows], W)
+    lse = row_logsumexp(Z)
+    valid, _ = valid_rows(y[rows], W.shape[0], ignore_index)
+    zy = np.full(len(rows), np.nan)
+    zy[valid] = Z[np.nonzero(valid)[0], y[rows][valid]]
+    return lse, zy
+
+
+def rows_dH(H, W, y, rows, n_valid: int, ignore_index: int = IGNORE_INDEX, dloss: float = 1.0):
+    """dH for the selected rows: (softmax(Z_i) - onehot(y_i)) * dloss/N_valid times W."""
+    H = as_f64(H)
+    W = as_f64(W)
+    y = as_labels(y)
+    rows = np.asarray(rows, dtype=np.int64)
+    Z = logits(H[rows], W)
+    lse = row_logsumexp(Z)
+    G = np.exp(Z - lse[:, None])
+    valid, _ = valid_rows(y[rows], W.shape[0], ignore_index)
+    idx = np.nonzero(valid)[0]
+    G[idx, y[rows][idx]] -= 1.0
+    G *= dloss / n_valid if n_valid else 0.0
+    G[~valid] = 0.0
+    return G @ W
+
+
+def cols_dW(H, W, y, vrows, lse_all, n_valid: int, ignore_index: int = IGNORE_INDEX,
+            dloss: float = 1.0):
+    """dW rows for the selected vocabulary ids, given every row's lse.
+
+    dW[v] = sum_i G[i, v] H[i], G[i, v] = (exp(z_iv - lse_i) - 1[y_i = v]) * dloss/N_valid.
+    """
+    H = as_f64(H)
+    W = as_f64(W)
+    y = as_labels(y)
+    vrows = np.asarray(vrows, dtype=np.int64)
+    lse_all = np.asarray(lse_all, dtype=np.float64)
+    Zc = H @ W[vrows].T                      # [N, len(vrows)]
+    G = np.exp(Zc - lse_all[:, None])
+    valid, _ = valid_rows(y, W.shape[0], ignore_index)
+    G -= (y[:, None] == vrows[None, :]) & valid[:, None]
+    G *= dloss / n_valid if n_valid else 0.0
+    G[~valid] = 0.0
+    return G.T @ H
