@@ -1,0 +1,117 @@
+/*
+ * lce.h -- C ABI of the GB300 (sm_103a) fused chunked linear + cross-entropy
+ * library (liblce_gb300.so).
+ *
+ * The operation. Given hidden states H[N,D], the LM-head weight W[V,D] and
+ * labels y[N], the library computes the logits Z = H W^T chunk by chunk on
+ * chip, the per-row log-sum-exp lse_i, the mean loss over non-ignored rows
+ *     loss = sum_{valid i} (lse_i - Z[i, y_i]) / N_valid,
+ * and the analytic gradients
+ *     G[i,j] = (exp(Z[i,j] - lse_i) - 1[j = y_i]) * dloss / N_valid  (0 for ignored rows)
+ *     dH = G W,   dW = G^T H,
+ * without ever holding the full [N,V] logits or G in device memory.
+ * Sources: "Arquitectura interna de Unsloth y optimizacion en Triton", section 3
+ * "Fused Cross Entropy" (token blocks, on-chip logits, online log-sum-exp, the
+ * softmax - onehot gradient, backpropagation into X and W_vocab); "Unsloth
+ * Architecture: Manual Triton Backpropagation, Fused Cross-Entropy, and 80% VRAM
+ * Cut", pillar 1 "Fused Chunked Cross-Entropy Loss" (chunks of tokens, the
+ * per-row loss -z_{i,y_i} + log sum_j exp z_ij and the gradient p - 1[j = y_i]);
+ * "Unsloth Kernel Architecture: Custom Triton Backpropagation and QLoRA Memory
+ * Scaling", section 1 "Fused Cross-Entropy Loss with Logit Streaming" (vocab
+ * blocks streamed per row with a running max and running sum).
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *    row-major and contiguous, and 16-byte aligned. H and W are bf16
+ *    (IEEE bfloat16, 2 bytes), y is int64, lse / dW / loss / dloss are fp32,
+ *    dH is bf16.
+ *  - D must be a multiple of 8 (16-byte rows for the tensor-memory copies);
+ *    N, V and chunk are otherwise arbitrary (ragged tails are masked).
+ *  - The caller owns every buffer, including the workspace (ws, ws_bytes) of at
+ *    least lce_workspace_size() bytes. The library allocates no device memory.
+ *    The workspace extent is O(chunk * V) plus O(N) bytes.
+ *  - All work is enqueued on `stream`; no entry point synchronises the host.
+ *    Argument errors are returned before anything is enqueued. Errors found on
+ *    the device (labels outside [0,V) that are not ignore_index, a bounded wait
+ *    that ran out) are recorded in the workspace and returned by
+ *    lce_read_status(), which synchronises the stream.
+ *  - Rows whose label is ignore_index (usually -100) add nothing to the loss and
+ *    get zero dH rows. Labels outside [0,V) other than ignore_index are treated
+ *    the same way and flag LCE_ERR_LABEL_RANGE. With no valid row at all the
+ *    loss is 0 and dH, dW are 0.
+ *  - Results are deterministic: two calls with the same inputs give the same
+ *    bits (fixed reduction orders, no floating-point atomics).
+ *  - The kernels are built for sm_103a only; other devices get
+ *    LCE_ERR_UNSUPPORTED.
+ */
+#ifndef LCE_GB300_H
+#define LCE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum lce_status {
+    LCE_OK = 0,
+    LCE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, D % 8 != 0, chunk <= 0 */
+    LCE_ERR_ALIGNMENT = 2,     /* a pointer not 16-byte aligned */
+    LCE_ERR_WORKSPACE = 3,     /* ws_bytes < lce_workspace_size() */
+    LCE_ERR_LABEL_RANGE = 4,   /* device: some label outside [0,V) and != ignore_index */
+    LCE_ERR_TIMEOUT = 5,       /* device: a bounded pipeline wait ran out; outputs invalid */
+    LCE_ERR_CUDA = 6,          /* a CUDA runtime call failed */
+    LCE_ERR_UNSUPPORTED = 7    /* current device is not sm_103 */
+} lce_status;
+
+/* Same type as cudaStream_t. NULL means the legacy default stream. */
+typedef struct CUstream_st *lce_stream_t;
+
+/* Bytes of workspace the calls below need for these sizes (same for all three
+ * calls). Writes *bytes; returns LCE_ERR_INVALID_ARG for bad sizes. */
+lce_status lce_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk, size_t *bytes);
+
+/* Forward: loss (device scalar, fp32) and lse[N] (device, fp32).
+ * Work: 2*N*D*V flops on the tensor cores, chunk rows at a time. */
+lce_status lce_forward(const void *H, const void *W, const int64_t *y,
+                       int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                       float *loss, float *lse,
+                       void *ws, size_t ws_bytes, lce_stream_t stream);
+
+/* Backward from a saved lse[N]: recomputes each chunk's logits (2*N*D*V flops),
+ * forms G in bf16 and writes dH[N,D] (bf16, overwritten) and dW[V,D] (fp32,
+ * overwritten) with 4*N*D*V more flops. dloss is a device fp32 scalar (the
+ * upstream gradient of the mean loss); NULL means 1. */
+lce_status lce_backward(const void *H, const void *W, const int64_t *y, const float *lse,
+                        const float *dloss, void *dH, float *dW,
+                        int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                        void *ws, size_t ws_bytes, lce_stream_t stream);
+
+/* Fused forward + backward without the recompute (6*N*D*V flops): writes loss,
+ * lse, dH (bf16) and dW (fp32). dloss as in lce_backward (NULL means 1). */
+lce_status lce_fwd_bwd(const void *H, const void *W, const int64_t *y, const float *dloss,
+                       int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                       float *loss, float *lse, void *dH, float *dW,
+                       void *ws, size_t ws_bytes, lce_stream_t stream);
+
+/* Synchronises `stream`, then returns the device-side status recorded in the
+ * workspace by the last call that used it (LCE_OK, LCE_ERR_LABEL_RANGE or
+ * LCE_ERR_TIMEOUT; a timeout wins over a label error) and clears it. Returns
+ * LCE_ERR_CUDA if the stream reports an error. */
+lce_status lce_read_status(const void *ws, lce_stream_t stream);
+
+/* Static string for a status code. */
+const char *lce_status_string(lce_status s);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int lce_version(void);
+
+/* Number of kernel launches the last lce_* call on this host thread enqueued. */
+int lce_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LCE_GB300_H */

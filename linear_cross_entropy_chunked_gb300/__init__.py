@@ -1,0 +1,21 @@
+"""GB300 (sm_103a) fused chunked linear + cross-entropy.
+
+The compute runs in liblce_gb300.so (tcgen05/TMEM/TMA kernels behind a C ABI,
+include/lce.h); this package is the thin ctypes binding around it.
+"""
+from ._binding import (  # noqa: F401
+    EXPORTED,
+    IGNORE_INDEX,
+    LCEError,
+    LinearCrossEntropyFunction,
+    alloc_workspace,
+    last_launch_count,
+    lce_backward,
+    lce_forward,
+    lce_fwd_bwd,
+    lib,
+    linear_cross_entropy,
+    read_status,
+    workspace_size,
+)
+from .build_lib import LIB_PATH, build  # noqa: F401

@@ -1,0 +1,223 @@
+"""ctypes binding of liblce_gb300.so: argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels. This module
+checks dtypes/devices, allocates outputs and the workspace with PyTorch (the
+library itself never allocates), passes raw pointers and the current CUDA
+stream, and turns a non-zero lce_status into an exception. There is no CPU
+fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build_lib import LIB_PATH
+
+IGNORE_INDEX = -100
+
+STATUS_NAMES = {
+    0: "LCE_OK",
+    1: "LCE_ERR_INVALID_ARG",
+    2: "LCE_ERR_ALIGNMENT",
+    3: "LCE_ERR_WORKSPACE",
+    4: "LCE_ERR_LABEL_RANGE",
+    5: "LCE_ERR_TIMEOUT",
+    6: "LCE_ERR_CUDA",
+    7: "LCE_ERR_UNSUPPORTED",
+}
+
+# Every function the C ABI (include/lce.h) exports.
+EXPORTED = (
+    "lce_workspace_size",
+    "lce_forward",
+    "lce_backward",
+    "lce_fwd_bwd",
+    "lce_read_status",
+    "lce_status_string",
+    "lce_version",
+    "lce_last_launch_count",
+)
+
+
+class LCEError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        name = STATUS_NAMES.get(status, str(status))
+        msg = f"{what}: {name}" if what else name
+        try:
+            msg += f" ({lib().lce_status_string(status).decode()})"
+        except Exception:
+            pass
+        super().__init__(msg)
+
+
+_LIB = None
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+def lib() -> ctypes.CDLL:
+    """Load liblce_gb300.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{os.path.basename(LIB_PATH)} is not built; run "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+    L = ctypes.CDLL(LIB_PATH)
+    L.lce_workspace_size.argtypes = [_i64, _i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]
+    L.lce_forward.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
+                              ctypes.c_size_t, _vp]
+    L.lce_backward.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                               _vp, ctypes.c_size_t, _vp]
+    L.lce_fwd_bwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
+                              _vp, _vp, ctypes.c_size_t, _vp]
+    L.lce_read_status.argtypes = [_vp, _vp]
+    L.lce_status_string.argtypes = [ctypes.c_int]
+    L.lce_status_string.restype = ctypes.c_char_p
+    L.lce_version.argtypes = []
+    L.lce_last_launch_count.argtypes = []
+    for name in ("lce_workspace_size", "lce_forward", "lce_backward", "lce_fwd_bwd",
+                 "lce_read_status", "lce_version", "lce_last_launch_count"):
+        getattr(L, name).restype = ctypes.c_int
+    _LIB = L
+    return L
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise LCEError(st, what)
+
+
+def workspace_size(N: int, D: int, V: int, chunk: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().lce_workspace_size(N, D, V, chunk, ctypes.byref(out)), "lce_workspace_size")
+    return out.value
+
+
+def alloc_workspace(N: int, D: int, V: int, chunk: int, device) -> torch.Tensor:
+    return torch.empty(workspace_size(N, D, V, chunk), dtype=torch.uint8, device=device)
+
+
+def _check_inputs(H, W, y):
+    if not (H.is_cuda and W.is_cuda and y.is_cuda):
+        raise ValueError("H, W and y must be CUDA tensors (there is no CPU path)")
+    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("H and W must be bfloat16")
+    if y.dtype != torch.int64:
+        raise TypeError("y must be int64")
+    if H.dim() != 2 or W.dim() != 2 or y.dim() != 1:
+        raise ValueError("expected H[N,D], W[V,D], y[N]")
+    if H.shape[1] != W.shape[1] or H.shape[0] != y.shape[0]:
+        raise ValueError(f"shape mismatch: H{tuple(H.shape)} W{tuple(W.shape)} y{tuple(y.shape)}")
+    if not (H.is_contiguous() and W.is_contiguous() and y.is_contiguous()):
+        raise ValueError("H, W and y must be contiguous")
+    return H.shape[0], H.shape[1], W.shape[0]
+
+
+def lce_forward(H, W, y, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
+                loss=None, lse=None, ws=None, stream=None):
+    """Mean loss (device scalar) and lse[N] via the library's lce_forward."""
+    N, D, V = _check_inputs(H, W, y)
+    dev = H.device
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = alloc_workspace(N, D, V, chunk, dev)
+    st = lib().lce_forward(_ptr(H), _ptr(W), _ptr(y), N, D, V, ignore_index, chunk,
+                           _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "lce_forward")
+    return loss, lse
+
+
+def lce_backward(H, W, y, lse, dloss=None, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
+                 dH=None, dW=None, ws=None, stream=None):
+    """dH (bf16) and dW (fp32) from a saved lse via the library's lce_backward."""
+    N, D, V = _check_inputs(H, W, y)
+    dev = H.device
+    if dH is None:
+        dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    if dW is None:
+        dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = alloc_workspace(N, D, V, chunk, dev)
+    if dloss is not None and (dloss.dtype != torch.float32 or not dloss.is_cuda):
+        raise TypeError("dloss must be a CUDA float32 scalar tensor")
+    st = lib().lce_backward(_ptr(H), _ptr(W), _ptr(y), _ptr(lse), _ptr(dloss), _ptr(dH), _ptr(dW),
+                            N, D, V, ignore_index, chunk, _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "lce_backward")
+    return dH, dW
+
+
+def lce_fwd_bwd(H, W, y, dloss=None, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
+                loss=None, lse=None, dH=None, dW=None, ws=None, stream=None):
+    """Fused forward + backward: (loss, lse, dH, dW) via the library's lce_fwd_bwd."""
+    N, D, V = _check_inputs(H, W, y)
+    dev = H.device
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    if dH is None:
+        dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    if dW is None:
+        dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = alloc_workspace(N, D, V, chunk, dev)
+    if dloss is not None and (dloss.dtype != torch.float32 or not dloss.is_cuda):
+        raise TypeError("dloss must be a CUDA float32 scalar tensor")
+    st = lib().lce_fwd_bwd(_ptr(H), _ptr(W), _ptr(y), _ptr(dloss), N, D, V, ignore_index, chunk,
+                           _ptr(loss), _ptr(lse), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(),
+                           _stream(stream))
+    _check(st, "lce_fwd_bwd")
+    return loss, lse, dH, dW
+
+
+def read_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device-side status."""
+    return lib().lce_read_status(_ptr(ws), _stream(stream))
+
+
+def last_launch_count() -> int:
+    return lib().lce_last_launch_count()
+
+
+class LinearCrossEntropyFunction(torch.autograd.Function):
+    """autograd wrapper: forward = lce_forward, backward = lce_backward (recompute)."""
+
+    @staticmethod
+    def forward(ctx, H, W, y, chunk=1024, ignore_index=IGNORE_INDEX):
+        loss, lse = lce_forward(H, W, y, chunk=chunk, ignore_index=ignore_index)
+        ctx.save_for_backward(H, W, y, lse)
+        ctx.chunk = chunk
+        ctx.ignore_index = ignore_index
+        return loss.view(())
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        H, W, y, lse = ctx.saved_tensors
+        g = grad_out.detach().reshape(1).to(torch.float32).contiguous()
+        dH, dW = lce_backward(H, W, y, lse, dloss=g, chunk=ctx.chunk,
+                              ignore_index=ctx.ignore_index)
+        return dH, dW.to(W.dtype), None, None, None
+
+
+def linear_cross_entropy(H, W, y, chunk: int = 1024, ignore_index: int = IGNORE_INDEX):
+    """Mean cross-entropy of softmax(H W^T) against y, differentiable in H and W."""
+    return LinearCrossEntropyFunction.apply(H, W, y, chunk, ignore_index)

@@ -1,0 +1,371 @@
+// C ABI of the fused chunked linear + cross-entropy library: argument checks,
+// workspace layout, tensor-map encoding and the per-chunk launch sequence.
+// Declarations and the contract of every entry point are in include/lce.h.
+//
+// The token axis is cut into chunks of `chunk` rows ("Arquitectura interna de
+// Unsloth y optimizacion en Triton", section 3: token blocks; "Unsloth
+// Architecture: Manual Triton Backpropagation, Fused Cross-Entropy, and 80% VRAM
+// Cut", pillar 1: chunks of tokens, logits discarded after each chunk). Per
+// chunk the only HBM state is O(chunk * V): the (max, sumexp) slab partials and
+// one bf16 [chunk, V] buffer that holds exp(z - slab max), then G.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/lce.h"
+#include "lce_internal.h"
+
+using namespace lce;
+
+namespace {
+
+thread_local int g_launches = 0;
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_mu;
+constexpr int kMaxDevices = 64;
+bool g_dev_ready[kMaxDevices] = {};
+int g_dev_sms[kMaxDevices] = {};
+
+lce_status init_device(int *sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LCE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return LCE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return LCE_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (!g_dev_ready[dev]) {
+        int major = 0, minor = 0, n = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return LCE_ERR_CUDA;
+        if (major != 10 || minor != 3) return LCE_ERR_UNSUPPORTED;
+        if (gemm_set_attributes() != cudaSuccess) return LCE_ERR_CUDA;
+        if (aux_set_attributes() != cudaSuccess) return LCE_ERR_CUDA;
+        g_dev_sms[dev] = n;
+        g_dev_ready[dev] = true;
+    }
+    *sms = g_dev_sms[dev];
+    return LCE_OK;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+struct Layout {
+    long long C = 0;         // rows per chunk
+    long long nchunks = 0;
+    int nparts = 0;          // 128-column slabs per row
+    int ldg = 0;             // row stride of the chunk buffer (elements)
+    size_t off_loss_rows = 0, off_zy = 0, off_parts = 0, off_G = 0, total = 0;
+    size_t hdr_bytes = 0;
+};
+
+bool make_layout(long long N, long long D, long long V, long long chunk, Layout &L) {
+    if (N < 0 || D <= 0 || V <= 0 || chunk <= 0) return false;
+    if (D % 8 != 0) return false;
+    if (N > 0x7fffffffll || D > 0x7fffffffll || V > MAX_V) return false;
+    L.C = chunk < (N > 0 ? N : 1) ? chunk : (N > 0 ? N : 1);
+    L.nchunks = N > 0 ? cdiv(N, L.C) : 0;
+    L.nparts = static_cast<int>(cdiv(V, PART_COLS));
+    L.ldg = static_cast<int>(align_up(static_cast<size_t>(V), BN));
+    if (static_cast<unsigned long long>(L.C) * L.ldg > (1ull << 40)) return false;
+    L.hdr_bytes = align_up(sizeof(int) * (HDR_COUNTERS + 2 * L.nchunks + 2), 1024);
+    size_t off = L.hdr_bytes;
+    L.off_loss_rows = off;
+    off += align_up(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1), 1024);
+    L.off_zy = off;
+    off += align_up(sizeof(float) * static_cast<size_t>(L.C), 1024);
+    L.off_parts = off;
+    off += align_up(sizeof(float2) * static_cast<size_t>(L.C) * L.nparts, 1024);
+    L.off_G = off;
+    off += align_up(2 * static_cast<size_t>(L.C) * L.ldg, 1024);
+    L.total = off;
+    return true;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
+bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct Ctx {
+    const __nv_bfloat16 *H, *W;
+    const long long *y;
+    long long N, D, V, ign;
+    Layout L;
+    uint8_t *ws;
+    int *hdr;
+    float *loss_rows, *zy;
+    float2 *parts;
+    __nv_bfloat16 *G;
+    int sms;
+    cudaStream_t s;
+    CUtensorMap tmH_K, tmW_K, tmW_MN;
+};
+
+#define LCE_LAUNCH(expr)                                  \
+    do {                                                  \
+        if ((expr) != cudaSuccess) return LCE_ERR_CUDA;   \
+        ++g_launches;                                     \
+    } while (0)
+
+lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
+                 int64_t V, int64_t ign, int64_t chunk, void *ws, size_t ws_bytes,
+                 lce_stream_t stream) {
+    g_launches = 0;
+    if (!make_layout(N, D, V, chunk, c.L)) return LCE_ERR_INVALID_ARG;
+    if (!ws) return LCE_ERR_INVALID_ARG;
+    if (N > 0 && (!H || !y)) return LCE_ERR_INVALID_ARG;
+    if (!W) return LCE_ERR_INVALID_ARG;
+    if (!aligned16(ws) || !aligned16(W) || (H && !aligned16(H)) || (y && !aligned16(y)))
+        return LCE_ERR_ALIGNMENT;
+    if (ws_bytes < c.L.total) return LCE_ERR_WORKSPACE;
+    lce_status st = init_device(&c.sms);
+    if (st != LCE_OK) return st;
+    c.H = static_cast<const __nv_bfloat16 *>(H);
+    c.W = static_cast<const __nv_bfloat16 *>(W);
+    c.y = reinterpret_cast<const long long *>(y);
+    c.N = N;
+    c.D = D;
+    c.V = V;
+    c.ign = ign;
+    c.ws = static_cast<uint8_t *>(ws);
+    c.hdr = reinterpret_cast<int *>(c.ws);
+    c.loss_rows = reinterpret_cast<float *>(c.ws + c.L.off_loss_rows);
+    c.zy = reinterpret_cast<float *>(c.ws + c.L.off_zy);
+    c.parts = reinterpret_cast<float2 *>(c.ws + c.L.off_parts);
+    c.G = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_G);
+    c.s = reinterpret_cast<cudaStream_t>(stream);
+    if (!encode_2d(&c.tmW_K, W, D, V, D * 2, BK, BN)) return LCE_ERR_CUDA;
+    if (!encode_2d(&c.tmW_MN, W, D, V, D * 2, 64, BK)) return LCE_ERR_CUDA;
+    if (N > 0 && !encode_2d(&c.tmH_K, H, D, N, D * 2, BK, BM)) return LCE_ERR_CUDA;
+    if (cudaMemsetAsync(c.ws, 0, c.L.hdr_bytes, c.s) != cudaSuccess) return LCE_ERR_CUDA;
+    LCE_LAUNCH(launch_label_scan(c.y, N, V, ign, c.hdr, c.s));
+    return LCE_OK;
+}
+
+void base_params(const Ctx &c, GemmParams &p, long long row0, long long rows, int slot) {
+    p.rows = static_cast<int>(rows);
+    p.row0 = static_cast<int>(row0);
+    p.V = static_cast<int>(c.V);
+    p.D = static_cast<int>(c.D);
+    p.ignore_index = c.ign;
+    p.y = c.y;
+    p.tile_counter = c.hdr + HDR_COUNTERS + slot;
+    p.hdr = c.hdr;
+    p.parts = c.parts;
+    p.nparts = c.L.nparts;
+    p.zy = c.zy;
+    p.G = c.G;
+    p.ldg = c.L.ldg;
+    p.timeout_ns = kDefaultTimeoutNs;
+}
+
+lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, int slot,
+                      const float *lse, const float *dloss) {
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    base_params(c, p, row0, rows, slot);
+    p.tmA0 = c.tmH_K;
+    p.tmB0 = c.tmW_K;
+    p.m_blocks0 = static_cast<int>(cdiv(rows, BM));
+    p.n_blocks0 = static_cast<int>(cdiv(c.V, BN));
+    p.k_blocks0 = static_cast<int>(cdiv(c.D, BK));
+    p.total_tiles = p.m_blocks0 * p.n_blocks0;
+    p.lse = lse;
+    p.dloss = dloss;
+    const int grid = p.total_tiles < c.sms ? p.total_tiles : c.sms;
+    LCE_LAUNCH(launch_gemm(mode, p, grid, c.s));
+    return LCE_OK;
+}
+
+lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void *dH, float *dW,
+                   bool accumulate) {
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    base_params(c, p, row0, rows, slot);
+    const __nv_bfloat16 *Hc = c.H + row0 * c.D;
+    if (!encode_2d(&p.tmA0, c.G, c.V, rows, 2ull * c.L.ldg, BK, BM)) return LCE_ERR_CUDA;
+    p.tmB0 = c.tmW_MN;
+    if (!encode_2d(&p.tmA1, c.G, c.V, rows, 2ull * c.L.ldg, 64, BK)) return LCE_ERR_CUDA;
+    if (!encode_2d(&p.tmB1, Hc, c.D, rows, 2ull * c.D, 64, BK)) return LCE_ERR_CUDA;
+    p.m_blocks0 = static_cast<int>(cdiv(rows, BM));
+    p.n_blocks0 = static_cast<int>(cdiv(c.D, BN));
+    p.k_blocks0 = static_cast<int>(cdiv(c.V, BK));
+    p.m_blocks1 = static_cast<int>(cdiv(c.V, BM));
+    p.n_blocks1 = static_cast<int>(cdiv(c.D, BN));
+    p.k_blocks1 = static_cast<int>(cdiv(rows, BK));
+    p.total_tiles = p.m_blocks0 * p.n_blocks0 + p.m_blocks1 * p.n_blocks1;
+    p.dH = static_cast<__nv_bfloat16 *>(dH);
+    p.dW = dW;
+    p.dw_accumulate = accumulate ? 1 : 0;
+    const int grid = p.total_tiles < c.sms ? p.total_tiles : c.sms;
+    LCE_LAUNCH(launch_gemm(MODE_BWD, p, grid, c.s));
+    return LCE_OK;
+}
+
+lce_status run_merge(const Ctx &c, bool fixup, long long row0, long long rows, float *lse,
+                     const float *dloss) {
+    MergeParams m;
+    m.parts = c.parts;
+    m.nparts = c.L.nparts;
+    m.zy = c.zy;
+    m.G = c.G;
+    m.ldg = c.L.ldg;
+    m.rows = static_cast<int>(rows);
+    m.row0 = static_cast<int>(row0);
+    m.V = static_cast<int>(c.V);
+    m.ignore_index = c.ign;
+    m.y = c.y;
+    m.hdr = c.hdr;
+    m.dloss = dloss;
+    m.lse = lse;
+    m.loss_rows = c.loss_rows;
+    LCE_LAUNCH(launch_merge(fixup, m, c.s));
+    return LCE_OK;
+}
+
+#define LCE_TRY(expr)                         \
+    do {                                      \
+        lce_status _st = (expr);              \
+        if (_st != LCE_OK) return _st;        \
+    } while (0)
+
+}  // namespace
+
+extern "C" {
+
+lce_status lce_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk, size_t *bytes) {
+    if (!bytes) return LCE_ERR_INVALID_ARG;
+    Layout L;
+    if (!make_layout(N, D, V, chunk, L)) return LCE_ERR_INVALID_ARG;
+    *bytes = L.total;
+    return LCE_OK;
+}
+
+lce_status lce_forward(const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
+                       int64_t V, int64_t ignore_index, int64_t chunk, float *loss, float *lse,
+                       void *ws, size_t ws_bytes, lce_stream_t stream) {
+    g_launches = 0;
+    if (!loss || (N > 0 && !lse)) return LCE_ERR_INVALID_ARG;
+    if (!aligned16(loss) || (lse && !aligned16(lse))) return LCE_ERR_ALIGNMENT;
+    Ctx c;
+    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream));
+    for (long long k = 0; k < c.L.nchunks; ++k) {
+        const long long row0 = k * c.L.C;
+        const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
+        LCE_TRY(run_logits(c, MODE_LSE, row0, rows, static_cast<int>(k), nullptr, nullptr));
+        LCE_TRY(run_merge(c, false, row0, rows, lse, nullptr));
+    }
+    LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss, c.s));
+    return LCE_OK;
+}
+
+lce_status lce_backward(const void *H, const void *W, const int64_t *y, const float *lse,
+                        const float *dloss, void *dH, float *dW, int64_t N, int64_t D, int64_t V,
+                        int64_t ignore_index, int64_t chunk, void *ws, size_t ws_bytes,
+                        lce_stream_t stream) {
+    g_launches = 0;
+    if (!dW || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
+    if (!aligned16(dW) || (dH && !aligned16(dH)) || (lse && !aligned16(lse)))
+        return LCE_ERR_ALIGNMENT;
+    Ctx c;
+    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream));
+    if (c.L.nchunks == 0) {
+        if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess)
+            return LCE_ERR_CUDA;
+        return LCE_OK;
+    }
+    for (long long k = 0; k < c.L.nchunks; ++k) {
+        const long long row0 = k * c.L.C;
+        const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
+        LCE_TRY(run_logits(c, MODE_G, row0, rows, static_cast<int>(2 * k), lse, dloss));
+        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dH, dW, k > 0));
+    }
+    return LCE_OK;
+}
+
+lce_status lce_fwd_bwd(const void *H, const void *W, const int64_t *y, const float *dloss,
+                       int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                       float *loss, float *lse, void *dH, float *dW, void *ws, size_t ws_bytes,
+                       lce_stream_t stream) {
+    g_launches = 0;
+    if (!loss || !dW || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
+    if (!aligned16(loss) || !aligned16(dW) || (dH && !aligned16(dH)) || (lse && !aligned16(lse)))
+        return LCE_ERR_ALIGNMENT;
+    Ctx c;
+    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream));
+    if (c.L.nchunks == 0) {
+        if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess)
+            return LCE_ERR_CUDA;
+    }
+    for (long long k = 0; k < c.L.nchunks; ++k) {
+        const long long row0 = k * c.L.C;
+        const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
+        LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr));
+        LCE_TRY(run_merge(c, true, row0, rows, lse, dloss));
+        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dH, dW, k > 0));
+    }
+    LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss, c.s));
+    return LCE_OK;
+}
+
+lce_status lce_read_status(const void *ws, lce_stream_t stream) {
+    if (!ws) return LCE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LCE_ERR_CUDA;
+    int flag = 0;
+    if (cudaMemcpy(&flag, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LCE_ERR_CUDA;
+    if (flag) {
+        const int zero = 0;
+        if (cudaMemcpy(const_cast<void *>(ws), &zero, sizeof(int), cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+            return LCE_ERR_CUDA;
+    }
+    if (flag & FLAG_TIMEOUT) return LCE_ERR_TIMEOUT;
+    if (flag & FLAG_LABEL) return LCE_ERR_LABEL_RANGE;
+    return LCE_OK;
+}
+
+const char *lce_status_string(lce_status s) {
+    switch (s) {
+        case LCE_OK: return "ok";
+        case LCE_ERR_INVALID_ARG: return "invalid argument";
+        case LCE_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case LCE_ERR_WORKSPACE: return "workspace too small";
+        case LCE_ERR_LABEL_RANGE: return "label outside [0, V) and not ignore_index";
+        case LCE_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case LCE_ERR_CUDA: return "CUDA runtime error";
+        case LCE_ERR_UNSUPPORTED: return "device is not sm_103";
+    }
+    return "unknown status";
+}
+
+int lce_version(void) { return 100; }
+
+int lce_last_launch_count(void) { return g_launches; }
+
+}  // extern "C"

@@ -1,0 +1,211 @@
+// Bandwidth-bound kernels around the tensor-core GEMMs:
+//   * label scan: N_valid and the out-of-range check;
+//   * slab merge: per row, combine the (max, sumexp) partials of the 128-column
+//     slabs into lse_i = M + log sum_p s_p exp(m_p - M), write the row's loss
+//     lse_i - z_{i,y_i}, and (fused path) turn the stored P' = exp(z - m_p) into
+//     G = (P' exp(m_p - lse_i) - 1[j = y_i]) * dloss / N_valid in place
+//     ("Unsloth Architecture: Manual Triton Backpropagation, Fused Cross-Entropy,
+//     and 80% VRAM Cut", pillar 1: the loss -z_{i,y_i} + log sum_j e^{z_ij} and
+//     the gradient p_ij - 1[j = y_i]);
+//   * loss finalisation: fixed-order fp64 sum of the per-row losses / N_valid.
+// Every reduction has a fixed order, so results are bit-reproducible.
+#include "lce_internal.h"
+
+namespace lce {
+
+constexpr float LOG2E_F = 1.4426950408889634f;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ------------------------------------------------------------------ label scan
+
+__global__ void __launch_bounds__(1024) lce_label_scan_kernel(const long long *__restrict__ y,
+                                                              long long N, long long V,
+                                                              long long ign, int *hdr) {
+    __shared__ int s_cnt[32];
+    __shared__ int s_bad[32];
+    int cnt = 0, bad = 0;
+    for (long long i = blockIdx.x * 1024ll + threadIdx.x; i < N; i += 1024ll * gridDim.x) {
+        const long long v = y[i];
+        if (v != ign) {
+            if (v >= 0 && v < V) ++cnt;
+            else bad = 1;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) { s_cnt[w] = cnt; s_bad[w] = bad; }
+    __syncthreads();
+    if (w == 0) {
+        cnt = s_cnt[l];
+        bad = s_bad[l];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+            bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+        }
+        if (l == 0) {
+            if (cnt) atomicAdd(hdr + HDR_NVALID, cnt);   // integer: order-independent
+            if (bad) atomicOr(hdr + HDR_FLAG, FLAG_LABEL);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ merge
+
+constexpr int MERGE_THREADS = 256;
+
+template <bool FIXUP>
+__global__ void __launch_bounds__(MERGE_THREADS) lce_merge_kernel(const MergeParams p) {
+    extern __shared__ float s_fac[];   // [nparts] (fixup only)
+    __shared__ float s_red[MERGE_THREADS / 32];
+    __shared__ float s_bcast;
+    const int r = blockIdx.x;          // row within the chunk
+    const int t = threadIdx.x, w = t >> 5, l = t & 31;
+    const float2 *parts = p.parts + static_cast<size_t>(r) * p.nparts;
+
+    // row maximum over the slab maxima
+    float m = -INFINITY;
+    for (int i = t; i < p.nparts; i += MERGE_THREADS) m = fmaxf(m, parts[i].x);
+    m = warp_max(m);
+    if (l == 0) s_red[w] = m;
+    __syncthreads();
+    if (w == 0) {
+        m = (l < MERGE_THREADS / 32) ? s_red[l] : -INFINITY;
+        m = warp_max(m);
+        if (l == 0) s_bcast = m;
+    }
+    __syncthreads();
+    const float M = s_bcast;
+    const float M2 = M * LOG2E_F;
+    // rescaled sum of the slab sums
+    float s = 0.f;
+    for (int i = t; i < p.nparts; i += MERGE_THREADS) {
+        const float2 q = parts[i];
+        s += q.y * exp2f(fmaf(q.x, LOG2E_F, -M2));
+    }
+    s = warp_sum(s);
+    __syncthreads();
+    if (l == 0) s_red[w] = s;
+    __syncthreads();
+    if (w == 0) {
+        s = (l < MERGE_THREADS / 32) ? s_red[l] : 0.f;
+        s = warp_sum(s);
+        if (l == 0) s_bcast = M + logf(s);
+    }
+    __syncthreads();
+    const float lse = s_bcast;
+
+    const int grow = p.row0 + r;
+    const long long yv = p.y[grow];
+    const bool y_ok = yv != p.ignore_index && yv >= 0 && yv < p.V;
+    if (t == 0) {
+        p.lse[grow] = lse;
+        p.loss_rows[grow] = y_ok ? lse - p.zy[r] : 0.f;
+    }
+    if constexpr (FIXUP) {
+        const int nv = p.hdr[HDR_NVALID];
+        const float dl = p.dloss ? *p.dloss : 1.f;
+        const float scale = (y_ok && nv > 0) ? dl / static_cast<float>(nv) : 0.f;
+        const float lse2 = lse * LOG2E_F;
+        for (int i = t; i < p.nparts; i += MERGE_THREADS)
+            s_fac[i] = scale != 0.f ? exp2f(fmaf(parts[i].x, LOG2E_F, -lse2)) * scale : 0.f;
+        __syncthreads();
+        uint4 *row = reinterpret_cast<uint4 *>(p.G + static_cast<size_t>(r) * p.ldg);
+        const int nvec = (p.V + 7) >> 3;
+        const int ycol = y_ok ? static_cast<int>(yv) : -1;
+        for (int i = t; i < nvec; i += MERGE_THREADS) {
+            uint4 u = row[i];
+            const float f = s_fac[i >> 4];            // 16 vectors of 8 = one 128-column slab
+            uint32_t *wv = reinterpret_cast<uint32_t *>(&u);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&wv[q]);
+                float2 x = __bfloat1622float2(h);
+                const int c = i * 8 + 2 * q;
+                x.x *= f;
+                x.y *= f;
+                if (c == ycol) x.x -= scale;
+                if (c + 1 == ycol) x.y -= scale;
+                h = __floats2bfloat162_rn(x.x, x.y);
+                wv[q] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            row[i] = u;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ loss
+
+__global__ void __launch_bounds__(1024) lce_loss_finalize_kernel(const float *__restrict__ loss_rows,
+                                                                 long long N, const int *hdr,
+                                                                 float *loss) {
+    __shared__ double s_red[32];
+    double s = 0.0;
+    for (long long i = threadIdx.x; i < N; i += 1024) s += static_cast<double>(loss_rows[i]);
+    s = warp_sum_d(s);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) s_red[w] = s;
+    __syncthreads();
+    if (w == 0) {
+        s = s_red[l];
+        s = warp_sum_d(s);
+        if (l == 0) {
+            const int nv = hdr[HDR_NVALID];
+            *loss = nv > 0 ? static_cast<float>(s / nv) : 0.f;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+
+cudaError_t launch_label_scan(const long long *y, long long N, long long V, long long ign, int *hdr,
+                              cudaStream_t s) {
+    long long blocks = (N + 1023) / 1024;
+    if (blocks < 1) blocks = 1;
+    if (blocks > 64) blocks = 64;
+    lce_label_scan_kernel<<<static_cast<int>(blocks), 1024, 0, s>>>(y, N, V, ign, hdr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge(bool fixup, const MergeParams &p, cudaStream_t s) {
+    if (p.rows <= 0) return cudaSuccess;
+    if (fixup) {
+        const size_t smem = static_cast<size_t>(p.nparts) * sizeof(float);
+        lce_merge_kernel<true><<<p.rows, MERGE_THREADS, smem, s>>>(p);
+    } else {
+        lce_merge_kernel<false><<<p.rows, MERGE_THREADS, 0, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t aux_set_attributes() {
+    return cudaFuncSetAttribute(lce_merge_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                MERGE_MAX_SMEM);
+}
+
+cudaError_t launch_loss_finalize(const float *loss_rows, long long N, const int *hdr, float *loss,
+                                 cudaStream_t s) {
+    lce_loss_finalize_kernel<<<1, 1024, 0, s>>>(loss_rows, N, hdr, loss);
+    return cudaGetLastError();
+}
+
+}  // namespace lce

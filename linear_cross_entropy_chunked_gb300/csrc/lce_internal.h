@@ -1,0 +1,109 @@
+// Internal declarations shared by the kernels and the C-ABI host code.
+// Not part of the public interface (that is include/lce.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lce {
+
+// ---------------------------------------------------------------- GEMM tiling
+// One CTA per SM, persistent. A 128 x 256 fp32 accumulator tile lives in TMEM
+// (256 columns); two of them (512 columns = all of TMEM) let the epilogue of
+// tile t overlap the MMAs of tile t+1.
+constexpr int BM = 128;            // UMMA M (TMEM lanes)
+constexpr int BN = 256;            // UMMA N (TMEM columns per accumulator)
+constexpr int BK = 64;             // one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;         // K of one tcgen05.mma kind::f16
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;             // 16 KB
+constexpr int B_BYTES = BN * BK * 2;             // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
+constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + 1 KB alignment slack
+constexpr int NUM_EPI_WARPS = 8;   // warps 0..7: TMEM lane quarter = warp % 4, column half = warp / 4
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int GEMM_THREADS = 320;
+constexpr int SCHED_DEPTH = 4;
+constexpr int TMEM_COLS = 512;
+constexpr int PART_COLS = 128;     // columns covered by one (max, sum) partial
+
+// Epilogue / tile-set modes of the GEMM kernel.
+enum GemmMode : int {
+    MODE_LSE = 0,     // logits tiles -> per-(row, 128-col) (max, sumexp) partials + target logit
+    MODE_LSE_P = 1,   // ... + store P' = exp(z - max_part) as bf16 into the chunk buffer
+    MODE_G = 2,       // logits tiles -> G = (exp(z - lse) - onehot) * scale as bf16 (given lse)
+    MODE_BWD = 3      // dH tiles (G W) followed by dW tiles (G^T H) in one persistent launch
+};
+
+// Workspace header (int32 words).
+enum : int {
+    HDR_FLAG = 0,       // bit 0: label out of range, bit 1: pipeline wait timed out
+    HDR_NVALID = 1,
+    HDR_COUNTERS = 16,  // one dynamic tile counter per GEMM launch of a call
+};
+constexpr int FLAG_LABEL = 1;
+constexpr int FLAG_TIMEOUT = 2;
+
+struct GemmParams {
+    CUtensorMap tmA0;      // type-0 tiles: logits A = H (K-major) | dH A = G (K-major)
+    CUtensorMap tmB0;      //               logits B = W (K-major) | dH B = W (MN-major)
+    CUtensorMap tmA1;      // type-1 tiles: dW A = G^T (MN-major)
+    CUtensorMap tmB1;      //               dW B = H chunk (MN-major)
+    int m_blocks0, n_blocks0, k_blocks0;
+    int m_blocks1, n_blocks1, k_blocks1;
+    int total_tiles;
+    int rows;              // rows in this chunk
+    int row0;              // first global row of this chunk
+    int V, D;
+    long long ignore_index;
+    const long long *y;    // labels, global [N]
+    int *tile_counter;
+    int *hdr;
+    const float *dloss;    // device scalar or null (= 1)
+    // logits epilogue
+    float2 *parts;         // [rows][nparts] (max, sumexp)
+    int nparts;
+    float *zy;             // [rows] target logits
+    __nv_bfloat16 *G;      // [rows][ldg] P' or G
+    int ldg;
+    const float *lse;      // global [N] (MODE_G)
+    // backward epilogues
+    __nv_bfloat16 *dH;     // global [N][D]
+    float *dW;             // [V][D]
+    int dw_accumulate;     // 0: store, 1: add to existing dW
+    unsigned long long timeout_ns;
+};
+
+struct MergeParams {
+    const float2 *parts;
+    int nparts;
+    const float *zy;
+    __nv_bfloat16 *G;
+    int ldg;
+    int rows, row0, V;
+    long long ignore_index;
+    const long long *y;
+    const int *hdr;
+    const float *dloss;
+    float *lse;            // global [N]
+    float *loss_rows;      // global [N]
+};
+
+// launchers (return cudaError_t of the launch)
+cudaError_t launch_gemm(int mode, const GemmParams &p, int grid, cudaStream_t s);
+cudaError_t launch_label_scan(const long long *y, long long N, long long V, long long ign,
+                              int *hdr, cudaStream_t s);
+cudaError_t launch_merge(bool fixup, const MergeParams &p, cudaStream_t s);
+cudaError_t launch_loss_finalize(const float *loss_rows, long long N, const int *hdr,
+                                 float *loss, cudaStream_t s);
+cudaError_t gemm_set_attributes();
+cudaError_t aux_set_attributes();
+
+// The merge kernel keeps one float per 128-column slab in shared memory.
+constexpr int MERGE_MAX_SMEM = 200 * 1024;
+constexpr long long MAX_V = static_cast<long long>(MERGE_MAX_SMEM / 4) * PART_COLS;
+
+}  // namespace lce

@@ -1,0 +1,161 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on
+the same seeded inputs, element by element at sizes the oracle finishes in
+seconds, plus edge cases and invariants."""
+import numpy as np
+import pytest
+import torch
+
+from lce_synth import IGNORE_INDEX, WORKLOADS, make_inputs, workload_inputs
+from oracle import lce_oracle as O
+from tests.gpu_util import check_grad, check_loss, check_lse, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lce():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import linear_cross_entropy_chunked_gb300 as pkg
+    pkg.build()
+    return pkg
+
+
+DEV = "cuda:0"
+
+
+def run_all_paths(lce, H, W, y, chunk, dloss=1.0):
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    dl = torch.tensor([dloss], dtype=torch.float32, device=DEV)
+    loss, lse, dH, dW = lce.lce_fwd_bwd(Hd, Wd, yd, dloss=dl, chunk=chunk)
+    floss, flse = lce.lce_forward(Hd, Wd, yd, chunk=chunk)
+    bdH, bdW = lce.lce_backward(Hd, Wd, yd, flse, dloss=dl, chunk=chunk)
+    torch.cuda.synchronize()
+    return dict(loss=loss.item(), lse=to64(lse), dH=to64(dH), dW=to64(dW),
+                floss=floss.item(), flse=to64(flse), bdH=to64(bdH), bdW=to64(bdW))
+
+
+def compare(r, ref):
+    check_loss(r["loss"], ref["loss"])
+    check_lse(r["lse"], ref["lse"])
+    check_grad("dH", r["dH"], ref["dH"])
+    check_grad("dW", r["dW"], ref["dW"])
+    check_loss(r["floss"], ref["loss"])
+    check_lse(r["flse"], ref["lse"])
+    check_grad("dH (backward)", r["bdH"], ref["dH"])
+    check_grad("dW (backward)", r["bdW"], ref["dW"])
+
+
+def test_tiny_workload(lce):
+    H, W, y = workload_inputs("tiny")
+    r = run_all_paths(lce, H, W, y, chunk=1024)
+    compare(r, O.forward_backward(H, W, y))
+
+
+@pytest.mark.parametrize("N,D,V,chunk,n_ign,dloss", [
+    (300, 264, 1000, 128, 17, 0.7),      # ragged in every dimension, several chunks
+    (129, 64, 257, 64, 5, 1.0),          # one row past a tile, V one past a tile
+    (1000, 520, 3000, 384, 40, 2.5),     # chunk not a multiple of the tile
+    (77, 128, 100, 1024, 3, 1.0),        # N < chunk, V < one tile
+    (256, 8, 513, 256, 0, 1.0),          # tiny D (one partial K block)
+])
+def test_ragged_shapes(lce, N, D, V, chunk, n_ign, dloss):
+    H, W, y = make_inputs(N, D, V, seed=N + D + V, labels="uniform", n_ignored=n_ign, w_std=0.05)
+    r = run_all_paths(lce, H, W, y, chunk=chunk, dloss=dloss)
+    compare(r, O.forward_backward(H, W, y, dloss=dloss))
+
+
+def test_labels_at_vocab_ends(lce):
+    N, D, V = 200, 128, 777
+    H, W, y = make_inputs(N, D, V, seed=3)
+    y[::2] = 0
+    y[1::2] = V - 1
+    r = run_all_paths(lce, H, W, y, chunk=128)
+    compare(r, O.forward_backward(H, W, y))
+
+
+def test_all_rows_ignored(lce):
+    N, D, V = 130, 64, 300
+    H, W, y = make_inputs(N, D, V, seed=4)
+    y[:] = IGNORE_INDEX
+    r = run_all_paths(lce, H, W, y, chunk=64)
+    assert r["loss"] == 0.0 and r["floss"] == 0.0
+    for k in ("dH", "dW", "bdH", "bdW"):
+        assert not np.any(r[k]), k
+    check_lse(r["lse"], O.forward(H, W, y)[1])
+
+
+def test_empty_batch(lce):
+    D, V = 64, 300
+    H = torch.zeros(0, D, dtype=torch.bfloat16, device=DEV)
+    W = torch.randn(V, D, device=DEV).to(torch.bfloat16)
+    y = torch.zeros(0, dtype=torch.int64, device=DEV)
+    loss, lse, dH, dW = lce.lce_fwd_bwd(H, W, y, chunk=128)
+    torch.cuda.synchronize()
+    assert loss.item() == 0.0 and dW.abs().max().item() == 0.0
+
+
+def test_label_out_of_range_reports_status(lce):
+    N, D, V = 140, 64, 500
+    H, W, y = make_inputs(N, D, V, seed=5)
+    y[3] = V
+    y[9] = -7
+    ws = lce.alloc_workspace(N, D, V, 64, DEV)
+    loss, lse, dH, dW = lce.lce_fwd_bwd(H.to(DEV), W.to(DEV), y.to(DEV), chunk=64, ws=ws)
+    assert lce.read_status(ws) == 4          # LCE_ERR_LABEL_RANGE
+    assert lce.read_status(ws) == 0          # cleared
+    ref = O.forward_backward(H, W, y)
+    assert ref["n_bad"] == 2
+    check_loss(loss.item(), ref["loss"])
+    check_grad("dH", to64(dH), ref["dH"])
+    check_grad("dW", to64(dW), ref["dW"])
+
+
+def test_deterministic_bits(lce):
+    H, W, y = make_inputs(520, 256, 4000, seed=6, n_ignored=20)
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    a = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=256)
+    b = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=256)
+    torch.cuda.synchronize()
+    for x, z in zip(a, b):
+        assert torch.equal(x, z)
+
+
+def test_chunk_invariance(lce):
+    H, W, y = make_inputs(1024, 512, 5000, seed=8, n_ignored=30)
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    outs = [lce.lce_fwd_bwd(Hd, Wd, yd, chunk=c) for c in (128, 512, 1024)]
+    torch.cuda.synchronize()
+    base = outs[0]
+    for o in outs[1:]:
+        assert abs(o[0].item() - base[0].item()) <= 1e-5 * abs(base[0].item())
+        assert (o[1] - base[1]).abs().max().item() <= 1e-5
+        check_grad("dH", to64(o[2]), to64(base[2]))
+        check_grad("dW", to64(o[3]), to64(base[3]))
+
+
+def test_autograd_wrapper(lce):
+    H, W, y = make_inputs(300, 128, 900, seed=9, n_ignored=10)
+    Hd = H.to(DEV).requires_grad_(True)
+    Wd = W.to(DEV).requires_grad_(True)
+    loss = lce.linear_cross_entropy(Hd, Wd, y.to(DEV), chunk=128)
+    (loss * 3.0).backward()
+    ref = O.forward_backward(H, W, y, dloss=3.0)
+    check_loss(loss.item(), ref["loss"])
+    check_grad("dH", to64(Hd.grad), ref["dH"])
+    check_grad("dW", to64(Wd.grad), ref["dW"])
+
+
+@pytest.mark.parametrize("name", ["llama2-7b", "mistral-7b"])
+def test_workload_full_oracle(lce, name):
+    """Whole-output comparison on the two mid-size workloads (oracle in fp64)."""
+    wl = WORKLOADS[name]
+    H, W, y = workload_inputs(wl)
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    loss, lse, dH, dW = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=wl.chunks[0])
+    torch.cuda.synchronize()
+    ref = O.forward_backward(H, W, y)
+    check_loss(loss.item(), ref["loss"])
+    check_lse(to64(lse), ref["lse"])
+    check_grad("dH", to64(dH), ref["dH"])
+    check_grad("dW", to64(dW), ref["dW"])
