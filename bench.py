@@ -1,0 +1,418 @@
+"""Benchmark of the fused chunked linear + cross-entropy forward+backward.
+
+One step = one lce_fwd_bwd call (label scan, per-chunk logits GEMM with the
+log-sum-exp epilogue, slab merge + G rescale, dH/dW GEMM tiles, loss) over the
+Llama-3-8B-shaped LM head: N=16384 tokens, D=4096, V=128256, chunk 1024, 5% of
+rows ignore_index, synthetic seeded inputs (no dataset).
+
+Prints one JSON line (rank 0). With --impl reference the fp64 CPU oracle is
+timed instead on the host cores, one bounded row sample per step.
+
+Multi-GPU (torchrun, --gpus N): every rank runs its own replica of the
+workload (independent problems, weak scaling, no collective on the data path);
+`value` is the tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "LCE fwd+bwd tokens/s at N=16384,D=4096,V=128256; % of bf16 tensor peak"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3-8b")
+    ap.add_argument("--chunk", type=int, default=0, help="0: the workload's own chunk")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int = 0):
+        self.proc = None
+        self.lines = []
+        self.dev = device_index
+
+    def start(self):
+        import torch
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.dev).uuid)
+        except Exception:
+            uuid = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], None, [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "power_w_max": max(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- reference arm
+
+def oracle_sample_rate(wl, rows: int, H64, W64, y):
+    """Time the fp64 oracle's forward+backward over the first `rows` tokens."""
+    from oracle import lce_oracle
+    t0 = time.perf_counter()
+    lce_oracle.forward_backward(H64[:rows], W64, y[:rows])
+    return time.perf_counter() - t0
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def prepare_oracle_inputs(wl):
+    import numpy as np
+    from lce_synth import workload_inputs
+    H, W, y = workload_inputs(wl)
+    import torch
+    return (H.to(torch.float64).numpy(), W.to(torch.float64).numpy(),
+            y.numpy().astype(np.int64))
+
+
+def calibrate_rows(wl, H64, W64, y, target_s: float) -> int:
+    rows = 32
+    t = oracle_sample_rate(wl, rows, H64, W64, y)
+    want = int(rows * target_s / max(t, 1e-3))
+    return max(32, min(wl.N, want))
+
+
+def run_reference(args, wl, chunk):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    H64, W64, y = prepare_oracle_inputs(wl)
+    rows = calibrate_rows(wl, H64, W64, y, target_s=2.0)
+    for _ in range(args.warmup):
+        oracle_sample_rate(wl, rows, H64, W64, y)
+    times = [oracle_sample_rate(wl, rows, H64, W64, y) for _ in range(args.steps)]
+    total = sum(times)
+    value = rows * args.steps / total
+    flops = 6.0 * wl.D * wl.V * rows
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl, chunk, l2="host CPU run"),
+        "tflops": flops * args.steps / total / 1e12,
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(),
+                         "kind": "oracle",
+                         "sample": f"first {rows} of {wl.N} tokens of the workload per step "
+                                   f"(fp64 numpy forward+backward incl. the full dW)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- our arm
+
+def workload_config(wl, chunk, l2):
+    return {"workload": f"{wl.name} LM head N={wl.N} D={wl.D} V={wl.V} chunk={chunk}",
+            "N": wl.N, "D": wl.D, "V": wl.V, "chunk": chunk,
+            "ignored_rows": wl.n_ignored, "labels": wl.labels, "seed": wl.seed,
+            "global_batch_tokens": wl.N, "l2": l2, "parallelism": "replicas"}
+
+
+def run_ours(args, wl, chunk):
+    import torch
+    import torch.distributed as dist
+
+    import linear_cross_entropy_chunked_gb300 as lce
+    from lce_synth import make_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    lce.build()
+    peaks, peak_src = load_peaks()
+
+    # inputs (each rank its own replica, seed offset by rank)
+    H, W, y = make_inputs(wl.N, wl.D, wl.V, wl.seed + 1000 * rank, wl.labels, wl.n_ignored)
+    Hd, Wd, yd = H.to(dev), W.to(dev), y.to(dev)
+    N, D, V = wl.N, wl.D, wl.V
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    mem0 = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    ws = lce.alloc_workspace(N, D, V, chunk, dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk, loss=loss, lse=lse, dH=dH, dW=dW, ws=ws,
+                        stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    st = lce.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+    launches_per_step = lce.last_launch_count()
+    extra_bytes = torch.cuda.max_memory_allocated(dev) - mem0 - (
+        lse.numel() * 4 + dH.numel() * 2 + dW.numel() * 4 + 4)
+
+    # ---- timed region: per-step CUDA events, L2 flushed between steps
+    lce.profile_reset()
+    lce.profile_enable(True)
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_wall0 = time.perf_counter()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    lce.profile_enable(False)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(step_ms)
+    grad_ms, grad_n = lce.profile_read("grad")
+    logit_ms, logit_n = lce.profile_read("logits")
+    merge_ms, merge_n = lce.profile_read("merge")
+    st = lce.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after timed steps")
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = t.item()
+
+    ms_per_step = total_ms / args.steps
+    tokens_per_s = world * N * args.steps / (total_ms / 1e3)
+    flops_step = 6.0 * N * D * V
+    tflops = flops_step / (ms_per_step / 1e3) / 1e12
+    peak_burst = peaks.get("bf16_tflops", 1900.0)
+    peak_sust = peaks.get("bf16_tflops_sustained", 1700.0)
+
+    # dominant kernel: the dH/dW gradient GEMM (4*C*D*V flops per launch)
+    nchunks = (N + chunk - 1) // chunk
+    grad_flops_launch = 4.0 * D * V * N / nchunks
+    grad_avg_ms = grad_ms / max(grad_n, 1)
+    grad_tflops = grad_flops_launch / (grad_avg_ms / 1e3) / 1e12
+    logit_avg_ms = logit_ms / max(logit_n, 1)
+    logit_tflops = 2.0 * D * V * N / nchunks / (logit_avg_ms / 1e3) / 1e12
+    traffic = load_traffic()
+
+    # ---- end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, lce, H, W, y, chunk, dev, stream, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(wl, chunk,
+                                      l2="L2 flushed between steps (256 MB write); "
+                                         "W 1.05 GB also exceeds L2"),
+            "tflops": tflops,
+            "pct_of_bf16_peak": {"vs_burst": tflops / peak_burst, "vs_sustained": tflops / peak_sust,
+                                 "flops": "6NDV algorithmic", "peak_source": peak_src},
+            "peak_extra_hbm_bytes": int(extra_bytes),
+            "workspace_bytes": int(ws.numel()),
+            "roofline": {"kernel": "lce_gemm_kernel<MODE_BWD> (dH+dW tiles)",
+                         "bound": "tensor", "achieved": grad_tflops, "peak": peak_sust,
+                         "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                         "unit": "TFLOP/s", "frac": grad_tflops / peak_sust,
+                         "traffic": traffic.get("grad"),
+                         "launch_ms": grad_avg_ms, "flops_per_launch": grad_flops_launch},
+            "kernels": {
+                "grad": {"ms_per_launch": grad_avg_ms, "launches": grad_n,
+                         "tflops": grad_tflops, "share": grad_ms / total_ms},
+                "logits": {"ms_per_launch": logit_avg_ms, "launches": logit_n,
+                           "tflops": logit_tflops, "share": logit_ms / total_ms},
+                "merge": {"ms_per_launch": merge_ms / max(merge_n, 1), "launches": merge_n,
+                          "share": merge_ms / total_ms},
+            },
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "wall_s_timed_region": wall,
+        }
+        if e2e:
+            line["e2e"] = e2e
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_cross_entropy_chunked_gb300", "csrc")
+    for f in ("lce_gemm.cu", "lce_internal.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """DRAM bytes per launch (scaled to the bench workload) from the committed ncu
+    summary; null when absent or when the kernel source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return {}
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_source_sha256_16") != kernel_source_hash():
+        return {}
+    return {k: v.get("dram_bytes_per_launch_bench") for k, v in d.get("kernels", {}).items()}
+
+
+def run_e2e(args, lce, H, W, y, chunk, dev, stream, world):
+    import torch
+    Hh, Wh, yh = H.pin_memory(), W.pin_memory(), y.pin_memory()
+    Hd = torch.empty_like(Hh, device=dev)
+    Wd = torch.empty_like(Wh, device=dev)
+    yd = torch.empty_like(yh, device=dev)
+    N, D = H.shape
+    V = W.shape[0]
+    ws = lce.alloc_workspace(N, D, V, chunk, dev)
+    loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+
+    def step():
+        Hd.copy_(Hh, non_blocking=True)
+        Wd.copy_(Wh, non_blocking=True)
+        yd.copy_(yh, non_blocking=True)
+        lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk, loss=loss, lse=lse, dH=dH, dW=dW, ws=ws,
+                        stream=stream)
+        loss_h.copy_(loss, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    steps = max(3, args.steps // 2)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / steps
+    h2d = Hh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8
+    return {"value": world * N / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
+            "note": "H, W and y copied from pinned host memory each step; loss read back"}
+
+
+def cpu_baseline(wl):
+    H64, W64, y = prepare_oracle_inputs(wl)
+    rows = calibrate_rows(wl, H64, W64, y, target_s=12.0)
+    t = oracle_sample_rate(wl, rows, H64, W64, y)
+    return {"value": rows / t, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"first {rows} of {wl.N} tokens of the workload (fp64 numpy forward+"
+                      f"backward incl. the full dW), {t:.1f} s"}
+
+
+def main():
+    args = parse()
+    from lce_synth import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    chunk = args.chunk or (1024 if 1024 in wl.chunks else wl.chunks[0])
+    if args.impl == "reference":
+        run_reference(args, wl, chunk)
+    else:
+        run_ours(args, wl, chunk)
+
+
+if __name__ == "__main__":
+    main()

@@ -110,6 +110,24 @@ int lce_version(void);
 /* Number of kernel launches the last lce_* call on this host thread enqueued. */
 int lce_last_launch_count(void);
 
+/* Optional per-kernel timing for profiling (off by default). When enabled, every
+ * kernel launch of the calls above is bracketed by two CUDA events recorded on
+ * the call's stream. lce_profile_read() waits for the recorded events, adds the
+ * elapsed times of every completed launch of one kernel kind to its running
+ * totals and returns them; lce_profile_reset() clears the totals. Host-side
+ * state only (the events are created by the library on the current device).
+ * Kinds: */
+enum {
+    LCE_KERNEL_LOGITS = 0,   /* chunk logits GEMM with the log-sum-exp / G epilogue */
+    LCE_KERNEL_GRAD = 1,     /* dH + dW gradient GEMM tiles */
+    LCE_KERNEL_MERGE = 2,    /* slab merge (lse, row loss, G rescale) */
+    LCE_KERNEL_OTHER = 3,    /* label scan, loss finalisation */
+    LCE_KERNEL_KINDS = 4
+};
+lce_status lce_profile_enable(int on);
+lce_status lce_profile_read(int kind, double *total_ms, int64_t *launches);
+void lce_profile_reset(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -6,6 +6,7 @@ include/lce.h); this package is the thin ctypes binding around it.
 from ._binding import (  # noqa: F401
     EXPORTED,
     IGNORE_INDEX,
+    KERNEL_KINDS,
     LCEError,
     LinearCrossEntropyFunction,
     alloc_workspace,
@@ -15,6 +16,9 @@ from ._binding import (  # noqa: F401
     lce_fwd_bwd,
     lib,
     linear_cross_entropy,
+    profile_enable,
+    profile_read,
+    profile_reset,
     read_status,
     workspace_size,
 )

@@ -38,7 +38,12 @@ EXPORTED = (
     "lce_status_string",
     "lce_version",
     "lce_last_launch_count",
+    "lce_profile_enable",
+    "lce_profile_read",
+    "lce_profile_reset",
 )
+
+KERNEL_KINDS = {"logits": 0, "grad": 1, "merge": 2, "other": 3}
 
 
 class LCEError(RuntimeError):
@@ -81,7 +86,12 @@ def lib() -> ctypes.CDLL:
     L.lce_status_string.restype = ctypes.c_char_p
     L.lce_version.argtypes = []
     L.lce_last_launch_count.argtypes = []
-    for name in ("lce_workspace_size", "lce_forward", "lce_backward", "lce_fwd_bwd",
+    L.lce_profile_enable.argtypes = [ctypes.c_int]
+    L.lce_profile_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                   ctypes.POINTER(ctypes.c_int64)]
+    L.lce_profile_reset.argtypes = []
+    L.lce_profile_reset.restype = None
+    for name in ("lce_profile_enable", "lce_profile_read", "lce_workspace_size", "lce_forward", "lce_backward", "lce_fwd_bwd",
                  "lce_read_status", "lce_version", "lce_last_launch_count"):
         getattr(L, name).restype = ctypes.c_int
     _LIB = L
@@ -196,6 +206,23 @@ def read_status(ws: torch.Tensor, stream=None) -> int:
 
 def last_launch_count() -> int:
     return lib().lce_last_launch_count()
+
+
+def profile_enable(on: bool = True):
+    _check(lib().lce_profile_enable(1 if on else 0), "lce_profile_enable")
+
+
+def profile_reset():
+    lib().lce_profile_reset()
+
+
+def profile_read(kind: str):
+    """(total_ms, launches) of every completed launch of one kernel kind."""
+    ms = ctypes.c_double(0)
+    n = ctypes.c_int64(0)
+    _check(lib().lce_profile_read(KERNEL_KINDS[kind], ctypes.byref(ms), ctypes.byref(n)),
+           "lce_profile_read")
+    return ms.value, n.value
 
 
 class LinearCrossEntropyFunction(torch.autograd.Function):

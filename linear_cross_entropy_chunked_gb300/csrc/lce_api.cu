@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <vector>
 
 #include "../../include/lce.h"
 #include "lce_internal.h"
@@ -125,11 +126,55 @@ struct Ctx {
     CUtensorMap tmH_K, tmW_K, tmW_MN;
 };
 
-#define LCE_LAUNCH(expr)                                  \
-    do {                                                  \
-        if ((expr) != cudaSuccess) return LCE_ERR_CUDA;   \
-        ++g_launches;                                     \
+// ---- optional per-kernel event timing (lce_profile_*)
+struct ProfPair {
+    int kind;
+    cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfPair> g_prof_pending;
+std::vector<cudaEvent_t> g_prof_pool;
+double g_prof_ms[LCE_KERNEL_KINDS] = {};
+int64_t g_prof_n[LCE_KERNEL_KINDS] = {};
+
+cudaEvent_t prof_event() {
+    if (!g_prof_pool.empty()) {
+        cudaEvent_t e = g_prof_pool.back();
+        g_prof_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Records the start event of a launch of `kind`; returns the pair index or -1.
+int prof_begin(int kind, cudaStream_t s) {
+    if (!g_prof_on) return -1;
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    ProfPair p{kind, prof_event(), prof_event()};
+    if (!p.a || !p.b) return -1;
+    cudaEventRecord(p.a, s);
+    g_prof_pending.push_back(p);
+    return static_cast<int>(g_prof_pending.size()) - 1;
+}
+
+void prof_end(int idx, cudaStream_t s) {
+    if (idx < 0) return;
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    cudaEventRecord(g_prof_pending[idx].b, s);
+}
+
+#define LCE_LAUNCH_KIND(kind, stream, expr)                 \
+    do {                                                    \
+        const int _pi = prof_begin((kind), (stream));       \
+        if ((expr) != cudaSuccess) return LCE_ERR_CUDA;     \
+        prof_end(_pi, (stream));                            \
+        ++g_launches;                                       \
     } while (0)
+
+#define LCE_LAUNCH(expr) LCE_LAUNCH_KIND(LCE_KERNEL_OTHER, c.s, expr)
 
 lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
                  int64_t V, int64_t ign, int64_t chunk, void *ws, size_t ws_bytes,
@@ -197,7 +242,7 @@ lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, in
     p.lse = lse;
     p.dloss = dloss;
     const int grid = p.total_tiles < c.sms ? p.total_tiles : c.sms;
-    LCE_LAUNCH(launch_gemm(mode, p, grid, c.s));
+    LCE_LAUNCH_KIND(LCE_KERNEL_LOGITS, c.s, launch_gemm(mode, p, grid, c.s));
     return LCE_OK;
 }
 
@@ -222,7 +267,7 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     p.dW = dW;
     p.dw_accumulate = accumulate ? 1 : 0;
     const int grid = p.total_tiles < c.sms ? p.total_tiles : c.sms;
-    LCE_LAUNCH(launch_gemm(MODE_BWD, p, grid, c.s));
+    LCE_LAUNCH_KIND(LCE_KERNEL_GRAD, c.s, launch_gemm(MODE_BWD, p, grid, c.s));
     return LCE_OK;
 }
 
@@ -243,7 +288,7 @@ lce_status run_merge(const Ctx &c, bool fixup, long long row0, long long rows, f
     m.dloss = dloss;
     m.lse = lse;
     m.loss_rows = c.loss_rows;
-    LCE_LAUNCH(launch_merge(fixup, m, c.s));
+    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_merge(fixup, m, c.s));
     return LCE_OK;
 }
 
@@ -367,5 +412,37 @@ const char *lce_status_string(lce_status s) {
 int lce_version(void) { return 100; }
 
 int lce_last_launch_count(void) { return g_launches; }
+
+lce_status lce_profile_enable(int on) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof_on = on != 0;
+    return LCE_OK;
+}
+
+lce_status lce_profile_read(int kind, double *total_ms, int64_t *launches) {
+    if (kind < 0 || kind >= LCE_KERNEL_KINDS || !total_ms || !launches) return LCE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    for (ProfPair &p : g_prof_pending) {
+        if (cudaEventSynchronize(p.b) != cudaSuccess) return LCE_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess) return LCE_ERR_CUDA;
+        g_prof_ms[p.kind] += ms;
+        g_prof_n[p.kind] += 1;
+        g_prof_pool.push_back(p.a);
+        g_prof_pool.push_back(p.b);
+    }
+    g_prof_pending.clear();
+    *total_ms = g_prof_ms[kind];
+    *launches = g_prof_n[kind];
+    return LCE_OK;
+}
+
+void lce_profile_reset(void) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    for (int k = 0; k < LCE_KERNEL_KINDS; ++k) {
+        g_prof_ms[k] = 0.0;
+        g_prof_n[k] = 0;
+    }
+}
 
 }  // extern "C"
