@@ -128,6 +128,28 @@ lce_status lce_profile_enable(int on);
 lce_status lce_profile_read(int kind, double *total_ms, int64_t *launches);
 void lce_profile_reset(void);
 
+/* lce_forward for callers that cannot allocate device memory. The pages have no
+ * counterpart: this is a library convenience. Some callers have no allocator to
+ * hand (a plugin inside another runtime that owns all device memory), may not
+ * call cudaMalloc on their hot path (it synchronises the device), or run with a
+ * device-memory budget fixed at start-up; they cannot provide a workspace.
+ * This call takes the same arguments as lce_forward minus the workspace and
+ * uses a 64 MiB array built into the library instead (held on every GPU that
+ * loads the library until the process exits). It allocates nothing.
+ *  - Sizes whose lce_workspace_size() exceeds 64 MiB return LCE_ERR_WORKSPACE
+ *    before anything is enqueued; a smaller chunk may fit.
+ *  - The first call on a device looks up the array's device address (one
+ *    cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Every call shares the array, which keeps the last call's contents; each
+ *    call clears what must start at zero on its stream. Calls that overlap on
+ *    the GPU race on the array: order them on one stream.
+ *  - Device-side status (out-of-range labels) is recorded in the shared array
+ *    and is not reported by this call. */
+lce_status lce_forward_noalloc(const void *H, const void *W, const int64_t *y,
+                               int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                               int64_t chunk, float *loss, float *lse, lce_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
