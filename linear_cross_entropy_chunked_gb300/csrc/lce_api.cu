@@ -97,14 +97,17 @@ bool make_layout(long long N, long long D, long long V, long long chunk, Layout 
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 2-D bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
+// 2-D tensor map (bf16 unless fp32 is asked for), 128-byte swizzle, zero fill
+// out of bounds on loads, clipping on stores.
 bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
-               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+               bool fp32 = false) {
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_stride_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+    CUresult r = g_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          2, const_cast<void *>(base), dims,
                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -241,6 +244,9 @@ lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, in
     p.total_tiles = p.m_blocks0 * p.n_blocks0;
     p.lse = lse;
     p.dloss = dloss;
+    if (mode != MODE_LSE &&
+        !encode_2d(&p.tmS0, c.G, c.V, rows, 2ull * c.L.ldg, 64, 32))
+        return LCE_ERR_CUDA;
     const int grid = p.total_tiles < c.sms ? p.total_tiles : c.sms;
     LCE_LAUNCH_KIND(LCE_KERNEL_LOGITS, c.s, launch_gemm(mode, p, grid, c.s));
     return LCE_OK;
@@ -256,6 +262,9 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     p.tmB0 = c.tmW_MN;
     if (!encode_2d(&p.tmA1, c.G, c.V, rows, 2ull * c.L.ldg, 64, BK)) return LCE_ERR_CUDA;
     if (!encode_2d(&p.tmB1, Hc, c.D, rows, 2ull * c.D, 64, BK)) return LCE_ERR_CUDA;
+    __nv_bfloat16 *dHc = static_cast<__nv_bfloat16 *>(dH) + row0 * c.D;
+    if (!encode_2d(&p.tmS0, dHc, c.D, rows, 2ull * c.D, 64, 32)) return LCE_ERR_CUDA;
+    if (!encode_2d(&p.tmS1, dW, c.D, c.V, 4ull * c.D, 32, 32, true)) return LCE_ERR_CUDA;
     p.m_blocks0 = static_cast<int>(cdiv(rows, BM));
     p.n_blocks0 = static_cast<int>(cdiv(c.D, BN));
     p.k_blocks0 = static_cast<int>(cdiv(c.V, BK));

@@ -190,12 +190,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ void st_v4(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-
 constexpr float LOG2E = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- tiles
@@ -227,12 +221,73 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t) {
 }
 
 // ---------------------------------------------------------------- epilogues
-// Each thread owns one accumulator row (TMEM lane) and 128 columns.
+// Each epilogue thread owns one accumulator row (TMEM lane) and 128 columns; a
+// warp owns a 32-row x 128-column slab. Outputs leave through a per-warp 4 KB
+// staging buffer in shared memory, laid out as a 32 x 128-byte TMA box with the
+// 128-byte swizzle (16-byte chunk j of row r at position j ^ (r % 8), so the
+// warp's 16-byte shared stores are conflict-free), and one TMA bulk-tensor
+// store (or reduce-add) per box. The tensor maps clip rows and columns outside
+// the output, so the stores need no masks.
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until the previous bulk store of this thread no longer reads its source.
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, const void *src, int x,
+                                                  int y) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y)
+        : "memory");
+}
+
+// Row `lane` of the staging box receives 8 16-byte chunks (128 bytes).
+__device__ __forceinline__ void stage_row(uint8_t *stg, int lane, int j, uint32_t a, uint32_t b,
+                                          uint32_t c, uint32_t d) {
+    uint4 *dst = reinterpret_cast<uint4 *>(stg + lane * 128 + ((j ^ (lane & 7)) << 4));
+    *dst = make_uint4(a, b, c, d);
+}
+
+// Hand the staged box to the TMA unit (lane 0 issues), after every lane's
+// shared-memory writes are made visible to the async proxy.
+__device__ __forceinline__ void flush_box(const CUtensorMap *map, uint8_t *stg, int lane, int x,
+                                          int y, bool reduce) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (reduce) tma_reduce_add_2d(map, stg, x, y);
+        else tma_store_2d(map, stg, x, y);
+        bulk_commit();
+    }
+}
+
+// Before writing the staging buffer again: the previous box has been read.
+__device__ __forceinline__ void staging_acquire(int lane) {
+    if (lane == 0) bulk_wait_read0();
+    __syncwarp();
+}
 
 template <int MODE>
 __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile &tl,
-                                                uint32_t taddr, int row_in_tile, int half) {
-    const int r = tl.m0 + row_in_tile;          // row within the chunk
+                                                uint32_t taddr, int quarter, int lane, int half,
+                                                uint8_t *stg) {
+    const int r = tl.m0 + quarter * 32 + lane;  // row within the chunk
     const bool row_ok = r < p.rows;
     const int col0 = tl.n0 + half * 128;        // first vocabulary column of this thread
     const int ncols = min(128, p.V - col0);     // valid columns (may be <= 0)
@@ -240,6 +295,7 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
     if (row_ok) yv = p.y[p.row0 + r];
     const bool y_ok = row_ok && yv != p.ignore_index && yv >= 0 && yv < p.V;
     const int yl = y_ok ? static_cast<int>(yv - col0) : -1;   // local target column
+    const int box_y = tl.m0 + quarter * 32;
 
     if constexpr (MODE == MODE_G) {
         float scale = 0.f, lse2 = 0.f;
@@ -249,28 +305,27 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
             scale = (y_ok && nv > 0) ? dl / static_cast<float>(nv) : 0.f;
             lse2 = p.lse[p.row0 + r] * LOG2E;
         }
-        __nv_bfloat16 *grow = p.G + static_cast<size_t>(r) * p.ldg + col0;
+        if (ncols <= 0) return;  // whole half past V: nothing to store (warp-uniform)
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
             float v[32];
             tmem_ld32(taddr + c * 32, v);
-            if (row_ok && c * 32 < ncols) {
-                uint32_t w[16];
+            uint32_t w[16];
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const int cj = c * 32 + j;
-                    float g0 = (cj < ncols) ? ex2(fmaf(v[j], LOG2E, -lse2)) * scale : 0.f;
-                    float g1 = (cj + 1 < ncols) ? ex2(fmaf(v[j + 1], LOG2E, -lse2)) * scale : 0.f;
-                    if (cj == yl) g0 -= scale;
-                    if (cj + 1 == yl) g1 -= scale;
-                    w[j / 2] = pack_bf16x2(g0, g1);
-                }
-                uint32_t *dst = reinterpret_cast<uint32_t *>(grow + c * 32);
-                st_v4(dst, w[0], w[1], w[2], w[3]);
-                st_v4(dst + 4, w[4], w[5], w[6], w[7]);
-                st_v4(dst + 8, w[8], w[9], w[10], w[11]);
-                st_v4(dst + 12, w[12], w[13], w[14], w[15]);
+            for (int j = 0; j < 32; j += 2) {
+                const int cj = c * 32 + j;
+                float g0 = (cj < ncols) ? ex2(fmaf(v[j], LOG2E, -lse2)) * scale : 0.f;
+                float g1 = (cj + 1 < ncols) ? ex2(fmaf(v[j + 1], LOG2E, -lse2)) * scale : 0.f;
+                if (cj == yl) g0 -= scale;
+                if (cj + 1 == yl) g1 -= scale;
+                w[j / 2] = pack_bf16x2(g0, g1);
             }
+            if ((c & 1) == 0) staging_acquire(lane);
+            const int jb = (c & 1) * 4;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                stage_row(stg, lane, jb + q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            if (c & 1) flush_box(&p.tmS0, stg, lane, col0 + (c >> 1) * 64, box_y, false);
         }
     } else {
         // pass 1: slab max (and the target logit when it falls in this slab)
@@ -289,7 +344,6 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
         // pass 2: sum of exp(z - m); optionally store P' = exp(z - m) as bf16
         const float m2 = (ncols > 0) ? m * LOG2E : 0.f;
         float s = 0.f;
-        __nv_bfloat16 *grow = p.G + static_cast<size_t>(r) * p.ldg + col0;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
             float v[32];
@@ -302,16 +356,16 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
                 s += e[j];
             }
             if constexpr (MODE == MODE_LSE_P) {
-                if (row_ok && c * 32 < ncols) {
-                    uint32_t *dst = reinterpret_cast<uint32_t *>(grow + c * 32);
-                    st_v4(dst, pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                          pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
-                    st_v4(dst + 4, pack_bf16x2(e[8], e[9]), pack_bf16x2(e[10], e[11]),
-                          pack_bf16x2(e[12], e[13]), pack_bf16x2(e[14], e[15]));
-                    st_v4(dst + 8, pack_bf16x2(e[16], e[17]), pack_bf16x2(e[18], e[19]),
-                          pack_bf16x2(e[20], e[21]), pack_bf16x2(e[22], e[23]));
-                    st_v4(dst + 12, pack_bf16x2(e[24], e[25]), pack_bf16x2(e[26], e[27]),
-                          pack_bf16x2(e[28], e[29]), pack_bf16x2(e[30], e[31]));
+                if (ncols > 0) {  // warp-uniform
+                    if ((c & 1) == 0) staging_acquire(lane);
+                    const int jb = (c & 1) * 4;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        stage_row(stg, lane, jb + q, pack_bf16x2(e[8 * q], e[8 * q + 1]),
+                                  pack_bf16x2(e[8 * q + 2], e[8 * q + 3]),
+                                  pack_bf16x2(e[8 * q + 4], e[8 * q + 5]),
+                                  pack_bf16x2(e[8 * q + 6], e[8 * q + 7]));
+                    if (c & 1) flush_box(&p.tmS0, stg, lane, col0 + (c >> 1) * 64, box_y, false);
                 }
             }
         }
@@ -323,67 +377,41 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
 }
 
 __device__ __forceinline__ void epilogue_dH(const GemmParams &p, const Tile &tl, uint32_t taddr,
-                                            int row_in_tile, int half) {
-    const int r = tl.m0 + row_in_tile;
-    const bool row_ok = r < p.rows;
+                                            int quarter, int lane, int half, uint8_t *stg) {
     const int col0 = tl.n0 + half * 128;
-    __nv_bfloat16 *dst_row = p.dH + static_cast<size_t>(p.row0 + r) * p.D;
+    if (col0 >= p.D) return;  // warp-uniform: this half is past D
+    const int box_y = tl.m0 + quarter * 32;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
-        const int cb = col0 + c * 32;
-        if (!row_ok || cb >= p.D) continue;
-        if (cb + 32 <= p.D) {
-            uint32_t *dst = reinterpret_cast<uint32_t *>(dst_row + cb);
+        if ((c & 1) == 0) staging_acquire(lane);
+        const int jb = (c & 1) * 4;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                st_v4(dst + 4 * q, pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
+        for (int q = 0; q < 4; ++q)
+            stage_row(stg, lane, jb + q, pack_bf16x2(v[8 * q], v[8 * q + 1]),
                       pack_bf16x2(v[8 * q + 2], v[8 * q + 3]), pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
                       pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-        } else {
-            // ragged D tail (D % 8 == 0): 8 columns at a time
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (cb + 8 * q < p.D) {
-                    uint32_t *dst = reinterpret_cast<uint32_t *>(dst_row + cb + 8 * q);
-                    st_v4(dst, pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
-                          pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                          pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                          pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-                }
-            }
-        }
+        if (c & 1) flush_box(&p.tmS0, stg, lane, col0 + (c >> 1) * 64, box_y, false);
     }
 }
 
 __device__ __forceinline__ void epilogue_dW(const GemmParams &p, const Tile &tl, uint32_t taddr,
-                                            int row_in_tile, int half) {
-    const int vr = tl.m0 + row_in_tile;          // vocabulary row of dW
-    const bool row_ok = vr < p.V;
+                                            int quarter, int lane, int half, uint8_t *stg) {
     const int col0 = tl.n0 + half * 128;
-    float *dst_row = p.dW + static_cast<size_t>(vr) * p.D;
+    if (col0 >= p.D) return;  // warp-uniform
+    const int box_y = tl.m0 + quarter * 32;   // vocabulary row
+    const bool reduce = p.dw_accumulate != 0;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
-        const int cb = col0 + c * 32;
-        if (!row_ok || cb >= p.D) continue;
+        staging_acquire(lane);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (cb + 4 * q < p.D) {
-                float4 *dst = reinterpret_cast<float4 *>(dst_row + cb + 4 * q);
-                float4 o = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                if (p.dw_accumulate) {
-                    const float4 old = *dst;
-                    o.x += old.x;
-                    o.y += old.y;
-                    o.z += old.z;
-                    o.w += old.w;
-                }
-                *dst = o;
-            }
-        }
+        for (int q = 0; q < 8; ++q)
+            stage_row(stg, lane, q, __float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                      __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
+        flush_box(&p.tmS1, stg, lane, col0 + c * 32, box_y, reduce);
     }
 }
 
@@ -428,9 +456,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
     if (warp == PRODUCER_WARP && lane == 0) {
         prefetch_tmap(&p.tmA0);
         prefetch_tmap(&p.tmB0);
+        if (MODE != MODE_LSE) prefetch_tmap(&p.tmS0);
         if (MODE == MODE_BWD) {
             prefetch_tmap(&p.tmA1);
             prefetch_tmap(&p.tmB1);
+            prefetch_tmap(&p.tmS1);
         }
     }
     if (warp == MMA_WARP) {
@@ -566,7 +596,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
         // epilogue warps 0..7
         const int quarter = warp & 3;
         const int half = warp >> 2;
-        const int row_in_tile = quarter * 32 + lane;
+        uint8_t *stg = smem + STAGES * STAGE_BYTES + warp * STAGING_BYTES;
         int sq = 0;
         uint32_t sphase = 0;
         int acc = 0;
@@ -584,17 +614,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN + half * 128);
             if (MODE != MODE_BWD) {
-                epilogue_logits<MODE>(p, tl, taddr, row_in_tile, half);
+                epilogue_logits<MODE>(p, tl, taddr, quarter, lane, half, stg);
             } else if (tl.type == 0) {
-                epilogue_dH(p, tl, taddr, row_in_tile, half);
+                epilogue_dH(p, tl, taddr, quarter, lane, half, stg);
             } else {
-                epilogue_dW(p, tl, taddr, row_in_tile, half);
+                epilogue_dW(p, tl, taddr, quarter, lane, half, stg);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty_bar[acc]);
             if (++acc == 2) { acc = 0; aphase ^= 1; }
         }
+        // all bulk stores of this warp complete before the CTA exits
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();

@@ -21,7 +21,8 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BYTES = BN * BK * 2;             // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
-constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + 1 KB alignment slack
+constexpr int STAGING_BYTES = 4096;  // per epilogue warp: 32 rows x 128 B, TMA-store staging
+constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 8 * STAGING_BYTES + 1024;  // + 1 KB alignment
 constexpr int NUM_EPI_WARPS = 8;   // warps 0..7: TMEM lane quarter = warp % 4, column half = warp / 4
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
@@ -52,6 +53,8 @@ struct GemmParams {
     CUtensorMap tmB0;      //               logits B = W (K-major) | dH B = W (MN-major)
     CUtensorMap tmA1;      // type-1 tiles: dW A = G^T (MN-major)
     CUtensorMap tmB1;      //               dW B = H chunk (MN-major)
+    CUtensorMap tmS0;      // type-0 output store: P' / G chunk buffer (bf16) | dH chunk (bf16)
+    CUtensorMap tmS1;      // type-1 output store / reduce-add: dW (fp32)
     int m_blocks0, n_blocks0, k_blocks0;
     int m_blocks1, n_blocks1, k_blocks1;
     int total_tiles;
