@@ -68,7 +68,9 @@ struct Layout {
     long long nchunks = 0;
     int nparts = 0;          // 128-column slabs per row
     int ldg = 0;             // row stride of the chunk buffer (elements)
-    size_t off_loss_rows = 0, off_zy = 0, off_parts = 0, off_G = 0, total = 0;
+    int ldt = 0;             // row stride (elements) of G^T and H^T: chunk rows rounded up
+    size_t off_loss_rows = 0, off_zy = 0, off_parts = 0, off_G = 0, off_GT = 0, off_HT = 0,
+           total = 0;
     size_t hdr_bytes = 0;
 };
 
@@ -91,27 +93,56 @@ bool make_layout(long long N, long long D, long long V, long long chunk, Layout 
     off += align_up(sizeof(float2) * static_cast<size_t>(L.C) * L.nparts, 1024);
     L.off_G = off;
     off += align_up(2 * static_cast<size_t>(L.C) * L.ldg, 1024);
+    // G^T [V][ldt] and H chunk^T [D][ldt] make every dW operand K-major
+    L.ldt = static_cast<int>(align_up(static_cast<size_t>(L.C), 64));
+    L.off_GT = off;
+    off += align_up(2 * static_cast<size_t>(V) * L.ldt, 1024);
+    L.off_HT = off;
+    off += align_up(2 * static_cast<size_t>(D) * L.ldt, 1024);
     L.total = off;
     return true;
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 2-D tensor map (bf16 unless fp32 is asked for), 128-byte swizzle, zero fill
-// out of bounds on loads, clipping on stores.
-bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
-               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
-               bool fp32 = false) {
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {row_stride_bytes};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t es[2] = {1, 1};
+// Tensor map over a row-major array (bf16 unless fp32 is asked for) with the
+// 128-byte swizzle of the MMA operand tiles and of the epilogue staging boxes;
+// zero fill out of bounds on loads, clipping on stores.
+bool encode_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
+                const uint64_t *strides_bytes, const uint32_t *box, bool fp32) {
+    cuuint64_t d[3];
+    cuuint64_t st[2];
+    cuuint32_t bx[3];
+    cuuint32_t es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i) st[i] = strides_bytes[i];
     CUresult r = g_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                          2, const_cast<void *>(base), dims,
-                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          rank, const_cast<void *>(base), d, st, bx, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// MMA operand tile load map: 2-D bf16, box {box_inner, box_outer}.
+bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    const uint64_t dims[2] = {inner, outer};
+    const uint64_t st[1] = {row_stride_bytes};
+    const uint32_t box[2] = {box_inner, box_outer};
+    return encode_map(m, base, 2, dims, st, box, false);
+}
+
+// Epilogue store map: 2-D, box = 128 bytes x box_rows rows (128: a column half
+// of a gradient tile; 32: one warp's rows of a logits tile).
+bool encode_store_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                     uint64_t row_stride_bytes, bool fp32, uint32_t box_rows = 128) {
+    const uint64_t dims[2] = {inner, outer};
+    const uint64_t st[1] = {row_stride_bytes};
+    const uint32_t box[2] = {fp32 ? 32u : 64u, box_rows};
+    return encode_map(m, base, 2, dims, st, box, fp32);
 }
 
 struct Ctx {
@@ -124,6 +155,7 @@ struct Ctx {
     float *loss_rows, *zy;
     float2 *parts;
     __nv_bfloat16 *G;
+    __nv_bfloat16 *GT, *HT;
     int sms;
     cudaStream_t s;
     CUtensorMap tmH_K, tmW_K, tmW_MN;
@@ -205,6 +237,8 @@ lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t
     c.zy = reinterpret_cast<float *>(c.ws + c.L.off_zy);
     c.parts = reinterpret_cast<float2 *>(c.ws + c.L.off_parts);
     c.G = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_G);
+    c.GT = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_GT);
+    c.HT = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_HT);
     c.s = reinterpret_cast<cudaStream_t>(stream);
     if (!encode_2d(&c.tmW_K, W, D, V, D * 2, BK, BN)) return LCE_ERR_CUDA;
     if (!encode_2d(&c.tmW_MN, W, D, V, D * 2, 64, BK)) return LCE_ERR_CUDA;
@@ -244,8 +278,7 @@ lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, in
     p.total_tiles = p.m_blocks0 * p.n_blocks0;
     p.lse = lse;
     p.dloss = dloss;
-    if (mode != MODE_LSE &&
-        !encode_2d(&p.tmS0, c.G, c.V, rows, 2ull * c.L.ldg, 64, 32))
+    if (mode != MODE_LSE && !encode_store_2d(&p.tmS0, c.G, c.V, rows, 2ull * c.L.ldg, false, 32))
         return LCE_ERR_CUDA;
     const int grid = p.total_tiles < c.sms ? p.total_tiles : c.sms;
     LCE_LAUNCH_KIND(LCE_KERNEL_LOGITS, c.s, launch_gemm(mode, p, grid, c.s));
@@ -258,13 +291,23 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     memset(&p, 0, sizeof(p));
     base_params(c, p, row0, rows, slot);
     const __nv_bfloat16 *Hc = c.H + row0 * c.D;
+    // G^T and the H chunk^T for the K-major dW operands
+    TransposeParams tp;
+    memset(&tp, 0, sizeof(tp));
+    tp.src = Hc;
+    tp.ld_src = static_cast<int>(c.D);
+    tp.dst_t = c.HT;
+    tp.ld_t = c.L.ldt;
+    tp.rows = static_cast<int>(rows);
+    tp.cols = static_cast<int>(c.D);
+    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_transpose(false, tp, c.s));
     if (!encode_2d(&p.tmA0, c.G, c.V, rows, 2ull * c.L.ldg, BK, BM)) return LCE_ERR_CUDA;
     p.tmB0 = c.tmW_MN;
-    if (!encode_2d(&p.tmA1, c.G, c.V, rows, 2ull * c.L.ldg, 64, BK)) return LCE_ERR_CUDA;
-    if (!encode_2d(&p.tmB1, Hc, c.D, rows, 2ull * c.D, 64, BK)) return LCE_ERR_CUDA;
+    if (!encode_2d(&p.tmA1, c.GT, rows, c.V, 2ull * c.L.ldt, BK, BM)) return LCE_ERR_CUDA;
+    if (!encode_2d(&p.tmB1, c.HT, rows, c.D, 2ull * c.L.ldt, BK, BN)) return LCE_ERR_CUDA;
     __nv_bfloat16 *dHc = static_cast<__nv_bfloat16 *>(dH) + row0 * c.D;
-    if (!encode_2d(&p.tmS0, dHc, c.D, rows, 2ull * c.D, 64, 32)) return LCE_ERR_CUDA;
-    if (!encode_2d(&p.tmS1, dW, c.D, c.V, 4ull * c.D, 32, 32, true)) return LCE_ERR_CUDA;
+    if (!encode_store_2d(&p.tmS0, dHc, c.D, rows, 2ull * c.D, false)) return LCE_ERR_CUDA;
+    if (!encode_store_2d(&p.tmS1, dW, c.D, c.V, 4ull * c.D, true)) return LCE_ERR_CUDA;
     p.m_blocks0 = static_cast<int>(cdiv(rows, BM));
     p.n_blocks0 = static_cast<int>(cdiv(c.D, BN));
     p.k_blocks0 = static_cast<int>(cdiv(c.V, BK));
@@ -280,7 +323,7 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     return LCE_OK;
 }
 
-lce_status run_merge(const Ctx &c, bool fixup, long long row0, long long rows, float *lse,
+lce_status run_merge(const Ctx &c, bool fused, long long row0, long long rows, float *lse,
                      const float *dloss) {
     MergeParams m;
     m.parts = c.parts;
@@ -297,7 +340,29 @@ lce_status run_merge(const Ctx &c, bool fixup, long long row0, long long rows, f
     m.dloss = dloss;
     m.lse = lse;
     m.loss_rows = c.loss_rows;
-    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_merge(fixup, m, c.s));
+    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_merge(fused, m, c.s));
+    return LCE_OK;
+}
+
+// G^T from the chunk buffer; with fix-up, P' -> G in place first (fused path).
+lce_status run_g_transpose(const Ctx &c, bool fixup, long long row0, long long rows,
+                           const float *dloss) {
+    TransposeParams tp;
+    memset(&tp, 0, sizeof(tp));
+    tp.src = c.G;
+    tp.ld_src = c.L.ldg;
+    tp.dst_t = c.GT;
+    tp.ld_t = c.L.ldt;
+    tp.rows = static_cast<int>(rows);
+    tp.cols = static_cast<int>(c.V);
+    tp.parts = c.parts;
+    tp.nparts = c.L.nparts;
+    tp.y = c.y;
+    tp.row0 = static_cast<int>(row0);
+    tp.ignore_index = c.ign;
+    tp.hdr = c.hdr;
+    tp.dloss = dloss;
+    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_transpose(fixup, tp, c.s));
     return LCE_OK;
 }
 
@@ -356,6 +421,7 @@ lce_status lce_backward(const void *H, const void *W, const int64_t *y, const fl
         const long long row0 = k * c.L.C;
         const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
         LCE_TRY(run_logits(c, MODE_G, row0, rows, static_cast<int>(2 * k), lse, dloss));
+        LCE_TRY(run_g_transpose(c, false, row0, rows, dloss));
         LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dH, dW, k > 0));
     }
     return LCE_OK;
@@ -380,6 +446,7 @@ lce_status lce_fwd_bwd(const void *H, const void *W, const int64_t *y, const flo
         const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
         LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr));
         LCE_TRY(run_merge(c, true, row0, rows, lse, dloss));
+        LCE_TRY(run_g_transpose(c, true, row0, rows, dloss));
         LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dH, dW, k > 0));
     }
     LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss, c.s));

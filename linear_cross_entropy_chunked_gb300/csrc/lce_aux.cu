@@ -2,8 +2,10 @@
 //   * label scan: N_valid and the out-of-range check;
 //   * slab merge: per row, combine the (max, sumexp) partials of the 128-column
 //     slabs into lse_i = M + log sum_p s_p exp(m_p - M), write the row's loss
-//     lse_i - z_{i,y_i}, and (fused path) turn the stored P' = exp(z - m_p) into
-//     G = (P' exp(m_p - lse_i) - 1[j = y_i]) * dloss / N_valid in place
+//     lse_i - z_{i,y_i} and (fused path) each slab's factor exp(m_p - lse_i) * scale;
+//   * fix-up + transpose (fused path): turn the stored P' = exp(z - m_p) into
+//     G = (P' exp(m_p - lse_i) - 1[j = y_i]) * dloss / N_valid in place and
+//     write G^T; the same kernel transposes the H chunk for the dW contraction
 //     ("Unsloth Architecture: Manual Triton Backpropagation, Fused Cross-Entropy,
 //     and 80% VRAM Cut", pillar 1: the loss -z_{i,y_i} + log sum_j e^{z_ij} and
 //     the gradient p_ij - 1[j = y_i]);
@@ -73,14 +75,16 @@ __global__ void __launch_bounds__(1024) lce_label_scan_kernel(const long long *_
 
 constexpr int MERGE_THREADS = 256;
 
-template <bool FIXUP>
+// One CTA per chunk row: lse_i from the slab partials, the row's loss, and
+// (FACTORS) each slab's rescale factor exp(m_p - lse_i) * dloss / N_valid,
+// written over the slab max so the fix-up pass reads one float per slab.
+template <bool FACTORS>
 __global__ void __launch_bounds__(MERGE_THREADS) lce_merge_kernel(const MergeParams p) {
-    extern __shared__ float s_fac[];   // [nparts] (fixup only)
     __shared__ float s_red[MERGE_THREADS / 32];
     __shared__ float s_bcast;
     const int r = blockIdx.x;          // row within the chunk
     const int t = threadIdx.x, w = t >> 5, l = t & 31;
-    const float2 *parts = p.parts + static_cast<size_t>(r) * p.nparts;
+    float2 *parts = const_cast<float2 *>(p.parts) + static_cast<size_t>(r) * p.nparts;
 
     // row maximum over the slab maxima
     float m = -INFINITY;
@@ -121,34 +125,99 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_merge_kernel(const MergePar
         p.lse[grow] = lse;
         p.loss_rows[grow] = y_ok ? lse - p.zy[r] : 0.f;
     }
-    if constexpr (FIXUP) {
+    if constexpr (FACTORS) {
         const int nv = p.hdr[HDR_NVALID];
         const float dl = p.dloss ? *p.dloss : 1.f;
         const float scale = (y_ok && nv > 0) ? dl / static_cast<float>(nv) : 0.f;
         const float lse2 = lse * LOG2E_F;
         for (int i = t; i < p.nparts; i += MERGE_THREADS)
-            s_fac[i] = scale != 0.f ? exp2f(fmaf(parts[i].x, LOG2E_F, -lse2)) * scale : 0.f;
-        __syncthreads();
-        uint4 *row = reinterpret_cast<uint4 *>(p.G + static_cast<size_t>(r) * p.ldg);
-        const int nvec = (p.V + 7) >> 3;
-        const int ycol = y_ok ? static_cast<int>(yv) : -1;
-        for (int i = t; i < nvec; i += MERGE_THREADS) {
-            uint4 u = row[i];
-            const float f = s_fac[i >> 4];            // 16 vectors of 8 = one 128-column slab
-            uint32_t *wv = reinterpret_cast<uint32_t *>(&u);
+            parts[i].x = scale != 0.f ? exp2f(fmaf(parts[i].x, LOG2E_F, -lse2)) * scale : 0.f;
+    }
+}
+
+// ------------------------------------------------------------------ fix-up + transpose
+// 64 x 64 tiles. FIX: the tile of the chunk buffer holds P' = exp(z - m_p); it
+// becomes G = P' * factor_p - 1[j = y_i] * dloss / N_valid (rounded to bf16),
+// written back in place and, transposed, into G^T [V][ld_t]. Without FIX the
+// kernel is a plain transpose (the H chunk into H^T [D][ld_t]).
+
+constexpr int TT = 64;
+constexpr int TSTRIDE = 66;   // bf16 elements per staged row: conflict-free row writes, 2-way column reads
+
+template <bool FIX>
+__global__ void __launch_bounds__(256) lce_transpose_kernel(const TransposeParams p) {
+    __shared__ __align__(16) __nv_bfloat16 tile[TT * TSTRIDE];
+    const int c0 = blockIdx.x * TT;      // first column of the tile (vocabulary id or D index)
+    const int r0 = blockIdx.y * TT;      // first chunk row of the tile
+    const int tid = threadIdx.x;
+    float scale_r[2] = {0.f, 0.f}, fac_r[2] = {0.f, 0.f};
+    int ycol_r[2] = {-1, -1};
+    if constexpr (FIX) {
+        const int nv = p.hdr[HDR_NVALID];
+        const float dl = p.dloss ? *p.dloss : 1.f;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int r = r0 + (tid + 256 * i) / 8;
+            if (r < p.rows) {
+                const long long yv = p.y[p.row0 + r];
+                const bool y_ok = yv != p.ignore_index && yv >= 0 && yv < p.cols;
+                scale_r[i] = (y_ok && nv > 0) ? dl / static_cast<float>(nv) : 0.f;
+                ycol_r[i] = y_ok ? static_cast<int>(yv) : -1;
+                fac_r[i] = p.parts[static_cast<size_t>(r) * p.nparts + c0 / 128].x;
+            }
+        }
+    }
+    // load (and fix up) 8 elements per chunk, two chunks per thread
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int k = tid + 256 * i;
+        const int rr = k >> 3, cb = (k & 7) * 8;
+        const int r = r0 + rr, c = c0 + cb;
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (r < p.rows && c < p.cols) {
+            uint4 *src = reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(p.src) +
+                                                   static_cast<size_t>(r) * p.ld_src + c);
+            u = *src;
+            if constexpr (FIX) {
+                uint32_t *wv = reinterpret_cast<uint32_t *>(&u);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&wv[q]);
+                    float2 x = __bfloat1622float2(h);
+                    x.x *= fac_r[i];
+                    x.y *= fac_r[i];
+                    if (c + 2 * q == ycol_r[i]) x.x -= scale_r[i];
+                    if (c + 2 * q + 1 == ycol_r[i]) x.y -= scale_r[i];
+                    h = __floats2bfloat162_rn(x.x, x.y);
+                    wv[q] = *reinterpret_cast<uint32_t *>(&h);
+                }
+                *src = u;
+            }
+        }
+        uint32_t *dst = reinterpret_cast<uint32_t *>(tile + rr * TSTRIDE + cb);
+        dst[0] = u.x;
+        dst[1] = u.y;
+        dst[2] = u.z;
+        dst[3] = u.w;
+    }
+    __syncthreads();
+    // transposed write: output row = tile column, 8 chunk rows per 16-byte store
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int k = tid + 256 * i;
+        const int cc = k >> 3, rb = (k & 7) * 8;
+        const int c = c0 + cc, r = r0 + rb;
+        if (c < p.cols && r < p.rows) {
+            uint32_t w[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&wv[q]);
-                float2 x = __bfloat1622float2(h);
-                const int c = i * 8 + 2 * q;
-                x.x *= f;
-                x.y *= f;
-                if (c == ycol) x.x -= scale;
-                if (c + 1 == ycol) x.y -= scale;
-                h = __floats2bfloat162_rn(x.x, x.y);
-                wv[q] = *reinterpret_cast<uint32_t *>(&h);
+                const uint32_t lo = reinterpret_cast<const uint16_t &>(tile[(rb + 2 * q) * TSTRIDE + cc]);
+                const uint32_t hi =
+                    reinterpret_cast<const uint16_t &>(tile[(rb + 2 * q + 1) * TSTRIDE + cc]);
+                w[q] = lo | (hi << 16);
             }
-            row[i] = u;
+            *reinterpret_cast<uint4 *>(p.dst_t + static_cast<size_t>(c) * p.ld_t + r) =
+                make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
 }
@@ -186,21 +255,22 @@ cudaError_t launch_label_scan(const long long *y, long long N, long long V, long
     return cudaGetLastError();
 }
 
-cudaError_t launch_merge(bool fixup, const MergeParams &p, cudaStream_t s) {
+cudaError_t launch_merge(bool factors, const MergeParams &p, cudaStream_t s) {
     if (p.rows <= 0) return cudaSuccess;
-    if (fixup) {
-        const size_t smem = static_cast<size_t>(p.nparts) * sizeof(float);
-        lce_merge_kernel<true><<<p.rows, MERGE_THREADS, smem, s>>>(p);
-    } else {
-        lce_merge_kernel<false><<<p.rows, MERGE_THREADS, 0, s>>>(p);
-    }
+    if (factors) lce_merge_kernel<true><<<p.rows, MERGE_THREADS, 0, s>>>(p);
+    else lce_merge_kernel<false><<<p.rows, MERGE_THREADS, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t aux_set_attributes() {
-    return cudaFuncSetAttribute(lce_merge_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                MERGE_MAX_SMEM);
+cudaError_t launch_transpose(bool fix, const TransposeParams &p, cudaStream_t s) {
+    if (p.rows <= 0 || p.cols <= 0) return cudaSuccess;
+    const dim3 grid((p.cols + TT - 1) / TT, (p.rows + TT - 1) / TT);
+    if (fix) lce_transpose_kernel<true><<<grid, 256, 0, s>>>(p);
+    else lce_transpose_kernel<false><<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError();
 }
+
+cudaError_t aux_set_attributes() { return cudaSuccess; }
 
 cudaError_t launch_loss_finalize(const float *loss_rows, long long N, const int *hdr, float *loss,
                                  cudaStream_t s) {

@@ -195,24 +195,28 @@ constexpr float LOG2E = 1.4426950408889634f;
 // ---------------------------------------------------------------- tiles
 
 struct Tile {
-    int type;   // 0: logits or dH, 1: dW
+    int type;   // TILE_MAIN: logits tile or dH tile; TILE_DW: dW tile
     int m0, n0; // element offsets of the output tile
     int nk;     // k blocks
 };
+enum : int { TILE_MAIN = 0, TILE_DW = 1 };
 
+// Logits launches: m fastest, so the chunk's row blocks that share one W slab
+// run together. Gradient launches: the few long dH tiles first (m fastest),
+// then the many short dW tiles (n fastest, so the tiles that share one G^T slab
+// run together); the dynamic schedule lets the SMs left over by the dH tiles
+// start on dW at once.
 __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t) {
     Tile tl;
-    const int n0t = p.m_blocks0 * p.n_blocks0;
-    if (t < n0t) {
-        // m fastest: the chunk's row blocks that share one W slab run together
-        tl.type = 0;
+    const int nH = p.m_blocks0 * p.n_blocks0;
+    if (t < nH) {
+        tl.type = TILE_MAIN;
         tl.m0 = (t % p.m_blocks0) * BM;
         tl.n0 = (t / p.m_blocks0) * BN;
         tl.nk = p.k_blocks0;
     } else {
-        // dW: n (= D) fastest, so the tiles that share one G column slab run together
-        t -= n0t;
-        tl.type = 1;
+        t -= nH;
+        tl.type = TILE_DW;
         tl.n0 = (t % p.n_blocks1) * BN;
         tl.m0 = (t / p.n_blocks1) * BM;
         tl.nk = p.k_blocks1;
@@ -221,13 +225,16 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t) {
 }
 
 // ---------------------------------------------------------------- epilogues
-// Each epilogue thread owns one accumulator row (TMEM lane) and 128 columns; a
-// warp owns a 32-row x 128-column slab. Outputs leave through a per-warp 4 KB
-// staging buffer in shared memory, laid out as a 32 x 128-byte TMA box with the
-// 128-byte swizzle (16-byte chunk j of row r at position j ^ (r % 8), so the
-// warp's 16-byte shared stores are conflict-free), and one TMA bulk-tensor
-// store (or reduce-add) per box. The tensor maps clip rows and columns outside
-// the output, so the stores need no masks.
+// Each epilogue thread owns one accumulator row (TMEM lane) and 128 columns;
+// the 4 warps of a column half own a 128-row x 128-column slab. Outputs leave
+// through one 16 KB staging box per half in shared memory: 128 rows x 128 bytes
+// with the 128-byte swizzle (16-byte chunk j of row r at position j ^ (r % 8),
+// which makes the warps' 16-byte shared stores conflict-free). When the box is
+// full, one thread of the half issues a single TMA bulk-tensor store (or
+// reduce-add) for it. The tensor maps clip rows and columns outside the
+// output, so the stores need no masks. The 4 warps of a half meet at a named
+// barrier (id 1 + half, 128 threads) before writing the box (it has been read)
+// and before issuing it (all rows are in).
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -235,12 +242,27 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// Wait until the previous bulk store of this thread no longer reads its source.
 __device__ __forceinline__ void bulk_wait_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Barrier over `n` threads that also returns the AND of every thread's `ok`.
+__device__ __forceinline__ bool named_bar_and(int id, int n, bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred q, a;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred a, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, a;\n\t}\n"
+        : "=r"(r)
+        : "r"(ok ? 1u : 0u), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
 }
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -257,47 +279,93 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, const 
         : "memory");
 }
 
-// Row `lane` of the staging box receives 8 16-byte chunks (128 bytes).
-__device__ __forceinline__ void stage_row(uint8_t *stg, int lane, int j, uint32_t a, uint32_t b,
-                                          uint32_t c, uint32_t d) {
-    uint4 *dst = reinterpret_cast<uint4 *>(stg + lane * 128 + ((j ^ (lane & 7)) << 4));
-    *dst = make_uint4(a, b, c, d);
-}
+enum StoreKind : int { ST_STORE = 0, ST_REDUCE = 1 };
 
-// Hand the staged box to the TMA unit (lane 0 issues), after every lane's
-// shared-memory writes are made visible to the async proxy.
-__device__ __forceinline__ void flush_box(const CUtensorMap *map, uint8_t *stg, int lane, int x,
-                                          int y, bool reduce) {
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-        if (reduce) tma_reduce_add_2d(map, stg, x, y);
-        else tma_store_2d(map, stg, x, y);
-        bulk_commit();
+struct HalfStager {
+    uint8_t *buf;   // 16 KB, 1 KB aligned
+    int bar_id;     // 1 + half
+    int row;        // 0..127 = quarter * 32 + lane
+    bool leader;    // quarter 0, lane 0: issues the stores
+
+    // The box may be written: its previous store has read it.
+    __device__ __forceinline__ void acquire() const {
+        if (leader) bulk_wait_read0();
+        named_bar_sync(bar_id, 128);
     }
-}
+    __device__ __forceinline__ void put(int j, uint32_t a, uint32_t b, uint32_t c,
+                                        uint32_t d) const {
+        *reinterpret_cast<uint4 *>(buf + row * 128 + ((j ^ (row & 7)) << 4)) = make_uint4(a, b, c, d);
+    }
+    // 32 fp32 values fill the whole 128-byte row.
+    __device__ __forceinline__ void put_f32(const float *v) const {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            put(j, __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+    }
+    // 32 values as bf16 fill half of the row: chunks jb .. jb + 3.
+    __device__ __forceinline__ void put_bf16(int jb, const float *v) const {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            put(jb + q, pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    }
+    __device__ __forceinline__ void issue(const CUtensorMap *map, int kind, int x, int y) const {
+        fence_proxy_async_smem();
+        named_bar_sync(bar_id, 128);
+        if (leader) {
+            if (kind == ST_REDUCE) tma_reduce_add_2d(map, buf, x, y);
+            else tma_store_2d(map, buf, x, y);
+            bulk_commit();
+        }
+    }
+};
 
-// Before writing the staging buffer again: the previous box has been read.
-__device__ __forceinline__ void staging_acquire(int lane) {
-    if (lane == 0) bulk_wait_read0();
-    __syncwarp();
-}
+// Logits epilogues stage per warp instead: a 4 KB box of 32 rows x 128 bytes
+// per warp (same swizzle), issued by the warp's lane 0 with no cross-warp
+// barrier. The logits epilogue does more arithmetic between stores, and the
+// per-warp boxes keep the warps independent.
+struct WarpStager {
+    uint8_t *buf;   // 4 KB, 1 KB aligned
+    int lane;
+    __device__ __forceinline__ void acquire() const {
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+    }
+    __device__ __forceinline__ void put_bf16(int jb, const float *v) const {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4 *>(buf + lane * 128 + (((jb + q) ^ (lane & 7)) << 4)) =
+                make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                           pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    }
+    __device__ __forceinline__ void issue(const CUtensorMap *map, int x, int y) const {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(map, buf, x, y);
+            bulk_commit();
+        }
+    }
+};
 
 template <int MODE>
 __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile &tl,
-                                                uint32_t taddr, int quarter, int lane, int half,
-                                                uint8_t *stg) {
-    const int r = tl.m0 + quarter * 32 + lane;  // row within the chunk
+                                                uint32_t taddr, int quarter, int half,
+                                                const WarpStager &st) {
+    const int r = tl.m0 + quarter * 32 + st.lane;  // row within the chunk
+    const int box_y = tl.m0 + quarter * 32;
     const bool row_ok = r < p.rows;
-    const int col0 = tl.n0 + half * 128;        // first vocabulary column of this thread
-    const int ncols = min(128, p.V - col0);     // valid columns (may be <= 0)
+    const int col0 = tl.n0 + half * 128;        // first vocabulary column of this half
+    const int ncols = min(128, p.V - col0);     // valid columns (may be <= 0); same for the half
     long long yv = p.ignore_index;
     if (row_ok) yv = p.y[p.row0 + r];
     const bool y_ok = row_ok && yv != p.ignore_index && yv >= 0 && yv < p.V;
     const int yl = y_ok ? static_cast<int>(yv - col0) : -1;   // local target column
-    const int box_y = tl.m0 + quarter * 32;
 
     if constexpr (MODE == MODE_G) {
+        if (ncols <= 0) return;
         float scale = 0.f, lse2 = 0.f;
         if (row_ok) {
             const int nv = p.hdr[HDR_NVALID];
@@ -305,27 +373,22 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
             scale = (y_ok && nv > 0) ? dl / static_cast<float>(nv) : 0.f;
             lse2 = p.lse[p.row0 + r] * LOG2E;
         }
-        if (ncols <= 0) return;  // whole half past V: nothing to store (warp-uniform)
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
+            const bool box_ok = (c >> 1) * 64 < ncols;
             float v[32];
             tmem_ld32(taddr + c * 32, v);
-            uint32_t w[16];
+            if (!box_ok) continue;
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
+            for (int j = 0; j < 32; ++j) {
                 const int cj = c * 32 + j;
-                float g0 = (cj < ncols) ? ex2(fmaf(v[j], LOG2E, -lse2)) * scale : 0.f;
-                float g1 = (cj + 1 < ncols) ? ex2(fmaf(v[j + 1], LOG2E, -lse2)) * scale : 0.f;
-                if (cj == yl) g0 -= scale;
-                if (cj + 1 == yl) g1 -= scale;
-                w[j / 2] = pack_bf16x2(g0, g1);
+                float g = (cj < ncols) ? ex2(fmaf(v[j], LOG2E, -lse2)) * scale : 0.f;
+                if (cj == yl) g -= scale;
+                v[j] = g;
             }
-            if ((c & 1) == 0) staging_acquire(lane);
-            const int jb = (c & 1) * 4;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                stage_row(stg, lane, jb + q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-            if (c & 1) flush_box(&p.tmS0, stg, lane, col0 + (c >> 1) * 64, box_y, false);
+            if ((c & 1) == 0) st.acquire();
+            st.put_bf16((c & 1) * 4, v);
+            if (c & 1) st.issue(&p.tmS0, col0 + (c >> 1) * 64, box_y);
         }
     } else {
         // pass 1: slab max (and the target logit when it falls in this slab)
@@ -348,24 +411,17 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
         for (int c = 0; c < 4; ++c) {
             float v[32];
             tmem_ld32(taddr + c * 32, v);
-            float e[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int cj = c * 32 + j;
-                e[j] = (cj < ncols) ? ex2(fmaf(v[j], LOG2E, -m2)) : 0.f;
-                s += e[j];
+                v[j] = (cj < ncols) ? ex2(fmaf(v[j], LOG2E, -m2)) : 0.f;
+                s += v[j];
             }
             if constexpr (MODE == MODE_LSE_P) {
-                if (ncols > 0) {  // warp-uniform
-                    if ((c & 1) == 0) staging_acquire(lane);
-                    const int jb = (c & 1) * 4;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        stage_row(stg, lane, jb + q, pack_bf16x2(e[8 * q], e[8 * q + 1]),
-                                  pack_bf16x2(e[8 * q + 2], e[8 * q + 3]),
-                                  pack_bf16x2(e[8 * q + 4], e[8 * q + 5]),
-                                  pack_bf16x2(e[8 * q + 6], e[8 * q + 7]));
-                    if (c & 1) flush_box(&p.tmS0, stg, lane, col0 + (c >> 1) * 64, box_y, false);
+                if ((c >> 1) * 64 < ncols) {
+                    if ((c & 1) == 0) st.acquire();
+                    st.put_bf16((c & 1) * 4, v);
+                    if (c & 1) st.issue(&p.tmS0, col0 + (c >> 1) * 64, box_y);
                 }
             }
         }
@@ -376,42 +432,27 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
     }
 }
 
-__device__ __forceinline__ void epilogue_dH(const GemmParams &p, const Tile &tl, uint32_t taddr,
-                                            int quarter, int lane, int half, uint8_t *stg) {
+// Gradient tiles: dH (bf16) or dW (fp32, stored for the first chunk,
+// reduce-added into dW afterwards).
+__device__ __forceinline__ void epilogue_grad(const GemmParams &p, const Tile &tl, uint32_t taddr,
+                                              int half, const HalfStager &st) {
     const int col0 = tl.n0 + half * 128;
-    if (col0 >= p.D) return;  // warp-uniform: this half is past D
-    const int box_y = tl.m0 + quarter * 32;
+    if (col0 >= p.D) return;  // this half is past D (same for the 4 warps)
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
-        if ((c & 1) == 0) staging_acquire(lane);
-        const int jb = (c & 1) * 4;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            stage_row(stg, lane, jb + q, pack_bf16x2(v[8 * q], v[8 * q + 1]),
-                      pack_bf16x2(v[8 * q + 2], v[8 * q + 3]), pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                      pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-        if (c & 1) flush_box(&p.tmS0, stg, lane, col0 + (c >> 1) * 64, box_y, false);
-    }
-}
-
-__device__ __forceinline__ void epilogue_dW(const GemmParams &p, const Tile &tl, uint32_t taddr,
-                                            int quarter, int lane, int half, uint8_t *stg) {
-    const int col0 = tl.n0 + half * 128;
-    if (col0 >= p.D) return;  // warp-uniform
-    const int box_y = tl.m0 + quarter * 32;   // vocabulary row
-    const bool reduce = p.dw_accumulate != 0;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(taddr + c * 32, v);
-        staging_acquire(lane);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            stage_row(stg, lane, q, __float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
-                      __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
-        flush_box(&p.tmS1, stg, lane, col0 + c * 32, box_y, reduce);
+        if (tl.type == TILE_MAIN) {
+            if (col0 + (c >> 1) * 64 >= p.D) continue;
+            if ((c & 1) == 0) st.acquire();
+            st.put_bf16((c & 1) * 4, v);
+            if (c & 1) st.issue(&p.tmS0, ST_STORE, col0 + (c >> 1) * 64, tl.m0);
+        } else {
+            if (col0 + c * 32 >= p.D) continue;
+            st.acquire();
+            st.put_f32(v);
+            st.issue(&p.tmS1, p.dw_accumulate ? ST_REDUCE : ST_STORE, col0 + c * 32, tl.m0);
+        }
     }
 }
 
@@ -508,20 +549,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                     if (MODE != MODE_BWD) {
                         tma_load_2d(sA, &p.tmA0, fb, kx, p.row0 + tl.m0);
                         tma_load_2d(sB, &p.tmB0, fb, kx, tl.n0);
-                    } else if (tl.type == 0) {
+                    } else if (tl.type != TILE_DW) {
                         // dH: A = G rows (K-major), B = W (MN-major, 4 blocks of 64 D-columns)
                         tma_load_2d(sA, &p.tmA0, fb, kx, tl.m0);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             tma_load_2d(sB + j * 8192, &p.tmB0, fb, tl.n0 + 64 * j, kx);
                     } else {
-                        // dW: A = G^T (MN-major, 2 blocks of 64 vocab columns), B = H chunk (MN-major)
-#pragma unroll
-                        for (int j = 0; j < 2; ++j)
-                            tma_load_2d(sA + j * 8192, &p.tmA1, fb, tl.m0 + 64 * j, kx);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            tma_load_2d(sB + j * 8192, &p.tmB1, fb, tl.n0 + 64 * j, kx);
+                        // dW: A = G^T rows (K-major), B = H chunk^T rows (K-major)
+                        tma_load_2d(sA, &p.tmA1, fb, kx, tl.m0);
+                        tma_load_2d(sB, &p.tmB1, fb, kx, tl.n0);
                     }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -557,11 +594,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 // operand layouts of this tile type
-                bool a_mn = false, b_mn = false;
-                if (MODE == MODE_BWD) {
-                    b_mn = true;
-                    a_mn = (tl.type == 1);
-                }
+                // only the dH tiles read an MN-major operand (W, for B)
+                const bool a_mn = false;
+                const bool b_mn = (MODE == MODE_BWD) && tl.type != TILE_DW;
                 const uint32_t idesc = idesc_bf16(BM, BN, a_mn, b_mn);
                 const uint32_t a_lbo = a_mn ? 8192u : 16u, b_lbo = b_mn ? 8192u : 16u;
                 const uint32_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);
@@ -593,39 +628,47 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
             }
         }
     } else {
-        // epilogue warps 0..7
+        // epilogue warps 0..7; the 4 warps of a half take every decision together
+        // (barrier votes), so an abort never leaves one of them at a named barrier.
         const int quarter = warp & 3;
         const int half = warp >> 2;
-        uint8_t *stg = smem + STAGES * STAGE_BYTES + warp * STAGING_BYTES;
+        HalfStager st;
+        st.buf = smem + STAGES * STAGE_BYTES + half * STAGING_BYTES;
+        st.bar_id = 1 + half;
+        st.row = quarter * 32 + lane;
+        st.leader = (quarter == 0 && lane == 0);
+        WarpStager wst;
+        wst.buf = smem + STAGES * STAGE_BYTES + warp * (2 * STAGING_BYTES / NUM_EPI_WARPS);
+        wst.lane = lane;
         int sq = 0;
         uint32_t sphase = 0;
         int acc = 0;
         uint32_t aphase = 0;
         while (true) {
-            if (!mbar_wait(&sfull_bar[sq], sphase, ab)) break;
+            bool ok = mbar_wait(&sfull_bar[sq], sphase, ab);
+            if (!named_bar_and(st.bar_id, 128, ok)) break;
             const int t = sched_tile[sq];
             __syncwarp();
             if (lane == 0) mbar_arrive(&sempty_bar[sq]);
             if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
             if (t < 0) break;
             const Tile tl = decode_tile(p, t);
-            if (!mbar_wait(&tfull_bar[acc], aphase, ab)) break;
+            ok = mbar_wait(&tfull_bar[acc], aphase, ab);
+            if (!named_bar_and(st.bar_id, 128, ok)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN + half * 128);
             if (MODE != MODE_BWD) {
-                epilogue_logits<MODE>(p, tl, taddr, quarter, lane, half, stg);
-            } else if (tl.type == 0) {
-                epilogue_dH(p, tl, taddr, quarter, lane, half, stg);
+                epilogue_logits<MODE>(p, tl, taddr, quarter, half, wst);
             } else {
-                epilogue_dW(p, tl, taddr, quarter, lane, half, stg);
+                epilogue_grad(p, tl, taddr, half, st);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty_bar[acc]);
             if (++acc == 2) { acc = 0; aphase ^= 1; }
         }
-        // all bulk stores of this warp complete before the CTA exits
+        // all bulk stores issued by this warp / half complete before the CTA exits
         if (lane == 0) bulk_wait_all();
         __syncwarp();
     }

@@ -21,8 +21,8 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BYTES = BN * BK * 2;             // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
-constexpr int STAGING_BYTES = 4096;  // per epilogue warp: 32 rows x 128 B, TMA-store staging
-constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 8 * STAGING_BYTES + 1024;  // + 1 KB alignment
+constexpr int STAGING_BYTES = 16384;  // per epilogue column half: one 128-row x 128-byte store box
+constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 2 * STAGING_BYTES + 1024;  // + 1 KB alignment
 constexpr int NUM_EPI_WARPS = 8;   // warps 0..7: TMEM lane quarter = warp % 4, column half = warp / 4
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
@@ -49,14 +49,14 @@ constexpr int FLAG_LABEL = 1;
 constexpr int FLAG_TIMEOUT = 2;
 
 struct GemmParams {
-    CUtensorMap tmA0;      // type-0 tiles: logits A = H (K-major) | dH A = G (K-major)
-    CUtensorMap tmB0;      //               logits B = W (K-major) | dH B = W (MN-major)
-    CUtensorMap tmA1;      // type-1 tiles: dW A = G^T (MN-major)
-    CUtensorMap tmB1;      //               dW B = H chunk (MN-major)
-    CUtensorMap tmS0;      // type-0 output store: P' / G chunk buffer (bf16) | dH chunk (bf16)
-    CUtensorMap tmS1;      // type-1 output store / reduce-add: dW (fp32)
+    CUtensorMap tmA0;      // logits A = H (K-major) | dH A = G (K-major)
+    CUtensorMap tmB0;      // logits B = W (K-major) | dH B = W (MN-major)
+    CUtensorMap tmA1;      // dW A = G^T [V][C] (K-major)
+    CUtensorMap tmB1;      // dW B = H chunk^T [D][C] (K-major)
+    CUtensorMap tmS0;      // output store: P' / G chunk buffer (bf16) | dH chunk (bf16)
+    CUtensorMap tmS1;      // dW output store / reduce-add (fp32)
     int m_blocks0, n_blocks0, k_blocks0;
-    int m_blocks1, n_blocks1, k_blocks1;
+    int m_blocks1, n_blocks1, k_blocks1;   // dW tiles (0 in logits launches)
     int total_tiles;
     int rows;              // rows in this chunk
     int row0;              // first global row of this chunk
@@ -81,7 +81,7 @@ struct GemmParams {
 };
 
 struct MergeParams {
-    const float2 *parts;
+    const float2 *parts;   // written in place (slab factors) by the FACTORS variant
     int nparts;
     const float *zy;
     __nv_bfloat16 *G;
@@ -95,18 +95,34 @@ struct MergeParams {
     float *loss_rows;      // global [N]
 };
 
+struct TransposeParams {
+    const __nv_bfloat16 *src;   // [rows][ld_src]; fixed up in place when FIX
+    int ld_src;
+    __nv_bfloat16 *dst_t;       // [cols][ld_t]
+    int ld_t;
+    int rows, cols;             // chunk rows; V (G) or D (H)
+    // fix-up only
+    const float2 *parts;        // .x = slab factor
+    int nparts;
+    const long long *y;
+    int row0;
+    long long ignore_index;
+    const int *hdr;
+    const float *dloss;
+};
+
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_gemm(int mode, const GemmParams &p, int grid, cudaStream_t s);
 cudaError_t launch_label_scan(const long long *y, long long N, long long V, long long ign,
                               int *hdr, cudaStream_t s);
-cudaError_t launch_merge(bool fixup, const MergeParams &p, cudaStream_t s);
+cudaError_t launch_merge(bool factors, const MergeParams &p, cudaStream_t s);
+cudaError_t launch_transpose(bool fix, const TransposeParams &p, cudaStream_t s);
 cudaError_t launch_loss_finalize(const float *loss_rows, long long N, const int *hdr,
                                  float *loss, cudaStream_t s);
 cudaError_t gemm_set_attributes();
 cudaError_t aux_set_attributes();
 
-// The merge kernel keeps one float per 128-column slab in shared memory.
-constexpr int MERGE_MAX_SMEM = 200 * 1024;
-constexpr long long MAX_V = static_cast<long long>(MERGE_MAX_SMEM / 4) * PART_COLS;
+// Largest vocabulary: keeps every TMA coordinate and tile index in int32.
+constexpr long long MAX_V = 1ll << 30;
 
 }  // namespace lce

@@ -41,7 +41,7 @@ def test_forward_noalloc_matches_forward():
     import linear_cross_entropy_chunked_gb300 as lce
     lce.build()
     f = _noalloc_fn(lce.lib())
-    N, D, V, chunk = 2048, 1024, 32000, 512
+    N, D, V, chunk = 2048, 1024, 32000, 256
     # two calls in a row, on different inputs, each against lce_forward
     for seed in (31, 32):
         H, W, y = make_inputs(N, D, V, seed=seed, n_ignored=40)
