@@ -50,6 +50,22 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """Slowest rank's time: all-reduce(MAX) when more than one rank runs."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_ms / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -143,10 +159,12 @@ def prepare_oracle_inputs(wl):
 
 
 def calibrate_rows(wl, H64, W64, y, target_s: float) -> int:
-    rows = 32
+    """Rows of the workload the oracle processes in about target_s seconds (the
+    cost is linear in rows; the pilot is large enough for BLAS to be efficient)."""
+    rows = min(wl.N, 128)
     t = oracle_sample_rate(wl, rows, H64, W64, y)
     want = int(rows * target_s / max(t, 1e-3))
-    return max(32, min(wl.N, want))
+    return max(16, min(wl.N, want))
 
 
 def run_reference(args, wl, chunk):
@@ -260,13 +278,10 @@ def run_ours(args, wl, chunk):
     st = lce.read_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {st} after timed steps")
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = t.item()
+    total_ms = max_over_ranks(total_ms, world, dev)
 
     ms_per_step = total_ms / args.steps
-    tokens_per_s = world * N * args.steps / (total_ms / 1e3)
+    tokens_per_s = job_tokens_per_s(world, N, args.steps, total_ms)
     flops_step = 6.0 * N * D * V
     tflops = flops_step / (ms_per_step / 1e3) / 1e12
     peak_burst = peaks.get("bf16_tflops", 1900.0)
@@ -396,7 +411,7 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world):
 
 def cpu_baseline(wl):
     H64, W64, y = prepare_oracle_inputs(wl)
-    rows = calibrate_rows(wl, H64, W64, y, target_s=12.0)
+    rows = calibrate_rows(wl, H64, W64, y, target_s=20.0)
     t = oracle_sample_rate(wl, rows, H64, W64, y)
     return {"value": rows / t, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
             "sample": f"first {rows} of {wl.N} tokens of the workload (fp64 numpy forward+"

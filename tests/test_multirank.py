@@ -1,0 +1,57 @@
+"""The multi-rank path of bench.py on CPU: world_size 2 over gloo (127.0.0.1).
+Every rank runs an independent replica; rank 0 reports the slowest rank's time
+and all ranks' tokens. The reference arm runs on rank 0 only."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    ms = 100.0 + 50.0 * rank          # rank 1 is the slower replica
+    worst = bench.max_over_ranks(ms, world, "cpu")
+    out[rank] = (worst, bench.job_tokens_per_s(world, 16384, 10, worst), bench.dist_env())
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_reduction_over_gloo():
+    world, port = 2, _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
+    for r in range(world):
+        worst, tps, env = out[r]
+        assert worst == 150.0
+        assert tps == pytest.approx(2 * 16384 * 10 / 0.150)
+        assert env == (r, world, r)
+
+
+def test_single_rank_needs_no_process_group():
+    import bench
+    assert bench.max_over_ranks(42.0, 1, "cpu") == 42.0
+    assert bench.job_tokens_per_s(1, 1000, 4, 2000.0) == pytest.approx(2000.0)
+
+
+def test_reference_arm_is_rank0_only(monkeypatch, capsys):
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    args = type("A", (), dict(gpus=2, steps=1, warmup=0))()
+    bench.run_reference(args, None, 1024)   # returns at once on rank 1, prints nothing
+    assert capsys.readouterr().out == ""
