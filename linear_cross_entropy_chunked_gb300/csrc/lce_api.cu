@@ -10,6 +10,7 @@
 // one bf16 [chunk, V] buffer that holds exp(z - slab max), then G.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -29,8 +30,17 @@ std::mutex g_mu;
 constexpr int kMaxDevices = 64;
 bool g_dev_ready[kMaxDevices] = {};
 int g_dev_sms[kMaxDevices] = {};
+int g_dev_pairs[kMaxDevices] = {};   // co-resident CTA pairs of the GEMM kernel (0: no pairs)
 
-lce_status init_device(int *sms) {
+// GEMM tiles run on CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles) when the
+// device can co-schedule them; LCE_GEMM_CLUSTER=1 selects one CTA per 128 x 256
+// tile instead (same work and results; measured ~8 % slower on the Llama-3 head).
+int cluster_choice() {
+    const char *e = getenv("LCE_GEMM_CLUSTER");
+    return (e && e[0] == '1') ? 1 : 2;
+}
+
+lce_status init_device(int *sms, int *pairs) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return LCE_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return LCE_ERR_UNSUPPORTED;
@@ -53,10 +63,17 @@ lce_status init_device(int *sms) {
         if (major != 10 || minor != 3) return LCE_ERR_UNSUPPORTED;
         if (gemm_set_attributes() != cudaSuccess) return LCE_ERR_CUDA;
         if (aux_set_attributes() != cudaSuccess) return LCE_ERR_CUDA;
+        int np = 0;
+        if (gemm_max_pairs(&np) != cudaSuccess) {
+            cudaGetLastError();
+            np = 0;
+        }
         g_dev_sms[dev] = n;
+        g_dev_pairs[dev] = np;
         g_dev_ready[dev] = true;
     }
     *sms = g_dev_sms[dev];
+    *pairs = cluster_choice() == 2 ? g_dev_pairs[dev] : 0;
     return LCE_OK;
 }
 
@@ -157,6 +174,7 @@ struct Ctx {
     __nv_bfloat16 *G;
     __nv_bfloat16 *GT, *HT;
     int sms;
+    int pairs;   // > 0: GEMMs run as CTA pairs (cluster of 2), at most this many at once
     cudaStream_t s;
     CUtensorMap tmH_K, tmW_K, tmW_MN;
 };
@@ -222,7 +240,7 @@ lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t
     if (!aligned16(ws) || !aligned16(W) || (H && !aligned16(H)) || (y && !aligned16(y)))
         return LCE_ERR_ALIGNMENT;
     if (ws_bytes < c.L.total) return LCE_ERR_WORKSPACE;
-    lce_status st = init_device(&c.sms);
+    lce_status st = init_device(&c.sms, &c.pairs);
     if (st != LCE_OK) return st;
     c.H = static_cast<const __nv_bfloat16 *>(H);
     c.W = static_cast<const __nv_bfloat16 *>(W);
@@ -240,7 +258,8 @@ lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t
     c.GT = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_GT);
     c.HT = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_HT);
     c.s = reinterpret_cast<cudaStream_t>(stream);
-    if (!encode_2d(&c.tmW_K, W, D, V, D * 2, BK, BN)) return LCE_ERR_CUDA;
+    // with CTA pairs each CTA loads half of a 256-row W tile (multicast to both)
+    if (!encode_2d(&c.tmW_K, W, D, V, D * 2, BK, c.pairs > 0 ? BN / 2 : BN)) return LCE_ERR_CUDA;
     if (!encode_2d(&c.tmW_MN, W, D, V, D * 2, 64, BK)) return LCE_ERR_CUDA;
     if (N > 0 && !encode_2d(&c.tmH_K, H, D, N, D * 2, BK, BM)) return LCE_ERR_CUDA;
     if (cudaMemsetAsync(c.ws, 0, c.L.hdr_bytes, c.s) != cudaSuccess) return LCE_ERR_CUDA;
@@ -275,13 +294,15 @@ lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, in
     p.m_blocks0 = static_cast<int>(cdiv(rows, BM));
     p.n_blocks0 = static_cast<int>(cdiv(c.V, BN));
     p.k_blocks0 = static_cast<int>(cdiv(c.D, BK));
-    p.total_tiles = p.m_blocks0 * p.n_blocks0;
+    const int cl = c.pairs > 0 ? 2 : 1;
+    p.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * p.n_blocks0;
     p.lse = lse;
     p.dloss = dloss;
     if (mode != MODE_LSE && !encode_store_2d(&p.tmS0, c.G, c.V, rows, 2ull * c.L.ldg, false, 32))
         return LCE_ERR_CUDA;
-    const int grid = p.total_tiles < c.sms ? p.total_tiles : c.sms;
-    LCE_LAUNCH_KIND(LCE_KERNEL_LOGITS, c.s, launch_gemm(mode, p, grid, c.s));
+    const int units = cl == 2 ? c.pairs : c.sms;
+    const int grid = cl * (p.total_tiles < units ? p.total_tiles : units);
+    LCE_LAUNCH_KIND(LCE_KERNEL_LOGITS, c.s, launch_gemm(mode, cl, p, grid, c.s));
     return LCE_OK;
 }
 
@@ -304,7 +325,8 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     if (!encode_2d(&p.tmA0, c.G, c.V, rows, 2ull * c.L.ldg, BK, BM)) return LCE_ERR_CUDA;
     p.tmB0 = c.tmW_MN;
     if (!encode_2d(&p.tmA1, c.GT, rows, c.V, 2ull * c.L.ldt, BK, BM)) return LCE_ERR_CUDA;
-    if (!encode_2d(&p.tmB1, c.HT, rows, c.D, 2ull * c.L.ldt, BK, BN)) return LCE_ERR_CUDA;
+    const int cl = c.pairs > 0 ? 2 : 1;
+    if (!encode_2d(&p.tmB1, c.HT, rows, c.D, 2ull * c.L.ldt, BK, BN / cl)) return LCE_ERR_CUDA;
     __nv_bfloat16 *dHc = static_cast<__nv_bfloat16 *>(dH) + row0 * c.D;
     if (!encode_store_2d(&p.tmS0, dHc, c.D, rows, 2ull * c.D, false)) return LCE_ERR_CUDA;
     if (!encode_store_2d(&p.tmS1, dW, c.D, c.V, 4ull * c.D, true)) return LCE_ERR_CUDA;
@@ -314,12 +336,14 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     p.m_blocks1 = static_cast<int>(cdiv(c.V, BM));
     p.n_blocks1 = static_cast<int>(cdiv(c.D, BN));
     p.k_blocks1 = static_cast<int>(cdiv(rows, BK));
-    p.total_tiles = p.m_blocks0 * p.n_blocks0 + p.m_blocks1 * p.n_blocks1;
+    p.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * p.n_blocks0 +
+                    static_cast<int>(cdiv(p.m_blocks1, cl)) * p.n_blocks1;
     p.dH = static_cast<__nv_bfloat16 *>(dH);
     p.dW = dW;
     p.dw_accumulate = accumulate ? 1 : 0;
-    const int grid = p.total_tiles < c.sms ? p.total_tiles : c.sms;
-    LCE_LAUNCH_KIND(LCE_KERNEL_GRAD, c.s, launch_gemm(MODE_BWD, p, grid, c.s));
+    const int units = cl == 2 ? c.pairs : c.sms;
+    const int grid = cl * (p.total_tiles < units ? p.total_tiles : units);
+    LCE_LAUNCH_KIND(LCE_KERNEL_GRAD, c.s, launch_gemm(MODE_BWD, cl, p, grid, c.s));
     return LCE_OK;
 }
 

@@ -201,24 +201,28 @@ struct Tile {
 };
 enum : int { TILE_MAIN = 0, TILE_DW = 1 };
 
-// Logits launches: m fastest, so the chunk's row blocks that share one W slab
-// run together. Gradient launches: the few long dH tiles first (m fastest),
-// then the many short dW tiles (n fastest, so the tiles that share one G^T slab
-// run together); the dynamic schedule lets the SMs left over by the dH tiles
-// start on dW at once.
-__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t) {
+// Tiles are scheduled in units of CL vertically adjacent 128-row tiles (CL = 1,
+// or 2 for a CTA pair that shares the B operand); `t` indexes those units and
+// `crank` picks the CTA's own 128 rows. Logits launches: m fastest, so the
+// chunk's row blocks that share one W slab run together. Gradient launches:
+// the few long dH tiles first (m fastest), then the many short dW tiles (n
+// fastest, so the tiles that share one G^T slab run together); the dynamic
+// schedule lets the SMs left over by the dH tiles start on dW at once.
+template <int CL>
+__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int crank) {
     Tile tl;
-    const int nH = p.m_blocks0 * p.n_blocks0;
+    const int mp0 = (p.m_blocks0 + CL - 1) / CL;
+    const int nH = mp0 * p.n_blocks0;
     if (t < nH) {
         tl.type = TILE_MAIN;
-        tl.m0 = (t % p.m_blocks0) * BM;
-        tl.n0 = (t / p.m_blocks0) * BN;
+        tl.m0 = ((t % mp0) * CL + crank) * BM;
+        tl.n0 = (t / mp0) * BN;
         tl.nk = p.k_blocks0;
     } else {
         t -= nH;
         tl.type = TILE_DW;
         tl.n0 = (t % p.n_blocks1) * BN;
-        tl.m0 = (t / p.n_blocks1) * BM;
+        tl.m0 = ((t / p.n_blocks1) * CL + crank) * BM;
         tl.nk = p.k_blocks1;
     }
     return tl;
@@ -356,6 +360,7 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
                                                 const WarpStager &st) {
     const int r = tl.m0 + quarter * 32 + st.lane;  // row within the chunk
     const int box_y = tl.m0 + quarter * 32;
+    const bool box_rows = box_y < p.rows;       // warp-uniform: any row of the box exists
     const bool row_ok = r < p.rows;
     const int col0 = tl.n0 + half * 128;        // first vocabulary column of this half
     const int ncols = min(128, p.V - col0);     // valid columns (may be <= 0); same for the half
@@ -365,7 +370,7 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
     const int yl = y_ok ? static_cast<int>(yv - col0) : -1;   // local target column
 
     if constexpr (MODE == MODE_G) {
-        if (ncols <= 0) return;
+        if (ncols <= 0 || !box_rows) return;
         float scale = 0.f, lse2 = 0.f;
         if (row_ok) {
             const int nv = p.hdr[HDR_NVALID];
@@ -418,7 +423,7 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
                 s += v[j];
             }
             if constexpr (MODE == MODE_LSE_P) {
-                if ((c >> 1) * 64 < ncols) {
+                if ((c >> 1) * 64 < ncols && box_rows) {
                     if ((c & 1) == 0) st.acquire();
                     st.put_bf16((c & 1) * 4, v);
                     if (c & 1) st.issue(&p.tmS0, col0 + (c >> 1) * 64, box_y);
@@ -438,6 +443,9 @@ __device__ __forceinline__ void epilogue_grad(const GemmParams &p, const Tile &t
                                               int half, const HalfStager &st) {
     const int col0 = tl.n0 + half * 128;
     if (col0 >= p.D) return;  // this half is past D (same for the 4 warps)
+    // a tile entirely past the output rows (the second tile of a CTA pair at an
+    // odd row-block count) stores nothing
+    if (tl.m0 >= (tl.type == TILE_MAIN ? p.rows : p.V)) return;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
         float v[32];
@@ -456,13 +464,102 @@ __device__ __forceinline__ void epilogue_grad(const GemmParams &p, const Tile &t
     }
 }
 
-// ---------------------------------------------------------------- the kernel
+// ---------------------------------------------------------------- cluster helpers
 
-template <int MODE>
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, int v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (for data another CTA wrote).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, const Abort &ab) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_cluster(a, parity)) return true;
+        if (*ab.flag_smem) return false;
+        if (global_timer_ns() - t0 > ab.limit_ns) {
+            *ab.flag_smem = 1;
+            atomicOr(ab.hdr + HDR_FLAG, FLAG_TIMEOUT);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                     "memory");
+}
+// Pair (cta_group::2) forms. The TMA load writes this CTA's smem and signals the
+// mbarrier at the shared::cluster address `bar` (the leader CTA's).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t bar,
+                                                 int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+// Completion of this CTA's pair MMAs arrives on `bar`'s offset in every CTA of `mask`.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+
+// ---------------------------------------------------------------- the kernel
+// CL = 1: one CTA per 128 x 256 output tile. CL = 2: a CTA pair (cluster of 2)
+// per 256 x 256 tile with tcgen05 cta_group::2 MMAs: each CTA loads its own 128
+// rows of A and one half (128 columns of N) of B, both TMA loads completing on
+// the leader CTA's stage barrier; the leader's single MMA thread issues M = 256
+// MMAs that read both CTAs' shared memory and write both CTAs' TMEM (each its
+// own 128 rows); its commits arrive on the stage and accumulator barriers of
+// both CTAs; both CTAs' epilogues release the leader's accumulator. Per SM this
+// halves the B bytes per MMA, so each SM streams 32 KB instead of 48 KB per
+// 64-deep k block. The leader also fetches the tiles and writes them into both
+// CTAs' schedule rings.
+
+template <int MODE, int CL>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_constant__ GemmParams p) {
+    using P = Pipe<CL>;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[STAGES];
-    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+    __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[MAX_STAGES];
     __shared__ __align__(8) uint64_t tfull_bar[2];
     __shared__ __align__(8) uint64_t tempty_bar[2];
     __shared__ __align__(8) uint64_t sfull_bar[SCHED_DEPTH];
@@ -476,19 +573,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                                                 ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t crank = (CL == 2) ? cluster_ctarank() : 0u;
+    const bool leader = crank == 0;
+    // consumers of one schedule slot: the leader's MMA thread, every epilogue
+    // warp of the pair, and the peer's producer
+    constexpr int kSchedConsumers = 1 + CL * NUM_EPI_WARPS + (CL - 1);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < P::kStages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull_bar[b], 1);
-            mbar_init(&tempty_bar[b], NUM_EPI_WARPS);
+            mbar_init(&tempty_bar[b], CL * NUM_EPI_WARPS);
         }
         for (int q = 0; q < SCHED_DEPTH; ++q) {
             mbar_init(&sfull_bar[q], 1);
-            mbar_init(&sempty_bar[q], 1 + NUM_EPI_WARPS);
+            mbar_init(&sempty_bar[q], kSchedConsumers);
         }
         mbar_init(&drain_bar, 1);
         abort_flag = 0;
@@ -505,14 +607,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
         }
     }
     if (warp == MMA_WARP) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(&tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        // with CL = 2 both CTAs allocate together: the same columns on both SMs
+        if constexpr (CL == 2) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(&tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(&tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (CL == 2) cluster_sync_all();   // the peer's barriers exist from here on
     tc_fence_after();
     const uint32_t tmem_base = tmem_slot;
 
@@ -520,6 +632,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
     ab.flag_smem = &abort_flag;
     ab.hdr = p.hdr;
     ab.limit_ns = p.timeout_ns;
+
+    // a consumer of schedule slot q (or of accumulator buffer b) releases it on
+    // the leader's barrier
+    auto release_on_leader = [&](uint64_t *bar) {
+        if (CL == 2 && !leader) mbar_arrive_cluster(map_to_rank(bar, 0));
+        else mbar_arrive(bar);
+    };
 
     if (warp == PRODUCER_WARP) {
         if (lane == 0) {
@@ -530,51 +649,79 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
             int issued = 0;  // loads issued (for the drain on abort)
             bool ok = true;
             while (ok) {
-                // publish the next tile index
-                if (!mbar_wait(&sempty_bar[sq], sphase ^ 1, ab)) { ok = false; break; }
-                int t = atomicAdd(p.tile_counter, 1);
-                if (t >= p.total_tiles) t = -1;
-                sched_tile[sq] = t;
-                mbar_arrive(&sfull_bar[sq]);
+                int t;
+                if (leader) {
+                    // the leader fetches the next tile and publishes it to both CTAs
+                    if (!mbar_wait_cluster(&sempty_bar[sq], sphase ^ 1, ab)) { ok = false; break; }
+                    t = atomicAdd(p.tile_counter, 1);
+                    if (t >= p.total_tiles) t = -1;
+                    sched_tile[sq] = t;
+                    if constexpr (CL == 2) {
+                        st_cluster_u32(map_to_rank(&sched_tile[sq], 1), t);
+                        mbar_arrive_cluster(map_to_rank(&sfull_bar[sq], 1));
+                    }
+                    mbar_arrive(&sfull_bar[sq]);
+                } else {
+                    if (!mbar_wait_cluster(&sfull_bar[sq], sphase, ab)) { ok = false; break; }
+                    t = sched_tile[sq];
+                    release_on_leader(&sempty_bar[sq]);
+                }
                 if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
                 if (t < 0) break;
-                const Tile tl = decode_tile(p, t);
+                const Tile tl = decode_tile<CL>(p, t, static_cast<int>(crank));
                 for (int kb = 0; kb < tl.nk; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, ab)) { ok = false; break; }
-                    uint8_t *sA = smem + stage * STAGE_BYTES;
+                    uint8_t *sA = smem + stage * P::kStageBytes;
                     uint8_t *sB = sA + A_BYTES;
                     uint64_t *fb = &full_bar[stage];
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
                     const int kx = kb * BK;
-                    if (MODE != MODE_BWD) {
-                        tma_load_2d(sA, &p.tmA0, fb, kx, p.row0 + tl.m0);
-                        tma_load_2d(sB, &p.tmB0, fb, kx, tl.n0);
-                    } else if (tl.type != TILE_DW) {
-                        // dH: A = G rows (K-major), B = W (MN-major, 4 blocks of 64 D-columns)
-                        tma_load_2d(sA, &p.tmA0, fb, kx, tl.m0);
+                    const CUtensorMap *ma = (MODE == MODE_BWD && tl.type == TILE_DW) ? &p.tmA1 : &p.tmA0;
+                    const int ya = (MODE == MODE_BWD) ? tl.m0 : p.row0 + tl.m0;
+                    const bool b_mn = (MODE == MODE_BWD) && tl.type != TILE_DW;
+                    const CUtensorMap *mb = (MODE == MODE_BWD && !b_mn) ? &p.tmB1 : &p.tmB0;
+                    if constexpr (CL == 1) {
+                        mbar_arrive_expect_tx(fb, P::kStageBytes);
+                        tma_load_2d(sA, ma, fb, kx, ya);
+                        if (b_mn) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            tma_load_2d(sB + j * 8192, &p.tmB0, fb, tl.n0 + 64 * j, kx);
+                            for (int j = 0; j < 4; ++j)
+                                tma_load_2d(sB + j * 8192, mb, fb, tl.n0 + 64 * j, kx);
+                        } else {
+                            tma_load_2d(sB, mb, fb, kx, tl.n0);
+                        }
                     } else {
-                        // dW: A = G^T rows (K-major), B = H chunk^T rows (K-major)
-                        tma_load_2d(sA, &p.tmA1, fb, kx, tl.m0);
-                        tma_load_2d(sB, &p.tmB1, fb, kx, tl.n0);
+                        // both CTAs' bytes complete on the leader's barrier
+                        if (leader) mbar_arrive_expect_tx(fb, 2 * P::kStageBytes);
+                        const uint32_t lfb = map_to_rank(fb, 0);
+                        const int nb = tl.n0 + static_cast<int>(crank) * (BN / 2);
+                        tma_load_2d_pair(sA, ma, lfb, kx, ya);
+                        if (b_mn) {
+                            tma_load_2d_pair(sB, mb, lfb, nb, kx);
+                            tma_load_2d_pair(sB + 8192, mb, lfb, nb + 64, kx);
+                        } else {
+                            tma_load_2d_pair(sB, mb, lfb, kx, nb);
+                        }
                     }
                     ++issued;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == P::kStages) { stage = 0; phase ^= 1; }
                 }
             }
             if (!ok) {
                 // drain: wait (bounded) for the copies still in flight into each stage
-                const int n = issued < STAGES ? issued : STAGES;
+                // (with CL = 2 only the leader's barriers count the bytes)
+                const int n = issued < P::kStages ? issued : P::kStages;
                 for (int i = 0; i < n; ++i) {
-                    if (--stage < 0) { stage = STAGES - 1; phase ^= 1; }
-                    mbar_wait_drain(&full_bar[stage], phase, 50000000ull);
+                    if (--stage < 0) { stage = P::kStages - 1; phase ^= 1; }
+                    if (leader) mbar_wait_drain(&full_bar[stage], phase, 50000000ull);
+                }
+                if (!leader) {
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 50000000ull) {}
                 }
             }
         }
     } else if (warp == MMA_WARP) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             int sq = 0;
@@ -583,47 +730,53 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
             uint32_t aphase = 0;
             bool ok = true;
             bool any_mma = false;
+            const uint16_t both = static_cast<uint16_t>((1u << CL) - 1u);
             while (ok) {
-                if (!mbar_wait(&sfull_bar[sq], sphase, ab)) { ok = false; break; }
+                if (!mbar_wait_cluster(&sfull_bar[sq], sphase, ab)) { ok = false; break; }
                 const int t = sched_tile[sq];
-                mbar_arrive(&sempty_bar[sq]);
+                release_on_leader(&sempty_bar[sq]);
                 if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
                 if (t < 0) break;
-                const Tile tl = decode_tile(p, t);
-                if (!mbar_wait(&tempty_bar[acc], aphase ^ 1, ab)) { ok = false; break; }
+                const Tile tl = decode_tile<CL>(p, t, 0);
+                if (!mbar_wait_cluster(&tempty_bar[acc], aphase ^ 1, ab)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                // operand layouts of this tile type
                 // only the dH tiles read an MN-major operand (W, for B)
-                const bool a_mn = false;
                 const bool b_mn = (MODE == MODE_BWD) && tl.type != TILE_DW;
-                const uint32_t idesc = idesc_bf16(BM, BN, a_mn, b_mn);
-                const uint32_t a_lbo = a_mn ? 8192u : 16u, b_lbo = b_mn ? 8192u : 16u;
-                const uint32_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);
+                const uint32_t idesc = idesc_bf16(CL * BM, BN, false, b_mn);
+                const uint32_t b_lbo = b_mn ? 8192u : 16u;
+                const uint32_t a_step = 32u >> 4;
                 const uint32_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
                 for (int kb = 0; kb < tl.nk; ++kb) {
                     if (!mbar_wait(&full_bar[stage], phase, ab)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t sA = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sA = smem_u32(smem + stage * P::kStageBytes);
                     const uint32_t sB = sA + A_BYTES;
-                    const uint64_t ad = sdesc(sA, a_lbo, 1024u);
+                    const uint64_t ad = sdesc(sA, 16u, 1024u);
                     const uint64_t bd = sdesc(sB, b_lbo, 1024u);
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k)
-                        umma_bf16(d_tmem, ad + static_cast<uint64_t>(k * a_step),
-                                  bd + static_cast<uint64_t>(k * b_step), idesc,
-                                  (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        const uint64_t a = ad + static_cast<uint64_t>(k * a_step);
+                        const uint64_t b = bd + static_cast<uint64_t>(k * b_step);
+                        const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
+                        if constexpr (CL == 2) umma_bf16_pair(d_tmem, a, b, idesc, accumulate);
+                        else umma_bf16(d_tmem, a, b, idesc, accumulate);
+                    }
                     any_mma = true;
-                    umma_commit(&empty_bar[stage]);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if constexpr (CL == 2) umma_commit_pair(&empty_bar[stage], both);
+                    else umma_commit(&empty_bar[stage]);
+                    if (++stage == P::kStages) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                umma_commit(&tfull_bar[acc]);
+                if constexpr (CL == 2) umma_commit_pair(&tfull_bar[acc], both);
+                else umma_commit(&tfull_bar[acc]);
                 if (++acc == 2) { acc = 0; aphase ^= 1; }
             }
-            if (!ok && any_mma) {
-                // make sure no MMA is still writing TMEM before it is freed
-                umma_commit(&drain_bar);
+            if (any_mma) {
+                // every MMA (and every arrival it sends to the peer) has completed
+                // before TMEM is freed and the CTAs leave
+                if constexpr (CL == 2) umma_commit_pair(&drain_bar, both);
+                else umma_commit(&drain_bar);
                 mbar_wait_drain(&drain_bar, 0, 50000000ull);
             }
         }
@@ -633,27 +786,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
         const int quarter = warp & 3;
         const int half = warp >> 2;
         HalfStager st;
-        st.buf = smem + STAGES * STAGE_BYTES + half * STAGING_BYTES;
+        st.buf = smem + PIPE_BYTES + half * STAGING_BYTES;
         st.bar_id = 1 + half;
         st.row = quarter * 32 + lane;
         st.leader = (quarter == 0 && lane == 0);
         WarpStager wst;
-        wst.buf = smem + STAGES * STAGE_BYTES + warp * (2 * STAGING_BYTES / NUM_EPI_WARPS);
+        wst.buf = smem + PIPE_BYTES + warp * (2 * STAGING_BYTES / NUM_EPI_WARPS);
         wst.lane = lane;
         int sq = 0;
         uint32_t sphase = 0;
         int acc = 0;
         uint32_t aphase = 0;
         while (true) {
-            bool ok = mbar_wait(&sfull_bar[sq], sphase, ab);
+            bool ok = mbar_wait_cluster(&sfull_bar[sq], sphase, ab);
             if (!named_bar_and(st.bar_id, 128, ok)) break;
             const int t = sched_tile[sq];
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sempty_bar[sq]);
+            if (lane == 0) release_on_leader(&sempty_bar[sq]);
             if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
             if (t < 0) break;
-            const Tile tl = decode_tile(p, t);
-            ok = mbar_wait(&tfull_bar[acc], aphase, ab);
+            const Tile tl = decode_tile<CL>(p, t, static_cast<int>(crank));
+            ok = mbar_wait_cluster(&tfull_bar[acc], aphase, ab);
             if (!named_bar_and(st.bar_id, 128, ok)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
@@ -665,7 +818,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+            if (lane == 0) release_on_leader(&tempty_bar[acc]);
             if (++acc == 2) { acc = 0; aphase ^= 1; }
         }
         // all bulk stores issued by this warp / half complete before the CTA exits
@@ -675,45 +828,92 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
 
     tc_fence_before();
     __syncthreads();
+    // no CTA of the pair leaves while the other may still write to it
+    if constexpr (CL == 2) cluster_sync_all();
     if (warp == MMA_WARP) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(TMEM_COLS)
-                     : "memory");
+        if constexpr (CL == 2)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"(TMEM_COLS)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"(TMEM_COLS)
+                         : "memory");
     }
+}
+
+template <int MODE, int CL>
+static cudaError_t set_attr() {
+    return cudaFuncSetAttribute(lce_gemm_kernel<MODE, CL>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
 }
 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
-    e = cudaFuncSetAttribute(lce_gemm_kernel<MODE_LSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             GEMM_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(lce_gemm_kernel<MODE_LSE_P>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(lce_gemm_kernel<MODE_G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             GEMM_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(lce_gemm_kernel<MODE_BWD>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+    if ((e = set_attr<MODE_LSE, 1>()) != cudaSuccess) return e;
+    if ((e = set_attr<MODE_LSE_P, 1>()) != cudaSuccess) return e;
+    if ((e = set_attr<MODE_G, 1>()) != cudaSuccess) return e;
+    if ((e = set_attr<MODE_BWD, 1>()) != cudaSuccess) return e;
+    if ((e = set_attr<MODE_LSE, 2>()) != cudaSuccess) return e;
+    if ((e = set_attr<MODE_LSE_P, 2>()) != cudaSuccess) return e;
+    if ((e = set_attr<MODE_G, 2>()) != cudaSuccess) return e;
+    return set_attr<MODE_BWD, 2>();
 }
 
-cudaError_t launch_gemm(int mode, const GemmParams &p, int grid, cudaStream_t s) {
-    switch (mode) {
-        case MODE_LSE:
-            lce_gemm_kernel<MODE_LSE><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(p);
-            break;
-        case MODE_LSE_P:
-            lce_gemm_kernel<MODE_LSE_P><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(p);
-            break;
-        case MODE_G:
-            lce_gemm_kernel<MODE_G><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(p);
-            break;
-        default:
-            lce_gemm_kernel<MODE_BWD><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(p);
-            break;
+template <int MODE, int CL>
+static cudaError_t launch_one(const GemmParams &p, int grid, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, lce_gemm_kernel<MODE, CL>, p);
+}
+
+cudaError_t launch_gemm(int mode, int cluster, const GemmParams &p, int grid, cudaStream_t s) {
+    cudaError_t e;
+    if (cluster == 2) {
+        switch (mode) {
+            case MODE_LSE: e = launch_one<MODE_LSE, 2>(p, grid, s); break;
+            case MODE_LSE_P: e = launch_one<MODE_LSE_P, 2>(p, grid, s); break;
+            case MODE_G: e = launch_one<MODE_G, 2>(p, grid, s); break;
+            default: e = launch_one<MODE_BWD, 2>(p, grid, s); break;
+        }
+    } else {
+        switch (mode) {
+            case MODE_LSE: e = launch_one<MODE_LSE, 1>(p, grid, s); break;
+            case MODE_LSE_P: e = launch_one<MODE_LSE_P, 1>(p, grid, s); break;
+            case MODE_G: e = launch_one<MODE_G, 1>(p, grid, s); break;
+            default: e = launch_one<MODE_BWD, 1>(p, grid, s); break;
+        }
     }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// Largest number of CTA pairs of the gradient kernel that fit on the device at
+// once (the persistent grid is sized to it).
+cudaError_t gemm_max_pairs(int *pairs) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(pairs, lce_gemm_kernel<MODE_BWD, 2>, &cfg);
 }
 
 }  // namespace lce

@@ -17,12 +17,22 @@ constexpr int BM = 128;            // UMMA M (TMEM lanes)
 constexpr int BN = 256;            // UMMA N (TMEM columns per accumulator)
 constexpr int BK = 64;             // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;         // K of one tcgen05.mma kind::f16
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BYTES = BN * BK * 2;             // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
+// Pipeline per CTA. One CTA per tile: 4 stages of A (16 KB) + B (32 KB). CTA
+// pair on one 256 x 256 tile (tcgen05 cta_group::2): each CTA holds its own A
+// rows and half of B, 6 stages of 16 + 16 KB.
+template <int CL> struct Pipe {
+    static constexpr int kStages = CL == 2 ? 6 : 4;
+    static constexpr int kBBytes = B_BYTES / CL;
+    static constexpr int kStageBytes = A_BYTES + kBBytes;
+};
+constexpr int MAX_STAGES = 6;
+constexpr int STAGES = 4;                                  // one-CTA pipeline
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;             // 48 KB
 constexpr int STAGING_BYTES = 16384;  // per epilogue column half: one 128-row x 128-byte store box
-constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 2 * STAGING_BYTES + 1024;  // + 1 KB alignment
+constexpr int PIPE_BYTES = 4 * 48 * 1024;      // both pipelines use 192 KB
+constexpr int GEMM_SMEM_BYTES = PIPE_BYTES + 2 * STAGING_BYTES + 1024;  // + 1 KB alignment
 constexpr int NUM_EPI_WARPS = 8;   // warps 0..7: TMEM lane quarter = warp % 4, column half = warp / 4
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
@@ -57,7 +67,7 @@ struct GemmParams {
     CUtensorMap tmS1;      // dW output store / reduce-add (fp32)
     int m_blocks0, n_blocks0, k_blocks0;
     int m_blocks1, n_blocks1, k_blocks1;   // dW tiles (0 in logits launches)
-    int total_tiles;
+    int total_tiles;       // scheduling units: tiles, or tile pairs for CTA pairs
     int rows;              // rows in this chunk
     int row0;              // first global row of this chunk
     int V, D;
@@ -112,7 +122,11 @@ struct TransposeParams {
 };
 
 // launchers (return cudaError_t of the launch)
-cudaError_t launch_gemm(int mode, const GemmParams &p, int grid, cudaStream_t s);
+// cluster = 1: one CTA per 128 x 256 tile; 2: a CTA pair per 256 x 256 tile
+// (tcgen05 cta_group::2, each CTA loading its own A rows and half of B).
+// `grid` counts CTAs (a multiple of `cluster`).
+cudaError_t launch_gemm(int mode, int cluster, const GemmParams &p, int grid, cudaStream_t s);
+cudaError_t gemm_max_pairs(int *pairs);
 cudaError_t launch_label_scan(const long long *y, long long N, long long V, long long ign,
                               int *hdr, cudaStream_t s);
 cudaError_t launch_merge(bool factors, const MergeParams &p, cudaStream_t s);

@@ -159,3 +159,15 @@ def test_workload_full_oracle(lce, name):
     check_lse(to64(lse), ref["lse"])
     check_grad("dH", to64(dH), ref["dH"])
     check_grad("dW", to64(dW), ref["dW"])
+
+
+@pytest.mark.parametrize("N,D,V,chunk", [(300, 264, 1000, 128), (1000, 520, 3000, 384),
+                                         (4096, 1024, 32000, 1024)])
+def test_single_cta_tiles_match_oracle(lce, monkeypatch, N, D, V, chunk):
+    """The one-CTA-per-tile GEMM variant (the default runs CTA pairs with
+    cta_group::2; odd row-block counts there give a pair whose second tile lies
+    past the output, covered by the other tests)."""
+    monkeypatch.setenv("LCE_GEMM_CLUSTER", "1")
+    H, W, y = make_inputs(N, D, V, seed=N + 7, labels="uniform", n_ignored=N // 20, w_std=0.05)
+    r = run_all_paths(lce, H, W, y, chunk=chunk, dloss=1.3)
+    compare(r, O.forward_backward(H, W, y, dloss=1.3))
