@@ -370,48 +370,74 @@ def load_traffic():
 
 
 def run_e2e(args, lce, H, W, y, chunk, dev, stream, world):
+    """The same metric through the public API from pinned host buffers: every
+    step copies its inputs (H, W, y) host -> device and reads its loss back.
+    The copies of step k+1 run on a copy stream while step k computes (two
+    device input buffers), as a training loop that prefetches its next batch
+    would; the timed region still contains every step's copies."""
     import torch
     Hh, Wh, yh = H.pin_memory(), W.pin_memory(), y.pin_memory()
-    Hd = torch.empty_like(Hh, device=dev)
-    Wd = torch.empty_like(Wh, device=dev)
-    yd = torch.empty_like(yh, device=dev)
+    bufs = [(torch.empty_like(Hh, device=dev), torch.empty_like(Wh, device=dev),
+             torch.empty_like(yh, device=dev)) for _ in range(2)]
     N, D = H.shape
     V = W.shape[0]
     ws = lce.alloc_workspace(N, D, V, chunk, dev)
-    loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    loss_h = torch.empty(2, dtype=torch.float32).pin_memory()
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
     dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+    copy_stream = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        Hd.copy_(Hh, non_blocking=True)
-        Wd.copy_(Wh, non_blocking=True)
-        yd.copy_(yh, non_blocking=True)
-        lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk, loss=loss, lse=lse, dH=dH, dW=dW, ws=ws,
+    def h2d(k):
+        b = bufs[k % 2]
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(consumed[k % 2])   # the step that last read this buffer
+            b[0].copy_(Hh, non_blocking=True)
+            b[1].copy_(Wh, non_blocking=True)
+            b[2].copy_(yh, non_blocking=True)
+            copied[k % 2].record(copy_stream)
+
+    def compute(k):
+        b = bufs[k % 2]
+        stream.wait_event(copied[k % 2])
+        lce.lce_fwd_bwd(b[0], b[1], b[2], chunk=chunk, loss=loss, lse=lse, dH=dH, dW=dW, ws=ws,
                         stream=stream)
-        loss_h.copy_(loss, non_blocking=True)
+        consumed[k % 2].record(stream)
+        loss_h[k % 2].copy_(loss[0], non_blocking=True)
 
-    for _ in range(3):
-        step()
+    def run(steps):
+        h2d(0)
+        for k in range(steps):
+            if k + 1 < steps:
+                h2d(k + 1)
+            compute(k)
+
+    for ev in consumed:
+        ev.record(stream)
+    run(3)
     torch.cuda.synchronize(dev)
     steps = max(3, args.steps // 2)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
     a.record(stream)
-    for _ in range(steps):
-        step()
+    copy_stream.wait_event(a)        # the first step's copies start inside the timed region
+    run(steps)
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / steps
-    h2d = Hh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8
+    h2d_bytes = Hh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8
     return {"value": world * N / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
-            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
-            "note": "H, W and y copied from pinned host memory each step; loss read back"}
+            "steps": steps, "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": 4,
+            "note": "every step copies H, W and y from pinned host memory (on a copy stream, "
+                    "overlapping the previous step's compute) and reads its loss back"}
 
 
 def cpu_baseline(wl):
     H64, W64, y = prepare_oracle_inputs(wl)
-    rows = calibrate_rows(wl, H64, W64, y, target_s=20.0)
+    rows = calibrate_rows(wl, H64, W64, y, target_s=40.0)
     t = oracle_sample_rate(wl, rows, H64, W64, y)
     return {"value": rows / t, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
             "sample": f"first {rows} of {wl.N} tokens of the workload (fp64 numpy forward+"

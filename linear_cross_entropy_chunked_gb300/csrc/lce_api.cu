@@ -85,9 +85,8 @@ struct Layout {
     long long nchunks = 0;
     int nparts = 0;          // 128-column slabs per row
     int ldg = 0;             // row stride of the chunk buffer (elements)
-    int ldt = 0;             // row stride (elements) of G^T and H^T: chunk rows rounded up
-    size_t off_loss_rows = 0, off_zy = 0, off_parts = 0, off_G = 0, off_GT = 0, off_HT = 0,
-           total = 0;
+    int ldt = 0;             // row stride (elements) of H^T: chunk rows rounded up
+    size_t off_loss_rows = 0, off_zy = 0, off_parts = 0, off_G = 0, off_HT = 0, total = 0;
     size_t hdr_bytes = 0;
 };
 
@@ -110,10 +109,8 @@ bool make_layout(long long N, long long D, long long V, long long chunk, Layout 
     off += align_up(sizeof(float2) * static_cast<size_t>(L.C) * L.nparts, 1024);
     L.off_G = off;
     off += align_up(2 * static_cast<size_t>(L.C) * L.ldg, 1024);
-    // G^T [V][ldt] and H chunk^T [D][ldt] make every dW operand K-major
+    // H chunk^T [D][ldt]: the K-major B operand of the dW contraction
     L.ldt = static_cast<int>(align_up(static_cast<size_t>(L.C), 64));
-    L.off_GT = off;
-    off += align_up(2 * static_cast<size_t>(V) * L.ldt, 1024);
     L.off_HT = off;
     off += align_up(2 * static_cast<size_t>(D) * L.ldt, 1024);
     L.total = off;
@@ -172,7 +169,7 @@ struct Ctx {
     float *loss_rows, *zy;
     float2 *parts;
     __nv_bfloat16 *G;
-    __nv_bfloat16 *GT, *HT;
+    __nv_bfloat16 *HT;
     int sms;
     int pairs;   // > 0: GEMMs run as CTA pairs (cluster of 2), at most this many at once
     cudaStream_t s;
@@ -255,7 +252,6 @@ lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t
     c.zy = reinterpret_cast<float *>(c.ws + c.L.off_zy);
     c.parts = reinterpret_cast<float2 *>(c.ws + c.L.off_parts);
     c.G = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_G);
-    c.GT = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_GT);
     c.HT = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_HT);
     c.s = reinterpret_cast<cudaStream_t>(stream);
     // with CTA pairs each CTA loads half of a 256-row W tile (multicast to both)
@@ -312,19 +308,19 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     memset(&p, 0, sizeof(p));
     base_params(c, p, row0, rows, slot);
     const __nv_bfloat16 *Hc = c.H + row0 * c.D;
-    // G^T and the H chunk^T for the K-major dW operands
+    // the H chunk^T for the K-major B operand of the dW tiles
     TransposeParams tp;
-    memset(&tp, 0, sizeof(tp));
     tp.src = Hc;
     tp.ld_src = static_cast<int>(c.D);
     tp.dst_t = c.HT;
     tp.ld_t = c.L.ldt;
     tp.rows = static_cast<int>(rows);
     tp.cols = static_cast<int>(c.D);
-    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_transpose(false, tp, c.s));
+    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_transpose(tp, c.s));
     if (!encode_2d(&p.tmA0, c.G, c.V, rows, 2ull * c.L.ldg, BK, BM)) return LCE_ERR_CUDA;
     p.tmB0 = c.tmW_MN;
-    if (!encode_2d(&p.tmA1, c.GT, rows, c.V, 2ull * c.L.ldt, BK, BM)) return LCE_ERR_CUDA;
+    // dW A = G^T read from G itself (MN-major boxes of 64 vocab columns x 64 rows)
+    if (!encode_2d(&p.tmA1, c.G, c.V, rows, 2ull * c.L.ldg, 64, BK)) return LCE_ERR_CUDA;
     const int cl = c.pairs > 0 ? 2 : 1;
     if (!encode_2d(&p.tmB1, c.HT, rows, c.D, 2ull * c.L.ldt, BK, BN / cl)) return LCE_ERR_CUDA;
     __nv_bfloat16 *dHc = static_cast<__nv_bfloat16 *>(dH) + row0 * c.D;
@@ -368,25 +364,21 @@ lce_status run_merge(const Ctx &c, bool fused, long long row0, long long rows, f
     return LCE_OK;
 }
 
-// G^T from the chunk buffer; with fix-up, P' -> G in place first (fused path).
-lce_status run_g_transpose(const Ctx &c, bool fixup, long long row0, long long rows,
-                           const float *dloss) {
-    TransposeParams tp;
-    memset(&tp, 0, sizeof(tp));
-    tp.src = c.G;
-    tp.ld_src = c.L.ldg;
-    tp.dst_t = c.GT;
-    tp.ld_t = c.L.ldt;
-    tp.rows = static_cast<int>(rows);
-    tp.cols = static_cast<int>(c.V);
-    tp.parts = c.parts;
-    tp.nparts = c.L.nparts;
-    tp.y = c.y;
-    tp.row0 = static_cast<int>(row0);
-    tp.ignore_index = c.ign;
-    tp.hdr = c.hdr;
-    tp.dloss = dloss;
-    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_transpose(fixup, tp, c.s));
+// Fused path: P' -> G in place in the chunk buffer.
+lce_status run_fixup(const Ctx &c, long long row0, long long rows, const float *dloss) {
+    FixupParams fp;
+    fp.G = c.G;
+    fp.ldg = c.L.ldg;
+    fp.rows = static_cast<int>(rows);
+    fp.V = static_cast<int>(c.V);
+    fp.parts = c.parts;
+    fp.nparts = c.L.nparts;
+    fp.y = c.y;
+    fp.row0 = static_cast<int>(row0);
+    fp.ignore_index = c.ign;
+    fp.hdr = c.hdr;
+    fp.dloss = dloss;
+    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_fixup(fp, c.s));
     return LCE_OK;
 }
 
@@ -445,7 +437,6 @@ lce_status lce_backward(const void *H, const void *W, const int64_t *y, const fl
         const long long row0 = k * c.L.C;
         const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
         LCE_TRY(run_logits(c, MODE_G, row0, rows, static_cast<int>(2 * k), lse, dloss));
-        LCE_TRY(run_g_transpose(c, false, row0, rows, dloss));
         LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dH, dW, k > 0));
     }
     return LCE_OK;
@@ -470,7 +461,7 @@ lce_status lce_fwd_bwd(const void *H, const void *W, const int64_t *y, const flo
         const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
         LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr));
         LCE_TRY(run_merge(c, true, row0, rows, lse, dloss));
-        LCE_TRY(run_g_transpose(c, true, row0, rows, dloss));
+        LCE_TRY(run_fixup(c, row0, rows, dloss));
         LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dH, dW, k > 0));
     }
     LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss, c.s));

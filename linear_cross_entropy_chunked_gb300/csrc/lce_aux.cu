@@ -3,9 +3,9 @@
 //   * slab merge: per row, combine the (max, sumexp) partials of the 128-column
 //     slabs into lse_i = M + log sum_p s_p exp(m_p - M), write the row's loss
 //     lse_i - z_{i,y_i} and (fused path) each slab's factor exp(m_p - lse_i) * scale;
-//   * fix-up + transpose (fused path): turn the stored P' = exp(z - m_p) into
-//     G = (P' exp(m_p - lse_i) - 1[j = y_i]) * dloss / N_valid in place and
-//     write G^T; the same kernel transposes the H chunk for the dW contraction
+//   * fix-up (fused path): turn the stored P' = exp(z - m_p) into
+//     G = (P' exp(m_p - lse_i) - 1[j = y_i]) * dloss / N_valid in place;
+//   * transpose of the H chunk (the K-major B operand of the dW contraction)
 //     ("Unsloth Architecture: Manual Triton Backpropagation, Fused Cross-Entropy,
 //     and 80% VRAM Cut", pillar 1: the loss -z_{i,y_i} + log sum_j e^{z_ij} and
 //     the gradient p_ij - 1[j = y_i]);
@@ -135,65 +135,62 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_merge_kernel(const MergePar
     }
 }
 
-// ------------------------------------------------------------------ fix-up + transpose
-// 64 x 64 tiles. FIX: the tile of the chunk buffer holds P' = exp(z - m_p); it
-// becomes G = P' * factor_p - 1[j = y_i] * dloss / N_valid (rounded to bf16),
-// written back in place and, transposed, into G^T [V][ld_t]. Without FIX the
-// kernel is a plain transpose (the H chunk into H^T [D][ld_t]).
+// ------------------------------------------------------------------ fix-up
+// The chunk buffer holds P' = exp(z - m_p) (bf16). In place it becomes
+// G = P' * factor_p - 1[j = y_i] * dloss / N_valid, rounded to bf16.
+// Grid: x over 8-column vectors of a row, y over rows.
+
+__global__ void __launch_bounds__(256) lce_fixup_kernel(const FixupParams p) {
+    const int nvec = (p.V + 7) >> 3;
+    const int i = blockIdx.x * 256 + threadIdx.x;
+    if (i >= nvec) return;
+    for (int r = blockIdx.y; r < p.rows; r += gridDim.y) {
+    const long long yv = p.y[p.row0 + r];
+    const bool y_ok = yv != p.ignore_index && yv >= 0 && yv < p.V;
+    const int nv = p.hdr[HDR_NVALID];
+    const float dl = p.dloss ? *p.dloss : 1.f;
+    const float scale = (y_ok && nv > 0) ? dl / static_cast<float>(nv) : 0.f;
+    const int ycol = y_ok ? static_cast<int>(yv) : -1;
+    const int c = i * 8;
+    const float f = p.parts[static_cast<size_t>(r) * p.nparts + (c >> 7)].x;
+    uint4 *ptr = reinterpret_cast<uint4 *>(p.G + static_cast<size_t>(r) * p.ldg + c);
+    uint4 u = *ptr;
+    uint32_t *wv = reinterpret_cast<uint32_t *>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&wv[q]);
+        float2 x = __bfloat1622float2(h);
+        x.x *= f;
+        x.y *= f;
+        if (c + 2 * q == ycol) x.x -= scale;
+        if (c + 2 * q + 1 == ycol) x.y -= scale;
+        h = __floats2bfloat162_rn(x.x, x.y);
+        wv[q] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    *ptr = u;
+    }
+}
+
+// ------------------------------------------------------------------ transpose
+// 64 x 64 tiles of the H chunk [rows][D] into H^T [D][ld_t] (the K-major B
+// operand of the dW contraction).
 
 constexpr int TT = 64;
 constexpr int TSTRIDE = 66;   // bf16 elements per staged row: conflict-free row writes, 2-way column reads
 
-template <bool FIX>
 __global__ void __launch_bounds__(256) lce_transpose_kernel(const TransposeParams p) {
     __shared__ __align__(16) __nv_bfloat16 tile[TT * TSTRIDE];
-    const int c0 = blockIdx.x * TT;      // first column of the tile (vocabulary id or D index)
+    const int c0 = blockIdx.x * TT;      // first column of the tile
     const int r0 = blockIdx.y * TT;      // first chunk row of the tile
     const int tid = threadIdx.x;
-    float scale_r[2] = {0.f, 0.f}, fac_r[2] = {0.f, 0.f};
-    int ycol_r[2] = {-1, -1};
-    if constexpr (FIX) {
-        const int nv = p.hdr[HDR_NVALID];
-        const float dl = p.dloss ? *p.dloss : 1.f;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int r = r0 + (tid + 256 * i) / 8;
-            if (r < p.rows) {
-                const long long yv = p.y[p.row0 + r];
-                const bool y_ok = yv != p.ignore_index && yv >= 0 && yv < p.cols;
-                scale_r[i] = (y_ok && nv > 0) ? dl / static_cast<float>(nv) : 0.f;
-                ycol_r[i] = y_ok ? static_cast<int>(yv) : -1;
-                fac_r[i] = p.parts[static_cast<size_t>(r) * p.nparts + c0 / 128].x;
-            }
-        }
-    }
-    // load (and fix up) 8 elements per chunk, two chunks per thread
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int k = tid + 256 * i;
         const int rr = k >> 3, cb = (k & 7) * 8;
         const int r = r0 + rr, c = c0 + cb;
         uint4 u = make_uint4(0u, 0u, 0u, 0u);
-        if (r < p.rows && c < p.cols) {
-            uint4 *src = reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(p.src) +
-                                                   static_cast<size_t>(r) * p.ld_src + c);
-            u = *src;
-            if constexpr (FIX) {
-                uint32_t *wv = reinterpret_cast<uint32_t *>(&u);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&wv[q]);
-                    float2 x = __bfloat1622float2(h);
-                    x.x *= fac_r[i];
-                    x.y *= fac_r[i];
-                    if (c + 2 * q == ycol_r[i]) x.x -= scale_r[i];
-                    if (c + 2 * q + 1 == ycol_r[i]) x.y -= scale_r[i];
-                    h = __floats2bfloat162_rn(x.x, x.y);
-                    wv[q] = *reinterpret_cast<uint32_t *>(&h);
-                }
-                *src = u;
-            }
-        }
+        if (r < p.rows && c < p.cols)
+            u = *reinterpret_cast<const uint4 *>(p.src + static_cast<size_t>(r) * p.ld_src + c);
         uint32_t *dst = reinterpret_cast<uint32_t *>(tile + rr * TSTRIDE + cb);
         dst[0] = u.x;
         dst[1] = u.y;
@@ -201,7 +198,6 @@ __global__ void __launch_bounds__(256) lce_transpose_kernel(const TransposeParam
         dst[3] = u.w;
     }
     __syncthreads();
-    // transposed write: output row = tile column, 8 chunk rows per 16-byte store
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int k = tid + 256 * i;
@@ -262,11 +258,18 @@ cudaError_t launch_merge(bool factors, const MergeParams &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_transpose(bool fix, const TransposeParams &p, cudaStream_t s) {
+cudaError_t launch_transpose(const TransposeParams &p, cudaStream_t s) {
     if (p.rows <= 0 || p.cols <= 0) return cudaSuccess;
     const dim3 grid((p.cols + TT - 1) / TT, (p.rows + TT - 1) / TT);
-    if (fix) lce_transpose_kernel<true><<<grid, 256, 0, s>>>(p);
-    else lce_transpose_kernel<false><<<grid, 256, 0, s>>>(p);
+    lce_transpose_kernel<<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fixup(const FixupParams &p, cudaStream_t s) {
+    if (p.rows <= 0) return cudaSuccess;
+    const int nvec = (p.V + 7) / 8;
+    const dim3 grid((nvec + 255) / 256, p.rows < 65535 ? p.rows : 65535);
+    lce_fixup_kernel<<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

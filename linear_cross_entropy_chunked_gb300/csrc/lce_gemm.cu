@@ -679,9 +679,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                     const int ya = (MODE == MODE_BWD) ? tl.m0 : p.row0 + tl.m0;
                     const bool b_mn = (MODE == MODE_BWD) && tl.type != TILE_DW;
                     const CUtensorMap *mb = (MODE == MODE_BWD && !b_mn) ? &p.tmB1 : &p.tmB0;
+                    // dW tiles read A = G^T straight from the row-major chunk buffer
+                    // (MN-major: two 64-wide vocabulary boxes per 64 chunk rows)
+                    const bool a_mn = (MODE == MODE_BWD) && tl.type == TILE_DW;
                     if constexpr (CL == 1) {
                         mbar_arrive_expect_tx(fb, P::kStageBytes);
-                        tma_load_2d(sA, ma, fb, kx, ya);
+                        if (a_mn) {
+                            tma_load_2d(sA, ma, fb, tl.m0, kx);
+                            tma_load_2d(sA + 8192, ma, fb, tl.m0 + 64, kx);
+                        } else {
+                            tma_load_2d(sA, ma, fb, kx, ya);
+                        }
                         if (b_mn) {
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
@@ -694,7 +702,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                         if (leader) mbar_arrive_expect_tx(fb, 2 * P::kStageBytes);
                         const uint32_t lfb = map_to_rank(fb, 0);
                         const int nb = tl.n0 + static_cast<int>(crank) * (BN / 2);
-                        tma_load_2d_pair(sA, ma, lfb, kx, ya);
+                        if (a_mn) {
+                            tma_load_2d_pair(sA, ma, lfb, tl.m0, kx);
+                            tma_load_2d_pair(sA + 8192, ma, lfb, tl.m0 + 64, kx);
+                        } else {
+                            tma_load_2d_pair(sA, ma, lfb, kx, ya);
+                        }
                         if (b_mn) {
                             tma_load_2d_pair(sB, mb, lfb, nb, kx);
                             tma_load_2d_pair(sB + 8192, mb, lfb, nb + 64, kx);
@@ -741,18 +754,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                 if (!mbar_wait_cluster(&tempty_bar[acc], aphase ^ 1, ab)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                // only the dH tiles read an MN-major operand (W, for B)
+                // MN-major operands: W for the dH tiles (B), the chunk buffer for the
+                // dW tiles (A = G^T); everything else is K-major
                 const bool b_mn = (MODE == MODE_BWD) && tl.type != TILE_DW;
-                const uint32_t idesc = idesc_bf16(CL * BM, BN, false, b_mn);
+                const bool a_mn = (MODE == MODE_BWD) && tl.type == TILE_DW;
+                const uint32_t idesc = idesc_bf16(CL * BM, BN, a_mn, b_mn);
+                const uint32_t a_lbo = a_mn ? 8192u : 16u;
                 const uint32_t b_lbo = b_mn ? 8192u : 16u;
-                const uint32_t a_step = 32u >> 4;
+                const uint32_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);
                 const uint32_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
                 for (int kb = 0; kb < tl.nk; ++kb) {
                     if (!mbar_wait(&full_bar[stage], phase, ab)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sA = smem_u32(smem + stage * P::kStageBytes);
                     const uint32_t sB = sA + A_BYTES;
-                    const uint64_t ad = sdesc(sA, 16u, 1024u);
+                    const uint64_t ad = sdesc(sA, a_lbo, 1024u);
                     const uint64_t bd = sdesc(sB, b_lbo, 1024u);
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {

@@ -61,7 +61,7 @@ constexpr int FLAG_TIMEOUT = 2;
 struct GemmParams {
     CUtensorMap tmA0;      // logits A = H (K-major) | dH A = G (K-major)
     CUtensorMap tmB0;      // logits B = W (K-major) | dH B = W (MN-major)
-    CUtensorMap tmA1;      // dW A = G^T [V][C] (K-major)
+    CUtensorMap tmA1;      // dW A = G^T, read from the chunk buffer G [C][ldg] (MN-major)
     CUtensorMap tmB1;      // dW B = H chunk^T [D][C] (K-major)
     CUtensorMap tmS0;      // output store: P' / G chunk buffer (bf16) | dH chunk (bf16)
     CUtensorMap tmS1;      // dW output store / reduce-add (fp32)
@@ -106,13 +106,18 @@ struct MergeParams {
 };
 
 struct TransposeParams {
-    const __nv_bfloat16 *src;   // [rows][ld_src]; fixed up in place when FIX
+    const __nv_bfloat16 *src;   // [rows][ld_src]
     int ld_src;
     __nv_bfloat16 *dst_t;       // [cols][ld_t]
     int ld_t;
-    int rows, cols;             // chunk rows; V (G) or D (H)
-    // fix-up only
-    const float2 *parts;        // .x = slab factor
+    int rows, cols;
+};
+
+struct FixupParams {
+    __nv_bfloat16 *G;           // [rows][ldg]: P' in, G out (in place)
+    int ldg;
+    int rows, V;
+    const float2 *parts;        // .x = slab factor exp(m_p - lse) * dloss / N_valid
     int nparts;
     const long long *y;
     int row0;
@@ -130,7 +135,8 @@ cudaError_t gemm_max_pairs(int *pairs);
 cudaError_t launch_label_scan(const long long *y, long long N, long long V, long long ign,
                               int *hdr, cudaStream_t s);
 cudaError_t launch_merge(bool factors, const MergeParams &p, cudaStream_t s);
-cudaError_t launch_transpose(bool fix, const TransposeParams &p, cudaStream_t s);
+cudaError_t launch_transpose(const TransposeParams &p, cudaStream_t s);
+cudaError_t launch_fixup(const FixupParams &p, cudaStream_t s);
 cudaError_t launch_loss_finalize(const float *loss_rows, long long N, const int *hdr,
                                  float *loss, cudaStream_t s);
 cudaError_t gemm_set_attributes();
