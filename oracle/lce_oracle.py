@@ -33,6 +33,10 @@ Readings where the pages are silent (each is listed in the design doc too):
   * N_valid == 0 gives loss 0 and zero gradients.
   * the loss uses lse - z_y exactly, with no clamp of p.
   * dloss is a scalar upstream gradient multiplying G.
+  * reduction variants (a library option the pages do not discuss): "mean"
+    (the pages' normalised loss), "sum" (sum over valid rows, G scaled by dloss)
+    and "none" (per-row losses, 0 for ignored rows; dloss is then a per-row
+    vector and row i of G is scaled by dloss[i]).
 
 Pins: tests/test_oracle.py checks this module against closed forms (W = 0),
 invariants (row sums of G, column sums of dW, shift invariance, ignored rows),
@@ -112,8 +116,13 @@ def forward(H, W, y, ignore_index: int = IGNORE_INDEX):
     return loss, lse, n_valid, n_bad
 
 
-def forward_backward(H, W, y, ignore_index: int = IGNORE_INDEX, dloss: float = 1.0):
-    """Steps 1-5. Returns dict(loss, lse[N], dH[N,D], dW[V,D], n_valid, n_bad), fp64."""
+def forward_backward(H, W, y, ignore_index: int = IGNORE_INDEX, dloss=1.0,
+                     reduction: str = "mean"):
+    """Steps 1-5. Returns dict(loss, lse[N], dH[N,D], dW[V,D], n_valid, n_bad), fp64.
+
+    reduction "mean": loss = sum / N_valid, G scaled by dloss / N_valid;
+    "sum": loss = sum, G scaled by dloss; "none": loss is the per-row vector and
+    dloss a per-row vector scaling the rows of G."""
     H = as_f64(H)
     W = as_f64(W)
     y = as_labels(y)
@@ -121,11 +130,18 @@ def forward_backward(H, W, y, ignore_index: int = IGNORE_INDEX, dloss: float = 1
     V = W.shape[0]
     valid, n_bad = valid_rows(y, V, ignore_index)
     n_valid = int(valid.sum())
-    scale = (dloss / n_valid) if n_valid else 0.0
+    if reduction == "mean":
+        row_scale = np.full(N, (float(dloss) / n_valid) if n_valid else 0.0)
+    elif reduction == "sum":
+        row_scale = np.full(N, float(dloss))
+    elif reduction == "none":
+        row_scale = np.broadcast_to(np.asarray(dloss, dtype=np.float64), (N,)).copy()
+    else:
+        raise ValueError(f"unknown reduction {reduction!r}")
     lse = np.empty(N, dtype=np.float64)
+    row_loss = np.zeros(N, dtype=np.float64)
     dH = np.zeros((N, D), dtype=np.float64)
     dW = np.zeros((V, D), dtype=np.float64)
-    total = 0.0
     for s, e in _block_iter(N, _block_rows(V)):
         Z = logits(H[s:e], W)
         lse_b = row_logsumexp(Z)
@@ -133,16 +149,22 @@ def forward_backward(H, W, y, ignore_index: int = IGNORE_INDEX, dloss: float = 1
         v = valid[s:e]
         idx = np.nonzero(v)[0]
         yb = y[s:e]
-        total += float(np.sum(lse_b[idx] - Z[idx, yb[idx]]))
-        # step 4: G = (softmax - onehot) * dloss / N_valid, ignored rows zero
+        row_loss[s:e][idx] = lse_b[idx] - Z[idx, yb[idx]]
+        # step 4: G = (softmax - onehot) * scale, ignored rows zero
         G = np.exp(Z - lse_b[:, None])
         G[idx, yb[idx]] -= 1.0
-        G *= scale
+        G *= row_scale[s:e, None]
         G[~v] = 0.0
         # step 5
         dH[s:e] = G @ W
         dW += G.T @ H[s:e]
-    loss = total / n_valid if n_valid else 0.0
+    total = float(np.sum(row_loss))
+    if reduction == "mean":
+        loss = total / n_valid if n_valid else 0.0
+    elif reduction == "sum":
+        loss = total
+    else:
+        loss = row_loss
     return dict(loss=loss, lse=lse, dH=dH, dW=dW, n_valid=n_valid, n_bad=n_bad)
 
 

@@ -257,6 +257,50 @@ def test_expected_loss_at_init_tiny_workload():
     assert abs(loss - (math.log(32000) + 512 * 0.02 ** 2 / 2)) < 0.05
 
 
+# ------------------------------------------------------- reduction variants
+
+def test_reductions_vs_torch():
+    """torch cross_entropy with reduction sum / none (+ autograd, fp64), and a
+    per-row upstream gradient for 'none'."""
+    H, W, y = _rand(25, 7, 19, 31, n_ign=3)
+    rng = np.random.default_rng(32)
+    g_rows = rng.standard_normal(25)
+    for red, dl in (("sum", 0.6), ("none", g_rows)):
+        Ht = torch.tensor(H, requires_grad=True)
+        Wt = torch.tensor(W, requires_grad=True)
+        out = torch.nn.functional.cross_entropy(Ht @ Wt.T, torch.tensor(y), ignore_index=IGN,
+                                                reduction=red)
+        (out * torch.as_tensor(dl)).sum().backward()
+        r = O.forward_backward(H, W, y, dloss=dl, reduction=red)
+        assert np.allclose(r["loss"], out.detach().numpy(), atol=1e-12)
+        assert np.allclose(r["dH"], Ht.grad.numpy(), atol=1e-13)
+        assert np.allclose(r["dW"], Wt.grad.numpy(), atol=1e-13)
+
+
+def test_reduction_relations_and_fd():
+    """sum = mean * N_valid; the per-row losses sum to it and are 0 on ignored
+    rows; a per-row dloss equal everywhere matches 'sum'; finite differences of
+    sum_i dloss_i L_i give the 'none' gradients."""
+    H, W, y = _rand(6, 5, 9, 33, n_ign=2, w_std=0.5)
+    m = O.forward_backward(H, W, y, reduction="mean")
+    s_ = O.forward_backward(H, W, y, reduction="sum", dloss=2.0)
+    n = O.forward_backward(H, W, y, reduction="none", dloss=np.full(6, 2.0))
+    assert abs(s_["loss"] - m["loss"] * m["n_valid"]) < 1e-12
+    assert abs(np.sum(n["loss"]) - s_["loss"]) < 1e-12
+    assert np.all(n["loss"][y == IGN] == 0.0)
+    assert np.allclose(n["dH"], s_["dH"], atol=1e-15) and np.allclose(n["dW"], s_["dW"], atol=1e-15)
+    g = np.random.default_rng(34).standard_normal(6)
+    r = O.forward_backward(H, W, y, reduction="none", dloss=g)
+    f = lambda Hx: float(np.dot(g, O.forward_backward(Hx, W, y, reduction="none")["loss"]))
+    eps = 1e-5
+    num = np.zeros_like(H)
+    for idx in np.ndindex(H.shape):
+        Hp = H.copy(); Hp[idx] += eps
+        Hm = H.copy(); Hm[idx] -= eps
+        num[idx] = (f(Hp) - f(Hm)) / (2 * eps)
+    assert np.abs(num - r["dH"]).max() <= 1e-6
+
+
 # ------------------------------------------------------- sampled helpers
 
 def test_sampled_helpers_match_full():
@@ -291,16 +335,16 @@ def test_blocking_does_not_change_results(monkeypatch):
 MUTATIONS = {
     "dropped onehot term": ("G[idx, yb[idx]] -= 1.0", "pass"),
     "wrong onehot sign": ("G[idx, yb[idx]] -= 1.0", "G[idx, yb[idx]] += 1.0"),
-    "divide by N not N_valid": ("scale = (dloss / n_valid) if n_valid else 0.0",
-                                "scale = dloss / N"),
+    "divide by N not N_valid": ("row_scale = np.full(N, (float(dloss) / n_valid) if n_valid else 0.0)",
+                                "row_scale = np.full(N, float(dloss) / N)"),
     "ignored rows not zeroed": ("G[~v] = 0.0", "pass"),
     "dW transposed operand": ("dW += G.T @ H[s:e]", "dW += (H[s:e].T @ G).T[::-1]"),
     "lse without log": ("return m + np.log(np.exp(Z - m[:, None]).sum(axis=1))",
                         "return m + np.exp(Z - m[:, None]).sum(axis=1)"),
     "max not added back": ("return m + np.log(np.exp(Z - m[:, None]).sum(axis=1))",
                            "return np.log(np.exp(Z - m[:, None]).sum(axis=1))"),
-    "loss sign": ("total += float(np.sum(lse_b[idx] - Z[idx, yb[idx]]))",
-                  "total += float(np.sum(Z[idx, yb[idx]] - lse_b[idx]))"),
+    "loss sign": ("row_loss[s:e][idx] = lse_b[idx] - Z[idx, yb[idx]]",
+                  "row_loss[s:e][idx] = Z[idx, yb[idx]] - lse_b[idx]"),
     "dH uses W transposed wrong": ("dH[s:e] = G @ W", "dH[s:e] = G @ W[::-1]"),
 }
 
