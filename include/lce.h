@@ -95,6 +95,27 @@ lce_status lce_fwd_bwd(const void *H, const void *W, const int64_t *y, const flo
                        float *loss, float *lse, void *dH, float *dW,
                        void *ws, size_t ws_bytes, lce_stream_t stream);
 
+/* Reductions of the loss (a library option; the pages use the mean):
+ *  MEAN: loss = sum over valid rows / N_valid (device scalar); G = (p - onehot) * dloss / N_valid.
+ *  SUM:  loss = sum over valid rows (device scalar); G = (p - onehot) * dloss.
+ *  NONE: loss[N] = per-row losses (0 for ignored rows); dloss is NULL (all 1) or a
+ *        device vector dloss[N], and row i of G is (p_i - onehot_i) * dloss[i].
+ * The _ex entry points take one of these; the entry points above are MEAN. */
+enum { LCE_REDUCTION_MEAN = 0, LCE_REDUCTION_SUM = 1, LCE_REDUCTION_NONE = 2 };
+
+lce_status lce_forward_ex(const void *H, const void *W, const int64_t *y,
+                          int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                          int reduction, float *loss, float *lse,
+                          void *ws, size_t ws_bytes, lce_stream_t stream);
+lce_status lce_backward_ex(const void *H, const void *W, const int64_t *y, const float *lse,
+                           const float *dloss, void *dH, float *dW,
+                           int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                           int reduction, void *ws, size_t ws_bytes, lce_stream_t stream);
+lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const float *dloss,
+                          int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                          int reduction, float *loss, float *lse, void *dH, float *dW,
+                          void *ws, size_t ws_bytes, lce_stream_t stream);
+
 /* Synchronises `stream`, then returns the device-side status recorded in the
  * workspace by the last call that used it (LCE_OK, LCE_ERR_LABEL_RANGE or
  * LCE_ERR_TIMEOUT; a timeout wins over a label error) and clears it. Returns

@@ -34,6 +34,9 @@ EXPORTED = (
     "lce_forward",
     "lce_backward",
     "lce_fwd_bwd",
+    "lce_forward_ex",
+    "lce_backward_ex",
+    "lce_fwd_bwd_ex",
     "lce_read_status",
     "lce_status_string",
     "lce_version",
@@ -44,6 +47,7 @@ EXPORTED = (
 )
 
 KERNEL_KINDS = {"logits": 0, "grad": 1, "merge": 2, "other": 3}
+REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 
 class LCEError(RuntimeError):
@@ -81,6 +85,12 @@ def lib() -> ctypes.CDLL:
                                _vp, ctypes.c_size_t, _vp]
     L.lce_fwd_bwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
                               _vp, _vp, ctypes.c_size_t, _vp]
+    L.lce_forward_ex.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _vp,
+                                 _vp, _vp, ctypes.c_size_t, _vp]
+    L.lce_backward_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                  ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+    L.lce_fwd_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
+                                 _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     L.lce_read_status.argtypes = [_vp, _vp]
     L.lce_status_string.argtypes = [ctypes.c_int]
     L.lce_status_string.restype = ctypes.c_char_p
@@ -91,8 +101,9 @@ def lib() -> ctypes.CDLL:
                                    ctypes.POINTER(ctypes.c_int64)]
     L.lce_profile_reset.argtypes = []
     L.lce_profile_reset.restype = None
-    for name in ("lce_profile_enable", "lce_profile_read", "lce_workspace_size", "lce_forward", "lce_backward", "lce_fwd_bwd",
-                 "lce_read_status", "lce_version", "lce_last_launch_count"):
+    for name in ("lce_profile_enable", "lce_profile_read", "lce_workspace_size", "lce_forward",
+                 "lce_backward", "lce_fwd_bwd", "lce_forward_ex", "lce_backward_ex",
+                 "lce_fwd_bwd_ex", "lce_read_status", "lce_version", "lce_last_launch_count"):
         getattr(L, name).restype = ctypes.c_int
     _LIB = L
     return L
@@ -139,49 +150,74 @@ def _check_inputs(H, W, y):
     return H.shape[0], H.shape[1], W.shape[0]
 
 
+def _reduction(reduction: str) -> int:
+    if reduction not in REDUCTIONS:
+        raise ValueError(f"reduction must be one of {sorted(REDUCTIONS)}")
+    return REDUCTIONS[reduction]
+
+
+def _loss_buffer(loss, N, reduction, dev):
+    if loss is None:
+        loss = torch.empty(N if reduction == "none" else 1, dtype=torch.float32, device=dev)
+    return loss
+
+
+def _check_dloss(dloss, N, reduction):
+    if dloss is None:
+        return
+    if dloss.dtype != torch.float32 or not dloss.is_cuda or not dloss.is_contiguous():
+        raise TypeError("dloss must be a contiguous CUDA float32 tensor")
+    want = N if reduction == "none" else 1
+    if dloss.numel() != want:
+        raise ValueError(f"dloss must have {want} element(s) for reduction={reduction!r}")
+
+
 def lce_forward(H, W, y, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
-                loss=None, lse=None, ws=None, stream=None):
-    """Mean loss (device scalar) and lse[N] via the library's lce_forward."""
+                loss=None, lse=None, ws=None, stream=None, reduction: str = "mean"):
+    """Loss (device scalar, or [N] for reduction="none") and lse[N]."""
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
-    if loss is None:
-        loss = torch.empty(1, dtype=torch.float32, device=dev)
+    red = _reduction(reduction)
+    loss = _loss_buffer(loss, N, reduction, dev)
     if lse is None:
         lse = torch.empty(N, dtype=torch.float32, device=dev)
     if ws is None:
         ws = alloc_workspace(N, D, V, chunk, dev)
-    st = lib().lce_forward(_ptr(H), _ptr(W), _ptr(y), N, D, V, ignore_index, chunk,
-                           _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    st = lib().lce_forward_ex(_ptr(H), _ptr(W), _ptr(y), N, D, V, ignore_index, chunk, red,
+                              _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "lce_forward")
     return loss, lse
 
 
 def lce_backward(H, W, y, lse, dloss=None, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
-                 dH=None, dW=None, ws=None, stream=None):
-    """dH (bf16) and dW (fp32) from a saved lse via the library's lce_backward."""
+                 dH=None, dW=None, ws=None, stream=None, reduction: str = "mean"):
+    """dH (bf16) and dW (fp32) from a saved lse. dloss: scalar tensor, or [N] for
+    reduction="none"; None means 1."""
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
+    red = _reduction(reduction)
     if dH is None:
         dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
     if dW is None:
         dW = torch.empty(V, D, dtype=torch.float32, device=dev)
     if ws is None:
         ws = alloc_workspace(N, D, V, chunk, dev)
-    if dloss is not None and (dloss.dtype != torch.float32 or not dloss.is_cuda):
-        raise TypeError("dloss must be a CUDA float32 scalar tensor")
-    st = lib().lce_backward(_ptr(H), _ptr(W), _ptr(y), _ptr(lse), _ptr(dloss), _ptr(dH), _ptr(dW),
-                            N, D, V, ignore_index, chunk, _ptr(ws), ws.numel(), _stream(stream))
+    _check_dloss(dloss, N, reduction)
+    st = lib().lce_backward_ex(_ptr(H), _ptr(W), _ptr(y), _ptr(lse), _ptr(dloss), _ptr(dH),
+                               _ptr(dW), N, D, V, ignore_index, chunk, red, _ptr(ws), ws.numel(),
+                               _stream(stream))
     _check(st, "lce_backward")
     return dH, dW
 
 
 def lce_fwd_bwd(H, W, y, dloss=None, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
-                loss=None, lse=None, dH=None, dW=None, ws=None, stream=None):
-    """Fused forward + backward: (loss, lse, dH, dW) via the library's lce_fwd_bwd."""
+                loss=None, lse=None, dH=None, dW=None, ws=None, stream=None,
+                reduction: str = "mean"):
+    """Fused forward + backward: (loss, lse, dH, dW)."""
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
-    if loss is None:
-        loss = torch.empty(1, dtype=torch.float32, device=dev)
+    red = _reduction(reduction)
+    loss = _loss_buffer(loss, N, reduction, dev)
     if lse is None:
         lse = torch.empty(N, dtype=torch.float32, device=dev)
     if dH is None:
@@ -190,11 +226,10 @@ def lce_fwd_bwd(H, W, y, dloss=None, chunk: int = 1024, ignore_index: int = IGNO
         dW = torch.empty(V, D, dtype=torch.float32, device=dev)
     if ws is None:
         ws = alloc_workspace(N, D, V, chunk, dev)
-    if dloss is not None and (dloss.dtype != torch.float32 or not dloss.is_cuda):
-        raise TypeError("dloss must be a CUDA float32 scalar tensor")
-    st = lib().lce_fwd_bwd(_ptr(H), _ptr(W), _ptr(y), _ptr(dloss), N, D, V, ignore_index, chunk,
-                           _ptr(loss), _ptr(lse), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(),
-                           _stream(stream))
+    _check_dloss(dloss, N, reduction)
+    st = lib().lce_fwd_bwd_ex(_ptr(H), _ptr(W), _ptr(y), _ptr(dloss), N, D, V, ignore_index,
+                              chunk, red, _ptr(loss), _ptr(lse), _ptr(dH), _ptr(dW), _ptr(ws),
+                              ws.numel(), _stream(stream))
     _check(st, "lce_fwd_bwd")
     return loss, lse, dH, dW
 
@@ -229,22 +264,26 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
     """autograd wrapper: forward = lce_forward, backward = lce_backward (recompute)."""
 
     @staticmethod
-    def forward(ctx, H, W, y, chunk=1024, ignore_index=IGNORE_INDEX):
-        loss, lse = lce_forward(H, W, y, chunk=chunk, ignore_index=ignore_index)
+    def forward(ctx, H, W, y, chunk=1024, ignore_index=IGNORE_INDEX, reduction="mean"):
+        loss, lse = lce_forward(H, W, y, chunk=chunk, ignore_index=ignore_index,
+                                reduction=reduction)
         ctx.save_for_backward(H, W, y, lse)
         ctx.chunk = chunk
         ctx.ignore_index = ignore_index
-        return loss.view(())
+        ctx.reduction = reduction
+        return loss if reduction == "none" else loss.view(())
 
     @staticmethod
     def backward(ctx, grad_out):
         H, W, y, lse = ctx.saved_tensors
-        g = grad_out.detach().reshape(1).to(torch.float32).contiguous()
+        g = grad_out.detach().reshape(-1).to(torch.float32).contiguous()
         dH, dW = lce_backward(H, W, y, lse, dloss=g, chunk=ctx.chunk,
-                              ignore_index=ctx.ignore_index)
-        return dH, dW.to(W.dtype), None, None, None
+                              ignore_index=ctx.ignore_index, reduction=ctx.reduction)
+        return dH, dW.to(W.dtype), None, None, None, None
 
 
-def linear_cross_entropy(H, W, y, chunk: int = 1024, ignore_index: int = IGNORE_INDEX):
-    """Mean cross-entropy of softmax(H W^T) against y, differentiable in H and W."""
-    return LinearCrossEntropyFunction.apply(H, W, y, chunk, ignore_index)
+def linear_cross_entropy(H, W, y, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
+                         reduction: str = "mean"):
+    """Cross-entropy of softmax(H W^T) against y (mean, sum or per-row), differentiable
+    in H and W."""
+    return LinearCrossEntropyFunction.apply(H, W, y, chunk, ignore_index, reduction)

@@ -172,6 +172,7 @@ struct Ctx {
     __nv_bfloat16 *HT;
     int sms;
     int pairs;   // > 0: GEMMs run as CTA pairs (cluster of 2), at most this many at once
+    int reduction;       // LCE_REDUCTION_*
     cudaStream_t s;
     CUtensorMap tmH_K, tmW_K, tmW_MN;
 };
@@ -254,6 +255,7 @@ lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t
     c.G = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_G);
     c.HT = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_HT);
     c.s = reinterpret_cast<cudaStream_t>(stream);
+    c.reduction = LCE_REDUCTION_MEAN;
     // with CTA pairs each CTA loads half of a 256-row W tile (multicast to both)
     if (!encode_2d(&c.tmW_K, W, D, V, D * 2, BK, c.pairs > 0 ? BN / 2 : BN)) return LCE_ERR_CUDA;
     if (!encode_2d(&c.tmW_MN, W, D, V, D * 2, 64, BK)) return LCE_ERR_CUDA;
@@ -278,6 +280,8 @@ void base_params(const Ctx &c, GemmParams &p, long long row0, long long rows, in
     p.G = c.G;
     p.ldg = c.L.ldg;
     p.timeout_ns = kDefaultTimeoutNs;
+    p.dloss_per_row = c.reduction == LCE_REDUCTION_NONE ? 1 : 0;
+    p.mean = c.reduction == LCE_REDUCTION_MEAN ? 1 : 0;
 }
 
 lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, int slot,
@@ -344,7 +348,7 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
 }
 
 lce_status run_merge(const Ctx &c, bool fused, long long row0, long long rows, float *lse,
-                     const float *dloss) {
+                     const float *dloss, float *loss_rows) {
     MergeParams m;
     m.parts = c.parts;
     m.nparts = c.L.nparts;
@@ -358,8 +362,10 @@ lce_status run_merge(const Ctx &c, bool fused, long long row0, long long rows, f
     m.y = c.y;
     m.hdr = c.hdr;
     m.dloss = dloss;
+    m.dloss_per_row = c.reduction == LCE_REDUCTION_NONE ? 1 : 0;
+    m.mean = c.reduction == LCE_REDUCTION_MEAN ? 1 : 0;
     m.lse = lse;
-    m.loss_rows = c.loss_rows;
+    m.loss_rows = loss_rows;
     LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_merge(fused, m, c.s));
     return LCE_OK;
 }
@@ -378,6 +384,8 @@ lce_status run_fixup(const Ctx &c, long long row0, long long rows, const float *
     fp.ignore_index = c.ign;
     fp.hdr = c.hdr;
     fp.dloss = dloss;
+    fp.dloss_per_row = c.reduction == LCE_REDUCTION_NONE ? 1 : 0;
+    fp.mean = c.reduction == LCE_REDUCTION_MEAN ? 1 : 0;
     LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_fixup(fp, c.s));
     return LCE_OK;
 }
@@ -400,34 +408,50 @@ lce_status lce_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk, si
     return LCE_OK;
 }
 
-lce_status lce_forward(const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
-                       int64_t V, int64_t ignore_index, int64_t chunk, float *loss, float *lse,
-                       void *ws, size_t ws_bytes, lce_stream_t stream) {
+lce_status lce_forward_ex(const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
+                          int64_t V, int64_t ignore_index, int64_t chunk, int reduction,
+                          float *loss, float *lse, void *ws, size_t ws_bytes,
+                          lce_stream_t stream) {
     g_launches = 0;
-    if (!loss || (N > 0 && !lse)) return LCE_ERR_INVALID_ARG;
-    if (!aligned16(loss) || (lse && !aligned16(lse))) return LCE_ERR_ALIGNMENT;
+    if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
+    const bool none = reduction == LCE_REDUCTION_NONE;
+    if ((!none && !loss) || (N > 0 && (!lse || !loss))) return LCE_ERR_INVALID_ARG;
+    if ((loss && !aligned16(loss)) || (lse && !aligned16(lse))) return LCE_ERR_ALIGNMENT;
     Ctx c;
     LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream));
+    c.reduction = reduction;
+    float *rows_out = none ? loss : c.loss_rows;
     for (long long k = 0; k < c.L.nchunks; ++k) {
         const long long row0 = k * c.L.C;
         const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
         LCE_TRY(run_logits(c, MODE_LSE, row0, rows, static_cast<int>(k), nullptr, nullptr));
-        LCE_TRY(run_merge(c, false, row0, rows, lse, nullptr));
+        LCE_TRY(run_merge(c, false, row0, rows, lse, nullptr, rows_out));
     }
-    LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss, c.s));
+    if (!none)
+        LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss,
+                                        reduction == LCE_REDUCTION_MEAN, c.s));
     return LCE_OK;
 }
 
-lce_status lce_backward(const void *H, const void *W, const int64_t *y, const float *lse,
-                        const float *dloss, void *dH, float *dW, int64_t N, int64_t D, int64_t V,
-                        int64_t ignore_index, int64_t chunk, void *ws, size_t ws_bytes,
-                        lce_stream_t stream) {
+lce_status lce_forward(const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
+                       int64_t V, int64_t ignore_index, int64_t chunk, float *loss, float *lse,
+                       void *ws, size_t ws_bytes, lce_stream_t stream) {
+    return lce_forward_ex(H, W, y, N, D, V, ignore_index, chunk, LCE_REDUCTION_MEAN, loss, lse, ws,
+                          ws_bytes, stream);
+}
+
+lce_status lce_backward_ex(const void *H, const void *W, const int64_t *y, const float *lse,
+                           const float *dloss, void *dH, float *dW, int64_t N, int64_t D,
+                           int64_t V, int64_t ignore_index, int64_t chunk, int reduction,
+                           void *ws, size_t ws_bytes, lce_stream_t stream) {
     g_launches = 0;
+    if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
     if (!dW || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
     if (!aligned16(dW) || (dH && !aligned16(dH)) || (lse && !aligned16(lse)))
         return LCE_ERR_ALIGNMENT;
     Ctx c;
     LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream));
+    c.reduction = reduction;
     if (c.L.nchunks == 0) {
         if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess)
             return LCE_ERR_CUDA;
@@ -442,16 +466,29 @@ lce_status lce_backward(const void *H, const void *W, const int64_t *y, const fl
     return LCE_OK;
 }
 
-lce_status lce_fwd_bwd(const void *H, const void *W, const int64_t *y, const float *dloss,
-                       int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
-                       float *loss, float *lse, void *dH, float *dW, void *ws, size_t ws_bytes,
-                       lce_stream_t stream) {
+lce_status lce_backward(const void *H, const void *W, const int64_t *y, const float *lse,
+                        const float *dloss, void *dH, float *dW, int64_t N, int64_t D, int64_t V,
+                        int64_t ignore_index, int64_t chunk, void *ws, size_t ws_bytes,
+                        lce_stream_t stream) {
+    return lce_backward_ex(H, W, y, lse, dloss, dH, dW, N, D, V, ignore_index, chunk,
+                           LCE_REDUCTION_MEAN, ws, ws_bytes, stream);
+}
+
+lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const float *dloss,
+                          int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                          int reduction, float *loss, float *lse, void *dH, float *dW, void *ws,
+                          size_t ws_bytes, lce_stream_t stream) {
     g_launches = 0;
-    if (!loss || !dW || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
-    if (!aligned16(loss) || !aligned16(dW) || (dH && !aligned16(dH)) || (lse && !aligned16(lse)))
+    if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
+    const bool none = reduction == LCE_REDUCTION_NONE;
+    if ((!none && !loss) || !dW || (N > 0 && (!lse || !dH || !loss))) return LCE_ERR_INVALID_ARG;
+    if ((loss && !aligned16(loss)) || !aligned16(dW) || (dH && !aligned16(dH)) ||
+        (lse && !aligned16(lse)))
         return LCE_ERR_ALIGNMENT;
     Ctx c;
     LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream));
+    c.reduction = reduction;
+    float *rows_out = none ? loss : c.loss_rows;
     if (c.L.nchunks == 0) {
         if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess)
             return LCE_ERR_CUDA;
@@ -460,12 +497,22 @@ lce_status lce_fwd_bwd(const void *H, const void *W, const int64_t *y, const flo
         const long long row0 = k * c.L.C;
         const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
         LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr));
-        LCE_TRY(run_merge(c, true, row0, rows, lse, dloss));
+        LCE_TRY(run_merge(c, true, row0, rows, lse, dloss, rows_out));
         LCE_TRY(run_fixup(c, row0, rows, dloss));
         LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dH, dW, k > 0));
     }
-    LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss, c.s));
+    if (!none)
+        LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss,
+                                        reduction == LCE_REDUCTION_MEAN, c.s));
     return LCE_OK;
+}
+
+lce_status lce_fwd_bwd(const void *H, const void *W, const int64_t *y, const float *dloss,
+                       int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                       float *loss, float *lse, void *dH, float *dW, void *ws, size_t ws_bytes,
+                       lce_stream_t stream) {
+    return lce_fwd_bwd_ex(H, W, y, dloss, N, D, V, ignore_index, chunk, LCE_REDUCTION_MEAN, loss,
+                          lse, dH, dW, ws, ws_bytes, stream);
 }
 
 lce_status lce_read_status(const void *ws, lce_stream_t stream) {

@@ -11,6 +11,8 @@
 //     the gradient p_ij - 1[j = y_i]);
 //   * loss finalisation: fixed-order fp64 sum of the per-row losses / N_valid.
 // Every reduction has a fixed order, so results are bit-reproducible.
+// Reductions of the loss: mean (sum / N_valid), sum, or none (the per-row losses
+// are the output; G's rows are then scaled by a per-row dloss).
 #include "lce_internal.h"
 
 namespace lce {
@@ -126,9 +128,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_merge_kernel(const MergePar
         p.loss_rows[grow] = y_ok ? lse - p.zy[r] : 0.f;
     }
     if constexpr (FACTORS) {
-        const int nv = p.hdr[HDR_NVALID];
-        const float dl = p.dloss ? *p.dloss : 1.f;
-        const float scale = (y_ok && nv > 0) ? dl / static_cast<float>(nv) : 0.f;
+        const float scale =
+            lce_row_scale(p.dloss, p.dloss_per_row, p.mean, p.hdr[HDR_NVALID], grow, y_ok);
         const float lse2 = lse * LOG2E_F;
         for (int i = t; i < p.nparts; i += MERGE_THREADS)
             parts[i].x = scale != 0.f ? exp2f(fmaf(parts[i].x, LOG2E_F, -lse2)) * scale : 0.f;
@@ -147,9 +148,8 @@ __global__ void __launch_bounds__(256) lce_fixup_kernel(const FixupParams p) {
     for (int r = blockIdx.y; r < p.rows; r += gridDim.y) {
     const long long yv = p.y[p.row0 + r];
     const bool y_ok = yv != p.ignore_index && yv >= 0 && yv < p.V;
-    const int nv = p.hdr[HDR_NVALID];
-    const float dl = p.dloss ? *p.dloss : 1.f;
-    const float scale = (y_ok && nv > 0) ? dl / static_cast<float>(nv) : 0.f;
+    const float scale = lce_row_scale(p.dloss, p.dloss_per_row, p.mean, p.hdr[HDR_NVALID],
+                                      p.row0 + r, y_ok);
     const int ycol = y_ok ? static_cast<int>(yv) : -1;
     const int c = i * 8;
     const float f = p.parts[static_cast<size_t>(r) * p.nparts + (c >> 7)].x;
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(256) lce_transpose_kernel(const TransposeParam
 
 __global__ void __launch_bounds__(1024) lce_loss_finalize_kernel(const float *__restrict__ loss_rows,
                                                                  long long N, const int *hdr,
-                                                                 float *loss) {
+                                                                 float *loss, int mean) {
     __shared__ double s_red[32];
     double s = 0.0;
     for (long long i = threadIdx.x; i < N; i += 1024) s += static_cast<double>(loss_rows[i]);
@@ -235,7 +235,8 @@ __global__ void __launch_bounds__(1024) lce_loss_finalize_kernel(const float *__
         s = warp_sum_d(s);
         if (l == 0) {
             const int nv = hdr[HDR_NVALID];
-            *loss = nv > 0 ? static_cast<float>(s / nv) : 0.f;
+            if (mean) *loss = nv > 0 ? static_cast<float>(s / nv) : 0.f;
+            else *loss = static_cast<float>(s);
         }
     }
 }
@@ -276,8 +277,8 @@ cudaError_t launch_fixup(const FixupParams &p, cudaStream_t s) {
 cudaError_t aux_set_attributes() { return cudaSuccess; }
 
 cudaError_t launch_loss_finalize(const float *loss_rows, long long N, const int *hdr, float *loss,
-                                 cudaStream_t s) {
-    lce_loss_finalize_kernel<<<1, 1024, 0, s>>>(loss_rows, N, hdr, loss);
+                                 int mean, cudaStream_t s) {
+    lce_loss_finalize_kernel<<<1, 1024, 0, s>>>(loss_rows, N, hdr, loss, mean);
     return cudaGetLastError();
 }
 

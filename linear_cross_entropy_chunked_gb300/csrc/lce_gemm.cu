@@ -373,9 +373,8 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
         if (ncols <= 0 || !box_rows) return;
         float scale = 0.f, lse2 = 0.f;
         if (row_ok) {
-            const int nv = p.hdr[HDR_NVALID];
-            const float dl = p.dloss ? *p.dloss : 1.f;
-            scale = (y_ok && nv > 0) ? dl / static_cast<float>(nv) : 0.f;
+            scale = lce_row_scale(p.dloss, p.dloss_per_row, p.mean, p.hdr[HDR_NVALID], p.row0 + r,
+                                  y_ok);
             lse2 = p.lse[p.row0 + r] * LOG2E;
         }
 #pragma unroll 1

@@ -49,6 +49,16 @@ enum GemmMode : int {
     MODE_BWD = 3      // dH tiles (G W) followed by dW tiles (G^T H) in one persistent launch
 };
 
+// Scale of row i of G: dloss (a scalar, or row i of a per-row vector) divided
+// by N_valid for the mean reduction; 0 for rows that do not count.
+__device__ __forceinline__ float lce_row_scale(const float *dloss, int dloss_per_row, int mean,
+                                               int n_valid, long long grow, bool y_ok) {
+    if (!y_ok) return 0.f;
+    const float d = dloss ? dloss[dloss_per_row ? grow : 0] : 1.f;
+    if (mean) return n_valid > 0 ? d / static_cast<float>(n_valid) : 0.f;
+    return d;
+}
+
 // Workspace header (int32 words).
 enum : int {
     HDR_FLAG = 0,       // bit 0: label out of range, bit 1: pipeline wait timed out
@@ -75,7 +85,9 @@ struct GemmParams {
     const long long *y;    // labels, global [N]
     int *tile_counter;
     int *hdr;
-    const float *dloss;    // device scalar or null (= 1)
+    const float *dloss;    // device scalar, per-row vector, or null (= 1)
+    int dloss_per_row;     // 1: dloss[N] (reduction none)
+    int mean;              // 1: G scaled by 1 / N_valid (reduction mean)
     // logits epilogue
     float2 *parts;         // [rows][nparts] (max, sumexp)
     int nparts;
@@ -101,8 +113,10 @@ struct MergeParams {
     const long long *y;
     const int *hdr;
     const float *dloss;
+    int dloss_per_row;
+    int mean;
     float *lse;            // global [N]
-    float *loss_rows;      // global [N]
+    float *loss_rows;      // global [N] (the caller's loss vector for reduction none)
 };
 
 struct TransposeParams {
@@ -124,6 +138,8 @@ struct FixupParams {
     long long ignore_index;
     const int *hdr;
     const float *dloss;
+    int dloss_per_row;
+    int mean;
 };
 
 // launchers (return cudaError_t of the launch)
@@ -138,7 +154,7 @@ cudaError_t launch_merge(bool factors, const MergeParams &p, cudaStream_t s);
 cudaError_t launch_transpose(const TransposeParams &p, cudaStream_t s);
 cudaError_t launch_fixup(const FixupParams &p, cudaStream_t s);
 cudaError_t launch_loss_finalize(const float *loss_rows, long long N, const int *hdr,
-                                 float *loss, cudaStream_t s);
+                                 float *loss, int mean, cudaStream_t s);
 cudaError_t gemm_set_attributes();
 cudaError_t aux_set_attributes();
 

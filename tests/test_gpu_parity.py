@@ -171,3 +171,45 @@ def test_single_cta_tiles_match_oracle(lce, monkeypatch, N, D, V, chunk):
     H, W, y = make_inputs(N, D, V, seed=N + 7, labels="uniform", n_ignored=N // 20, w_std=0.05)
     r = run_all_paths(lce, H, W, y, chunk=chunk, dloss=1.3)
     compare(r, O.forward_backward(H, W, y, dloss=1.3))
+
+
+@pytest.mark.parametrize("reduction", ["sum", "none"])
+@pytest.mark.parametrize("N,D,V,chunk", [(300, 264, 1000, 128), (1000, 520, 3000, 384)])
+def test_reduction_variants(lce, reduction, N, D, V, chunk):
+    """reduction sum / none through the three paths; 'none' with a per-row dloss."""
+    H, W, y = make_inputs(N, D, V, seed=N + 11, labels="uniform", n_ignored=N // 25, w_std=0.05)
+    rng = np.random.default_rng(N)
+    dl_host = rng.standard_normal(N) if reduction == "none" else 0.37
+    dl = torch.tensor(np.atleast_1d(dl_host), dtype=torch.float32, device=DEV)
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    loss, lse, dH, dW = lce.lce_fwd_bwd(Hd, Wd, yd, dloss=dl, chunk=chunk, reduction=reduction)
+    floss, flse = lce.lce_forward(Hd, Wd, yd, chunk=chunk, reduction=reduction)
+    bdH, bdW = lce.lce_backward(Hd, Wd, yd, flse, dloss=dl, chunk=chunk, reduction=reduction)
+    torch.cuda.synchronize()
+    ref = O.forward_backward(H, W, y, dloss=np.float64(dl_host) if reduction == "sum" else dl_host,
+                             reduction=reduction)
+    if reduction == "sum":
+        check_loss(loss.item(), ref["loss"])
+        check_loss(floss.item(), ref["loss"])
+    else:
+        assert loss.shape == (N,)
+        for got in (loss, floss):
+            err = np.abs(to64(got) - ref["loss"]).max()
+            assert err <= 1e-3 * np.abs(ref["loss"]).max(), err
+    check_lse(to64(lse), ref["lse"])
+    for name, got, exp in (("dH", dH, ref["dH"]), ("dW", dW, ref["dW"]),
+                           ("dH (backward)", bdH, ref["dH"]), ("dW (backward)", bdW, ref["dW"])):
+        check_grad(name, to64(got), exp)
+
+
+def test_autograd_per_row_losses(lce):
+    H, W, y = make_inputs(260, 128, 700, seed=21, n_ignored=9)
+    Hd = H.to(DEV).requires_grad_(True)
+    Wd = W.to(DEV).requires_grad_(True)
+    rows = lce.linear_cross_entropy(Hd, Wd, y.to(DEV), chunk=128, reduction="none")
+    g = torch.linspace(-1, 1, 260, device=DEV)
+    (rows * g).sum().backward()
+    ref = O.forward_backward(H, W, y, dloss=g.double().cpu().numpy(), reduction="none")
+    assert np.abs(to64(rows) - ref["loss"]).max() <= 1e-3 * np.abs(ref["loss"]).max()
+    check_grad("dH", to64(Hd.grad), ref["dH"])
+    check_grad("dW", to64(Wd.grad), ref["dW"])
