@@ -116,6 +116,23 @@ lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const 
                           int reduction, float *loss, float *lse, void *dH, float *dW,
                           void *ws, size_t ws_bytes, lce_stream_t stream);
 
+/* Cross-entropy over logits the caller already has (no projection): the
+ * streaming row kernel of "Unsloth Kernel Architecture: Custom Triton
+ * Backpropagation and QLoRA Memory Scaling", section 1 (a row of logits
+ * streamed in vocabulary blocks with a running max and a running sum of
+ * exponentials). Z is [N][ld] row-major, bf16 (z_fp32 = 0) or fp32 (z_fp32 = 1),
+ * ld >= V and a multiple of 8 (bf16) or 4 (fp32) elements. Writes lse[N] and
+ * the loss under `reduction` (as above); when dZ is not NULL it also writes
+ * dZ = (softmax(Z) - onehot(y)) * scale in Z's dtype, with the same layout
+ * (dZ == Z computes the gradient in place). Work: one read of Z (forward) or
+ * two reads and one write (with dZ); bound by HBM bandwidth. The workspace is
+ * lce_ce_logits_workspace_size(N) bytes; device status as for lce_forward. */
+lce_status lce_ce_logits_workspace_size(int64_t N, size_t *bytes);
+lce_status lce_ce_logits(const void *Z, int z_fp32, int64_t ld, const int64_t *y,
+                         int64_t N, int64_t V, int64_t ignore_index, int reduction,
+                         const float *dloss, float *loss, float *lse, void *dZ,
+                         void *ws, size_t ws_bytes, lce_stream_t stream);
+
 /* Synchronises `stream`, then returns the device-side status recorded in the
  * workspace by the last call that used it (LCE_OK, LCE_ERR_LABEL_RANGE or
  * LCE_ERR_TIMEOUT; a timeout wins over a label error) and clears it. Returns

@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     LCEError,
     LinearCrossEntropyFunction,
     alloc_workspace,
+    ce_logits,
     last_launch_count,
     lce_backward,
     lce_forward,

@@ -37,6 +37,8 @@ EXPORTED = (
     "lce_forward_ex",
     "lce_backward_ex",
     "lce_fwd_bwd_ex",
+    "lce_ce_logits_workspace_size",
+    "lce_ce_logits",
     "lce_read_status",
     "lce_status_string",
     "lce_version",
@@ -91,6 +93,9 @@ def lib() -> ctypes.CDLL:
                                   ctypes.c_int, _vp, ctypes.c_size_t, _vp]
     L.lce_fwd_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
                                  _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    L.lce_ce_logits_workspace_size.argtypes = [_i64, ctypes.POINTER(ctypes.c_size_t)]
+    L.lce_ce_logits.argtypes = [_vp, ctypes.c_int, _i64, _vp, _i64, _i64, _i64, ctypes.c_int, _vp,
+                                _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     L.lce_read_status.argtypes = [_vp, _vp]
     L.lce_status_string.argtypes = [ctypes.c_int]
     L.lce_status_string.restype = ctypes.c_char_p
@@ -103,7 +108,8 @@ def lib() -> ctypes.CDLL:
     L.lce_profile_reset.restype = None
     for name in ("lce_profile_enable", "lce_profile_read", "lce_workspace_size", "lce_forward",
                  "lce_backward", "lce_fwd_bwd", "lce_forward_ex", "lce_backward_ex",
-                 "lce_fwd_bwd_ex", "lce_read_status", "lce_version", "lce_last_launch_count"):
+                 "lce_fwd_bwd_ex", "lce_read_status", "lce_version", "lce_last_launch_count",
+                 "lce_ce_logits_workspace_size", "lce_ce_logits"):
         getattr(L, name).restype = ctypes.c_int
     _LIB = L
     return L
@@ -232,6 +238,39 @@ def lce_fwd_bwd(H, W, y, dloss=None, chunk: int = 1024, ignore_index: int = IGNO
                               ws.numel(), _stream(stream))
     _check(st, "lce_fwd_bwd")
     return loss, lse, dH, dW
+
+
+def ce_logits(Z, y, dloss=None, ignore_index: int = IGNORE_INDEX, reduction: str = "mean",
+              grad: bool = True, inplace: bool = False, loss=None, lse=None, ws=None, stream=None):
+    """Cross-entropy over precomputed logits Z [N, V] (bf16 or fp32, row stride may
+    exceed V): (loss, lse, dZ). dZ is None when grad is False; with inplace=True
+    it overwrites Z."""
+    if not (Z.is_cuda and y.is_cuda):
+        raise ValueError("Z and y must be CUDA tensors (there is no CPU path)")
+    if Z.dtype not in (torch.bfloat16, torch.float32) or y.dtype != torch.int64:
+        raise TypeError("Z must be bfloat16 or float32 and y int64")
+    if Z.dim() != 2 or Z.stride(1) != 1 or y.dim() != 1 or y.shape[0] != Z.shape[0]:
+        raise ValueError("expected Z[N, V] with unit column stride and y[N]")
+    N, V = Z.shape
+    ld = Z.stride(0) if N > 1 else V
+    dev = Z.device
+    red = _reduction(reduction)
+    loss = _loss_buffer(loss, N, reduction, dev)
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    dZ = None
+    if grad:
+        dZ = Z if inplace else torch.empty_strided(Z.shape, Z.stride(), dtype=Z.dtype, device=dev)
+    if ws is None:
+        nbytes = ctypes.c_size_t(0)
+        _check(lib().lce_ce_logits_workspace_size(N, ctypes.byref(nbytes)), "workspace")
+        ws = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
+    _check_dloss(dloss, N, reduction)
+    st = lib().lce_ce_logits(_ptr(Z), 1 if Z.dtype == torch.float32 else 0, ld, _ptr(y), N, V,
+                             ignore_index, red, _ptr(dloss), _ptr(loss), _ptr(lse), _ptr(dZ),
+                             _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "lce_ce_logits")
+    return loss, lse, dZ
 
 
 def read_status(ws: torch.Tensor, stream=None) -> int:

@@ -515,6 +515,63 @@ lce_status lce_fwd_bwd(const void *H, const void *W, const int64_t *y, const flo
                           lse, dH, dW, ws, ws_bytes, stream);
 }
 
+lce_status lce_ce_logits_workspace_size(int64_t N, size_t *bytes) {
+    if (!bytes || N < 0) return LCE_ERR_INVALID_ARG;
+    *bytes = 1024 + align_up(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1), 1024);
+    return LCE_OK;
+}
+
+lce_status lce_ce_logits(const void *Z, int z_fp32, int64_t ld, const int64_t *y, int64_t N,
+                         int64_t V, int64_t ignore_index, int reduction, const float *dloss,
+                         float *loss, float *lse, void *dZ, void *ws, size_t ws_bytes,
+                         lce_stream_t stream) {
+    g_launches = 0;
+    if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
+    const bool none = reduction == LCE_REDUCTION_NONE;
+    if (N < 0 || V <= 0 || ld < V || !ws) return LCE_ERR_INVALID_ARG;
+    if (N > 0 && (!Z || !y || !lse || !loss)) return LCE_ERR_INVALID_ARG;
+    if (!none && !loss) return LCE_ERR_INVALID_ARG;
+    const int vec = z_fp32 ? 4 : 8;
+    if (ld % vec != 0) return LCE_ERR_ALIGNMENT;
+    if ((Z && !aligned16(Z)) || (dZ && !aligned16(dZ)) || !aligned16(ws) ||
+        (loss && !aligned16(loss)) || (lse && !aligned16(lse)) || (y && !aligned16(y)))
+        return LCE_ERR_ALIGNMENT;
+    size_t need = 0;
+    lce_ce_logits_workspace_size(N, &need);
+    if (ws_bytes < need) return LCE_ERR_WORKSPACE;
+    int sms = 0, pairs = 0;
+    lce_status st = init_device(&sms, &pairs);
+    if (st != LCE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    int *hdr = reinterpret_cast<int *>(w);
+    float *loss_rows = reinterpret_cast<float *>(w + 1024);
+    if (cudaMemsetAsync(hdr, 0, 1024, s) != cudaSuccess) return LCE_ERR_CUDA;
+    LCE_LAUNCH_KIND(LCE_KERNEL_OTHER, s,
+                    launch_label_scan(reinterpret_cast<const long long *>(y), N, V, ignore_index, hdr, s));
+    CELogitsParams p;
+    p.Z = Z;
+    p.dZ = dZ;
+    p.ld = ld;
+    p.fp32 = z_fp32 ? 1 : 0;
+    p.N = N;
+    p.V = V;
+    p.ignore_index = ignore_index;
+    p.y = reinterpret_cast<const long long *>(y);
+    p.hdr = hdr;
+    p.dloss = dloss;
+    p.dloss_per_row = none ? 1 : 0;
+    p.mean = reduction == LCE_REDUCTION_MEAN ? 1 : 0;
+    p.lse = lse;
+    p.loss_rows = none ? loss : loss_rows;
+    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, s, launch_ce_logits(p, sms, s));
+    if (!none)
+        LCE_LAUNCH_KIND(LCE_KERNEL_OTHER, s,
+                        launch_loss_finalize(loss_rows, N, hdr, loss,
+                                             reduction == LCE_REDUCTION_MEAN, s));
+    return LCE_OK;
+}
+
 lce_status lce_read_status(const void *ws, lce_stream_t stream) {
     if (!ws) return LCE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -142,6 +142,23 @@ struct FixupParams {
     int mean;
 };
 
+// Cross-entropy over precomputed logits Z [N][ld] (bf16 or fp32), one row at a time.
+struct CELogitsParams {
+    const void *Z;
+    void *dZ;              // null: forward only; may equal Z (gradient written in place)
+    long long ld;          // row stride of Z and dZ (elements)
+    int fp32;              // 0: bf16 logits, 1: fp32 logits
+    long long N, V;
+    long long ignore_index;
+    const long long *y;
+    const int *hdr;
+    const float *dloss;
+    int dloss_per_row;
+    int mean;
+    float *lse;            // [N]
+    float *loss_rows;      // [N]
+};
+
 // launchers (return cudaError_t of the launch)
 // cluster = 1: one CTA per 128 x 256 tile; 2: a CTA pair per 256 x 256 tile
 // (tcgen05 cta_group::2, each CTA loading its own A rows and half of B).
@@ -155,6 +172,7 @@ cudaError_t launch_transpose(const TransposeParams &p, cudaStream_t s);
 cudaError_t launch_fixup(const FixupParams &p, cudaStream_t s);
 cudaError_t launch_loss_finalize(const float *loss_rows, long long N, const int *hdr,
                                  float *loss, int mean, cudaStream_t s);
+cudaError_t launch_ce_logits(const CELogitsParams &p, int sms, cudaStream_t s);
 cudaError_t gemm_set_attributes();
 cudaError_t aux_set_attributes();
 

@@ -168,6 +168,36 @@ def forward_backward(H, W, y, ignore_index: int = IGNORE_INDEX, dloss=1.0,
     return dict(loss=loss, lse=lse, dH=dH, dW=dW, n_valid=n_valid, n_bad=n_bad)
 
 
+def ce_from_logits(Z, y, ignore_index: int = IGNORE_INDEX, dloss=1.0, reduction: str = "mean"):
+    """Steps 2-4 on logits the caller already has (no projection): lse, the loss
+    under `reduction`, and dZ = (softmax(Z) - onehot(y)) * scale. fp64."""
+    Z = as_f64(Z)
+    y = as_labels(y)
+    N, V = Z.shape
+    valid, n_bad = valid_rows(y, V, ignore_index)
+    n_valid = int(valid.sum())
+    lse = row_logsumexp(Z) if N else np.zeros(0)
+    idx = np.nonzero(valid)[0]
+    row_loss = np.zeros(N)
+    row_loss[idx] = lse[idx] - Z[idx, y[idx]]
+    if reduction == "mean":
+        row_scale = np.full(N, (float(dloss) / n_valid) if n_valid else 0.0)
+        loss = float(row_loss.sum()) / n_valid if n_valid else 0.0
+    elif reduction == "sum":
+        row_scale = np.full(N, float(dloss))
+        loss = float(row_loss.sum())
+    elif reduction == "none":
+        row_scale = np.broadcast_to(np.asarray(dloss, dtype=np.float64), (N,)).copy()
+        loss = row_loss
+    else:
+        raise ValueError(f"unknown reduction {reduction!r}")
+    dZ = np.exp(Z - lse[:, None]) if N else np.zeros((0, V))
+    dZ[idx, y[idx]] -= 1.0
+    dZ *= row_scale[:, None]
+    dZ[~valid] = 0.0
+    return dict(loss=loss, lse=lse, dZ=dZ, n_valid=n_valid, n_bad=n_bad)
+
+
 # ---------------------------------------------------------------------------
 # Sampled outputs for workloads too large to materialise on the host in a test.
 # Each one is the same definition restricted to the requested rows / columns.

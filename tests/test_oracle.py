@@ -301,6 +301,36 @@ def test_reduction_relations_and_fd():
     assert np.abs(num - r["dH"]).max() <= 1e-6
 
 
+# ------------------------------------------------------- CE over given logits
+
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+def test_ce_from_logits_vs_torch(reduction):
+    rng = np.random.default_rng(41)
+    N, V = 19, 37
+    Z = rng.standard_normal((N, V)) * 4.0
+    y = rng.integers(0, V, size=N)
+    y[[3, 11]] = IGN
+    dl = rng.standard_normal(N) if reduction == "none" else 1.3
+    Zt = torch.tensor(Z, requires_grad=True)
+    out = torch.nn.functional.cross_entropy(Zt, torch.tensor(y), ignore_index=IGN,
+                                            reduction=reduction)
+    (out * torch.as_tensor(dl)).sum().backward()
+    r = O.ce_from_logits(Z, y, dloss=dl, reduction=reduction)
+    assert np.allclose(r["loss"], out.detach().numpy(), atol=1e-12)
+    assert np.allclose(r["dZ"], Zt.grad.numpy(), atol=1e-14)
+    assert np.allclose(r["lse"], torch.logsumexp(torch.tensor(Z), 1).numpy(), atol=1e-12)
+
+
+def test_ce_from_logits_rows_sum_to_zero_and_large_logits():
+    """Rows of dZ sum to 0 for valid rows; logits near +-1000 stay finite."""
+    rng = np.random.default_rng(42)
+    Z = rng.standard_normal((8, 50)) * 400.0
+    y = rng.integers(0, 50, size=8)
+    r = O.ce_from_logits(Z, y, reduction="sum")
+    assert np.all(np.isfinite(r["dZ"])) and np.all(np.isfinite(r["lse"]))
+    assert np.abs(r["dZ"].sum(axis=1)).max() < 1e-12
+
+
 # ------------------------------------------------------- sampled helpers
 
 def test_sampled_helpers_match_full():
