@@ -224,9 +224,10 @@ __global__ void __launch_bounds__(256) lce_transpose_kernel(const TransposeParam
 // vocabulary blocks with a running max and a running sum of exponentials, then
 // (backward) streamed again to write (p - onehot) * scale. A persistent grid of
 // 2 CTAs per SM walks the rows, so the few hundred rows in flight stay in L2
-// between the two passes.
+// between the two passes; each thread keeps CE_UNROLL 16-byte loads in flight.
 
-constexpr int CE_THREADS = 512;
+constexpr int CE_THREADS = 1024;
+constexpr int CE_UNROLL = 4;   // independent 16-byte loads in flight per thread
 
 __device__ __forceinline__ void ce_merge(float &m, float &s, float m2, float s2) {
     const float M = fmaxf(m, m2);
@@ -263,13 +264,15 @@ template <> __device__ __forceinline__ __nv_bfloat16 ce_from_float<__nv_bfloat16
 template <> __device__ __forceinline__ float ce_from_float<float>(float v) { return v; }
 
 template <typename T>
-__global__ void __launch_bounds__(CE_THREADS) lce_ce_logits_kernel(const CELogitsParams p) {
+__global__ void __launch_bounds__(CE_THREADS, 2) lce_ce_logits_kernel(const CELogitsParams p) {
     constexpr int VEC = 16 / sizeof(T);
+    constexpr int STEP = CE_THREADS * VEC;          // elements per block-wide sweep
     __shared__ float s_m[CE_THREADS / 32], s_s[CE_THREADS / 32];
     __shared__ float s_lse;
     const int t = threadIdx.x, w = t >> 5, l = t & 31;
     const int nv = p.hdr[HDR_NVALID];
     const long long vmain = (p.V / VEC) * VEC;     // vectorised part of a row
+    const long long vunroll = (p.V / (STEP * CE_UNROLL)) * (STEP * CE_UNROLL);
     for (long long r = blockIdx.x; r < p.N; r += gridDim.x) {
         const T *row = static_cast<const T *>(p.Z) + r * p.ld;
         const long long yv = p.y[r];
@@ -277,7 +280,23 @@ __global__ void __launch_bounds__(CE_THREADS) lce_ce_logits_kernel(const CELogit
         // the target logit is read before any thread can overwrite it (dZ == Z)
         const float zy = (t == 0 && y_ok) ? static_cast<float>(row[yv]) : 0.f;
         float m = -INFINITY, s = 0.f;
-        for (long long i = static_cast<long long>(t) * VEC; i < vmain; i += CE_THREADS * VEC) {
+        // pass 1: running max and sum of exponentials
+        for (long long i0 = static_cast<long long>(t) * VEC; i0 < vunroll; i0 += STEP * CE_UNROLL) {
+            float x[CE_UNROLL][8];
+#pragma unroll
+            for (int u = 0; u < CE_UNROLL; ++u) ce_vec_load<T>(row, i0 + u * STEP, x[u]);
+#pragma unroll
+            for (int u = 0; u < CE_UNROLL; ++u) {
+                float mv = x[u][0];
+#pragma unroll
+                for (int j = 1; j < VEC; ++j) mv = fmaxf(mv, x[u][j]);
+                float sv = 0.f;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) sv += exp2f((x[u][j] - mv) * LOG2E_F);
+                ce_merge(m, s, mv, sv);
+            }
+        }
+        for (long long i = vunroll + static_cast<long long>(t) * VEC; i < vmain; i += STEP) {
             float x[8];
             ce_vec_load<T>(row, i, x);
             float mv = x[0];
@@ -318,10 +337,29 @@ __global__ void __launch_bounds__(CE_THREADS) lce_ce_logits_kernel(const CELogit
             p.loss_rows[r] = y_ok ? lse - zy : 0.f;
         }
         if (p.dZ) {
+            // pass 2: (p - onehot) * scale in the logits' dtype
             const float scale = lce_row_scale(p.dloss, p.dloss_per_row, p.mean, nv, r, y_ok);
             const float lse2 = lse * LOG2E_F;
             T *drow = static_cast<T *>(p.dZ) + r * p.ld;
-            for (long long i = static_cast<long long>(t) * VEC; i < vmain; i += CE_THREADS * VEC) {
+            for (long long i0 = static_cast<long long>(t) * VEC; i0 < vunroll;
+                 i0 += STEP * CE_UNROLL) {
+                float x[CE_UNROLL][8];
+#pragma unroll
+                for (int u = 0; u < CE_UNROLL; ++u) ce_vec_load<T>(row, i0 + u * STEP, x[u]);
+#pragma unroll
+                for (int u = 0; u < CE_UNROLL; ++u) {
+                    const long long i = i0 + u * STEP;
+                    T out[VEC];
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        float g = exp2f(fmaf(x[u][j], LOG2E_F, -lse2)) * scale;
+                        if (i + j == yv) g -= scale;
+                        out[j] = ce_from_float<T>(g);
+                    }
+                    *reinterpret_cast<uint4 *>(drow + i) = *reinterpret_cast<const uint4 *>(out);
+                }
+            }
+            for (long long i = vunroll + static_cast<long long>(t) * VEC; i < vmain; i += STEP) {
                 float x[8];
                 ce_vec_load<T>(row, i, x);
                 T out[VEC];
@@ -401,7 +439,16 @@ cudaError_t launch_fixup(const FixupParams &p, cudaStream_t s) {
 
 cudaError_t launch_ce_logits(const CELogitsParams &p, int sms, cudaStream_t s) {
     if (p.N <= 0) return cudaSuccess;
-    long long grid = 2ll * sms;
+    // a persistent grid of exactly the CTAs that fit at once (1024 threads each;
+    // the rows in flight stay in L2 between the two passes)
+    int per_sm = 1;
+    cudaError_t e = p.fp32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                 &per_sm, lce_ce_logits_kernel<float>, CE_THREADS, 0)
+                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                 &per_sm, lce_ce_logits_kernel<__nv_bfloat16>, CE_THREADS, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    long long grid = static_cast<long long>(per_sm) * sms;
     if (grid > p.N) grid = p.N;
     if (p.fp32) lce_ce_logits_kernel<float><<<static_cast<int>(grid), CE_THREADS, 0, s>>>(p);
     else lce_ce_logits_kernel<__nv_bfloat16><<<static_cast<int>(grid), CE_THREADS, 0, s>>>(p);
