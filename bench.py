@@ -354,7 +354,7 @@ def kernel_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_cross_entropy_chunked_gb300", "csrc")
-    for f in ("lce_gemm.cu", "lce_internal.h"):
+    for f in ("lce_gemm.cu", "lce_internal.h", "lce_ptx.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -484,7 +484,7 @@ def run_ce_logits(args, wl):
         "data": "synthetic",
         "config": {"workload": f"{wl.name} logits N={N} V={V} bf16 ({N * V * 2 / 1e9:.2f} GB)",
                    "N": N, "V": V, "l2": "logits (4.2 GB) exceed L2"},
-        "roofline": {"kernel": "lce_ce_logits_kernel<bf16>", "bound": "hbm", "achieved": gbs,
+        "roofline": {"kernel": "lce_ce_logits_cluster_kernel<bf16>", "bound": "hbm", "achieved": gbs,
                      "peak": peaks.get("hbm_gbs", 6800.0), "unit": "GB/s",
                      "frac": gbs / peaks.get("hbm_gbs", 6800.0), "traffic": None,
                      "alg_bytes_per_launch": alg_bytes, "launch_ms": kernel_ms,

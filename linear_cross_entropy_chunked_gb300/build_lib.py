@@ -21,8 +21,9 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "liblce_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ["lce_gemm.cu", "lce_aux.cu", "lce_api.cu", "lce_noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "lce_internal.h"), os.path.join(INCLUDE, "lce.h")]
+SOURCES = ["lce_gemm.cu", "lce_aux.cu", "lce_ce.cu", "lce_api.cu", "lce_noalloc.cu"]
+HEADERS = [os.path.join(CSRC, "lce_internal.h"), os.path.join(CSRC, "lce_ptx.cuh"),
+           os.path.join(INCLUDE, "lce.h")]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -63,6 +63,7 @@ lce_status init_device(int *sms, int *pairs) {
         if (major != 10 || minor != 3) return LCE_ERR_UNSUPPORTED;
         if (gemm_set_attributes() != cudaSuccess) return LCE_ERR_CUDA;
         if (aux_set_attributes() != cudaSuccess) return LCE_ERR_CUDA;
+        if (ce_set_attributes() != cudaSuccess) return LCE_ERR_CUDA;
         int np = 0;
         if (gemm_max_pairs(&np) != cudaSuccess) {
             cudaGetLastError();

@@ -17,8 +17,6 @@
 
 namespace lce {
 
-constexpr float LOG2E_F = 1.4426950408889634f;
-
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -218,169 +216,6 @@ __global__ void __launch_bounds__(256) lce_transpose_kernel(const TransposeParam
     }
 }
 
-// ------------------------------------------------------------------ CE over given logits
-// The row kernel of "Unsloth Kernel Architecture ...", section 1 "Fused
-// Cross-Entropy Loss with Logit Streaming": a row of logits is streamed in
-// vocabulary blocks with a running max and a running sum of exponentials, then
-// (backward) streamed again to write (p - onehot) * scale. A persistent grid of
-// 2 CTAs per SM walks the rows, so the few hundred rows in flight stay in L2
-// between the two passes; each thread keeps CE_UNROLL 16-byte loads in flight.
-
-constexpr int CE_THREADS = 1024;
-constexpr int CE_UNROLL = 4;   // independent 16-byte loads in flight per thread
-
-__device__ __forceinline__ void ce_merge(float &m, float &s, float m2, float s2) {
-    const float M = fmaxf(m, m2);
-    if (M == -INFINITY) return;
-    s = s * exp2f((m - M) * LOG2E_F) + s2 * exp2f((m2 - M) * LOG2E_F);
-    m = M;
-}
-
-template <typename T>
-__device__ __forceinline__ int ce_vec_load(const T *row, long long i, float (&x)[8]);
-template <>
-__device__ __forceinline__ int ce_vec_load<__nv_bfloat16>(const __nv_bfloat16 *row, long long i,
-                                                          float (&x)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4 *>(row + i);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[q]));
-        x[2 * q] = f.x;
-        x[2 * q + 1] = f.y;
-    }
-    return 8;
-}
-template <>
-__device__ __forceinline__ int ce_vec_load<float>(const float *row, long long i, float (&x)[8]) {
-    const float4 a = *reinterpret_cast<const float4 *>(row + i);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    return 4;
-}
-template <typename T> __device__ __forceinline__ T ce_from_float(float v);
-template <> __device__ __forceinline__ __nv_bfloat16 ce_from_float<__nv_bfloat16>(float v) {
-    return __float2bfloat16_rn(v);
-}
-template <> __device__ __forceinline__ float ce_from_float<float>(float v) { return v; }
-
-template <typename T>
-__global__ void __launch_bounds__(CE_THREADS, 2) lce_ce_logits_kernel(const CELogitsParams p) {
-    constexpr int VEC = 16 / sizeof(T);
-    constexpr int STEP = CE_THREADS * VEC;          // elements per block-wide sweep
-    __shared__ float s_m[CE_THREADS / 32], s_s[CE_THREADS / 32];
-    __shared__ float s_lse;
-    const int t = threadIdx.x, w = t >> 5, l = t & 31;
-    const int nv = p.hdr[HDR_NVALID];
-    const long long vmain = (p.V / VEC) * VEC;     // vectorised part of a row
-    const long long vunroll = (p.V / (STEP * CE_UNROLL)) * (STEP * CE_UNROLL);
-    for (long long r = blockIdx.x; r < p.N; r += gridDim.x) {
-        const T *row = static_cast<const T *>(p.Z) + r * p.ld;
-        const long long yv = p.y[r];
-        const bool y_ok = yv != p.ignore_index && yv >= 0 && yv < p.V;
-        // the target logit is read before any thread can overwrite it (dZ == Z)
-        const float zy = (t == 0 && y_ok) ? static_cast<float>(row[yv]) : 0.f;
-        float m = -INFINITY, s = 0.f;
-        // pass 1: running max and sum of exponentials
-        for (long long i0 = static_cast<long long>(t) * VEC; i0 < vunroll; i0 += STEP * CE_UNROLL) {
-            float x[CE_UNROLL][8];
-#pragma unroll
-            for (int u = 0; u < CE_UNROLL; ++u) ce_vec_load<T>(row, i0 + u * STEP, x[u]);
-#pragma unroll
-            for (int u = 0; u < CE_UNROLL; ++u) {
-                float mv = x[u][0];
-#pragma unroll
-                for (int j = 1; j < VEC; ++j) mv = fmaxf(mv, x[u][j]);
-                float sv = 0.f;
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) sv += exp2f((x[u][j] - mv) * LOG2E_F);
-                ce_merge(m, s, mv, sv);
-            }
-        }
-        for (long long i = vunroll + static_cast<long long>(t) * VEC; i < vmain; i += STEP) {
-            float x[8];
-            ce_vec_load<T>(row, i, x);
-            float mv = x[0];
-#pragma unroll
-            for (int j = 1; j < VEC; ++j) mv = fmaxf(mv, x[j]);
-            float sv = 0.f;
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) sv += exp2f((x[j] - mv) * LOG2E_F);
-            ce_merge(m, s, mv, sv);
-        }
-        for (long long i = vmain + t; i < p.V; i += CE_THREADS) {
-            const float x = static_cast<float>(row[i]);
-            ce_merge(m, s, x, 1.f);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-            const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-            ce_merge(m, s, m2, s2);
-        }
-        if (l == 0) { s_m[w] = m; s_s[w] = s; }
-        __syncthreads();
-        if (w == 0) {
-            m = (l < CE_THREADS / 32) ? s_m[l] : -INFINITY;
-            s = (l < CE_THREADS / 32) ? s_s[l] : 0.f;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-                const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-                ce_merge(m, s, m2, s2);
-            }
-            if (l == 0) s_lse = m + logf(s);
-        }
-        __syncthreads();
-        const float lse = s_lse;
-        if (t == 0) {
-            p.lse[r] = lse;
-            p.loss_rows[r] = y_ok ? lse - zy : 0.f;
-        }
-        if (p.dZ) {
-            // pass 2: (p - onehot) * scale in the logits' dtype
-            const float scale = lce_row_scale(p.dloss, p.dloss_per_row, p.mean, nv, r, y_ok);
-            const float lse2 = lse * LOG2E_F;
-            T *drow = static_cast<T *>(p.dZ) + r * p.ld;
-            for (long long i0 = static_cast<long long>(t) * VEC; i0 < vunroll;
-                 i0 += STEP * CE_UNROLL) {
-                float x[CE_UNROLL][8];
-#pragma unroll
-                for (int u = 0; u < CE_UNROLL; ++u) ce_vec_load<T>(row, i0 + u * STEP, x[u]);
-#pragma unroll
-                for (int u = 0; u < CE_UNROLL; ++u) {
-                    const long long i = i0 + u * STEP;
-                    T out[VEC];
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        float g = exp2f(fmaf(x[u][j], LOG2E_F, -lse2)) * scale;
-                        if (i + j == yv) g -= scale;
-                        out[j] = ce_from_float<T>(g);
-                    }
-                    *reinterpret_cast<uint4 *>(drow + i) = *reinterpret_cast<const uint4 *>(out);
-                }
-            }
-            for (long long i = vunroll + static_cast<long long>(t) * VEC; i < vmain; i += STEP) {
-                float x[8];
-                ce_vec_load<T>(row, i, x);
-                T out[VEC];
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    float g = exp2f(fmaf(x[j], LOG2E_F, -lse2)) * scale;
-                    if (i + j == yv) g -= scale;
-                    out[j] = ce_from_float<T>(g);
-                }
-                *reinterpret_cast<uint4 *>(drow + i) = *reinterpret_cast<const uint4 *>(out);
-            }
-            for (long long i = vmain + t; i < p.V; i += CE_THREADS) {
-                float g = exp2f(fmaf(static_cast<float>(row[i]), LOG2E_F, -lse2)) * scale;
-                if (i == yv) g -= scale;
-                drow[i] = ce_from_float<T>(g);
-            }
-        }
-        __syncthreads();   // s_m / s_s / s_lse are reused by the next row
-    }
-}
-
 // ------------------------------------------------------------------ loss
 
 __global__ void __launch_bounds__(1024) lce_loss_finalize_kernel(const float *__restrict__ loss_rows,
@@ -434,24 +269,6 @@ cudaError_t launch_fixup(const FixupParams &p, cudaStream_t s) {
     const int nvec = (p.V + 7) / 8;
     const dim3 grid((nvec + 255) / 256, p.rows < 65535 ? p.rows : 65535);
     lce_fixup_kernel<<<grid, 256, 0, s>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_ce_logits(const CELogitsParams &p, int sms, cudaStream_t s) {
-    if (p.N <= 0) return cudaSuccess;
-    // a persistent grid of exactly the CTAs that fit at once (1024 threads each;
-    // the rows in flight stay in L2 between the two passes)
-    int per_sm = 1;
-    cudaError_t e = p.fp32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                 &per_sm, lce_ce_logits_kernel<float>, CE_THREADS, 0)
-                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                 &per_sm, lce_ce_logits_kernel<__nv_bfloat16>, CE_THREADS, 0);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    long long grid = static_cast<long long>(per_sm) * sms;
-    if (grid > p.N) grid = p.N;
-    if (p.fp32) lce_ce_logits_kernel<float><<<static_cast<int>(grid), CE_THREADS, 0, s>>>(p);
-    else lce_ce_logits_kernel<__nv_bfloat16><<<static_cast<int>(grid), CE_THREADS, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -151,7 +151,7 @@ struct CELogitsParams {
     long long N, V;
     long long ignore_index;
     const long long *y;
-    const int *hdr;
+    int *hdr;              // workspace header: N_valid in, status flags out
     const float *dloss;
     int dloss_per_row;
     int mean;
@@ -175,6 +175,9 @@ cudaError_t launch_loss_finalize(const float *loss_rows, long long N, const int 
 cudaError_t launch_ce_logits(const CELogitsParams &p, int sms, cudaStream_t s);
 cudaError_t gemm_set_attributes();
 cudaError_t aux_set_attributes();
+cudaError_t ce_set_attributes();
+
+constexpr float LOG2E_F = 1.4426950408889634f;
 
 // Largest vocabulary: keeps every TMA coordinate and tile index in int32.
 constexpr long long MAX_V = 1ll << 30;
