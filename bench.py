@@ -350,11 +350,12 @@ def run_ours(args, wl, chunk):
         dist.destroy_process_group()
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files) -> str:
+    """First 16 hex digits of the SHA-256 of the named csrc files, in order."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_cross_entropy_chunked_gb300", "csrc")
-    for f in ("lce_gemm.cu", "lce_internal.h", "lce_ptx.cuh"):
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -362,81 +363,18 @@ def kernel_source_hash() -> str:
 
 def load_traffic():
     """DRAM bytes per launch (scaled to the bench workload) from the committed ncu
-    summary; null when absent or when the kernel source changed since the capture."""
+    summary, per kernel; a kernel is left out when its sources changed since the
+    capture (or the file is absent)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return {}
     with open(p) as f:
         d = json.load(f)
-    if d.get("kernel_source_sha256_16") != kernel_source_hash():
-        return {}
-    return {k: v.get("dram_bytes_per_launch_bench") for k, v in d.get("kernels", {}).items()}
-
-
-def run_e2e(args, lce, H, W, y, chunk, dev, stream, world):
-    """The same metric through the public API from pinned host buffers: every
-    step copies its inputs (H, W, y) host -> device and reads its loss back.
-    The copies of step k+1 run on a copy stream while step k computes (two
-    device input buffers), as a training loop that prefetches its next batch
-    would; the timed region still contains every step's copies."""
-    import torch
-    Hh, Wh, yh = H.pin_memory(), W.pin_memory(), y.pin_memory()
-    bufs = [(torch.empty_like(Hh, device=dev), torch.empty_like(Wh, device=dev),
-             torch.empty_like(yh, device=dev)) for _ in range(2)]
-    N, D = H.shape
-    V = W.shape[0]
-    ws = lce.alloc_workspace(N, D, V, chunk, dev)
-    loss_h = torch.empty(2, dtype=torch.float32).pin_memory()
-    loss = torch.empty(1, dtype=torch.float32, device=dev)
-    lse = torch.empty(N, dtype=torch.float32, device=dev)
-    dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
-    dW = torch.empty(V, D, dtype=torch.float32, device=dev)
-    copy_stream = torch.cuda.Stream(dev)
-    copied = [torch.cuda.Event() for _ in range(2)]
-    consumed = [torch.cuda.Event() for _ in range(2)]
-
-    def h2d(k):
-        b = bufs[k % 2]
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(consumed[k % 2])   # the step that last read this buffer
-            b[0].copy_(Hh, non_blocking=True)
-            b[1].copy_(Wh, non_blocking=True)
-            b[2].copy_(yh, non_blocking=True)
-            copied[k % 2].record(copy_stream)
-
-    def compute(k):
-        b = bufs[k % 2]
-        stream.wait_event(copied[k % 2])
-        lce.lce_fwd_bwd(b[0], b[1], b[2], chunk=chunk, loss=loss, lse=lse, dH=dH, dW=dW, ws=ws,
-                        stream=stream)
-        consumed[k % 2].record(stream)
-        loss_h[k % 2].copy_(loss[0], non_blocking=True)
-
-    def run(steps):
-        h2d(0)
-        for k in range(steps):
-            if k + 1 < steps:
-                h2d(k + 1)
-            compute(k)
-
-    for ev in consumed:
-        ev.record(stream)
-    run(3)
-    torch.cuda.synchronize(dev)
-    steps = max(3, args.steps // 2)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    a.record(stream)
-    copy_stream.wait_event(a)        # the first step's copies start inside the timed region
-    run(steps)
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / steps
-    h2d_bytes = Hh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8
-    return {"value": world * N / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
-            "steps": steps, "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": 4,
-            "note": "every step copies H, W and y from pinned host memory (on a copy stream, "
-                    "overlapping the previous step's compute) and reads its loss back"}
+    out = {}
+    for k, v in d.get("kernels", {}).items():
+        if v.get("sha256_16") == kernel_source_hash(v.get("sources", [])):
+            out[k] = v.get("dram_bytes_per_launch_bench")
+    return out
 
 
 def run_ce_logits(args, wl):
@@ -486,7 +424,8 @@ def run_ce_logits(args, wl):
                    "N": N, "V": V, "l2": "logits (4.2 GB) exceed L2"},
         "roofline": {"kernel": "lce_ce_logits_cluster_kernel<bf16>", "bound": "hbm", "achieved": gbs,
                      "peak": peaks.get("hbm_gbs", 6800.0), "unit": "GB/s",
-                     "frac": gbs / peaks.get("hbm_gbs", 6800.0), "traffic": None,
+                     "frac": gbs / peaks.get("hbm_gbs", 6800.0),
+                     "traffic": load_traffic().get("ce_logits"),
                      "alg_bytes_per_launch": alg_bytes, "launch_ms": kernel_ms,
                      "peak_source": peak_src},
         "gpu_launches": 3 * args.steps,

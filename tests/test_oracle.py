@@ -321,6 +321,66 @@ def test_ce_from_logits_vs_torch(reduction):
     assert np.allclose(r["lse"], torch.logsumexp(torch.tensor(Z), 1).numpy(), atol=1e-12)
 
 
+def check_ce_torch(orc, reduction="mean"):
+    """ce_from_logits against torch cross_entropy(ignore_index=-100) + autograd, fp64."""
+    rng = np.random.default_rng(41)
+    N, V = 19, 37
+    Z = rng.standard_normal((N, V)) * 4.0
+    y = rng.integers(0, V, size=N)
+    y[[3, 11]] = IGN
+    dl = rng.standard_normal(N) if reduction == "none" else 1.3
+    Zt = torch.tensor(Z, requires_grad=True)
+    out = torch.nn.functional.cross_entropy(Zt, torch.tensor(y), ignore_index=IGN,
+                                            reduction=reduction)
+    (out * torch.as_tensor(dl)).sum().backward()
+    r = orc.ce_from_logits(Z, y, dloss=dl, reduction=reduction)
+    assert np.allclose(r["loss"], out.detach().numpy(), atol=1e-12)
+    assert np.allclose(r["dZ"], Zt.grad.numpy(), atol=1e-14)
+    assert np.allclose(r["lse"], torch.logsumexp(torch.tensor(Z), 1).numpy(), atol=1e-12)
+
+
+def check_ce_matches_projection_path(orc):
+    """With Z = H W^T, the CE over logits gives the fused path's loss and lse, and
+    dZ W / dZ^T H are its dH / dW (the chain rule through the projection)."""
+    H, W, y = _rand(23, 7, 29, 5, n_ign=3)
+    r = orc.forward_backward(H, W, y, dloss=0.6)
+    c = orc.ce_from_logits(H @ W.T, y, dloss=0.6)
+    assert abs(c["loss"] - r["loss"]) < 1e-12
+    assert np.allclose(c["lse"], r["lse"], atol=1e-12)
+    assert np.allclose(c["dZ"] @ W, r["dH"], atol=1e-13)
+    assert np.allclose(c["dZ"].T @ H, r["dW"], atol=1e-13)
+
+
+def test_ce_from_logits_matches_projection_path():
+    check_ce_matches_projection_path(O)
+
+
+CE_MUTATIONS = {
+    "CE dropped onehot": ("dZ[idx, y[idx]] -= 1.0", "pass"),
+    "CE loss sign": ("row_loss[idx] = lse[idx] - Z[idx, y[idx]]", "row_loss[idx] = Z[idx, y[idx]] - lse[idx]"),
+    "CE ignored rows not zeroed": ("dZ[~valid] = 0.0", "pass"),
+    "CE softmax without lse": ("dZ = np.exp(Z - lse[:, None]) if N else np.zeros((0, V))",
+                               "dZ = np.exp(Z) if N else np.zeros((0, V))"),
+    "CE sum scaled as mean": ("row_scale = np.full(N, float(dloss))\n",
+                              "row_scale = np.full(N, float(dloss) / max(n_valid, 1))\n"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CE_MUTATIONS))
+def test_ce_pins_catch_planted_mistakes(name):
+    old, new = CE_MUTATIONS[name]
+    m = _mutant(old, new)
+    caught = 0
+    for pin in (lambda o: check_ce_torch(o, "mean"), lambda o: check_ce_torch(o, "sum"),
+                lambda o: check_ce_torch(o, "none"), check_ce_matches_projection_path):
+        try:
+            with np.errstate(all="ignore"):
+                pin(m)
+        except Exception:
+            caught += 1
+    assert caught >= 1, f"no pin caught mutation {name!r}"
+
+
 def test_ce_from_logits_rows_sum_to_zero_and_large_logits():
     """Rows of dZ sum to 0 for valid rows; logits near +-1000 stay finite."""
     rng = np.random.default_rng(42)
