@@ -18,6 +18,13 @@ Recipe for workload k (seed k):
   exactly round(frac * N) rows, chosen by rng.permutation(N), set to -100.
 The draw order is fixed (H, W, labels, ignored rows) so every consumer sees
 identical tensors.
+
+Inputs of the final-RMSNorm path (make_norm_inputs, seed k): the pre-norm
+hidden state X drawn like H and then scaled per row by exp(0.5 * z_i), z_i
+standard normal (rows of different magnitude, as a residual stream has), and
+the RMSNorm weight gamma = 1 + 0.1 * standard normal per channel; then W,
+labels and ignored rows as above. Draw order: X, row scales, gamma, W, labels,
+ignored rows.
 """
 from __future__ import annotations
 
@@ -96,3 +103,28 @@ def workload_inputs(w: Workload | str):
     if isinstance(w, str):
         w = WORKLOADS[w]
     return make_inputs(w.N, w.D, w.V, w.seed, w.labels, w.n_ignored)
+
+
+def make_norm_inputs(N: int, D: int, V: int, seed: int, labels: str = "uniform",
+                     n_ignored: int = 0, w_std: float = 0.02):
+    """Draw (X bf16 [N,D], gamma bf16 [D], W bf16 [V,D], y int64 [N]) on the CPU."""
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((N, D), dtype=np.float32)
+    X *= np.exp(0.5 * rng.standard_normal((N, 1))).astype(np.float32)
+    gamma = (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    W = rng.standard_normal((V, D), dtype=np.float32) * np.float32(w_std)
+    if labels == "uniform":
+        y = rng.integers(0, V, size=N, dtype=np.int64)
+    elif labels == "zipf":
+        y = zipf_labels(rng, N, V)
+    else:
+        raise ValueError(f"unknown label distribution {labels!r}")
+    if n_ignored:
+        y[rng.permutation(N)[:n_ignored]] = IGNORE_INDEX
+    return to_bf16(X), to_bf16(gamma), to_bf16(W), torch.from_numpy(y)
+
+
+def workload_norm_inputs(w: Workload | str):
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    return make_norm_inputs(w.N, w.D, w.V, w.seed, w.labels, w.n_ignored)

@@ -38,6 +38,10 @@ Readings where the pages are silent (each is listed in the design doc too):
     and "none" (per-row losses, 0 for ignored rows; dloss is then a per-row
     vector and row i of G is scaled by dloss[i]).
 
+The module also holds the final RMSNorm that produces H and its backward
+(rmsnorm_forward / rmsnorm_backward / norm_forward_backward), the step before
+the LM head in the same pages.
+
 Pins: tests/test_oracle.py checks this module against closed forms (W = 0),
 invariants (row sums of G, column sums of dW, shift invariance, ignored rows),
 central finite differences, scipy's logsumexp and torch's cross_entropy in fp64.
@@ -196,6 +200,68 @@ def ce_from_logits(Z, y, ignore_index: int = IGNORE_INDEX, dloss=1.0, reduction:
     dZ *= row_scale[:, None]
     dZ[~valid] = 0.0
     return dict(loss=loss, lse=lse, dZ=dZ, n_valid=n_valid, n_bad=n_bad)
+
+
+# ---------------------------------------------------------------------------
+# The final RMSNorm that produces H ("Unsloth Architecture: Manual Triton
+# Backpropagation, Fused Cross-Entropy, and 80% VRAM Cut", pillar 3 "Fused
+# RMSNorm & SwiGLU Kernels": the normalisation x / sqrt(mean x^2 + eps) * gamma
+# and its hand-derived gradient with respect to x).
+# ---------------------------------------------------------------------------
+
+def rmsnorm_forward(X, gamma, eps: float):
+    """h = x * rstd * gamma per row, rstd = 1 / sqrt(mean_i x_i^2 + eps).
+    Returns (H [N, D], rstd [N]) in fp64."""
+    X = as_f64(X)
+    g = as_f64(gamma)
+    ms = np.mean(X * X, axis=1)
+    rstd = 1.0 / np.sqrt(ms + eps)
+    return X * rstd[:, None] * g[None, :], rstd
+
+
+def rmsnorm_backward(X, gamma, eps: float, dH):
+    """Gradient of RMSNorm for the upstream gradient dH. Returns (dX, dgamma), fp64.
+
+    With r = rstd of the row and u = gamma * dH (elementwise):
+        dx = r * u - x * r^3 * (sum_i u_i x_i) / d,      dgamma = sum_rows dH * x * r.
+    Reading: the page writes the leading factor as gamma / RMS(x) and the inner
+    sum as sum_i x_i dL/dy_i; that is this expression when every channel has the
+    same gamma. For a general gamma the derivative needs gamma inside the sum,
+    as here (pinned against autograd and finite differences)."""
+    X = as_f64(X)
+    g = as_f64(gamma)
+    dH = as_f64(dH)
+    d = X.shape[1]
+    rstd = 1.0 / np.sqrt(np.mean(X * X, axis=1) + eps)
+    u = dH * g[None, :]
+    c = np.sum(u * X, axis=1)
+    dX = rstd[:, None] * u - X * (rstd ** 3 * c / d)[:, None]
+    dgamma = np.sum(dH * X * rstd[:, None], axis=0)
+    return dX, dgamma
+
+
+def round_bf16(a: np.ndarray) -> np.ndarray:
+    """Round fp64 values to bf16 (nearest even) and back to fp64."""
+    import torch  # the rounding only
+    return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def norm_forward_backward(X, gamma, eps: float, W, y, ignore_index: int = IGNORE_INDEX,
+                          dloss=1.0, reduction: str = "mean", round_h: bool = True):
+    """RMSNorm -> LM head + cross-entropy -> backward into X, gamma and W.
+
+    H = RMSNorm(X); with round_h the normalised hidden state is rounded to bf16,
+    the dtype it is stored in and multiplied by the projection (the rounding is
+    passed through unchanged by the backward). Then steps 1-5 on H, and dX,
+    dgamma from rmsnorm_backward with the fp64 dH.
+    Returns dict(loss, lse, dX, dgamma, dW, rstd, H, n_valid, n_bad)."""
+    H, rstd = rmsnorm_forward(X, gamma, eps)
+    if round_h:
+        H = round_bf16(H)
+    r = forward_backward(H, W, y, ignore_index=ignore_index, dloss=dloss, reduction=reduction)
+    dX, dgamma = rmsnorm_backward(X, gamma, eps, r["dH"])
+    return dict(loss=r["loss"], lse=r["lse"], dX=dX, dgamma=dgamma, dW=r["dW"], rstd=rstd, H=H,
+                n_valid=r["n_valid"], n_bad=r["n_bad"])
 
 
 # ---------------------------------------------------------------------------

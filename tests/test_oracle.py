@@ -391,6 +391,145 @@ def test_ce_from_logits_rows_sum_to_zero_and_large_logits():
     assert np.abs(r["dZ"].sum(axis=1)).max() < 1e-12
 
 
+# ------------------------------------------------------- final RMSNorm
+
+def _norm_case(seed, N=7, D=12, eps=1e-5):
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((N, D)) * np.exp(rng.standard_normal((N, 1)) * 0.7)
+    gamma = 1.0 + 0.3 * rng.standard_normal(D)
+    dH = rng.standard_normal((N, D))
+    return X, gamma, dH, eps
+
+
+def check_rmsnorm_torch(orc, seed=51):
+    """Forward and backward against torch.nn.functional.rms_norm + autograd, fp64."""
+    X, gamma, dH, eps = _norm_case(seed)
+    Xt = torch.tensor(X, requires_grad=True)
+    gt = torch.tensor(gamma, requires_grad=True)
+    Ht = torch.nn.functional.rms_norm(Xt, (X.shape[1],), gt, eps=eps)
+    (Ht * torch.tensor(dH)).sum().backward()
+    H, rstd = orc.rmsnorm_forward(X, gamma, eps)
+    dX, dgamma = orc.rmsnorm_backward(X, gamma, eps, dH)
+    assert np.allclose(H, Ht.detach().numpy(), atol=1e-13)
+    assert np.allclose(dX, Xt.grad.numpy(), atol=1e-12)
+    assert np.allclose(dgamma, gt.grad.numpy(), atol=1e-12)
+    assert np.allclose(rstd, 1.0 / np.sqrt((X ** 2).mean(axis=1) + eps), atol=1e-14)
+
+
+def check_rmsnorm_fd(orc, seed=52):
+    """Central finite differences of L = sum(dH * RMSNorm(X)) in X and gamma."""
+    X, gamma, dH, eps = _norm_case(seed, N=3, D=5)
+    f = lambda X_, g_: float(np.sum(dH * orc.rmsnorm_forward(X_, g_, eps)[0]))
+    dX, dgamma = orc.rmsnorm_backward(X, gamma, eps, dH)
+    h = 1e-6
+    for idx in np.ndindex(X.shape):
+        Xp = X.copy(); Xp[idx] += h
+        Xm = X.copy(); Xm[idx] -= h
+        assert abs((f(Xp, gamma) - f(Xm, gamma)) / (2 * h) - dX[idx]) < 1e-7
+    for j in range(gamma.size):
+        gp = gamma.copy(); gp[j] += h
+        gm = gamma.copy(); gm[j] -= h
+        assert abs((f(X, gp) - f(X, gm)) / (2 * h) - dgamma[j]) < 1e-7
+
+
+def test_rmsnorm_vs_torch():
+    check_rmsnorm_torch(O)
+
+
+def test_rmsnorm_finite_differences():
+    check_rmsnorm_fd(O)
+
+
+def test_rmsnorm_page_closed_form_with_uniform_gamma():
+    """With the same gamma on every channel the page's closed form (gamma / RMS
+    outside, sum_i x_i dL/dy_i inside) is exact; the oracle agrees with it there."""
+    X, _, dH, eps = _norm_case(53)
+    gamma = np.full(X.shape[1], 1.7)
+    dX, _ = O.rmsnorm_backward(X, gamma, eps, dH)
+    d = X.shape[1]
+    rms = np.sqrt((X ** 2).mean(axis=1) + eps)[:, None]
+    page = gamma / rms * (dH - X * np.sum(X * dH, axis=1, keepdims=True) / (d * rms ** 2))
+    assert np.allclose(dX, page, atol=1e-12)
+
+
+def test_rmsnorm_scale_invariance_without_eps():
+    """eps = 0: RMSNorm(c x) = RMSNorm(x), so dX is orthogonal to x in every row."""
+    X, gamma, dH, _ = _norm_case(54)
+    H1, _ = O.rmsnorm_forward(X, gamma, 0.0)
+    H2, _ = O.rmsnorm_forward(3.5 * X, gamma, 0.0)
+    assert np.allclose(H1, H2, atol=1e-13)
+    dX, _ = O.rmsnorm_backward(X, gamma, 0.0, dH)
+    assert np.abs(np.sum(dX * X, axis=1)).max() < 1e-12
+
+
+def check_norm_composition_torch(orc, seed=55):
+    """RMSNorm -> X W^T -> cross_entropy(ignore_index) in fp64 autograd against
+    norm_forward_backward without the bf16 rounding of H."""
+    rng = np.random.default_rng(seed)
+    N, D, V = 21, 10, 17
+    X = rng.standard_normal((N, D)) * 2.0
+    gamma = 1.0 + 0.2 * rng.standard_normal(D)
+    W = rng.standard_normal((V, D)) * 0.5
+    y = rng.integers(0, V, size=N)
+    y[[2, 9]] = IGN
+    Xt = torch.tensor(X, requires_grad=True)
+    gt = torch.tensor(gamma, requires_grad=True)
+    Wt = torch.tensor(W, requires_grad=True)
+    H = torch.nn.functional.rms_norm(Xt, (D,), gt, eps=1e-6)
+    loss = torch.nn.functional.cross_entropy(H @ Wt.T, torch.tensor(y), ignore_index=IGN)
+    (loss * 0.8).backward()
+    r = orc.norm_forward_backward(X, gamma, 1e-6, W, y, dloss=0.8, round_h=False)
+    assert abs(r["loss"] - loss.item()) < 1e-12
+    assert np.allclose(r["dX"], Xt.grad.numpy(), atol=1e-13)
+    assert np.allclose(r["dgamma"], gt.grad.numpy(), atol=1e-13)
+    assert np.allclose(r["dW"], Wt.grad.numpy(), atol=1e-13)
+
+
+def test_norm_composition_vs_torch():
+    check_norm_composition_torch(O)
+
+
+def test_norm_round_h_is_bf16_of_exact_h():
+    rng = np.random.default_rng(56)
+    X = rng.standard_normal((6, 16))
+    gamma = 1.0 + 0.1 * rng.standard_normal(16)
+    W = rng.standard_normal((9, 16)) * 0.1
+    y = rng.integers(0, 9, size=6)
+    r = O.norm_forward_backward(X, gamma, 1e-5, W, y)
+    H, _ = O.rmsnorm_forward(X, gamma, 1e-5)
+    expect = torch.tensor(H).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(r["H"], expect)
+    assert np.abs(r["H"] - H).max() <= 2.0 ** -8 * np.abs(H).max()
+
+
+NORM_MUTATIONS = {
+    "gamma outside the sum (page literal)": (
+        "    u = dH * g[None, :]\n    c = np.sum(u * X, axis=1)\n    dX = rstd[:, None] * u - X * (rstd ** 3 * c / d)[:, None]",
+        "    u = dH * g[None, :]\n    c = np.sum(dH * X, axis=1)\n    dX = rstd[:, None] * u - X * g[None, :] * (rstd ** 3 * c / d)[:, None]"),
+    "r instead of r^3": ("dX = rstd[:, None] * u - X * (rstd ** 3 * c / d)[:, None]",
+                         "dX = rstd[:, None] * u - X * (rstd * c / d)[:, None]"),
+    "dgamma without rstd": ("dgamma = np.sum(dH * X * rstd[:, None], axis=0)", "dgamma = np.sum(dH * X, axis=0)"),
+    "sum instead of mean of squares": ("    ms = np.mean(X * X, axis=1)\n", "    ms = np.sum(X * X, axis=1)\n"),
+    "eps outside the sqrt": ("    rstd = 1.0 / np.sqrt(ms + eps)\n", "    rstd = 1.0 / (np.sqrt(ms) + eps)\n"),
+    "backward drops the cross term": ("dX = rstd[:, None] * u - X * (rstd ** 3 * c / d)[:, None]",
+                                      "dX = rstd[:, None] * u"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(NORM_MUTATIONS))
+def test_norm_pins_catch_planted_mistakes(name):
+    old, new = NORM_MUTATIONS[name]
+    m = _mutant(old, new)
+    caught = 0
+    for pin in (check_rmsnorm_torch, check_rmsnorm_fd, check_norm_composition_torch):
+        try:
+            with np.errstate(all="ignore"):
+                pin(m)
+        except Exception:
+            caught += 1
+    assert caught >= 1, f"no pin caught mutation {name!r}"
+
+
 # ------------------------------------------------------- sampled helpers
 
 def test_sampled_helpers_match_full():
