@@ -40,10 +40,11 @@ def parse():
     ap.add_argument("--chunk", type=int, default=0, help="0: the workload's own chunk")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--path", choices=["fused", "ce-logits"], default="fused",
+    ap.add_argument("--path", choices=["fused", "ce-logits", "norm"], default="fused",
                     help="fused: the LM-head linear + CE forward+backward (the headline); "
-                         "ce-logits: the streaming CE over precomputed bf16 logits of the "
-                         "same workload (gradient in place)")
+                         "ce-logits: the CE over precomputed bf16 logits of the same workload "
+                         "(gradient in place); norm: final RMSNorm + LM head + CE forward and "
+                         "backward into the pre-norm hidden state (lce_norm_fwd_bwd)")
     return ap.parse_args()
 
 
@@ -432,6 +433,116 @@ def run_ce_logits(args, wl):
     }), flush=True)
 
 
+def run_norm(args, wl, chunk):
+    """Final RMSNorm + LM head + cross-entropy, forward and backward to X, gamma and
+    W, on the workload's shape (lce_norm_fwd_bwd). Inputs resident, L2 flushed
+    between steps. The roofline is the gradient GEMM's, as on the fused path; the
+    RMSNorm kernels are reported against HBM."""
+    import torch
+    import linear_cross_entropy_chunked_gb300 as lce
+    from lce_synth import make_norm_inputs
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    dev = torch.device("cuda", torch.cuda.current_device())
+    lce.build()
+    peaks, peak_src = load_peaks()
+    N, D, V = wl.N, wl.D, wl.V
+    X, g, W, y = make_norm_inputs(N, D, V, wl.seed, wl.labels, wl.n_ignored)
+    Xd, gd, Wd, yd = X.to(dev), g.to(dev), W.to(dev), y.to(dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    ws = torch.empty(lce.norm_workspace_size(N, D, V, chunk), dtype=torch.uint8, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return lce.norm_fwd_bwd(Xd, gd, Wd, yd, eps=1e-6, chunk=chunk, ws=ws, loss=loss, lse=lse,
+                                stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if lce.read_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    launches = lce.last_launch_count()
+    lce.profile_reset()
+    lce.profile_enable(True)
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    lce.profile_enable(False)
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    grad_ms, grad_n = lce.profile_read("grad")
+    norm_ms, norm_n = lce.profile_read("norm")
+    nchunks = (N + chunk - 1) // chunk
+    grad_flops = 4.0 * D * V * N / nchunks
+    grad_avg = grad_ms / max(grad_n, 1)
+    peak_sust = peaks.get("bf16_tflops_sustained", 1700.0)
+    # RMSNorm kernels per step: forward reads X and writes H (bf16); backward reads
+    # X (bf16) and dH (fp32) and writes dX (bf16)
+    norm_bytes = N * D * (2 + 2) + N * D * (2 + 4 + 2)
+    norm_step_ms = norm_ms / args.steps
+    norm_gbs = norm_bytes / (norm_step_ms / 1e3) / 1e9
+    hbm = peaks.get("hbm_gbs", 6800.0)
+
+    # the standalone RMSNorm kernels over all N rows at once (forward, then the
+    # backward from an fp32 dH): algorithmic bytes as above
+    dH32 = torch.randn(N, D, device=dev, generator=torch.Generator(device=dev).manual_seed(5))
+    Hs = torch.empty_like(Xd)
+    bws = torch.empty(4 * 256 * D, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        lce.rmsnorm_forward(Xd, gd, eps=1e-6)
+        lce.rmsnorm_backward(Xd, gd, dH32, eps=1e-6, ws=bws)
+    torch.cuda.synchronize(dev)
+    lce.profile_reset()
+    lce.profile_enable(True)
+    for _ in range(args.steps):
+        flush.zero_()
+        lce.rmsnorm_forward(Xd, gd, eps=1e-6)
+        flush.zero_()
+        lce.rmsnorm_backward(Xd, gd, dH32, eps=1e-6, ws=bws)
+    torch.cuda.synchronize(dev)
+    lce.profile_enable(False)
+    sa_ms, sa_n = lce.profile_read("norm")
+    sa_step = sa_ms / args.steps
+    sa_gbs = norm_bytes / (sa_step / 1e3) / 1e9
+    del dH32, Hs
+
+    print(json.dumps({
+        "metric": "RMSNorm + LM head + CE fwd+bwd (to X, gamma, W) tokens/s",
+        "value": N / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(wl, chunk, l2="L2 flushed between steps (256 MB write)"),
+                       eps=1e-6, gamma="1 + 0.1 N(0,1)", x_rows="N(0,1) * exp(0.5 N(0,1)) per row"),
+        "tflops": 6.0 * N * D * V / (ms / 1e3) / 1e12,
+        "roofline": {"kernel": "lce_gemm_kernel<MODE_BWD> (dH+dW tiles)", "bound": "tensor",
+                     "achieved": grad_flops / (grad_avg / 1e3) / 1e12, "peak": peak_sust,
+                     "unit": "TFLOP/s", "frac": grad_flops / (grad_avg / 1e3) / 1e12 / peak_sust,
+                     "traffic": None, "launch_ms": grad_avg},
+        "norm_kernels": {"ms_per_step": norm_step_ms, "launches_per_step": norm_n / args.steps,
+                         "alg_bytes_per_step": norm_bytes, "achieved_gbs": norm_gbs,
+                         "peak_gbs": hbm, "frac": norm_gbs / hbm, "share": norm_step_ms / ms,
+                         "what": "per-chunk launches inside lce_norm_fwd_bwd (1024 rows each)"},
+        "norm_kernels_standalone": {"ms_fwd_plus_bwd": sa_step, "launches": sa_n / args.steps,
+                                    "alg_bytes": norm_bytes, "achieved_gbs": sa_gbs,
+                                    "peak_gbs": hbm, "frac": sa_gbs / hbm,
+                                    "what": "lce_rmsnorm_forward + lce_rmsnorm_backward (fp32 dH) "
+                                            "over all N rows, L2 flushed before each"},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+    }), flush=True)
+
+
 def cpu_baseline(wl):
     H64, W64, y = prepare_oracle_inputs(wl)
     rows = calibrate_rows(wl, H64, W64, y, target_s=40.0)
@@ -450,6 +561,8 @@ def main():
         run_reference(args, wl, chunk)
     elif args.path == "ce-logits":
         run_ce_logits(args, wl)
+    elif args.path == "norm":
+        run_norm(args, wl, chunk)
     else:
         run_ours(args, wl, chunk)
 

@@ -124,14 +124,57 @@ lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const 
  * ld >= V and a multiple of 8 (bf16) or 4 (fp32) elements. Writes lse[N] and
  * the loss under `reduction` (as above); when dZ is not NULL it also writes
  * dZ = (softmax(Z) - onehot(y)) * scale in Z's dtype, with the same layout
- * (dZ == Z computes the gradient in place). Work: one read of Z (forward) or
- * two reads and one write (with dZ); bound by HBM bandwidth. The workspace is
- * lce_ce_logits_workspace_size(N) bytes; device status as for lce_forward. */
+ * (dZ == Z computes the gradient in place). Work: one read of Z, plus one write
+ * with dZ, for V up to 524288 (bf16) / 262144 (fp32); larger rows take a second
+ * read. Bound by HBM bandwidth. The workspace is lce_ce_logits_workspace_size(N)
+ * bytes; device status as for lce_forward. */
 lce_status lce_ce_logits_workspace_size(int64_t N, size_t *bytes);
 lce_status lce_ce_logits(const void *Z, int z_fp32, int64_t ld, const int64_t *y,
                          int64_t N, int64_t V, int64_t ignore_index, int reduction,
                          const float *dloss, float *loss, float *lse, void *dZ,
                          void *ws, size_t ws_bytes, lce_stream_t stream);
+
+/* The final RMSNorm in front of the LM head ("Unsloth Architecture: Manual
+ * Triton Backpropagation, Fused Cross-Entropy, and 80% VRAM Cut", pillar 3
+ * "Fused RMSNorm & SwiGLU Kernels"): per row of X [N][D] (bf16, row-major),
+ *   H = X * r * gamma,  r = 1 / sqrt(mean(X^2) + eps),  gamma [D] bf16.
+ * D must be a multiple of 8 and at most 8192; pointers 16-byte aligned.
+ *
+ * lce_rmsnorm_forward: writes H [N][D] bf16 and, if rstd is not NULL, r [N] fp32.
+ * No workspace.
+ *
+ * lce_rmsnorm_backward: for the upstream gradient dH [N][D] (bf16, or fp32 when
+ * dh_fp32 = 1) writes dX [N][D] bf16 and dgamma [D] fp32:
+ *   dX = r * (gamma * dH) - X * r^3 * (sum_i gamma_i dH_i X_i) / D,
+ *   dgamma = sum over rows of dH * X * r.
+ * (The page prints the first line with gamma outside the sum, which is exact
+ * only for a uniform gamma; this is the exact derivative.) r is recomputed from
+ * X (nothing else is kept from the forward). The workspace is
+ * lce_rmsnorm_backward_workspace_size(D) bytes (the dgamma partials); results
+ * are deterministic. Bound by HBM bandwidth. */
+lce_status lce_rmsnorm_forward(const void *X, const void *gamma, int64_t N, int64_t D, float eps,
+                               void *H, float *rstd, lce_stream_t stream);
+lce_status lce_rmsnorm_backward_workspace_size(int64_t D, size_t *bytes);
+lce_status lce_rmsnorm_backward(const void *X, const void *gamma, const void *dH, int dh_fp32,
+                                int64_t N, int64_t D, float eps, void *dX, float *dgamma,
+                                void *ws, size_t ws_bytes, lce_stream_t stream);
+
+/* RMSNorm + LM head + cross-entropy, forward and backward in one call: the
+ * chunked path of lce_fwd_bwd_ex applied to H = RMSNorm(X), returning the
+ * gradients of the pre-norm X and of gamma instead of dH. Per chunk the rows
+ * are normalised into a chunk-sized buffer, the chunk's dH is kept in fp32 and
+ * fed to the RMSNorm backward at once, so neither H nor dH exists for all N
+ * rows. Outputs: loss and lse as for lce_fwd_bwd_ex (reduction MEAN / SUM /
+ * NONE), dX [N][D] bf16, dgamma [D] fp32, dW [V][D] fp32 (overwritten). The
+ * workspace is lce_norm_workspace_size(N, D, V, chunk) bytes: that of
+ * lce_workspace_size plus the chunk's H (bf16) and dH (fp32) and the dgamma
+ * partials. Device status as for lce_fwd_bwd. */
+lce_status lce_norm_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk, size_t *bytes);
+lce_status lce_norm_fwd_bwd(const void *X, const void *gamma, float eps, const void *W,
+                            const int64_t *y, const float *dloss, int64_t N, int64_t D, int64_t V,
+                            int64_t ignore_index, int64_t chunk, int reduction, float *loss,
+                            float *lse, void *dX, float *dgamma, float *dW, void *ws,
+                            size_t ws_bytes, lce_stream_t stream);
 
 /* Synchronises `stream`, then returns the device-side status recorded in the
  * workspace by the last call that used it (LCE_OK, LCE_ERR_LABEL_RANGE or
@@ -160,7 +203,8 @@ enum {
     LCE_KERNEL_GRAD = 1,     /* dH + dW gradient GEMM tiles */
     LCE_KERNEL_MERGE = 2,    /* slab merge (lse, row loss, G rescale) */
     LCE_KERNEL_OTHER = 3,    /* label scan, loss finalisation */
-    LCE_KERNEL_KINDS = 4
+    LCE_KERNEL_NORM = 4,     /* RMSNorm forward / backward row kernels, dgamma reduction */
+    LCE_KERNEL_KINDS = 5
 };
 lce_status lce_profile_enable(int on);
 lce_status lce_profile_read(int kind, double *total_ms, int64_t *launches);

@@ -9,6 +9,7 @@ from ._binding import (  # noqa: F401
     KERNEL_KINDS,
     LCEError,
     LinearCrossEntropyFunction,
+    NormLinearCrossEntropyFunction,
     alloc_workspace,
     ce_logits,
     last_launch_count,
@@ -17,10 +18,15 @@ from ._binding import (  # noqa: F401
     lce_fwd_bwd,
     lib,
     linear_cross_entropy,
+    norm_fwd_bwd,
+    norm_linear_cross_entropy,
+    norm_workspace_size,
     profile_enable,
     profile_read,
     profile_reset,
     read_status,
+    rmsnorm_backward,
+    rmsnorm_forward,
     workspace_size,
 )
 from .build_lib import LIB_PATH, build  # noqa: F401

@@ -39,6 +39,11 @@ EXPORTED = (
     "lce_fwd_bwd_ex",
     "lce_ce_logits_workspace_size",
     "lce_ce_logits",
+    "lce_rmsnorm_forward",
+    "lce_rmsnorm_backward_workspace_size",
+    "lce_rmsnorm_backward",
+    "lce_norm_workspace_size",
+    "lce_norm_fwd_bwd",
     "lce_read_status",
     "lce_status_string",
     "lce_version",
@@ -48,7 +53,7 @@ EXPORTED = (
     "lce_profile_reset",
 )
 
-KERNEL_KINDS = {"logits": 0, "grad": 1, "merge": 2, "other": 3}
+KERNEL_KINDS = {"logits": 0, "grad": 1, "merge": 2, "other": 3, "norm": 4}
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 
@@ -96,6 +101,15 @@ def lib() -> ctypes.CDLL:
     L.lce_ce_logits_workspace_size.argtypes = [_i64, ctypes.POINTER(ctypes.c_size_t)]
     L.lce_ce_logits.argtypes = [_vp, ctypes.c_int, _i64, _vp, _i64, _i64, _i64, ctypes.c_int, _vp,
                                 _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    _f = ctypes.c_float
+    _sz = ctypes.POINTER(ctypes.c_size_t)
+    L.lce_rmsnorm_forward.argtypes = [_vp, _vp, _i64, _i64, _f, _vp, _vp, _vp]
+    L.lce_rmsnorm_backward_workspace_size.argtypes = [_i64, _sz]
+    L.lce_rmsnorm_backward.argtypes = [_vp, _vp, _vp, ctypes.c_int, _i64, _i64, _f, _vp, _vp, _vp,
+                                       ctypes.c_size_t, _vp]
+    L.lce_norm_workspace_size.argtypes = [_i64, _i64, _i64, _i64, _sz]
+    L.lce_norm_fwd_bwd.argtypes = [_vp, _vp, _f, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                   ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     L.lce_read_status.argtypes = [_vp, _vp]
     L.lce_status_string.argtypes = [ctypes.c_int]
     L.lce_status_string.restype = ctypes.c_char_p
@@ -109,7 +123,9 @@ def lib() -> ctypes.CDLL:
     for name in ("lce_profile_enable", "lce_profile_read", "lce_workspace_size", "lce_forward",
                  "lce_backward", "lce_fwd_bwd", "lce_forward_ex", "lce_backward_ex",
                  "lce_fwd_bwd_ex", "lce_read_status", "lce_version", "lce_last_launch_count",
-                 "lce_ce_logits_workspace_size", "lce_ce_logits"):
+                 "lce_ce_logits_workspace_size", "lce_ce_logits", "lce_rmsnorm_forward",
+                 "lce_rmsnorm_backward_workspace_size", "lce_rmsnorm_backward",
+                 "lce_norm_workspace_size", "lce_norm_fwd_bwd"):
         getattr(L, name).restype = ctypes.c_int
     _LIB = L
     return L
@@ -271,6 +287,110 @@ def ce_logits(Z, y, dloss=None, ignore_index: int = IGNORE_INDEX, reduction: str
                              _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "lce_ce_logits")
     return loss, lse, dZ
+
+
+def _check_norm_inputs(X, gamma):
+    if not (X.is_cuda and gamma.is_cuda):
+        raise ValueError("X and gamma must be CUDA tensors (there is no CPU path)")
+    if X.dtype != torch.bfloat16 or gamma.dtype != torch.bfloat16:
+        raise TypeError("X and gamma must be bfloat16")
+    if X.dim() != 2 or gamma.dim() != 1 or gamma.shape[0] != X.shape[1]:
+        raise ValueError("expected X[N, D] and gamma[D]")
+    if not (X.is_contiguous() and gamma.is_contiguous()):
+        raise ValueError("X and gamma must be contiguous")
+
+
+def rmsnorm_forward(X, gamma, eps: float = 1e-6, want_rstd: bool = False, stream=None):
+    """H = X / sqrt(mean(X^2) + eps) * gamma (bf16); with want_rstd also r [N] fp32."""
+    _check_norm_inputs(X, gamma)
+    N, D = X.shape
+    H = torch.empty_like(X)
+    rstd = torch.empty(N, dtype=torch.float32, device=X.device) if want_rstd else None
+    _check(lib().lce_rmsnorm_forward(_ptr(X), _ptr(gamma), N, D, eps, _ptr(H), _ptr(rstd),
+                                     _stream(stream)), "lce_rmsnorm_forward")
+    return (H, rstd) if want_rstd else H
+
+
+def rmsnorm_backward(X, gamma, dH, eps: float = 1e-6, ws=None, stream=None):
+    """(dX bf16, dgamma fp32) of RMSNorm for the upstream gradient dH (bf16 or fp32)."""
+    _check_norm_inputs(X, gamma)
+    if dH.shape != X.shape or dH.dtype not in (torch.bfloat16, torch.float32) or not dH.is_contiguous():
+        raise ValueError("dH must be a contiguous bf16 or fp32 tensor shaped like X")
+    N, D = X.shape
+    dX = torch.empty_like(X)
+    dgamma = torch.empty(D, dtype=torch.float32, device=X.device)
+    if ws is None:
+        nbytes = ctypes.c_size_t(0)
+        _check(lib().lce_rmsnorm_backward_workspace_size(D, ctypes.byref(nbytes)), "workspace")
+        ws = torch.empty(nbytes.value, dtype=torch.uint8, device=X.device)
+    _check(lib().lce_rmsnorm_backward(_ptr(X), _ptr(gamma), _ptr(dH),
+                                      1 if dH.dtype == torch.float32 else 0, N, D, eps, _ptr(dX),
+                                      _ptr(dgamma), _ptr(ws), ws.numel(), _stream(stream)),
+           "lce_rmsnorm_backward")
+    return dX, dgamma
+
+
+def norm_workspace_size(N: int, D: int, V: int, chunk: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().lce_norm_workspace_size(N, D, V, chunk, ctypes.byref(out)), "lce_norm_workspace_size")
+    return out.value
+
+
+def norm_fwd_bwd(X, gamma, W, y, eps: float = 1e-6, dloss=None, chunk: int = 1024,
+                 ignore_index: int = IGNORE_INDEX, reduction: str = "mean", ws=None, loss=None,
+                 lse=None, stream=None):
+    """RMSNorm + LM head + cross-entropy, forward and backward in one call:
+    (loss, lse, dX bf16, dgamma fp32, dW fp32)."""
+    _check_norm_inputs(X, gamma)
+    _check_inputs(X, W, y)
+    N, D = X.shape
+    V = W.shape[0]
+    dev = X.device
+    red = _reduction(reduction)
+    loss = _loss_buffer(loss, N, reduction, dev)
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    dX = torch.empty_like(X)
+    dgamma = torch.empty(D, dtype=torch.float32, device=dev)
+    dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = torch.empty(norm_workspace_size(N, D, V, chunk), dtype=torch.uint8, device=dev)
+    _check_dloss(dloss, N, reduction)
+    _check(lib().lce_norm_fwd_bwd(_ptr(X), _ptr(gamma), eps, _ptr(W), _ptr(y), _ptr(dloss), N, D,
+                                  V, ignore_index, chunk, red, _ptr(loss), _ptr(lse), _ptr(dX),
+                                  _ptr(dgamma), _ptr(dW), _ptr(ws), ws.numel(), _stream(stream)),
+           "lce_norm_fwd_bwd")
+    return loss, lse, dX, dgamma, dW
+
+
+class NormLinearCrossEntropyFunction(torch.autograd.Function):
+    """loss = CE(RMSNorm(X; gamma) W^T, y) with reduction mean or sum. The forward
+    runs lce_norm_fwd_bwd (gradients for an upstream gradient of 1); the backward
+    scales them by the incoming gradient, which the loss is linear in."""
+
+    @staticmethod
+    def forward(ctx, X, gamma, W, y, eps, chunk, ignore_index, reduction):
+        loss, _, dX, dgamma, dW = norm_fwd_bwd(X, gamma, W, y, eps=eps, chunk=chunk,
+                                               ignore_index=ignore_index, reduction=reduction)
+        ctx.save_for_backward(dX, dgamma, dW)
+        ctx.dtypes = (gamma.dtype, W.dtype)
+        return loss.reshape(())
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        dX, dgamma, dW = ctx.saved_tensors
+        g = grad_out.to(torch.float32)
+        return ((dX.float() * g).to(dX.dtype), (dgamma * g).to(ctx.dtypes[0]),
+                (dW * g).to(ctx.dtypes[1]), None, None, None, None, None)
+
+
+def norm_linear_cross_entropy(X, gamma, W, y, eps: float = 1e-6, chunk: int = 1024,
+                              ignore_index: int = IGNORE_INDEX, reduction: str = "mean"):
+    """Differentiable CE(RMSNorm(X) W^T, y) for reduction mean / sum (the per-row
+    reduction needs the upstream gradient before the backward: call norm_fwd_bwd)."""
+    if reduction not in ("mean", "sum"):
+        raise ValueError("norm_linear_cross_entropy supports reduction 'mean' or 'sum'")
+    return NormLinearCrossEntropyFunction.apply(X, gamma, W, y, eps, chunk, ignore_index, reduction)
 
 
 def read_status(ws: torch.Tensor, stream=None) -> int:

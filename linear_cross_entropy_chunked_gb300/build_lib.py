@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "liblce_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ["lce_gemm.cu", "lce_aux.cu", "lce_ce.cu", "lce_api.cu", "lce_noalloc.cu"]
+SOURCES = ["lce_gemm.cu", "lce_aux.cu", "lce_ce.cu", "lce_norm.cu", "lce_api.cu", "lce_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "lce_internal.h"), os.path.join(CSRC, "lce_ptx.cuh"),
            os.path.join(INCLUDE, "lce.h")]
 

@@ -120,6 +120,27 @@ bool make_layout(long long N, long long D, long long V, long long chunk, Layout 
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Workspace of the final-RMSNorm path: the loss path's layout, then the chunk's
+// normalised rows H (bf16), the chunk's dH (fp32) and the dgamma partials.
+struct NormLayout {
+    Layout L;
+    size_t off_H = 0, off_dH = 0, off_part = 0, total = 0;
+};
+
+bool make_norm_layout(long long N, long long D, long long V, long long chunk, NormLayout &NL) {
+    if (!make_layout(N, D, V, chunk, NL.L)) return false;
+    if (D > NRM_MAX_D) return false;
+    size_t off = NL.L.total;
+    NL.off_H = off;
+    off += align_up(2 * static_cast<size_t>(NL.L.C) * D, 1024);
+    NL.off_dH = off;
+    off += align_up(4 * static_cast<size_t>(NL.L.C) * D, 1024);
+    NL.off_part = off;
+    off += align_up(4 * static_cast<size_t>(NRM_GRID) * D, 1024);
+    NL.total = off;
+    return true;
+}
+
 // Tensor map over a row-major array (bf16 unless fp32 is asked for) with the
 // 128-byte swizzle of the MMA operand tiles and of the epilogue staging boxes;
 // zero fill out of bounds on loads, clipping on stores.
@@ -174,6 +195,7 @@ struct Ctx {
     int sms;
     int pairs;   // > 0: GEMMs run as CTA pairs (cluster of 2), at most this many at once
     int reduction;       // LCE_REDUCTION_*
+    bool h_chunked;      // H is a chunk-sized buffer (rows 0..C-1), refilled per chunk
     cudaStream_t s;
     CUtensorMap tmH_K, tmW_K, tmW_MN;
 };
@@ -230,7 +252,7 @@ void prof_end(int idx, cudaStream_t s) {
 
 lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
                  int64_t V, int64_t ign, int64_t chunk, void *ws, size_t ws_bytes,
-                 lce_stream_t stream) {
+                 lce_stream_t stream, bool h_chunked = false) {
     g_launches = 0;
     if (!make_layout(N, D, V, chunk, c.L)) return LCE_ERR_INVALID_ARG;
     if (!ws) return LCE_ERR_INVALID_ARG;
@@ -257,10 +279,11 @@ lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t
     c.HT = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_HT);
     c.s = reinterpret_cast<cudaStream_t>(stream);
     c.reduction = LCE_REDUCTION_MEAN;
+    c.h_chunked = h_chunked;
     // with CTA pairs each CTA loads half of a 256-row W tile (multicast to both)
     if (!encode_2d(&c.tmW_K, W, D, V, D * 2, BK, c.pairs > 0 ? BN / 2 : BN)) return LCE_ERR_CUDA;
     if (!encode_2d(&c.tmW_MN, W, D, V, D * 2, 64, BK)) return LCE_ERR_CUDA;
-    if (N > 0 && !encode_2d(&c.tmH_K, H, D, N, D * 2, BK, BM)) return LCE_ERR_CUDA;
+    if (N > 0 && !encode_2d(&c.tmH_K, H, D, h_chunked ? c.L.C : N, D * 2, BK, BM)) return LCE_ERR_CUDA;
     if (cudaMemsetAsync(c.ws, 0, c.L.hdr_bytes, c.s) != cudaSuccess) return LCE_ERR_CUDA;
     LCE_LAUNCH(launch_label_scan(c.y, N, V, ign, c.hdr, c.s));
     return LCE_OK;
@@ -291,6 +314,7 @@ lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, in
     memset(&p, 0, sizeof(p));
     base_params(c, p, row0, rows, slot);
     p.tmA0 = c.tmH_K;
+    p.a_row0 = c.h_chunked ? 0 : static_cast<int>(row0);
     p.tmB0 = c.tmW_K;
     p.m_blocks0 = static_cast<int>(cdiv(rows, BM));
     p.n_blocks0 = static_cast<int>(cdiv(c.V, BN));
@@ -307,12 +331,13 @@ lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, in
     return LCE_OK;
 }
 
-lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void *dH, float *dW,
-                   bool accumulate) {
+// dHc: this chunk's dH rows (bf16, or fp32 when dh_fp32).
+lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void *dHc, bool dh_fp32,
+                   float *dW, bool accumulate) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
     base_params(c, p, row0, rows, slot);
-    const __nv_bfloat16 *Hc = c.H + row0 * c.D;
+    const __nv_bfloat16 *Hc = c.h_chunked ? c.H : c.H + row0 * c.D;
     // the H chunk^T for the K-major B operand of the dW tiles
     TransposeParams tp;
     tp.src = Hc;
@@ -328,8 +353,8 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     if (!encode_2d(&p.tmA1, c.G, c.V, rows, 2ull * c.L.ldg, 64, BK)) return LCE_ERR_CUDA;
     const int cl = c.pairs > 0 ? 2 : 1;
     if (!encode_2d(&p.tmB1, c.HT, rows, c.D, 2ull * c.L.ldt, BK, BN / cl)) return LCE_ERR_CUDA;
-    __nv_bfloat16 *dHc = static_cast<__nv_bfloat16 *>(dH) + row0 * c.D;
-    if (!encode_store_2d(&p.tmS0, dHc, c.D, rows, 2ull * c.D, false)) return LCE_ERR_CUDA;
+    if (!encode_store_2d(&p.tmS0, dHc, c.D, rows, (dh_fp32 ? 4ull : 2ull) * c.D, dh_fp32))
+        return LCE_ERR_CUDA;
     if (!encode_store_2d(&p.tmS1, dW, c.D, c.V, 4ull * c.D, true)) return LCE_ERR_CUDA;
     p.m_blocks0 = static_cast<int>(cdiv(rows, BM));
     p.n_blocks0 = static_cast<int>(cdiv(c.D, BN));
@@ -339,7 +364,8 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     p.k_blocks1 = static_cast<int>(cdiv(rows, BK));
     p.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * p.n_blocks0 +
                     static_cast<int>(cdiv(p.m_blocks1, cl)) * p.n_blocks1;
-    p.dH = static_cast<__nv_bfloat16 *>(dH);
+    p.dH = static_cast<__nv_bfloat16 *>(dHc);
+    p.dh_fp32 = dh_fp32 ? 1 : 0;
     p.dW = dW;
     p.dw_accumulate = accumulate ? 1 : 0;
     const int units = cl == 2 ? c.pairs : c.sms;
@@ -462,7 +488,8 @@ lce_status lce_backward_ex(const void *H, const void *W, const int64_t *y, const
         const long long row0 = k * c.L.C;
         const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
         LCE_TRY(run_logits(c, MODE_G, row0, rows, static_cast<int>(2 * k), lse, dloss));
-        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dH, dW, k > 0));
+        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1),
+                        static_cast<__nv_bfloat16 *>(dH) + row0 * c.D, false, dW, k > 0));
     }
     return LCE_OK;
 }
@@ -500,7 +527,8 @@ lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const 
         LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr));
         LCE_TRY(run_merge(c, true, row0, rows, lse, dloss, rows_out));
         LCE_TRY(run_fixup(c, row0, rows, dloss));
-        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dH, dW, k > 0));
+        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1),
+                        static_cast<__nv_bfloat16 *>(dH) + row0 * c.D, false, dW, k > 0));
     }
     if (!none)
         LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss,
@@ -514,6 +542,141 @@ lce_status lce_fwd_bwd(const void *H, const void *W, const int64_t *y, const flo
                        lce_stream_t stream) {
     return lce_fwd_bwd_ex(H, W, y, dloss, N, D, V, ignore_index, chunk, LCE_REDUCTION_MEAN, loss,
                           lse, dH, dW, ws, ws_bytes, stream);
+}
+
+lce_status lce_rmsnorm_forward(const void *X, const void *gamma, int64_t N, int64_t D, float eps,
+                               void *H, float *rstd, lce_stream_t stream) {
+    g_launches = 0;
+    if (N < 0 || D <= 0 || D % 8 != 0 || D > NRM_MAX_D || !(eps >= 0.f)) return LCE_ERR_INVALID_ARG;
+    if (N > 0 && (!X || !gamma || !H)) return LCE_ERR_INVALID_ARG;
+    if ((X && !aligned16(X)) || (gamma && !aligned16(gamma)) || (H && !aligned16(H)))
+        return LCE_ERR_ALIGNMENT;
+    int sms = 0, pairs = 0;
+    lce_status st = init_device(&sms, &pairs);
+    if (st != LCE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    NormParams p;
+    memset(&p, 0, sizeof(p));
+    p.X = static_cast<const __nv_bfloat16 *>(X);
+    p.gamma = static_cast<const __nv_bfloat16 *>(gamma);
+    p.H = static_cast<__nv_bfloat16 *>(H);
+    p.rstd = rstd;
+    p.rows = N;
+    p.D = static_cast<int>(D);
+    p.eps = eps;
+    LCE_LAUNCH_KIND(LCE_KERNEL_NORM, s, launch_rmsnorm_fwd(p, s));
+    return LCE_OK;
+}
+
+lce_status lce_rmsnorm_backward_workspace_size(int64_t D, size_t *bytes) {
+    if (!bytes || D <= 0 || D % 8 != 0 || D > NRM_MAX_D) return LCE_ERR_INVALID_ARG;
+    *bytes = align_up(4 * static_cast<size_t>(NRM_GRID) * static_cast<size_t>(D), 1024);
+    return LCE_OK;
+}
+
+lce_status lce_rmsnorm_backward(const void *X, const void *gamma, const void *dH, int dh_fp32,
+                                int64_t N, int64_t D, float eps, void *dX, float *dgamma, void *ws,
+                                size_t ws_bytes, lce_stream_t stream) {
+    g_launches = 0;
+    size_t need = 0;
+    if (lce_rmsnorm_backward_workspace_size(D, &need) != LCE_OK || N < 0 || !(eps >= 0.f))
+        return LCE_ERR_INVALID_ARG;
+    if (!gamma || !dgamma || !ws || (N > 0 && (!X || !dH || !dX))) return LCE_ERR_INVALID_ARG;
+    if ((X && !aligned16(X)) || !aligned16(gamma) || (dH && !aligned16(dH)) ||
+        (dX && !aligned16(dX)) || !aligned16(ws))
+        return LCE_ERR_ALIGNMENT;
+    if (ws_bytes < need) return LCE_ERR_WORKSPACE;
+    int sms = 0, pairs = 0;
+    lce_status st = init_device(&sms, &pairs);
+    if (st != LCE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    NormParams p;
+    memset(&p, 0, sizeof(p));
+    p.X = static_cast<const __nv_bfloat16 *>(X);
+    p.gamma = static_cast<const __nv_bfloat16 *>(gamma);
+    p.dH = dH;
+    p.dh_fp32 = dh_fp32 ? 1 : 0;
+    p.dX = static_cast<__nv_bfloat16 *>(dX);
+    p.part = static_cast<float *>(ws);
+    p.first = 1;
+    p.rows = N;
+    p.D = static_cast<int>(D);
+    p.eps = eps;
+    LCE_LAUNCH_KIND(LCE_KERNEL_NORM, s, launch_rmsnorm_bwd(p, s));
+    LCE_LAUNCH_KIND(LCE_KERNEL_NORM, s, launch_dgamma_reduce(p.part, p.D, dgamma, s));
+    return LCE_OK;
+}
+
+lce_status lce_norm_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk, size_t *bytes) {
+    if (!bytes) return LCE_ERR_INVALID_ARG;
+    NormLayout NL;
+    if (!make_norm_layout(N, D, V, chunk, NL)) return LCE_ERR_INVALID_ARG;
+    *bytes = NL.total;
+    return LCE_OK;
+}
+
+lce_status lce_norm_fwd_bwd(const void *X, const void *gamma, float eps, const void *W,
+                            const int64_t *y, const float *dloss, int64_t N, int64_t D, int64_t V,
+                            int64_t ignore_index, int64_t chunk, int reduction, float *loss,
+                            float *lse, void *dX, float *dgamma, float *dW, void *ws,
+                            size_t ws_bytes, lce_stream_t stream) {
+    g_launches = 0;
+    if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
+    const bool none = reduction == LCE_REDUCTION_NONE;
+    NormLayout NL;
+    if (!make_norm_layout(N, D, V, chunk, NL) || !(eps >= 0.f)) return LCE_ERR_INVALID_ARG;
+    if (!gamma || !dgamma || !dW || (!none && !loss) || (N > 0 && (!X || !lse || !dX || !loss)))
+        return LCE_ERR_INVALID_ARG;
+    if ((X && !aligned16(X)) || !aligned16(gamma) || !aligned16(dW) || (dX && !aligned16(dX)) ||
+        (loss && !aligned16(loss)) || (lse && !aligned16(lse)))
+        return LCE_ERR_ALIGNMENT;
+    if (!ws) return LCE_ERR_INVALID_ARG;
+    if (ws_bytes < NL.total) return LCE_ERR_WORKSPACE;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    __nv_bfloat16 *Hbuf = reinterpret_cast<__nv_bfloat16 *>(w + NL.off_H);
+    float *dHbuf = reinterpret_cast<float *>(w + NL.off_dH);
+    float *part = reinterpret_cast<float *>(w + NL.off_part);
+    Ctx c;
+    LCE_TRY(setup(c, Hbuf, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, true));
+    c.reduction = reduction;
+    float *rows_out = none ? loss : c.loss_rows;
+    if (c.L.nchunks == 0) {
+        if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess ||
+            cudaMemsetAsync(dgamma, 0, sizeof(float) * static_cast<size_t>(D), c.s) != cudaSuccess)
+            return LCE_ERR_CUDA;
+    }
+    const __nv_bfloat16 *Xb = static_cast<const __nv_bfloat16 *>(X);
+    __nv_bfloat16 *dXb = static_cast<__nv_bfloat16 *>(dX);
+    for (long long k = 0; k < c.L.nchunks; ++k) {
+        const long long row0 = k * c.L.C;
+        const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
+        NormParams np;
+        memset(&np, 0, sizeof(np));
+        np.X = Xb + row0 * c.D;
+        np.gamma = static_cast<const __nv_bfloat16 *>(gamma);
+        np.H = Hbuf;
+        np.rows = rows;
+        np.D = static_cast<int>(c.D);
+        np.eps = eps;
+        LCE_LAUNCH_KIND(LCE_KERNEL_NORM, c.s, launch_rmsnorm_fwd(np, c.s));
+        LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr));
+        LCE_TRY(run_merge(c, true, row0, rows, lse, dloss, rows_out));
+        LCE_TRY(run_fixup(c, row0, rows, dloss));
+        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dHbuf, true, dW, k > 0));
+        np.H = nullptr;
+        np.dH = dHbuf;
+        np.dh_fp32 = 1;
+        np.dX = dXb + row0 * c.D;
+        np.part = part;
+        np.first = k == 0 ? 1 : 0;
+        LCE_LAUNCH_KIND(LCE_KERNEL_NORM, c.s, launch_rmsnorm_bwd(np, c.s));
+    }
+    if (!none)
+        LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss,
+                                        reduction == LCE_REDUCTION_MEAN, c.s));
+    if (c.L.nchunks > 0)
+        LCE_LAUNCH_KIND(LCE_KERNEL_NORM, c.s, launch_dgamma_reduce(part, static_cast<int>(c.D), dgamma, c.s));
+    return LCE_OK;
 }
 
 lce_status lce_ce_logits_workspace_size(int64_t N, size_t *bytes) {

@@ -377,11 +377,16 @@ __device__ __forceinline__ void epilogue_grad(const GemmParams &p, const Tile &t
     for (int c = 0; c < 4; ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
-        if (tl.type == TILE_MAIN) {
+        if (tl.type == TILE_MAIN && !p.dh_fp32) {
             if (col0 + (c >> 1) * 64 >= p.D) continue;
             if ((c & 1) == 0) st.acquire();
             st.put_bf16((c & 1) * 4, v);
             if (c & 1) st.issue(&p.tmS0, ST_STORE, col0 + (c >> 1) * 64, tl.m0);
+        } else if (tl.type == TILE_MAIN) {
+            if (col0 + c * 32 >= p.D) continue;
+            st.acquire();
+            st.put_f32(v);
+            st.issue(&p.tmS0, ST_STORE, col0 + c * 32, tl.m0);
         } else {
             if (col0 + c * 32 >= p.D) continue;
             st.acquire();
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                     uint64_t *fb = &full_bar[stage];
                     const int kx = kb * BK;
                     const CUtensorMap *ma = (MODE == MODE_BWD && tl.type == TILE_DW) ? &p.tmA1 : &p.tmA0;
-                    const int ya = (MODE == MODE_BWD) ? tl.m0 : p.row0 + tl.m0;
+                    const int ya = (MODE == MODE_BWD) ? tl.m0 : p.a_row0 + tl.m0;
                     const bool b_mn = (MODE == MODE_BWD) && tl.type != TILE_DW;
                     const CUtensorMap *mb = (MODE == MODE_BWD && !b_mn) ? &p.tmB1 : &p.tmB0;
                     // dW tiles read A = G^T straight from the row-major chunk buffer

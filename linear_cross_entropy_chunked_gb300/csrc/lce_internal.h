@@ -80,6 +80,7 @@ struct GemmParams {
     int total_tiles;       // scheduling units: tiles, or tile pairs for CTA pairs
     int rows;              // rows in this chunk
     int row0;              // first global row of this chunk
+    int a_row0;            // logits: row coordinate of the chunk's first row in the H map
     int V, D;
     long long ignore_index;
     const long long *y;    // labels, global [N]
@@ -99,6 +100,7 @@ struct GemmParams {
     __nv_bfloat16 *dH;     // global [N][D]
     float *dW;             // [V][D]
     int dw_accumulate;     // 0: store, 1: add to existing dW
+    int dh_fp32;           // 1: dH tiles stored as fp32 (tmS0 an fp32 map)
     unsigned long long timeout_ns;
 };
 
@@ -159,6 +161,26 @@ struct CELogitsParams {
     float *loss_rows;      // [N]
 };
 
+// final RMSNorm (forward and backward row kernels)
+constexpr int NRM_THREADS = 256;
+constexpr int NRM_GRID = 256;                        // fixed: one dgamma partial slot per CTA
+constexpr long long NRM_MAX_D = NRM_THREADS * 8 * 4; // 4 vectors of 8 bf16 per thread
+
+struct NormParams {
+    const __nv_bfloat16 *X;      // [rows][D]
+    const __nv_bfloat16 *gamma;  // [D]
+    __nv_bfloat16 *H;            // forward output [rows][D]
+    float *rstd;                 // forward output [rows] or null
+    const void *dH;              // backward input [rows][D], bf16 or fp32
+    int dh_fp32;
+    __nv_bfloat16 *dX;           // backward output [rows][D]
+    float *part;                 // backward: [NRM_GRID][D] dgamma partials
+    int first;                   // 1: the partials start from zero
+    long long rows;
+    int D;
+    float eps;
+};
+
 // launchers (return cudaError_t of the launch)
 // cluster = 1: one CTA per 128 x 256 tile; 2: a CTA pair per 256 x 256 tile
 // (tcgen05 cta_group::2, each CTA loading its own A rows and half of B).
@@ -176,6 +198,9 @@ cudaError_t launch_ce_logits(const CELogitsParams &p, int sms, cudaStream_t s);
 cudaError_t gemm_set_attributes();
 cudaError_t aux_set_attributes();
 cudaError_t ce_set_attributes();
+cudaError_t launch_rmsnorm_fwd(const NormParams &p, cudaStream_t s);
+cudaError_t launch_rmsnorm_bwd(const NormParams &p, cudaStream_t s);
+cudaError_t launch_dgamma_reduce(const float *part, int D, float *dgamma, cudaStream_t s);
 
 constexpr float LOG2E_F = 1.4426950408889634f;
 

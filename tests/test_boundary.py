@@ -153,3 +153,54 @@ def test_binding_refuses_cpu_tensors():
     y = torch.zeros(4, dtype=torch.int64)
     with pytest.raises(ValueError):
         pkg.lce_forward(H, W, y)
+
+
+# ---------------------------------------------------------------- final RMSNorm
+
+def test_norm_workspace_sizes(L):
+    N, D, V, chunk = 16384, 4096, 128256, 1024
+    base = ws_size(L, N, D, V, chunk)[1]
+    out = ctypes.c_size_t(0)
+    assert L.lce_norm_workspace_size(N, D, V, chunk, ctypes.byref(out)) == OK
+    # the loss path's workspace + the chunk's H (bf16) and dH (fp32) + 256 dgamma partial rows
+    assert out.value == base + 2 * chunk * D + 4 * chunk * D + 4 * 256 * D
+    assert L.lce_norm_workspace_size(N, 8200, V, chunk, ctypes.byref(out)) == INVALID  # D > 8192
+    assert L.lce_rmsnorm_backward_workspace_size(D, ctypes.byref(out)) == OK
+    assert out.value == 4 * 256 * D
+    assert L.lce_rmsnorm_backward_workspace_size(12, ctypes.byref(out)) == INVALID
+    assert L.lce_rmsnorm_backward_workspace_size(D, None) == INVALID
+
+
+def test_rmsnorm_argument_errors_return_before_launch(L):
+    vp = ctypes.c_void_p
+    f = L.lce_rmsnorm_forward
+    assert f(vp(FAKE), vp(FAKE), 8, 12, 1e-6, vp(FAKE), None, None) == INVALID      # D % 8
+    assert f(vp(FAKE), vp(FAKE), 8, 8200, 1e-6, vp(FAKE), None, None) == INVALID    # D > 8192
+    assert f(vp(FAKE), vp(FAKE), 8, 64, -1.0, vp(FAKE), None, None) == INVALID      # eps < 0
+    assert f(vp(FAKE), vp(FAKE), 8, 64, 1e-6, None, None, None) == INVALID          # null H
+    assert f(vp(FAKE + 2), vp(FAKE), 8, 64, 1e-6, vp(FAKE), None, None) == ALIGN
+    b = L.lce_rmsnorm_backward
+    need = 4 * 256 * 64
+    assert b(vp(FAKE), vp(FAKE), vp(FAKE), 0, 8, 64, 1e-6, vp(FAKE), None, vp(FAKE), need,
+             None) == INVALID                                                        # null dgamma
+    assert b(vp(FAKE), vp(FAKE), vp(FAKE), 1, 8, 64, 1e-6, vp(FAKE), vp(FAKE), vp(FAKE), need - 4,
+             None) == WORKSPACE
+    assert b(vp(FAKE), vp(FAKE), vp(FAKE + 8), 1, 8, 64, 1e-6, vp(FAKE), vp(FAKE), vp(FAKE), need,
+             None) == ALIGN
+
+
+def test_norm_fwd_bwd_argument_errors(L):
+    vp = ctypes.c_void_p
+    N, D, V, chunk = 128, 64, 1000, 64
+    out = ctypes.c_size_t(0)
+    assert L.lce_norm_workspace_size(N, D, V, chunk, ctypes.byref(out)) == OK
+    need = out.value
+
+    def call(dgamma=FAKE, ws_bytes=need, D_=D, X=FAKE):
+        return L.lce_norm_fwd_bwd(vp(X), vp(FAKE), 1e-6, vp(FAKE), vp(FAKE), None, N, D_, V, -100,
+                                  chunk, 0, vp(FAKE), vp(FAKE), vp(FAKE), vp(dgamma), vp(FAKE),
+                                  vp(FAKE), ws_bytes, None)
+    assert call(dgamma=0) == INVALID
+    assert call(D_=12) == INVALID
+    assert call(ws_bytes=need - 1) == WORKSPACE
+    assert call(X=FAKE + 2) == ALIGN
