@@ -116,6 +116,27 @@ lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const 
                           int reduction, float *loss, float *lse, void *dH, float *dW,
                           void *ws, size_t ws_bytes, lce_stream_t stream);
 
+/* Accumulating variants: flags LCE_ACCUMULATE_DW adds this call's dW into the
+ * existing contents of dW (fp32) instead of overwriting it, and
+ * LCE_ACCUMULATE_DH adds dH into the existing bf16 contents of dH (the sum is
+ * formed in fp32 and rounded once), e.g. to accumulate gradients over
+ * micro-batches or over several losses sharing H. With LCE_ACCUMULATE_DH the
+ * workspace is lce_workspace_size_acc(..., flags) bytes (the chunk's dH in fp32,
+ * 4 * chunk * D bytes more); otherwise it is lce_workspace_size(). Other
+ * arguments and outputs as for the _ex entry points. */
+enum { LCE_ACCUMULATE_DW = 1, LCE_ACCUMULATE_DH = 2 };
+lce_status lce_workspace_size_acc(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
+                                  size_t *bytes);
+lce_status lce_backward_acc(const void *H, const void *W, const int64_t *y, const float *lse,
+                            const float *dloss, void *dH, float *dW,
+                            int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                            int reduction, int flags, void *ws, size_t ws_bytes,
+                            lce_stream_t stream);
+lce_status lce_fwd_bwd_acc(const void *H, const void *W, const int64_t *y, const float *dloss,
+                           int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                           int reduction, int flags, float *loss, float *lse, void *dH, float *dW,
+                           void *ws, size_t ws_bytes, lce_stream_t stream);
+
 /* Cross-entropy over logits the caller already has (no projection): the
  * streaming row kernel of "Unsloth Kernel Architecture: Custom Triton
  * Backpropagation and QLoRA Memory Scaling", section 1 (a row of logits
@@ -181,6 +202,15 @@ lce_status lce_norm_fwd_bwd(const void *X, const void *gamma, float eps, const v
  * LCE_ERR_TIMEOUT; a timeout wins over a label error) and clears it. Returns
  * LCE_ERR_CUDA if the stream reports an error. */
 lce_status lce_read_status(const void *ws, lce_stream_t stream);
+
+/* Self-test of the bounded waits (a library diagnostic; the pages have no
+ * counterpart). Clears the first 1024 bytes of ws (a workspace header), then
+ * runs one warp that waits, with the wait the pipelines use, on an mbarrier
+ * nothing signals: after limit_us microseconds (1 .. 2000000) the wait gives up,
+ * records the timeout in the header and the kernel returns.
+ * lce_read_status(ws) then returns LCE_ERR_TIMEOUT and the stream stays usable. */
+lce_status lce_selftest_wait_timeout(void *ws, size_t ws_bytes, int64_t limit_us,
+                                     lce_stream_t stream);
 
 /* Static string for a status code. */
 const char *lce_status_string(lce_status s);

@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     read_status,
     rmsnorm_backward,
     rmsnorm_forward,
+    selftest_wait_timeout,
     workspace_size,
 )
 from .build_lib import LIB_PATH, build  # noqa: F401

@@ -37,6 +37,9 @@ EXPORTED = (
     "lce_forward_ex",
     "lce_backward_ex",
     "lce_fwd_bwd_ex",
+    "lce_workspace_size_acc",
+    "lce_backward_acc",
+    "lce_fwd_bwd_acc",
     "lce_ce_logits_workspace_size",
     "lce_ce_logits",
     "lce_rmsnorm_forward",
@@ -44,6 +47,7 @@ EXPORTED = (
     "lce_rmsnorm_backward",
     "lce_norm_workspace_size",
     "lce_norm_fwd_bwd",
+    "lce_selftest_wait_timeout",
     "lce_read_status",
     "lce_status_string",
     "lce_version",
@@ -98,6 +102,12 @@ def lib() -> ctypes.CDLL:
                                   ctypes.c_int, _vp, ctypes.c_size_t, _vp]
     L.lce_fwd_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
                                  _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    L.lce_workspace_size_acc.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int,
+                                         ctypes.POINTER(ctypes.c_size_t)]
+    L.lce_backward_acc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                   ctypes.c_int, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+    L.lce_fwd_bwd_acc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
+                                  ctypes.c_int, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     L.lce_ce_logits_workspace_size.argtypes = [_i64, ctypes.POINTER(ctypes.c_size_t)]
     L.lce_ce_logits.argtypes = [_vp, ctypes.c_int, _i64, _vp, _i64, _i64, _i64, ctypes.c_int, _vp,
                                 _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
@@ -110,6 +120,7 @@ def lib() -> ctypes.CDLL:
     L.lce_norm_workspace_size.argtypes = [_i64, _i64, _i64, _i64, _sz]
     L.lce_norm_fwd_bwd.argtypes = [_vp, _vp, _f, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                    ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    L.lce_selftest_wait_timeout.argtypes = [_vp, ctypes.c_size_t, _i64, _vp]
     L.lce_read_status.argtypes = [_vp, _vp]
     L.lce_status_string.argtypes = [ctypes.c_int]
     L.lce_status_string.restype = ctypes.c_char_p
@@ -124,6 +135,8 @@ def lib() -> ctypes.CDLL:
                  "lce_backward", "lce_fwd_bwd", "lce_forward_ex", "lce_backward_ex",
                  "lce_fwd_bwd_ex", "lce_read_status", "lce_version", "lce_last_launch_count",
                  "lce_ce_logits_workspace_size", "lce_ce_logits", "lce_rmsnorm_forward",
+                 "lce_workspace_size_acc", "lce_backward_acc", "lce_fwd_bwd_acc",
+                 "lce_selftest_wait_timeout",
                  "lce_rmsnorm_backward_workspace_size", "lce_rmsnorm_backward",
                  "lce_norm_workspace_size", "lce_norm_fwd_bwd"):
         getattr(L, name).restype = ctypes.c_int
@@ -152,8 +165,30 @@ def workspace_size(N: int, D: int, V: int, chunk: int) -> int:
     return out.value
 
 
-def alloc_workspace(N: int, D: int, V: int, chunk: int, device) -> torch.Tensor:
-    return torch.empty(workspace_size(N, D, V, chunk), dtype=torch.uint8, device=device)
+ACCUMULATE = {"dW": 1, "dH": 2}
+
+
+def _acc_flags(accumulate, dH, dW) -> int:
+    flags = 0
+    for name in accumulate:
+        if name not in ACCUMULATE:
+            raise ValueError(f"accumulate takes a subset of {sorted(ACCUMULATE)}, not {name!r}")
+        flags |= ACCUMULATE[name]
+    if (flags & 1 and dW is None) or (flags & 2 and dH is None):
+        raise ValueError("accumulating needs the existing dW / dH tensors passed in")
+    return flags
+
+
+def workspace_size_acc(N: int, D: int, V: int, chunk: int, flags: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().lce_workspace_size_acc(N, D, V, chunk, flags, ctypes.byref(out)),
+           "lce_workspace_size_acc")
+    return out.value
+
+
+def alloc_workspace(N: int, D: int, V: int, chunk: int, device, flags: int = 0) -> torch.Tensor:
+    n = workspace_size_acc(N, D, V, chunk, flags) if flags else workspace_size(N, D, V, chunk)
+    return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def _check_inputs(H, W, y):
@@ -212,33 +247,38 @@ def lce_forward(H, W, y, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
 
 
 def lce_backward(H, W, y, lse, dloss=None, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
-                 dH=None, dW=None, ws=None, stream=None, reduction: str = "mean"):
+                 dH=None, dW=None, ws=None, stream=None, reduction: str = "mean",
+                 accumulate=()):
     """dH (bf16) and dW (fp32) from a saved lse. dloss: scalar tensor, or [N] for
-    reduction="none"; None means 1."""
+    reduction="none"; None means 1. accumulate: a subset of ("dW", "dH") added
+    into the given dW / dH instead of overwriting them."""
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
     red = _reduction(reduction)
+    flags = _acc_flags(accumulate, dH, dW)
     if dH is None:
         dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
     if dW is None:
         dW = torch.empty(V, D, dtype=torch.float32, device=dev)
     if ws is None:
-        ws = alloc_workspace(N, D, V, chunk, dev)
+        ws = alloc_workspace(N, D, V, chunk, dev, flags)
     _check_dloss(dloss, N, reduction)
-    st = lib().lce_backward_ex(_ptr(H), _ptr(W), _ptr(y), _ptr(lse), _ptr(dloss), _ptr(dH),
-                               _ptr(dW), N, D, V, ignore_index, chunk, red, _ptr(ws), ws.numel(),
-                               _stream(stream))
+    st = lib().lce_backward_acc(_ptr(H), _ptr(W), _ptr(y), _ptr(lse), _ptr(dloss), _ptr(dH),
+                                _ptr(dW), N, D, V, ignore_index, chunk, red, flags, _ptr(ws),
+                                ws.numel(), _stream(stream))
     _check(st, "lce_backward")
     return dH, dW
 
 
 def lce_fwd_bwd(H, W, y, dloss=None, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
                 loss=None, lse=None, dH=None, dW=None, ws=None, stream=None,
-                reduction: str = "mean"):
-    """Fused forward + backward: (loss, lse, dH, dW)."""
+                reduction: str = "mean", accumulate=()):
+    """Fused forward + backward: (loss, lse, dH, dW). accumulate: a subset of
+    ("dW", "dH") added into the given dW / dH instead of overwriting them."""
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
     red = _reduction(reduction)
+    flags = _acc_flags(accumulate, dH, dW)
     loss = _loss_buffer(loss, N, reduction, dev)
     if lse is None:
         lse = torch.empty(N, dtype=torch.float32, device=dev)
@@ -247,11 +287,11 @@ def lce_fwd_bwd(H, W, y, dloss=None, chunk: int = 1024, ignore_index: int = IGNO
     if dW is None:
         dW = torch.empty(V, D, dtype=torch.float32, device=dev)
     if ws is None:
-        ws = alloc_workspace(N, D, V, chunk, dev)
+        ws = alloc_workspace(N, D, V, chunk, dev, flags)
     _check_dloss(dloss, N, reduction)
-    st = lib().lce_fwd_bwd_ex(_ptr(H), _ptr(W), _ptr(y), _ptr(dloss), N, D, V, ignore_index,
-                              chunk, red, _ptr(loss), _ptr(lse), _ptr(dH), _ptr(dW), _ptr(ws),
-                              ws.numel(), _stream(stream))
+    st = lib().lce_fwd_bwd_acc(_ptr(H), _ptr(W), _ptr(y), _ptr(dloss), N, D, V, ignore_index,
+                               chunk, red, flags, _ptr(loss), _ptr(lse), _ptr(dH), _ptr(dW),
+                               _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "lce_fwd_bwd")
     return loss, lse, dH, dW
 
@@ -391,6 +431,12 @@ def norm_linear_cross_entropy(X, gamma, W, y, eps: float = 1e-6, chunk: int = 10
     if reduction not in ("mean", "sum"):
         raise ValueError("norm_linear_cross_entropy supports reduction 'mean' or 'sum'")
     return NormLinearCrossEntropyFunction.apply(X, gamma, W, y, eps, chunk, ignore_index, reduction)
+
+
+def selftest_wait_timeout(ws: torch.Tensor, limit_us: int = 20000, stream=None):
+    """Runs the bounded-wait self-test kernel (a wait nothing ends) on ws's device."""
+    _check(lib().lce_selftest_wait_timeout(_ptr(ws), ws.numel(), limit_us, _stream(stream)),
+           "lce_selftest_wait_timeout")
 
 
 def read_status(ws: torch.Tensor, stream=None) -> int:

@@ -127,6 +127,12 @@ struct NormLayout {
     size_t off_H = 0, off_dH = 0, off_part = 0, total = 0;
 };
 
+// Bytes past the loss path's workspace that accumulating into dH needs: the
+// chunk's dH in fp32, added to the caller's dH once the chunk is done.
+size_t acc_dh_bytes(const Layout &L, long long D) {
+    return align_up(4 * static_cast<size_t>(L.C) * static_cast<size_t>(D), 1024);
+}
+
 bool make_norm_layout(long long N, long long D, long long V, long long chunk, NormLayout &NL) {
     if (!make_layout(N, D, V, chunk, NL.L)) return false;
     if (D > NRM_MAX_D) return false;
@@ -435,6 +441,15 @@ lce_status lce_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk, si
     return LCE_OK;
 }
 
+lce_status lce_workspace_size_acc(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
+                                  size_t *bytes) {
+    if (!bytes || (flags & ~(LCE_ACCUMULATE_DW | LCE_ACCUMULATE_DH))) return LCE_ERR_INVALID_ARG;
+    Layout L;
+    if (!make_layout(N, D, V, chunk, L)) return LCE_ERR_INVALID_ARG;
+    *bytes = L.total + ((flags & LCE_ACCUMULATE_DH) ? acc_dh_bytes(L, D) : 0);
+    return LCE_OK;
+}
+
 lce_status lce_forward_ex(const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
                           int64_t V, int64_t ignore_index, int64_t chunk, int reduction,
                           float *loss, float *lse, void *ws, size_t ws_bytes,
@@ -467,31 +482,46 @@ lce_status lce_forward(const void *H, const void *W, const int64_t *y, int64_t N
                           ws_bytes, stream);
 }
 
-lce_status lce_backward_ex(const void *H, const void *W, const int64_t *y, const float *lse,
-                           const float *dloss, void *dH, float *dW, int64_t N, int64_t D,
-                           int64_t V, int64_t ignore_index, int64_t chunk, int reduction,
-                           void *ws, size_t ws_bytes, lce_stream_t stream) {
+lce_status lce_backward_acc(const void *H, const void *W, const int64_t *y, const float *lse,
+                            const float *dloss, void *dH, float *dW, int64_t N, int64_t D,
+                            int64_t V, int64_t ignore_index, int64_t chunk, int reduction,
+                            int flags, void *ws, size_t ws_bytes, lce_stream_t stream) {
     g_launches = 0;
     if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
+    if (flags & ~(LCE_ACCUMULATE_DW | LCE_ACCUMULATE_DH)) return LCE_ERR_INVALID_ARG;
     if (!dW || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
     if (!aligned16(dW) || (dH && !aligned16(dH)) || (lse && !aligned16(lse)))
         return LCE_ERR_ALIGNMENT;
+    const bool acc_dh = (flags & LCE_ACCUMULATE_DH) != 0;
+    Layout L0;
+    if (!make_layout(N, D, V, chunk, L0)) return LCE_ERR_INVALID_ARG;
+    if (acc_dh && ws_bytes < L0.total + acc_dh_bytes(L0, D)) return LCE_ERR_WORKSPACE;
     Ctx c;
     LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream));
     c.reduction = reduction;
-    if (c.L.nchunks == 0) {
+    float *dHacc = reinterpret_cast<float *>(c.ws + c.L.total);
+    if (c.L.nchunks == 0 && !(flags & LCE_ACCUMULATE_DW)) {
         if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess)
             return LCE_ERR_CUDA;
-        return LCE_OK;
     }
     for (long long k = 0; k < c.L.nchunks; ++k) {
         const long long row0 = k * c.L.C;
         const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
+        __nv_bfloat16 *dHc = static_cast<__nv_bfloat16 *>(dH) + row0 * c.D;
         LCE_TRY(run_logits(c, MODE_G, row0, rows, static_cast<int>(2 * k), lse, dloss));
-        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1),
-                        static_cast<__nv_bfloat16 *>(dH) + row0 * c.D, false, dW, k > 0));
+        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), acc_dh ? static_cast<void *>(dHacc) : dHc,
+                        acc_dh, dW, k > 0 || (flags & LCE_ACCUMULATE_DW)));
+        if (acc_dh) LCE_LAUNCH(launch_add_dh(dHacc, dHc, rows * c.D, c.sms, c.s));
     }
     return LCE_OK;
+}
+
+lce_status lce_backward_ex(const void *H, const void *W, const int64_t *y, const float *lse,
+                           const float *dloss, void *dH, float *dW, int64_t N, int64_t D,
+                           int64_t V, int64_t ignore_index, int64_t chunk, int reduction,
+                           void *ws, size_t ws_bytes, lce_stream_t stream) {
+    return lce_backward_acc(H, W, y, lse, dloss, dH, dW, N, D, V, ignore_index, chunk, reduction, 0,
+                            ws, ws_bytes, stream);
 }
 
 lce_status lce_backward(const void *H, const void *W, const int64_t *y, const float *lse,
@@ -502,38 +532,54 @@ lce_status lce_backward(const void *H, const void *W, const int64_t *y, const fl
                            LCE_REDUCTION_MEAN, ws, ws_bytes, stream);
 }
 
-lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const float *dloss,
-                          int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
-                          int reduction, float *loss, float *lse, void *dH, float *dW, void *ws,
-                          size_t ws_bytes, lce_stream_t stream) {
+lce_status lce_fwd_bwd_acc(const void *H, const void *W, const int64_t *y, const float *dloss,
+                           int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                           int reduction, int flags, float *loss, float *lse, void *dH, float *dW,
+                           void *ws, size_t ws_bytes, lce_stream_t stream) {
     g_launches = 0;
     if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
+    if (flags & ~(LCE_ACCUMULATE_DW | LCE_ACCUMULATE_DH)) return LCE_ERR_INVALID_ARG;
     const bool none = reduction == LCE_REDUCTION_NONE;
     if ((!none && !loss) || !dW || (N > 0 && (!lse || !dH || !loss))) return LCE_ERR_INVALID_ARG;
     if ((loss && !aligned16(loss)) || !aligned16(dW) || (dH && !aligned16(dH)) ||
         (lse && !aligned16(lse)))
         return LCE_ERR_ALIGNMENT;
+    const bool acc_dh = (flags & LCE_ACCUMULATE_DH) != 0;
+    Layout L0;
+    if (!make_layout(N, D, V, chunk, L0)) return LCE_ERR_INVALID_ARG;
+    if (acc_dh && ws_bytes < L0.total + acc_dh_bytes(L0, D)) return LCE_ERR_WORKSPACE;
     Ctx c;
     LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream));
     c.reduction = reduction;
     float *rows_out = none ? loss : c.loss_rows;
-    if (c.L.nchunks == 0) {
+    float *dHacc = reinterpret_cast<float *>(c.ws + c.L.total);
+    if (c.L.nchunks == 0 && !(flags & LCE_ACCUMULATE_DW)) {
         if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess)
             return LCE_ERR_CUDA;
     }
     for (long long k = 0; k < c.L.nchunks; ++k) {
         const long long row0 = k * c.L.C;
         const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
+        __nv_bfloat16 *dHc = static_cast<__nv_bfloat16 *>(dH) + row0 * c.D;
         LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr));
         LCE_TRY(run_merge(c, true, row0, rows, lse, dloss, rows_out));
         LCE_TRY(run_fixup(c, row0, rows, dloss));
-        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1),
-                        static_cast<__nv_bfloat16 *>(dH) + row0 * c.D, false, dW, k > 0));
+        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), acc_dh ? static_cast<void *>(dHacc) : dHc,
+                        acc_dh, dW, k > 0 || (flags & LCE_ACCUMULATE_DW)));
+        if (acc_dh) LCE_LAUNCH(launch_add_dh(dHacc, dHc, rows * c.D, c.sms, c.s));
     }
     if (!none)
         LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss,
                                         reduction == LCE_REDUCTION_MEAN, c.s));
     return LCE_OK;
+}
+
+lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const float *dloss,
+                          int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                          int reduction, float *loss, float *lse, void *dH, float *dW, void *ws,
+                          size_t ws_bytes, lce_stream_t stream) {
+    return lce_fwd_bwd_acc(H, W, y, dloss, N, D, V, ignore_index, chunk, reduction, 0, loss, lse,
+                           dH, dW, ws, ws_bytes, stream);
 }
 
 lce_status lce_fwd_bwd(const void *H, const void *W, const int64_t *y, const float *dloss,
@@ -733,6 +779,23 @@ lce_status lce_ce_logits(const void *Z, int z_fp32, int64_t ld, const int64_t *y
         LCE_LAUNCH_KIND(LCE_KERNEL_OTHER, s,
                         launch_loss_finalize(loss_rows, N, hdr, loss,
                                              reduction == LCE_REDUCTION_MEAN, s));
+    return LCE_OK;
+}
+
+lce_status lce_selftest_wait_timeout(void *ws, size_t ws_bytes, int64_t limit_us,
+                                     lce_stream_t stream) {
+    g_launches = 0;
+    if (!ws || ws_bytes < 1024) return LCE_ERR_INVALID_ARG;
+    if (limit_us < 1 || limit_us > 2000000) return LCE_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return LCE_ERR_ALIGNMENT;
+    int sms = 0, pairs = 0;
+    lce_status st = init_device(&sms, &pairs);
+    if (st != LCE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, 1024, s) != cudaSuccess) return LCE_ERR_CUDA;
+    LCE_LAUNCH_KIND(LCE_KERNEL_OTHER, s,
+                    launch_wait_selftest(static_cast<int *>(ws),
+                                         static_cast<unsigned long long>(limit_us) * 1000ull, s));
     return LCE_OK;
 }
 

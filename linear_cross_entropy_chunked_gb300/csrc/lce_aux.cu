@@ -14,6 +14,7 @@
 // Reductions of the loss: mean (sum / N_valid), sum, or none (the per-row losses
 // are the output; G's rows are then scaled by a per-row dloss).
 #include "lce_internal.h"
+#include "lce_ptx.cuh"
 
 namespace lce {
 
@@ -239,6 +240,46 @@ __global__ void __launch_bounds__(1024) lce_loss_finalize_kernel(const float *__
     }
 }
 
+// ------------------------------------------------------------------ dH accumulation
+// dst[rows][D] (bf16) += src[rows][D] (fp32, a chunk's dH), rounded once.
+__global__ void __launch_bounds__(256) lce_add_dh_kernel(const float *__restrict__ src,
+                                                        __nv_bfloat16 *__restrict__ dst,
+                                                        long long nvec) {
+    for (long long i = blockIdx.x * 256ll + threadIdx.x; i < nvec; i += 256ll * gridDim.x) {
+        const float4 a = reinterpret_cast<const float4 *>(src)[2 * i];
+        const float4 b = reinterpret_cast<const float4 *>(src)[2 * i + 1];
+        uint4 d = reinterpret_cast<const uint4 *>(dst)[i];
+        const float s[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t *w = &d.x;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float lo = __uint_as_float(w[q] << 16) + s[2 * q];
+            const float hi = __uint_as_float(w[q] & 0xffff0000u) + s[2 * q + 1];
+            __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+            w[q] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        reinterpret_cast<uint4 *>(dst)[i] = d;
+    }
+}
+
+// ------------------------------------------------------------------ bounded-wait self-test
+// One warp waits, with the same bounded wait the pipelines use, on an mbarrier
+// that nothing signals; the wait runs out after limit_ns, records FLAG_TIMEOUT in
+// the workspace header and the kernel returns. Lets a test check, on the GPU,
+// that a stuck pipeline ends as a status instead of a hang.
+__global__ void __launch_bounds__(32) lce_wait_selftest_kernel(int *hdr, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int s_abort;
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        mbar_init(&bar, 1);   // expects one arrival that never comes
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    const Abort ab{&s_abort, hdr, limit_ns};
+    mbar_wait(&bar, 0, ab);
+}
+
 // ------------------------------------------------------------------ launchers
 
 cudaError_t launch_label_scan(const long long *y, long long N, long long V, long long ign, int *hdr,
@@ -273,6 +314,21 @@ cudaError_t launch_fixup(const FixupParams &p, cudaStream_t s) {
 }
 
 cudaError_t aux_set_attributes() { return cudaSuccess; }
+
+cudaError_t launch_wait_selftest(int *hdr, unsigned long long limit_ns, cudaStream_t s) {
+    lce_wait_selftest_kernel<<<1, 32, 0, s>>>(hdr, limit_ns);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_add_dh(const float *src, __nv_bfloat16 *dst, long long n, int sms,
+                          cudaStream_t s) {
+    const long long nvec = n / 8;
+    if (nvec <= 0) return cudaSuccess;
+    long long blocks = (nvec + 255) / 256;
+    if (blocks > 8ll * sms) blocks = 8ll * sms;
+    lce_add_dh_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(src, dst, nvec);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_loss_finalize(const float *loss_rows, long long N, const int *hdr, float *loss,
                                  int mean, cudaStream_t s) {

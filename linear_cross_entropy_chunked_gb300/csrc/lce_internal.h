@@ -198,6 +198,9 @@ cudaError_t launch_ce_logits(const CELogitsParams &p, int sms, cudaStream_t s);
 cudaError_t gemm_set_attributes();
 cudaError_t aux_set_attributes();
 cudaError_t ce_set_attributes();
+cudaError_t launch_wait_selftest(int *hdr, unsigned long long limit_ns, cudaStream_t s);
+cudaError_t launch_add_dh(const float *src, __nv_bfloat16 *dst, long long n, int sms,
+                          cudaStream_t s);
 cudaError_t launch_rmsnorm_fwd(const NormParams &p, cudaStream_t s);
 cudaError_t launch_rmsnorm_bwd(const NormParams &p, cudaStream_t s);
 cudaError_t launch_dgamma_reduce(const float *part, int D, float *dgamma, cudaStream_t s);

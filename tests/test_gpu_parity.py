@@ -213,3 +213,54 @@ def test_autograd_per_row_losses(lce):
     assert np.abs(to64(rows) - ref["loss"]).max() <= 1e-3 * np.abs(ref["loss"]).max()
     check_grad("dH", to64(Hd.grad), ref["dH"])
     check_grad("dW", to64(Wd.grad), ref["dW"])
+
+
+@pytest.mark.parametrize("acc", [("dW",), ("dH",), ("dW", "dH")])
+def test_accumulate_into_existing_gradients(lce, acc):
+    """accumulate=... adds this call's dW / dH to what the tensors hold."""
+    N, D, V, chunk = 700, 264, 3000, 256
+    H, W, y = make_inputs(N, D, V, seed=31, n_ignored=20, w_std=0.05)
+    gen = torch.Generator().manual_seed(7)
+    dH0 = (torch.randn(N, D, generator=gen) * 1e-4).to(torch.bfloat16).to(DEV)
+    dW0 = (torch.randn(V, D, generator=gen) * 1e-4).to(DEV)
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    dH, dW = dH0.clone(), dW0.clone()
+    loss, lse, dH, dW = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk, dH=dH, dW=dW, accumulate=acc)
+    bdH, bdW = dH0.clone(), dW0.clone()
+    bdH, bdW = lce.lce_backward(Hd, Wd, yd, lse, chunk=chunk, dH=bdH, dW=bdW, accumulate=acc)
+    torch.cuda.synchronize()
+    ref = O.forward_backward(H, W, y)
+    exp_dH = ref["dH"] + (to64(dH0) if "dH" in acc else 0.0)
+    exp_dW = ref["dW"] + (to64(dW0) if "dW" in acc else 0.0)
+    for name, got, exp in (("dH", dH, exp_dH), ("dW", dW, exp_dW), ("dH (backward)", bdH, exp_dH),
+                           ("dW (backward)", bdW, exp_dW)):
+        check_grad(name, to64(got), exp)
+
+
+def test_accumulate_dw_over_micro_batches(lce):
+    """dW summed over two micro-batches (reduction sum) equals the oracle's dW of
+    the whole batch."""
+    N, D, V = 1000, 256, 2000
+    H, W, y = make_inputs(N, D, V, seed=33, n_ignored=30, w_std=0.05)
+    Wd = W.to(DEV)
+    dW = torch.empty(V, D, dtype=torch.float32, device=DEV)
+    half = N // 2
+    lce.lce_fwd_bwd(H[:half].to(DEV), Wd, y[:half].to(DEV), chunk=128, dW=dW, reduction="sum")
+    lce.lce_fwd_bwd(H[half:].to(DEV), Wd, y[half:].to(DEV), chunk=128, dW=dW, reduction="sum",
+                    accumulate=("dW",))
+    torch.cuda.synchronize()
+    ref = O.forward_backward(H, W, y, reduction="sum")
+    check_grad("dW (two micro-batches)", to64(dW), ref["dW"])
+
+
+def test_bounded_wait_times_out_and_context_survives(lce):
+    """A wait that nothing ends gives up after its limit, reports LCE_ERR_TIMEOUT
+    through the workspace, and the device keeps working."""
+    ws = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+    lce.selftest_wait_timeout(ws, limit_us=20000)
+    assert lce.read_status(ws) == 5          # LCE_ERR_TIMEOUT
+    assert lce.read_status(ws) == 0          # cleared
+    H, W, y = make_inputs(200, 64, 500, seed=35)
+    loss, lse = lce.lce_forward(H.to(DEV), W.to(DEV), y.to(DEV), chunk=64)
+    torch.cuda.synchronize()
+    check_loss(loss.item(), O.forward_backward(H, W, y)["loss"])
