@@ -141,16 +141,17 @@ lce_status lce_fwd_bwd_acc(const void *H, const void *W, const int64_t *y, const
  * streaming row kernel of "Unsloth Kernel Architecture: Custom Triton
  * Backpropagation and QLoRA Memory Scaling", section 1 (a row of logits
  * streamed in vocabulary blocks with a running max and a running sum of
- * exponentials). Z is [N][ld] row-major, bf16 (z_fp32 = 0) or fp32 (z_fp32 = 1),
- * ld >= V and a multiple of 8 (bf16) or 4 (fp32) elements. Writes lse[N] and
+ * exponentials). Z is [N][ld] row-major, bf16 (z_dtype = 0), fp32 (z_dtype = 1)
+ * or fp16 (z_dtype = 2), ld >= V and a multiple of 8 (bf16, fp16) or 4 (fp32)
+ * elements. Writes lse[N] and
  * the loss under `reduction` (as above); when dZ is not NULL it also writes
  * dZ = (softmax(Z) - onehot(y)) * scale in Z's dtype, with the same layout
  * (dZ == Z computes the gradient in place). Work: one read of Z, plus one write
- * with dZ, for V up to 524288 (bf16) / 262144 (fp32); larger rows take a second
+ * with dZ, for V up to 524288 (bf16, fp16) / 262144 (fp32); larger rows take a second
  * read. Bound by HBM bandwidth. The workspace is lce_ce_logits_workspace_size(N)
  * bytes; device status as for lce_forward. */
 lce_status lce_ce_logits_workspace_size(int64_t N, size_t *bytes);
-lce_status lce_ce_logits(const void *Z, int z_fp32, int64_t ld, const int64_t *y,
+lce_status lce_ce_logits(const void *Z, int z_dtype, int64_t ld, const int64_t *y,
                          int64_t N, int64_t V, int64_t ignore_index, int reduction,
                          const float *dloss, float *loss, float *lse, void *dZ,
                          void *ws, size_t ws_bytes, lce_stream_t stream);

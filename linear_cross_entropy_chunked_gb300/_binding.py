@@ -296,15 +296,18 @@ def lce_fwd_bwd(H, W, y, dloss=None, chunk: int = 1024, ignore_index: int = IGNO
     return loss, lse, dH, dW
 
 
+_CE_DTYPES = {torch.bfloat16: 0, torch.float32: 1, torch.float16: 2}
+
+
 def ce_logits(Z, y, dloss=None, ignore_index: int = IGNORE_INDEX, reduction: str = "mean",
               grad: bool = True, inplace: bool = False, loss=None, lse=None, ws=None, stream=None):
-    """Cross-entropy over precomputed logits Z [N, V] (bf16 or fp32, row stride may
+    """Cross-entropy over precomputed logits Z [N, V] (bf16, fp16 or fp32, row stride may
     exceed V): (loss, lse, dZ). dZ is None when grad is False; with inplace=True
     it overwrites Z."""
     if not (Z.is_cuda and y.is_cuda):
         raise ValueError("Z and y must be CUDA tensors (there is no CPU path)")
-    if Z.dtype not in (torch.bfloat16, torch.float32) or y.dtype != torch.int64:
-        raise TypeError("Z must be bfloat16 or float32 and y int64")
+    if Z.dtype not in _CE_DTYPES or y.dtype != torch.int64:
+        raise TypeError("Z must be bfloat16, float16 or float32 and y int64")
     if Z.dim() != 2 or Z.stride(1) != 1 or y.dim() != 1 or y.shape[0] != Z.shape[0]:
         raise ValueError("expected Z[N, V] with unit column stride and y[N]")
     N, V = Z.shape
@@ -322,7 +325,7 @@ def ce_logits(Z, y, dloss=None, ignore_index: int = IGNORE_INDEX, reduction: str
         _check(lib().lce_ce_logits_workspace_size(N, ctypes.byref(nbytes)), "workspace")
         ws = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
     _check_dloss(dloss, N, reduction)
-    st = lib().lce_ce_logits(_ptr(Z), 1 if Z.dtype == torch.float32 else 0, ld, _ptr(y), N, V,
+    st = lib().lce_ce_logits(_ptr(Z), _CE_DTYPES[Z.dtype], ld, _ptr(y), N, V,
                              ignore_index, red, _ptr(dloss), _ptr(loss), _ptr(lse), _ptr(dZ),
                              _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "lce_ce_logits")

@@ -731,7 +731,7 @@ lce_status lce_ce_logits_workspace_size(int64_t N, size_t *bytes) {
     return LCE_OK;
 }
 
-lce_status lce_ce_logits(const void *Z, int z_fp32, int64_t ld, const int64_t *y, int64_t N,
+lce_status lce_ce_logits(const void *Z, int z_dtype, int64_t ld, const int64_t *y, int64_t N,
                          int64_t V, int64_t ignore_index, int reduction, const float *dloss,
                          float *loss, float *lse, void *dZ, void *ws, size_t ws_bytes,
                          lce_stream_t stream) {
@@ -741,7 +741,8 @@ lce_status lce_ce_logits(const void *Z, int z_fp32, int64_t ld, const int64_t *y
     if (N < 0 || V <= 0 || ld < V || !ws) return LCE_ERR_INVALID_ARG;
     if (N > 0 && (!Z || !y || !lse || !loss)) return LCE_ERR_INVALID_ARG;
     if (!none && !loss) return LCE_ERR_INVALID_ARG;
-    const int vec = z_fp32 ? 4 : 8;
+    if (z_dtype < CE_BF16 || z_dtype > CE_FP16) return LCE_ERR_INVALID_ARG;
+    const int vec = z_dtype == CE_FP32 ? 4 : 8;
     if (ld % vec != 0) return LCE_ERR_ALIGNMENT;
     if ((Z && !aligned16(Z)) || (dZ && !aligned16(dZ)) || !aligned16(ws) ||
         (loss && !aligned16(loss)) || (lse && !aligned16(lse)) || (y && !aligned16(y)))
@@ -763,7 +764,7 @@ lce_status lce_ce_logits(const void *Z, int z_fp32, int64_t ld, const int64_t *y
     p.Z = Z;
     p.dZ = dZ;
     p.ld = ld;
-    p.fp32 = z_fp32 ? 1 : 0;
+    p.dtype = z_dtype;
     p.N = N;
     p.V = V;
     p.ignore_index = ignore_index;

@@ -1,4 +1,4 @@
-// Cross-entropy over logits the caller already holds (Z [N, ld], bf16 or fp32):
+// Cross-entropy over logits the caller already holds (Z [N, ld], bf16, fp16 or fp32):
 // per row the log-sum-exp, the loss lse - z_y, and optionally the gradient
 // (softmax - onehot) * scale, written over Z or into a separate dZ. This is the
 // row kernel of "Unsloth Kernel Architecture: Custom Triton Backpropagation and
@@ -9,7 +9,7 @@
 //
 // Two kernels, chosen by the row's size:
 //   * cluster kernel (a row fits in the registers of at most 8 CTAs of 512
-//     threads: V up to 524288 bf16 or 262144 fp32 logits): a cluster of CL CTAs
+//     threads: V up to 524288 bf16 / fp16 or 262144 fp32 logits): a cluster of CL CTAs
 //     owns one row at a time, each CTA one contiguous segment of it, which a
 //     bulk copy brings into shared memory and the threads then hold in
 //     registers. Every logit is read from HBM once and written once: the max,
@@ -21,6 +21,9 @@
 // Both use fixed reduction orders, so results are bit-reproducible.
 #include <map>
 #include <mutex>
+#include <type_traits>
+
+#include <cuda_fp16.h>
 
 #include "lce_internal.h"
 #include "lce_ptx.cuh"
@@ -70,6 +73,18 @@ __device__ __forceinline__ int ce_vec_load<__nv_bfloat16>(const __nv_bfloat16 *r
     return 8;
 }
 template <>
+__device__ __forceinline__ int ce_vec_load<__half>(const __half *row, long long i, float (&x)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(row + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[q]));
+        x[2 * q] = f.x;
+        x[2 * q + 1] = f.y;
+    }
+    return 8;
+}
+template <>
 __device__ __forceinline__ int ce_vec_load<float>(const float *row, long long i, float (&x)[8]) {
     const float4 a = *reinterpret_cast<const float4 *>(row + i);
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
@@ -78,6 +93,9 @@ __device__ __forceinline__ int ce_vec_load<float>(const float *row, long long i,
 template <typename T> __device__ __forceinline__ T ce_from_float(float v);
 template <> __device__ __forceinline__ __nv_bfloat16 ce_from_float<__nv_bfloat16>(float v) {
     return __float2bfloat16_rn(v);
+}
+template <> __device__ __forceinline__ __half ce_from_float<__half>(float v) {
+    return __float2half_rn(v);
 }
 template <> __device__ __forceinline__ float ce_from_float<float>(float v) { return v; }
 
@@ -280,6 +298,18 @@ template <> struct CeVec<__nv_bfloat16> {
         (&u.x)[q] = *reinterpret_cast<uint32_t *>(&h);
     }
 };
+template <> struct CeVec<__half> {
+    static constexpr int ELEMS = 8, PAIRS = 4;
+    static constexpr uint32_t NEG_INF = 0xfc00fc00u;   // two fp16 -inf
+    __device__ static float2 pair(const uint4 &u, int q) {
+        const uint32_t w = (&u.x)[q];
+        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+    }
+    __device__ static void set_pair(uint4 &u, int q, float2 v) {
+        __half2 h = __floats2half2_rn(v.x, v.y);
+        (&u.x)[q] = *reinterpret_cast<uint32_t *>(&h);
+    }
+};
 template <> struct CeVec<float> {
     static constexpr int ELEMS = 4, PAIRS = 2;
     static constexpr uint32_t NEG_INF = 0xff800000u;
@@ -380,13 +410,21 @@ __global__ void __launch_bounds__(CEC_THREADS, 1)
 
         // max of the segment
         float m = -INFINITY;
-        if constexpr (EL == 8) {
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) {
             __nv_bfloat162 mx2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
 #pragma unroll
             for (int k = 0; k < VPT; ++k)
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&(&d[k].x)[q]));
+            m = fmaxf(__low2float(mx2), __high2float(mx2));
+        } else if constexpr (std::is_same<T, __half>::value) {
+            __half2 mx2 = __floats2half2_rn(-INFINITY, -INFINITY);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    mx2 = __hmax2(mx2, *reinterpret_cast<const __half2 *>(&(&d[k].x)[q]));
             m = fmaxf(__low2float(mx2), __high2float(mx2));
         } else {
 #pragma unroll
@@ -510,11 +548,16 @@ namespace {
 
 using ClusterKernel = void (*)(const CELogitsParams, const long long, const int);
 
-ClusterKernel cluster_kernel(int fp32, int vpt) {
-    if (fp32) {
+ClusterKernel cluster_kernel(int dtype, int vpt) {
+    if (dtype == CE_FP32) {
         if (vpt == 4) return lce_ce_logits_cluster_kernel<float, 4>;
         if (vpt == 8) return lce_ce_logits_cluster_kernel<float, 8>;
         return lce_ce_logits_cluster_kernel<float, 16>;
+    }
+    if (dtype == CE_FP16) {
+        if (vpt == 4) return lce_ce_logits_cluster_kernel<__half, 4>;
+        if (vpt == 8) return lce_ce_logits_cluster_kernel<__half, 8>;
+        return lce_ce_logits_cluster_kernel<__half, 16>;
     }
     if (vpt == 4) return lce_ce_logits_cluster_kernel<__nv_bfloat16, 4>;
     if (vpt == 8) return lce_ce_logits_cluster_kernel<__nv_bfloat16, 8>;
@@ -532,8 +575,8 @@ int g_ce_max_dyn[64];   // per device: dynamic shared memory the cluster kernel 
 // The smallest cluster whose per-CTA segment fits in the registers of 512
 // threads (at most 16 vectors each); then the fewest vectors per thread that
 // hold it, and as many copy buffers (up to 3) as fit in shared memory.
-bool cluster_shape(long long V, int fp32, int max_dyn, ClusterShape *o) {
-    const long long elem = fp32 ? 4 : 2, vec = 16 / elem;
+bool cluster_shape(long long V, int dtype, int max_dyn, ClusterShape *o) {
+    const long long elem = dtype == CE_FP32 ? 4 : 2, vec = 16 / elem;
     for (int cl = 1; cl <= CEC_MAX_CLUSTER; ++cl) {
         long long seg = (V + cl - 1) / cl;
         seg = (seg + vec - 1) / vec * vec;
@@ -559,7 +602,7 @@ std::map<long long, int> g_occ;   // (device, kernel, cluster, smem) -> co-resid
 cudaError_t launch_cluster_kernel(const CELogitsParams &p, const ClusterShape &sh, int dev,
                                   bool *launched, cudaStream_t s) {
     *launched = false;
-    const ClusterKernel fn = cluster_kernel(p.fp32, sh.vpt);
+    const ClusterKernel fn = cluster_kernel(p.dtype, sh.vpt);
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = sh.cl;
@@ -573,7 +616,7 @@ cudaError_t launch_cluster_kernel(const CELogitsParams &p, const ClusterShape &s
     cfg.attrs = at;
     cfg.numAttrs = 1;
     const long long key =
-        (((static_cast<long long>(dev) * 2 + (p.fp32 ? 1 : 0)) * 32 + sh.vpt) * 16 + sh.cl) *
+        (((static_cast<long long>(dev) * 4 + p.dtype) * 32 + sh.vpt) * 16 + sh.cl) *
             (1ll << 24) +
         static_cast<long long>(sh.smem);
     int nclusters = -1;
@@ -601,15 +644,22 @@ cudaError_t launch_streaming_kernel(const CELogitsParams &p, int sms, cudaStream
     // a persistent grid of exactly the CTAs that fit at once (1024 threads each;
     // the rows in flight stay in L2 between the two passes)
     int per_sm = 1;
-    cudaError_t e = p.fp32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                 &per_sm, lce_ce_logits_kernel<float>, CE_THREADS, 0)
-                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                 &per_sm, lce_ce_logits_kernel<__nv_bfloat16>, CE_THREADS, 0);
+    cudaError_t e =
+        p.dtype == CE_FP32
+            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, lce_ce_logits_kernel<float>,
+                                                            CE_THREADS, 0)
+        : p.dtype == CE_FP16
+            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, lce_ce_logits_kernel<__half>,
+                                                            CE_THREADS, 0)
+            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                  &per_sm, lce_ce_logits_kernel<__nv_bfloat16>, CE_THREADS, 0);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     long long grid = static_cast<long long>(per_sm) * sms;
     if (grid > p.N) grid = p.N;
-    if (p.fp32) lce_ce_logits_kernel<float><<<static_cast<int>(grid), CE_THREADS, 0, s>>>(p);
+    if (p.dtype == CE_FP32) lce_ce_logits_kernel<float><<<static_cast<int>(grid), CE_THREADS, 0, s>>>(p);
+    else if (p.dtype == CE_FP16)
+        lce_ce_logits_kernel<__half><<<static_cast<int>(grid), CE_THREADS, 0, s>>>(p);
     else lce_ce_logits_kernel<__nv_bfloat16><<<static_cast<int>(grid), CE_THREADS, 0, s>>>(p);
     return cudaGetLastError();
 }
@@ -624,17 +674,17 @@ cudaError_t ce_set_attributes() {
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
     int static_max = 0;
-    for (int fp32 = 0; fp32 < 2; ++fp32)
+    for (int dt = 0; dt < 3; ++dt)
         for (int vpt = 4; vpt <= CEC_MAX_VPT; vpt *= 2) {
             cudaFuncAttributes fa{};
-            e = cudaFuncGetAttributes(&fa, cluster_kernel(fp32, vpt));
+            e = cudaFuncGetAttributes(&fa, cluster_kernel(dt, vpt));
             if (e != cudaSuccess) return e;
             if (static_cast<int>(fa.sharedSizeBytes) > static_max) static_max = static_cast<int>(fa.sharedSizeBytes);
         }
     const int max_dyn = optin - static_max - 1024;
-    for (int fp32 = 0; fp32 < 2; ++fp32)
+    for (int dt = 0; dt < 3; ++dt)
         for (int vpt = 4; vpt <= CEC_MAX_VPT; vpt *= 2) {
-            e = cudaFuncSetAttribute(cluster_kernel(fp32, vpt),
+            e = cudaFuncSetAttribute(cluster_kernel(dt, vpt),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
             if (e != cudaSuccess) return e;
         }
@@ -648,7 +698,7 @@ cudaError_t launch_ce_logits(const CELogitsParams &p, int sms, cudaStream_t s) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     ClusterShape sh;
-    if (dev >= 0 && dev < 64 && cluster_shape(p.V, p.fp32, g_ce_max_dyn[dev], &sh)) {
+    if (dev >= 0 && dev < 64 && cluster_shape(p.V, p.dtype, g_ce_max_dyn[dev], &sh)) {
         bool launched = false;
         e = launch_cluster_kernel(p, sh, dev, &launched, s);
         if (e != cudaSuccess || launched) return e;

@@ -145,11 +145,13 @@ struct FixupParams {
 };
 
 // Cross-entropy over precomputed logits Z [N][ld] (bf16 or fp32), one row at a time.
+enum : int { CE_BF16 = 0, CE_FP32 = 1, CE_FP16 = 2 };   // logits dtype codes of lce_ce_logits
+
 struct CELogitsParams {
     const void *Z;
     void *dZ;              // null: forward only; may equal Z (gradient written in place)
     long long ld;          // row stride of Z and dZ (elements)
-    int fp32;              // 0: bf16 logits, 1: fp32 logits
+    int dtype;             // CE_BF16, CE_FP32 or CE_FP16
     long long N, V;
     long long ignore_index;
     const long long *y;

@@ -19,6 +19,7 @@ shared memory; larger rows go to the streaming kernel. The shapes below reach:
     fp32 V = 152064                   cluster 5
     bf16 V = 500000                   cluster 8
     bf16 V = 600000, fp32 V = 300000  streaming kernel
+    fp16 logits take the bf16 shapes (same element size).
 """
 import numpy as np
 import pytest
@@ -47,7 +48,7 @@ def _logits(N, V, ld, dtype, seed, scale=3.0):
     return Zfull[:, :V].contiguous(), Zfull.to(DEV)[:, :V]
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32, torch.float16])
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
 @pytest.mark.parametrize("N,V,ld", [(300, 1003, 1008), (64, 32000, 32000), (5, 7, 8)])
 def test_ce_logits_matches_oracle(lce, dtype, reduction, N, V, ld):
@@ -130,6 +131,8 @@ def _check_against_oracle(Z, y, dl, reduction, loss, lse, dZ):
     (70, 32769, 32772, torch.float32, "mean"),        # cluster 2, one-element tail
     (16, 500000, 500000, torch.bfloat16, "mean"),     # cluster 8
     (8, 600000, 600000, torch.bfloat16, "sum"),       # streaming kernel
+    (200, 128256, 128256, torch.float16, "mean"),     # fp16, cluster 2
+    (6, 600000, 600008, torch.float16, "none"),       # fp16, streaming kernel
     (12, 300000, 300000, torch.float32, "none"),      # streaming kernel
 ])
 def test_ce_logits_cluster_shapes(lce, N, V, ld, dtype, reduction):
