@@ -116,23 +116,36 @@ lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const 
                           int reduction, float *loss, float *lse, void *dH, float *dW,
                           void *ws, size_t ws_bytes, lce_stream_t stream);
 
-/* Accumulating variants: flags LCE_ACCUMULATE_DW adds this call's dW into the
- * existing contents of dW (fp32) instead of overwriting it, and
- * LCE_ACCUMULATE_DH adds dH into the existing bf16 contents of dH (the sum is
- * formed in fp32 and rounded once), e.g. to accumulate gradients over
- * micro-batches or over several losses sharing H. With LCE_ACCUMULATE_DH the
- * workspace is lce_workspace_size_acc(..., flags) bytes (the chunk's dH in fp32,
- * 4 * chunk * D bytes more); otherwise it is lce_workspace_size(). Other
- * arguments and outputs as for the _ex entry points. */
-enum { LCE_ACCUMULATE_DW = 1, LCE_ACCUMULATE_DH = 2 };
-lce_status lce_workspace_size_acc(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
+/* Variants with option flags (the _ex entry points are these with flags = 0):
+ *  LCE_ACCUMULATE_DW  add this call's dW into the existing contents of dW (fp32)
+ *                     instead of overwriting it;
+ *  LCE_ACCUMULATE_DH  add dH into the existing contents of dH (the sum is formed
+ *                     in fp32 and rounded once), e.g. to accumulate gradients
+ *                     over micro-batches or over several losses sharing H;
+ *  LCE_INPUT_FP16     H, W (and dH) are fp16 instead of bf16 (the pages name both
+ *                     formats). The chunk buffer then holds fp16 values; because
+ *                     dloss / N_valid would push G below fp16's range, G is stored
+ *                     as (p - onehot) * 2^14 and the gradient GEMMs apply
+ *                     dloss / (N_valid * 2^14) to their fp32 accumulators. Reduction
+ *                     NONE (a per-row dloss of unknown range inside G) returns
+ *                     LCE_ERR_UNSUPPORTED with fp16.
+ * With LCE_ACCUMULATE_DH the workspace is lce_workspace_size_opt(..., flags) bytes
+ * (the chunk's dH in fp32, 4 * chunk * D bytes more); otherwise it is
+ * lce_workspace_size(). lce_forward_opt takes LCE_INPUT_FP16 only. Other arguments
+ * and outputs as for the _ex entry points. */
+enum { LCE_ACCUMULATE_DW = 1, LCE_ACCUMULATE_DH = 2, LCE_INPUT_FP16 = 4, LCE_FLAGS_ALL = 7 };
+lce_status lce_workspace_size_opt(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
                                   size_t *bytes);
-lce_status lce_backward_acc(const void *H, const void *W, const int64_t *y, const float *lse,
+lce_status lce_forward_opt(const void *H, const void *W, const int64_t *y,
+                           int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                           int reduction, int flags, float *loss, float *lse,
+                           void *ws, size_t ws_bytes, lce_stream_t stream);
+lce_status lce_backward_opt(const void *H, const void *W, const int64_t *y, const float *lse,
                             const float *dloss, void *dH, float *dW,
                             int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
                             int reduction, int flags, void *ws, size_t ws_bytes,
                             lce_stream_t stream);
-lce_status lce_fwd_bwd_acc(const void *H, const void *W, const int64_t *y, const float *dloss,
+lce_status lce_fwd_bwd_opt(const void *H, const void *W, const int64_t *y, const float *dloss,
                            int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
                            int reduction, int flags, float *loss, float *lse, void *dH, float *dW,
                            void *ws, size_t ws_bytes, lce_stream_t stream);

@@ -80,9 +80,15 @@ def to_bf16(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
 
 
+def to_fp16(a: np.ndarray) -> torch.Tensor:
+    """Round an fp32 array to fp16 (round to nearest even)."""
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.float16)
+
+
 def make_inputs(N: int, D: int, V: int, seed: int, labels: str = "uniform",
-                n_ignored: int = 0, w_std: float = 0.02, h_std: float = 1.0):
-    """Draw (H bf16 [N,D], W bf16 [V,D], y int64 [N]) on the CPU."""
+                n_ignored: int = 0, w_std: float = 0.02, h_std: float = 1.0, dtype: str = "bf16"):
+    """Draw (H [N,D], W [V,D], y int64 [N]) on the CPU; H and W rounded to bf16
+    (default) or fp16 from the same fp32 draws."""
     rng = np.random.default_rng(seed)
     H = rng.standard_normal((N, D), dtype=np.float32)
     if h_std != 1.0:
@@ -96,7 +102,8 @@ def make_inputs(N: int, D: int, V: int, seed: int, labels: str = "uniform",
         raise ValueError(f"unknown label distribution {labels!r}")
     if n_ignored:
         y[rng.permutation(N)[:n_ignored]] = IGNORE_INDEX
-    return to_bf16(H), to_bf16(W), torch.from_numpy(y)
+    rnd = to_fp16 if dtype == "fp16" else to_bf16
+    return rnd(H), rnd(W), torch.from_numpy(y)
 
 
 def workload_inputs(w: Workload | str):

@@ -37,9 +37,10 @@ EXPORTED = (
     "lce_forward_ex",
     "lce_backward_ex",
     "lce_fwd_bwd_ex",
-    "lce_workspace_size_acc",
-    "lce_backward_acc",
-    "lce_fwd_bwd_acc",
+    "lce_workspace_size_opt",
+    "lce_forward_opt",
+    "lce_backward_opt",
+    "lce_fwd_bwd_opt",
     "lce_ce_logits_workspace_size",
     "lce_ce_logits",
     "lce_rmsnorm_forward",
@@ -102,11 +103,13 @@ def lib() -> ctypes.CDLL:
                                   ctypes.c_int, _vp, ctypes.c_size_t, _vp]
     L.lce_fwd_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
                                  _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
-    L.lce_workspace_size_acc.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int,
+    L.lce_workspace_size_opt.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_size_t)]
-    L.lce_backward_acc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+    L.lce_forward_opt.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
+                                  ctypes.c_int, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    L.lce_backward_opt.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                    ctypes.c_int, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
-    L.lce_fwd_bwd_acc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
+    L.lce_fwd_bwd_opt.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
                                   ctypes.c_int, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     L.lce_ce_logits_workspace_size.argtypes = [_i64, ctypes.POINTER(ctypes.c_size_t)]
     L.lce_ce_logits.argtypes = [_vp, ctypes.c_int, _i64, _vp, _i64, _i64, _i64, ctypes.c_int, _vp,
@@ -135,7 +138,7 @@ def lib() -> ctypes.CDLL:
                  "lce_backward", "lce_fwd_bwd", "lce_forward_ex", "lce_backward_ex",
                  "lce_fwd_bwd_ex", "lce_read_status", "lce_version", "lce_last_launch_count",
                  "lce_ce_logits_workspace_size", "lce_ce_logits", "lce_rmsnorm_forward",
-                 "lce_workspace_size_acc", "lce_backward_acc", "lce_fwd_bwd_acc",
+                 "lce_workspace_size_opt", "lce_forward_opt", "lce_backward_opt", "lce_fwd_bwd_opt",
                  "lce_selftest_wait_timeout",
                  "lce_rmsnorm_backward_workspace_size", "lce_rmsnorm_backward",
                  "lce_norm_workspace_size", "lce_norm_fwd_bwd"):
@@ -166,6 +169,7 @@ def workspace_size(N: int, D: int, V: int, chunk: int) -> int:
 
 
 ACCUMULATE = {"dW": 1, "dH": 2}
+INPUT_FP16 = 4
 
 
 def _acc_flags(accumulate, dH, dW) -> int:
@@ -179,23 +183,23 @@ def _acc_flags(accumulate, dH, dW) -> int:
     return flags
 
 
-def workspace_size_acc(N: int, D: int, V: int, chunk: int, flags: int) -> int:
+def workspace_size_opt(N: int, D: int, V: int, chunk: int, flags: int) -> int:
     out = ctypes.c_size_t(0)
-    _check(lib().lce_workspace_size_acc(N, D, V, chunk, flags, ctypes.byref(out)),
-           "lce_workspace_size_acc")
+    _check(lib().lce_workspace_size_opt(N, D, V, chunk, flags, ctypes.byref(out)),
+           "lce_workspace_size_opt")
     return out.value
 
 
 def alloc_workspace(N: int, D: int, V: int, chunk: int, device, flags: int = 0) -> torch.Tensor:
-    n = workspace_size_acc(N, D, V, chunk, flags) if flags else workspace_size(N, D, V, chunk)
+    n = workspace_size_opt(N, D, V, chunk, flags) if flags & 2 else workspace_size(N, D, V, chunk)
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def _check_inputs(H, W, y):
     if not (H.is_cuda and W.is_cuda and y.is_cuda):
         raise ValueError("H, W and y must be CUDA tensors (there is no CPU path)")
-    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
-        raise TypeError("H and W must be bfloat16")
+    if H.dtype not in (torch.bfloat16, torch.float16) or W.dtype != H.dtype:
+        raise TypeError("H and W must both be bfloat16 or both float16")
     if y.dtype != torch.int64:
         raise TypeError("y must be int64")
     if H.dim() != 2 or W.dim() != 2 or y.dim() != 1:
@@ -240,8 +244,9 @@ def lce_forward(H, W, y, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
         lse = torch.empty(N, dtype=torch.float32, device=dev)
     if ws is None:
         ws = alloc_workspace(N, D, V, chunk, dev)
-    st = lib().lce_forward_ex(_ptr(H), _ptr(W), _ptr(y), N, D, V, ignore_index, chunk, red,
-                              _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    flags = INPUT_FP16 if H.dtype == torch.float16 else 0
+    st = lib().lce_forward_opt(_ptr(H), _ptr(W), _ptr(y), N, D, V, ignore_index, chunk, red, flags,
+                               _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "lce_forward")
     return loss, lse
 
@@ -255,15 +260,15 @@ def lce_backward(H, W, y, lse, dloss=None, chunk: int = 1024, ignore_index: int 
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
     red = _reduction(reduction)
-    flags = _acc_flags(accumulate, dH, dW)
+    flags = _acc_flags(accumulate, dH, dW) | (INPUT_FP16 if H.dtype == torch.float16 else 0)
     if dH is None:
-        dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+        dH = torch.empty(N, D, dtype=H.dtype, device=dev)
     if dW is None:
         dW = torch.empty(V, D, dtype=torch.float32, device=dev)
     if ws is None:
         ws = alloc_workspace(N, D, V, chunk, dev, flags)
     _check_dloss(dloss, N, reduction)
-    st = lib().lce_backward_acc(_ptr(H), _ptr(W), _ptr(y), _ptr(lse), _ptr(dloss), _ptr(dH),
+    st = lib().lce_backward_opt(_ptr(H), _ptr(W), _ptr(y), _ptr(lse), _ptr(dloss), _ptr(dH),
                                 _ptr(dW), N, D, V, ignore_index, chunk, red, flags, _ptr(ws),
                                 ws.numel(), _stream(stream))
     _check(st, "lce_backward")
@@ -278,18 +283,18 @@ def lce_fwd_bwd(H, W, y, dloss=None, chunk: int = 1024, ignore_index: int = IGNO
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
     red = _reduction(reduction)
-    flags = _acc_flags(accumulate, dH, dW)
+    flags = _acc_flags(accumulate, dH, dW) | (INPUT_FP16 if H.dtype == torch.float16 else 0)
     loss = _loss_buffer(loss, N, reduction, dev)
     if lse is None:
         lse = torch.empty(N, dtype=torch.float32, device=dev)
     if dH is None:
-        dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+        dH = torch.empty(N, D, dtype=H.dtype, device=dev)
     if dW is None:
         dW = torch.empty(V, D, dtype=torch.float32, device=dev)
     if ws is None:
         ws = alloc_workspace(N, D, V, chunk, dev, flags)
     _check_dloss(dloss, N, reduction)
-    st = lib().lce_fwd_bwd_acc(_ptr(H), _ptr(W), _ptr(y), _ptr(dloss), N, D, V, ignore_index,
+    st = lib().lce_fwd_bwd_opt(_ptr(H), _ptr(W), _ptr(y), _ptr(dloss), N, D, V, ignore_index,
                                chunk, red, flags, _ptr(loss), _ptr(lse), _ptr(dH), _ptr(dW),
                                _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "lce_fwd_bwd")

@@ -147,11 +147,14 @@ bool make_norm_layout(long long N, long long D, long long V, long long chunk, No
     return true;
 }
 
-// Tensor map over a row-major array (bf16 unless fp32 is asked for) with the
-// 128-byte swizzle of the MMA operand tiles and of the epilogue staging boxes;
-// zero fill out of bounds on loads, clipping on stores.
+// Element types of the tensor maps.
+enum MapType { MAP_BF16, MAP_F16, MAP_F32 };
+
+// Tensor map over a row-major array with the 128-byte swizzle of the MMA
+// operand tiles and of the epilogue staging boxes; zero fill out of bounds on
+// loads, clipping on stores.
 bool encode_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
-                const uint64_t *strides_bytes, const uint32_t *box, bool fp32) {
+                const uint64_t *strides_bytes, const uint32_t *box, MapType type) {
     cuuint64_t d[3];
     cuuint64_t st[2];
     cuuint32_t bx[3];
@@ -161,30 +164,35 @@ bool encode_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims
         bx[i] = box[i];
     }
     for (int i = 0; i + 1 < rank; ++i) st[i] = strides_bytes[i];
-    CUresult r = g_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+    const CUtensorMapDataType dt = type == MAP_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : type == MAP_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = g_encode(m, dt,
                           rank, const_cast<void *>(base), d, st, bx, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-// MMA operand tile load map: 2-D bf16, box {box_inner, box_outer}.
+// MMA operand tile load map: 2-D, 16-bit elements (bf16 or fp16), box
+// {box_inner, box_outer}.
 bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
-               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+               MapType type = MAP_BF16) {
     const uint64_t dims[2] = {inner, outer};
     const uint64_t st[1] = {row_stride_bytes};
     const uint32_t box[2] = {box_inner, box_outer};
-    return encode_map(m, base, 2, dims, st, box, false);
+    return encode_map(m, base, 2, dims, st, box, type);
 }
 
 // Epilogue store map: 2-D, box = 128 bytes x box_rows rows (128: a column half
 // of a gradient tile; 32: one warp's rows of a logits tile).
 bool encode_store_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
-                     uint64_t row_stride_bytes, bool fp32, uint32_t box_rows = 128) {
+                     uint64_t row_stride_bytes, MapType type, uint32_t box_rows = 128) {
     const uint64_t dims[2] = {inner, outer};
     const uint64_t st[1] = {row_stride_bytes};
-    const uint32_t box[2] = {fp32 ? 32u : 64u, box_rows};
-    return encode_map(m, base, 2, dims, st, box, fp32);
+    const uint32_t box[2] = {type == MAP_F32 ? 32u : 64u, box_rows};
+    return encode_map(m, base, 2, dims, st, box, type);
 }
 
 struct Ctx {
@@ -202,6 +210,8 @@ struct Ctx {
     int pairs;   // > 0: GEMMs run as CTA pairs (cluster of 2), at most this many at once
     int reduction;       // LCE_REDUCTION_*
     bool h_chunked;      // H is a chunk-sized buffer (rows 0..C-1), refilled per chunk
+    bool f16;            // H, W, G and dH are fp16 (bf16 otherwise)
+    MapType t16;         // the 16-bit map type of this call
     cudaStream_t s;
     CUtensorMap tmH_K, tmW_K, tmW_MN;
 };
@@ -258,7 +268,7 @@ void prof_end(int idx, cudaStream_t s) {
 
 lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
                  int64_t V, int64_t ign, int64_t chunk, void *ws, size_t ws_bytes,
-                 lce_stream_t stream, bool h_chunked = false) {
+                 lce_stream_t stream, bool h_chunked = false, bool f16 = false) {
     g_launches = 0;
     if (!make_layout(N, D, V, chunk, c.L)) return LCE_ERR_INVALID_ARG;
     if (!ws) return LCE_ERR_INVALID_ARG;
@@ -286,10 +296,13 @@ lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t
     c.s = reinterpret_cast<cudaStream_t>(stream);
     c.reduction = LCE_REDUCTION_MEAN;
     c.h_chunked = h_chunked;
+    c.f16 = f16;
+    c.t16 = f16 ? MAP_F16 : MAP_BF16;
     // with CTA pairs each CTA loads half of a 256-row W tile (multicast to both)
-    if (!encode_2d(&c.tmW_K, W, D, V, D * 2, BK, c.pairs > 0 ? BN / 2 : BN)) return LCE_ERR_CUDA;
-    if (!encode_2d(&c.tmW_MN, W, D, V, D * 2, 64, BK)) return LCE_ERR_CUDA;
-    if (N > 0 && !encode_2d(&c.tmH_K, H, D, h_chunked ? c.L.C : N, D * 2, BK, BM)) return LCE_ERR_CUDA;
+    if (!encode_2d(&c.tmW_K, W, D, V, D * 2, BK, c.pairs > 0 ? BN / 2 : BN, c.t16)) return LCE_ERR_CUDA;
+    if (!encode_2d(&c.tmW_MN, W, D, V, D * 2, 64, BK, c.t16)) return LCE_ERR_CUDA;
+    if (N > 0 && !encode_2d(&c.tmH_K, H, D, h_chunked ? c.L.C : N, D * 2, BK, BM, c.t16))
+        return LCE_ERR_CUDA;
     if (cudaMemsetAsync(c.ws, 0, c.L.hdr_bytes, c.s) != cudaSuccess) return LCE_ERR_CUDA;
     LCE_LAUNCH(launch_label_scan(c.y, N, V, ign, c.hdr, c.s));
     return LCE_OK;
@@ -312,6 +325,7 @@ void base_params(const Ctx &c, GemmParams &p, long long row0, long long rows, in
     p.timeout_ns = kDefaultTimeoutNs;
     p.dloss_per_row = c.reduction == LCE_REDUCTION_NONE ? 1 : 0;
     p.mean = c.reduction == LCE_REDUCTION_MEAN ? 1 : 0;
+    p.f16 = c.f16 ? 1 : 0;
 }
 
 lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, int slot,
@@ -329,7 +343,7 @@ lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, in
     p.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * p.n_blocks0;
     p.lse = lse;
     p.dloss = dloss;
-    if (mode != MODE_LSE && !encode_store_2d(&p.tmS0, c.G, c.V, rows, 2ull * c.L.ldg, false, 32))
+    if (mode != MODE_LSE && !encode_store_2d(&p.tmS0, c.G, c.V, rows, 2ull * c.L.ldg, c.t16, 32))
         return LCE_ERR_CUDA;
     const int units = cl == 2 ? c.pairs : c.sms;
     const int grid = cl * (p.total_tiles < units ? p.total_tiles : units);
@@ -339,7 +353,7 @@ lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, in
 
 // dHc: this chunk's dH rows (bf16, or fp32 when dh_fp32).
 lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void *dHc, bool dh_fp32,
-                   float *dW, bool accumulate) {
+                   float *dW, bool accumulate, const float *dloss) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
     base_params(c, p, row0, rows, slot);
@@ -353,15 +367,16 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     tp.rows = static_cast<int>(rows);
     tp.cols = static_cast<int>(c.D);
     LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_transpose(tp, c.s));
-    if (!encode_2d(&p.tmA0, c.G, c.V, rows, 2ull * c.L.ldg, BK, BM)) return LCE_ERR_CUDA;
+    if (!encode_2d(&p.tmA0, c.G, c.V, rows, 2ull * c.L.ldg, BK, BM, c.t16)) return LCE_ERR_CUDA;
     p.tmB0 = c.tmW_MN;
     // dW A = G^T read from G itself (MN-major boxes of 64 vocab columns x 64 rows)
-    if (!encode_2d(&p.tmA1, c.G, c.V, rows, 2ull * c.L.ldg, 64, BK)) return LCE_ERR_CUDA;
+    if (!encode_2d(&p.tmA1, c.G, c.V, rows, 2ull * c.L.ldg, 64, BK, c.t16)) return LCE_ERR_CUDA;
     const int cl = c.pairs > 0 ? 2 : 1;
-    if (!encode_2d(&p.tmB1, c.HT, rows, c.D, 2ull * c.L.ldt, BK, BN / cl)) return LCE_ERR_CUDA;
-    if (!encode_store_2d(&p.tmS0, dHc, c.D, rows, (dh_fp32 ? 4ull : 2ull) * c.D, dh_fp32))
+    if (!encode_2d(&p.tmB1, c.HT, rows, c.D, 2ull * c.L.ldt, BK, BN / cl, c.t16)) return LCE_ERR_CUDA;
+    if (!encode_store_2d(&p.tmS0, dHc, c.D, rows, (dh_fp32 ? 4ull : 2ull) * c.D,
+                         dh_fp32 ? MAP_F32 : c.t16))
         return LCE_ERR_CUDA;
-    if (!encode_store_2d(&p.tmS1, dW, c.D, c.V, 4ull * c.D, true)) return LCE_ERR_CUDA;
+    if (!encode_store_2d(&p.tmS1, dW, c.D, c.V, 4ull * c.D, MAP_F32)) return LCE_ERR_CUDA;
     p.m_blocks0 = static_cast<int>(cdiv(rows, BM));
     p.n_blocks0 = static_cast<int>(cdiv(c.D, BN));
     p.k_blocks0 = static_cast<int>(cdiv(c.V, BK));
@@ -372,6 +387,7 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
                     static_cast<int>(cdiv(p.m_blocks1, cl)) * p.n_blocks1;
     p.dH = static_cast<__nv_bfloat16 *>(dHc);
     p.dh_fp32 = dh_fp32 ? 1 : 0;
+    p.dloss = dloss;   // fp16: the epilogues apply the uniform part of the scale
     p.dW = dW;
     p.dw_accumulate = accumulate ? 1 : 0;
     const int units = cl == 2 ? c.pairs : c.sms;
@@ -397,6 +413,7 @@ lce_status run_merge(const Ctx &c, bool fused, long long row0, long long rows, f
     m.dloss = dloss;
     m.dloss_per_row = c.reduction == LCE_REDUCTION_NONE ? 1 : 0;
     m.mean = c.reduction == LCE_REDUCTION_MEAN ? 1 : 0;
+    m.f16 = c.f16 ? 1 : 0;
     m.lse = lse;
     m.loss_rows = loss_rows;
     LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_merge(fused, m, c.s));
@@ -419,6 +436,7 @@ lce_status run_fixup(const Ctx &c, long long row0, long long rows, const float *
     fp.dloss = dloss;
     fp.dloss_per_row = c.reduction == LCE_REDUCTION_NONE ? 1 : 0;
     fp.mean = c.reduction == LCE_REDUCTION_MEAN ? 1 : 0;
+    fp.f16 = c.f16 ? 1 : 0;
     LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_fixup(fp, c.s));
     return LCE_OK;
 }
@@ -441,26 +459,28 @@ lce_status lce_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk, si
     return LCE_OK;
 }
 
-lce_status lce_workspace_size_acc(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
+lce_status lce_workspace_size_opt(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
                                   size_t *bytes) {
-    if (!bytes || (flags & ~(LCE_ACCUMULATE_DW | LCE_ACCUMULATE_DH))) return LCE_ERR_INVALID_ARG;
+    if (!bytes || (flags & ~LCE_FLAGS_ALL)) return LCE_ERR_INVALID_ARG;
     Layout L;
     if (!make_layout(N, D, V, chunk, L)) return LCE_ERR_INVALID_ARG;
     *bytes = L.total + ((flags & LCE_ACCUMULATE_DH) ? acc_dh_bytes(L, D) : 0);
     return LCE_OK;
 }
 
-lce_status lce_forward_ex(const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
-                          int64_t V, int64_t ignore_index, int64_t chunk, int reduction,
-                          float *loss, float *lse, void *ws, size_t ws_bytes,
-                          lce_stream_t stream) {
+lce_status lce_forward_opt(const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
+                           int64_t V, int64_t ignore_index, int64_t chunk, int reduction, int flags,
+                           float *loss, float *lse, void *ws, size_t ws_bytes,
+                           lce_stream_t stream) {
     g_launches = 0;
     if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
+    if (flags & ~LCE_INPUT_FP16) return LCE_ERR_INVALID_ARG;   // nothing to accumulate here
     const bool none = reduction == LCE_REDUCTION_NONE;
     if ((!none && !loss) || (N > 0 && (!lse || !loss))) return LCE_ERR_INVALID_ARG;
     if ((loss && !aligned16(loss)) || (lse && !aligned16(lse))) return LCE_ERR_ALIGNMENT;
     Ctx c;
-    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream));
+    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, false,
+                  (flags & LCE_INPUT_FP16) != 0));
     c.reduction = reduction;
     float *rows_out = none ? loss : c.loss_rows;
     for (long long k = 0; k < c.L.nchunks; ++k) {
@@ -475,6 +495,14 @@ lce_status lce_forward_ex(const void *H, const void *W, const int64_t *y, int64_
     return LCE_OK;
 }
 
+lce_status lce_forward_ex(const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
+                          int64_t V, int64_t ignore_index, int64_t chunk, int reduction,
+                          float *loss, float *lse, void *ws, size_t ws_bytes,
+                          lce_stream_t stream) {
+    return lce_forward_opt(H, W, y, N, D, V, ignore_index, chunk, reduction, 0, loss, lse, ws,
+                           ws_bytes, stream);
+}
+
 lce_status lce_forward(const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
                        int64_t V, int64_t ignore_index, int64_t chunk, float *loss, float *lse,
                        void *ws, size_t ws_bytes, lce_stream_t stream) {
@@ -482,13 +510,15 @@ lce_status lce_forward(const void *H, const void *W, const int64_t *y, int64_t N
                           ws_bytes, stream);
 }
 
-lce_status lce_backward_acc(const void *H, const void *W, const int64_t *y, const float *lse,
+lce_status lce_backward_opt(const void *H, const void *W, const int64_t *y, const float *lse,
                             const float *dloss, void *dH, float *dW, int64_t N, int64_t D,
                             int64_t V, int64_t ignore_index, int64_t chunk, int reduction,
                             int flags, void *ws, size_t ws_bytes, lce_stream_t stream) {
     g_launches = 0;
     if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
-    if (flags & ~(LCE_ACCUMULATE_DW | LCE_ACCUMULATE_DH)) return LCE_ERR_INVALID_ARG;
+    if (flags & ~LCE_FLAGS_ALL) return LCE_ERR_INVALID_ARG;
+    const bool f16 = (flags & LCE_INPUT_FP16) != 0;
+    if (f16 && reduction == LCE_REDUCTION_NONE) return LCE_ERR_UNSUPPORTED;
     if (!dW || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
     if (!aligned16(dW) || (dH && !aligned16(dH)) || (lse && !aligned16(lse)))
         return LCE_ERR_ALIGNMENT;
@@ -497,7 +527,7 @@ lce_status lce_backward_acc(const void *H, const void *W, const int64_t *y, cons
     if (!make_layout(N, D, V, chunk, L0)) return LCE_ERR_INVALID_ARG;
     if (acc_dh && ws_bytes < L0.total + acc_dh_bytes(L0, D)) return LCE_ERR_WORKSPACE;
     Ctx c;
-    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream));
+    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, false, f16));
     c.reduction = reduction;
     float *dHacc = reinterpret_cast<float *>(c.ws + c.L.total);
     if (c.L.nchunks == 0 && !(flags & LCE_ACCUMULATE_DW)) {
@@ -510,8 +540,8 @@ lce_status lce_backward_acc(const void *H, const void *W, const int64_t *y, cons
         __nv_bfloat16 *dHc = static_cast<__nv_bfloat16 *>(dH) + row0 * c.D;
         LCE_TRY(run_logits(c, MODE_G, row0, rows, static_cast<int>(2 * k), lse, dloss));
         LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), acc_dh ? static_cast<void *>(dHacc) : dHc,
-                        acc_dh, dW, k > 0 || (flags & LCE_ACCUMULATE_DW)));
-        if (acc_dh) LCE_LAUNCH(launch_add_dh(dHacc, dHc, rows * c.D, c.sms, c.s));
+                        acc_dh, dW, k > 0 || (flags & LCE_ACCUMULATE_DW), dloss));
+        if (acc_dh) LCE_LAUNCH(launch_add_dh(dHacc, dHc, rows * c.D, c.f16, c.sms, c.s));
     }
     return LCE_OK;
 }
@@ -520,7 +550,7 @@ lce_status lce_backward_ex(const void *H, const void *W, const int64_t *y, const
                            const float *dloss, void *dH, float *dW, int64_t N, int64_t D,
                            int64_t V, int64_t ignore_index, int64_t chunk, int reduction,
                            void *ws, size_t ws_bytes, lce_stream_t stream) {
-    return lce_backward_acc(H, W, y, lse, dloss, dH, dW, N, D, V, ignore_index, chunk, reduction, 0,
+    return lce_backward_opt(H, W, y, lse, dloss, dH, dW, N, D, V, ignore_index, chunk, reduction, 0,
                             ws, ws_bytes, stream);
 }
 
@@ -532,14 +562,16 @@ lce_status lce_backward(const void *H, const void *W, const int64_t *y, const fl
                            LCE_REDUCTION_MEAN, ws, ws_bytes, stream);
 }
 
-lce_status lce_fwd_bwd_acc(const void *H, const void *W, const int64_t *y, const float *dloss,
+lce_status lce_fwd_bwd_opt(const void *H, const void *W, const int64_t *y, const float *dloss,
                            int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
                            int reduction, int flags, float *loss, float *lse, void *dH, float *dW,
                            void *ws, size_t ws_bytes, lce_stream_t stream) {
     g_launches = 0;
     if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
-    if (flags & ~(LCE_ACCUMULATE_DW | LCE_ACCUMULATE_DH)) return LCE_ERR_INVALID_ARG;
+    if (flags & ~LCE_FLAGS_ALL) return LCE_ERR_INVALID_ARG;
+    const bool f16 = (flags & LCE_INPUT_FP16) != 0;
     const bool none = reduction == LCE_REDUCTION_NONE;
+    if (f16 && none) return LCE_ERR_UNSUPPORTED;
     if ((!none && !loss) || !dW || (N > 0 && (!lse || !dH || !loss))) return LCE_ERR_INVALID_ARG;
     if ((loss && !aligned16(loss)) || !aligned16(dW) || (dH && !aligned16(dH)) ||
         (lse && !aligned16(lse)))
@@ -549,7 +581,7 @@ lce_status lce_fwd_bwd_acc(const void *H, const void *W, const int64_t *y, const
     if (!make_layout(N, D, V, chunk, L0)) return LCE_ERR_INVALID_ARG;
     if (acc_dh && ws_bytes < L0.total + acc_dh_bytes(L0, D)) return LCE_ERR_WORKSPACE;
     Ctx c;
-    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream));
+    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, false, f16));
     c.reduction = reduction;
     float *rows_out = none ? loss : c.loss_rows;
     float *dHacc = reinterpret_cast<float *>(c.ws + c.L.total);
@@ -565,8 +597,8 @@ lce_status lce_fwd_bwd_acc(const void *H, const void *W, const int64_t *y, const
         LCE_TRY(run_merge(c, true, row0, rows, lse, dloss, rows_out));
         LCE_TRY(run_fixup(c, row0, rows, dloss));
         LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), acc_dh ? static_cast<void *>(dHacc) : dHc,
-                        acc_dh, dW, k > 0 || (flags & LCE_ACCUMULATE_DW)));
-        if (acc_dh) LCE_LAUNCH(launch_add_dh(dHacc, dHc, rows * c.D, c.sms, c.s));
+                        acc_dh, dW, k > 0 || (flags & LCE_ACCUMULATE_DW), dloss));
+        if (acc_dh) LCE_LAUNCH(launch_add_dh(dHacc, dHc, rows * c.D, c.f16, c.sms, c.s));
     }
     if (!none)
         LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss,
@@ -578,7 +610,7 @@ lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const 
                           int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
                           int reduction, float *loss, float *lse, void *dH, float *dW, void *ws,
                           size_t ws_bytes, lce_stream_t stream) {
-    return lce_fwd_bwd_acc(H, W, y, dloss, N, D, V, ignore_index, chunk, reduction, 0, loss, lse,
+    return lce_fwd_bwd_opt(H, W, y, dloss, N, D, V, ignore_index, chunk, reduction, 0, loss, lse,
                            dH, dW, ws, ws_bytes, stream);
 }
 
@@ -708,7 +740,7 @@ lce_status lce_norm_fwd_bwd(const void *X, const void *gamma, float eps, const v
         LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr));
         LCE_TRY(run_merge(c, true, row0, rows, lse, dloss, rows_out));
         LCE_TRY(run_fixup(c, row0, rows, dloss));
-        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dHbuf, true, dW, k > 0));
+        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dHbuf, true, dW, k > 0, dloss));
         np.H = nullptr;
         np.dH = dHbuf;
         np.dh_fp32 = 1;

@@ -127,8 +127,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_merge_kernel(const MergePar
         p.loss_rows[grow] = y_ok ? lse - p.zy[r] : 0.f;
     }
     if constexpr (FACTORS) {
-        const float scale =
-            lce_row_scale(p.dloss, p.dloss_per_row, p.mean, p.hdr[HDR_NVALID], grow, y_ok);
+        const float scale = lce_store_scale(p.dloss, p.dloss_per_row, p.mean, p.hdr[HDR_NVALID],
+                                            grow, y_ok, p.f16);
         const float lse2 = lse * LOG2E_F;
         for (int i = t; i < p.nparts; i += MERGE_THREADS)
             parts[i].x = scale != 0.f ? exp2f(fmaf(parts[i].x, LOG2E_F, -lse2)) * scale : 0.f;
@@ -136,9 +136,10 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_merge_kernel(const MergePar
 }
 
 // ------------------------------------------------------------------ fix-up
-// The chunk buffer holds P' = exp(z - m_p) (bf16). In place it becomes
-// G = P' * factor_p - 1[j = y_i] * dloss / N_valid, rounded to bf16.
-// Grid: x over 8-column vectors of a row, y over rows.
+// The chunk buffer holds P' = exp(z - m_p) (bf16, or fp16 for fp16 inputs). In
+// place it becomes G = P' * factor_p - 1[j = y_i] * s_i, rounded to the same
+// dtype, with s_i the stored-G row scale (dloss / N_valid for bf16; see
+// lce_store_scale for fp16). Grid: x over 8-column vectors of a row, y over rows.
 
 __global__ void __launch_bounds__(256) lce_fixup_kernel(const FixupParams p) {
     const int nvec = (p.V + 7) >> 3;
@@ -147,8 +148,8 @@ __global__ void __launch_bounds__(256) lce_fixup_kernel(const FixupParams p) {
     for (int r = blockIdx.y; r < p.rows; r += gridDim.y) {
     const long long yv = p.y[p.row0 + r];
     const bool y_ok = yv != p.ignore_index && yv >= 0 && yv < p.V;
-    const float scale = lce_row_scale(p.dloss, p.dloss_per_row, p.mean, p.hdr[HDR_NVALID],
-                                      p.row0 + r, y_ok);
+    const float scale = lce_store_scale(p.dloss, p.dloss_per_row, p.mean, p.hdr[HDR_NVALID],
+                                        p.row0 + r, y_ok, p.f16);
     const int ycol = y_ok ? static_cast<int>(yv) : -1;
     const int c = i * 8;
     const float f = p.parts[static_cast<size_t>(r) * p.nparts + (c >> 7)].x;
@@ -157,14 +158,20 @@ __global__ void __launch_bounds__(256) lce_fixup_kernel(const FixupParams p) {
     uint32_t *wv = reinterpret_cast<uint32_t *>(&u);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&wv[q]);
-        float2 x = __bfloat1622float2(h);
+        float2 x;
+        if (p.f16) x = __half22float2(*reinterpret_cast<__half2 *>(&wv[q]));
+        else x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&wv[q]));
         x.x *= f;
         x.y *= f;
         if (c + 2 * q == ycol) x.x -= scale;
         if (c + 2 * q + 1 == ycol) x.y -= scale;
-        h = __floats2bfloat162_rn(x.x, x.y);
-        wv[q] = *reinterpret_cast<uint32_t *>(&h);
+        if (p.f16) {
+            __half2 h = __floats2half2_rn(x.x, x.y);
+            wv[q] = *reinterpret_cast<uint32_t *>(&h);
+        } else {
+            __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
+            wv[q] = *reinterpret_cast<uint32_t *>(&h);
+        }
     }
     *ptr = u;
     }
@@ -241,24 +248,32 @@ __global__ void __launch_bounds__(1024) lce_loss_finalize_kernel(const float *__
 }
 
 // ------------------------------------------------------------------ dH accumulation
-// dst[rows][D] (bf16) += src[rows][D] (fp32, a chunk's dH), rounded once.
+// dst[rows][D] (bf16, or fp16 when F16) += src[rows][D] (fp32, a chunk's dH),
+// rounded once.
+template <bool F16>
 __global__ void __launch_bounds__(256) lce_add_dh_kernel(const float *__restrict__ src,
-                                                        __nv_bfloat16 *__restrict__ dst,
-                                                        long long nvec) {
+                                                        void *__restrict__ dst_, long long nvec) {
+    uint4 *dst = static_cast<uint4 *>(dst_);
     for (long long i = blockIdx.x * 256ll + threadIdx.x; i < nvec; i += 256ll * gridDim.x) {
         const float4 a = reinterpret_cast<const float4 *>(src)[2 * i];
         const float4 b = reinterpret_cast<const float4 *>(src)[2 * i + 1];
-        uint4 d = reinterpret_cast<const uint4 *>(dst)[i];
+        uint4 d = dst[i];
         const float s[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         uint32_t *w = &d.x;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float lo = __uint_as_float(w[q] << 16) + s[2 * q];
-            const float hi = __uint_as_float(w[q] & 0xffff0000u) + s[2 * q + 1];
-            __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-            w[q] = *reinterpret_cast<uint32_t *>(&h);
+            if constexpr (F16) {
+                const float2 x = __half22float2(*reinterpret_cast<__half2 *>(&w[q]));
+                __half2 h = __floats2half2_rn(x.x + s[2 * q], x.y + s[2 * q + 1]);
+                w[q] = *reinterpret_cast<uint32_t *>(&h);
+            } else {
+                const float lo = __uint_as_float(w[q] << 16) + s[2 * q];
+                const float hi = __uint_as_float(w[q] & 0xffff0000u) + s[2 * q + 1];
+                __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+                w[q] = *reinterpret_cast<uint32_t *>(&h);
+            }
         }
-        reinterpret_cast<uint4 *>(dst)[i] = d;
+        dst[i] = d;
     }
 }
 
@@ -320,13 +335,14 @@ cudaError_t launch_wait_selftest(int *hdr, unsigned long long limit_ns, cudaStre
     return cudaGetLastError();
 }
 
-cudaError_t launch_add_dh(const float *src, __nv_bfloat16 *dst, long long n, int sms,
+cudaError_t launch_add_dh(const float *src, void *dst, long long n, bool f16, int sms,
                           cudaStream_t s) {
     const long long nvec = n / 8;
     if (nvec <= 0) return cudaSuccess;
     long long blocks = (nvec + 255) / 256;
     if (blocks > 8ll * sms) blocks = 8ll * sms;
-    lce_add_dh_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(src, dst, nvec);
+    if (f16) lce_add_dh_kernel<true><<<static_cast<int>(blocks), 256, 0, s>>>(src, dst, nvec);
+    else lce_add_dh_kernel<false><<<static_cast<int>(blocks), 256, 0, s>>>(src, dst, nvec);
     return cudaGetLastError();
 }
 

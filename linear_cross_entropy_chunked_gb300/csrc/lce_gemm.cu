@@ -63,11 +63,13 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: bf16 x bf16 -> fp32.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+// Instruction descriptor of tcgen05.mma kind::f16: bf16 x bf16 or fp16 x fp16
+// (both operands always the same type) -> fp32.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                     bool fp16) {
     return (1u << 4)                                   // D format: f32
-           | (1u << 7)                                 // A format: bf16
-           | (1u << 10)                                // B format: bf16
+           | ((fp16 ? 0u : 1u) << 7)                   // A format: f16 (0) / bf16 (1)
+           | ((fp16 ? 0u : 1u) << 10)                  // B format: f16 (0) / bf16 (1)
            | ((a_mn_major ? 1u : 0u) << 15)            // A major-ness
            | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
@@ -119,6 +121,14 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+// Two 16-bit values in the operand dtype of the call.
+__device__ __forceinline__ uint32_t pack_h16x2(float lo, float hi, int f16) {
+    return f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
 
 constexpr float LOG2E = 1.4426950408889634f;
@@ -235,12 +245,14 @@ struct HalfStager {
             put(j, __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
                 __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
     }
-    // 32 values as bf16 fill half of the row: chunks jb .. jb + 3.
-    __device__ __forceinline__ void put_bf16(int jb, const float *v) const {
+    // 32 values as 16-bit floats (bf16, or fp16 when f16) fill half of the row:
+    // chunks jb .. jb + 3.
+    __device__ __forceinline__ void put_h16(int jb, const float *v, int f16) const {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-            put(jb + q, pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+            put(jb + q, pack_h16x2(v[8 * q], v[8 * q + 1], f16),
+                pack_h16x2(v[8 * q + 2], v[8 * q + 3], f16), pack_h16x2(v[8 * q + 4], v[8 * q + 5], f16),
+                pack_h16x2(v[8 * q + 6], v[8 * q + 7], f16));
     }
     __device__ __forceinline__ void issue(const CUtensorMap *map, int kind, int x, int y) const {
         fence_proxy_async_smem();
@@ -264,13 +276,14 @@ struct WarpStager {
         if (lane == 0) bulk_wait_read0();
         __syncwarp();
     }
-    __device__ __forceinline__ void put_bf16(int jb, const float *v) const {
+    __device__ __forceinline__ void put_h16(int jb, const float *v, int f16) const {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
             *reinterpret_cast<uint4 *>(buf + lane * 128 + (((jb + q) ^ (lane & 7)) << 4)) =
-                make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                           pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+                make_uint4(pack_h16x2(v[8 * q], v[8 * q + 1], f16),
+                           pack_h16x2(v[8 * q + 2], v[8 * q + 3], f16),
+                           pack_h16x2(v[8 * q + 4], v[8 * q + 5], f16),
+                           pack_h16x2(v[8 * q + 6], v[8 * q + 7], f16));
     }
     __device__ __forceinline__ void issue(const CUtensorMap *map, int x, int y) const {
         fence_proxy_async_smem();
@@ -301,8 +314,8 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
         if (ncols <= 0 || !box_rows) return;
         float scale = 0.f, lse2 = 0.f;
         if (row_ok) {
-            scale = lce_row_scale(p.dloss, p.dloss_per_row, p.mean, p.hdr[HDR_NVALID], p.row0 + r,
-                                  y_ok);
+            scale = lce_store_scale(p.dloss, p.dloss_per_row, p.mean, p.hdr[HDR_NVALID],
+                                    p.row0 + r, y_ok, p.f16);
             lse2 = p.lse[p.row0 + r] * LOG2E;
         }
 #pragma unroll 1
@@ -319,7 +332,7 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
                 v[j] = g;
             }
             if ((c & 1) == 0) st.acquire();
-            st.put_bf16((c & 1) * 4, v);
+            st.put_h16((c & 1) * 4, v, p.f16);
             if (c & 1) st.issue(&p.tmS0, col0 + (c >> 1) * 64, box_y);
         }
     } else {
@@ -352,7 +365,7 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
             if constexpr (MODE == MODE_LSE_P) {
                 if ((c >> 1) * 64 < ncols && box_rows) {
                     if ((c & 1) == 0) st.acquire();
-                    st.put_bf16((c & 1) * 4, v);
+                    st.put_h16((c & 1) * 4, v, p.f16);
                     if (c & 1) st.issue(&p.tmS0, col0 + (c >> 1) * 64, box_y);
                 }
             }
@@ -364,10 +377,11 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
     }
 }
 
-// Gradient tiles: dH (bf16) or dW (fp32, stored for the first chunk,
-// reduce-added into dW afterwards).
+// Gradient tiles: dH (bf16 / fp16, or fp32 when dh_fp32) or dW (fp32, stored
+// for the first chunk, reduce-added into dW afterwards). out_scale: the factor
+// fp16 calls apply here instead of in G (1 for bf16).
 __device__ __forceinline__ void epilogue_grad(const GemmParams &p, const Tile &tl, uint32_t taddr,
-                                              int half, const HalfStager &st) {
+                                              int half, const HalfStager &st, float out_scale) {
     const int col0 = tl.n0 + half * 128;
     if (col0 >= p.D) return;  // this half is past D (same for the 4 warps)
     // a tile entirely past the output rows (the second tile of a CTA pair at an
@@ -377,10 +391,14 @@ __device__ __forceinline__ void epilogue_grad(const GemmParams &p, const Tile &t
     for (int c = 0; c < 4; ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
+        if (p.f16) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= out_scale;
+        }
         if (tl.type == TILE_MAIN && !p.dh_fp32) {
             if (col0 + (c >> 1) * 64 >= p.D) continue;
             if ((c & 1) == 0) st.acquire();
-            st.put_bf16((c & 1) * 4, v);
+            st.put_h16((c & 1) * 4, v, p.f16);
             if (c & 1) st.issue(&p.tmS0, ST_STORE, col0 + (c >> 1) * 64, tl.m0);
         } else if (tl.type == TILE_MAIN) {
             if (col0 + c * 32 >= p.D) continue;
@@ -641,7 +659,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                 // dW tiles (A = G^T); everything else is K-major
                 const bool b_mn = (MODE == MODE_BWD) && tl.type != TILE_DW;
                 const bool a_mn = (MODE == MODE_BWD) && tl.type == TILE_DW;
-                const uint32_t idesc = idesc_bf16(CL * BM, BN, a_mn, b_mn);
+                const uint32_t idesc = idesc_f16kind(CL * BM, BN, a_mn, b_mn, p.f16 != 0);
                 const uint32_t a_lbo = a_mn ? 8192u : 16u;
                 const uint32_t b_lbo = b_mn ? 8192u : 16u;
                 const uint32_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);
@@ -692,6 +710,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
         WarpStager wst;
         wst.buf = smem + PIPE_BYTES + warp * (2 * STAGING_BYTES / NUM_EPI_WARPS);
         wst.lane = lane;
+        const float out_scale =
+            MODE == MODE_BWD ? lce_out_scale(p.dloss, p.mean, p.hdr[HDR_NVALID], p.f16) : 1.f;
         int sq = 0;
         uint32_t sphase = 0;
         int acc = 0;
@@ -713,7 +733,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
             if (MODE != MODE_BWD) {
                 epilogue_logits<MODE>(p, tl, taddr, quarter, half, wst);
             } else {
-                epilogue_grad(p, tl, taddr, half, st);
+                epilogue_grad(p, tl, taddr, half, st, out_scale);
             }
             tc_fence_before();
             __syncwarp();

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -59,6 +60,28 @@ __device__ __forceinline__ float lce_row_scale(const float *dloss, int dloss_per
     return d;
 }
 
+// fp16 inputs: G is stored in fp16, where dloss / N_valid (~1e-4 at the
+// workloads' sizes) would push it below the format's range. So for fp16 the
+// stored G is (p - onehot) * F16_G_SCALE (|G| <= 2^14), and the gradient
+// epilogues multiply the dH / dW accumulators by (dloss / N_valid) / F16_G_SCALE
+// (reduction mean; dloss / F16_G_SCALE for sum). bf16 keeps the full scale in G.
+constexpr float F16_G_SCALE = 16384.f;
+
+// Scale of row i of the stored G.
+__device__ __forceinline__ float lce_store_scale(const float *dloss, int dloss_per_row, int mean,
+                                                 int n_valid, long long grow, bool y_ok, int f16) {
+    if (!f16) return lce_row_scale(dloss, dloss_per_row, mean, n_valid, grow, y_ok);
+    return y_ok ? F16_G_SCALE : 0.f;
+}
+
+// Factor the gradient epilogues apply to their accumulators (1 for bf16).
+__device__ __forceinline__ float lce_out_scale(const float *dloss, int mean, int n_valid, int f16) {
+    if (!f16) return 1.f;
+    const float d = dloss ? dloss[0] : 1.f;
+    if (mean) return n_valid > 0 ? d / (static_cast<float>(n_valid) * F16_G_SCALE) : 0.f;
+    return d / F16_G_SCALE;
+}
+
 // Workspace header (int32 words).
 enum : int {
     HDR_FLAG = 0,       // bit 0: label out of range, bit 1: pipeline wait timed out
@@ -101,6 +124,7 @@ struct GemmParams {
     float *dW;             // [V][D]
     int dw_accumulate;     // 0: store, 1: add to existing dW
     int dh_fp32;           // 1: dH tiles stored as fp32 (tmS0 an fp32 map)
+    int f16;               // 1: fp16 operands (H, W, G) and fp16 P' / G / dH stores
     unsigned long long timeout_ns;
 };
 
@@ -117,6 +141,7 @@ struct MergeParams {
     const float *dloss;
     int dloss_per_row;
     int mean;
+    int f16;               // fp16 inputs: slab factors use lce_store_scale
     float *lse;            // global [N]
     float *loss_rows;      // global [N] (the caller's loss vector for reduction none)
 };
@@ -142,6 +167,7 @@ struct FixupParams {
     const float *dloss;
     int dloss_per_row;
     int mean;
+    int f16;                    // fp16 P' / G (scale from lce_store_scale)
 };
 
 // Cross-entropy over precomputed logits Z [N][ld] (bf16 or fp32), one row at a time.
@@ -201,7 +227,7 @@ cudaError_t gemm_set_attributes();
 cudaError_t aux_set_attributes();
 cudaError_t ce_set_attributes();
 cudaError_t launch_wait_selftest(int *hdr, unsigned long long limit_ns, cudaStream_t s);
-cudaError_t launch_add_dh(const float *src, __nv_bfloat16 *dst, long long n, int sms,
+cudaError_t launch_add_dh(const float *src, void *dst, long long n, bool f16, int sms,
                           cudaStream_t s);
 cudaError_t launch_rmsnorm_fwd(const NormParams &p, cudaStream_t s);
 cudaError_t launch_rmsnorm_bwd(const NormParams &p, cudaStream_t s);

@@ -210,15 +210,22 @@ def test_accumulate_workspace_and_flags(L):
     N, D, V, chunk = 16384, 4096, 128256, 1024
     base = ws_size(L, N, D, V, chunk)[1]
     out = ctypes.c_size_t(0)
-    assert L.lce_workspace_size_acc(N, D, V, chunk, 1, ctypes.byref(out)) == OK
+    assert L.lce_workspace_size_opt(N, D, V, chunk, 1, ctypes.byref(out)) == OK
     assert out.value == base                                   # dW accumulation needs nothing
-    assert L.lce_workspace_size_acc(N, D, V, chunk, 3, ctypes.byref(out)) == OK
+    assert L.lce_workspace_size_opt(N, D, V, chunk, 3, ctypes.byref(out)) == OK
     assert out.value == base + 4 * chunk * D                   # the chunk's dH in fp32
-    assert L.lce_workspace_size_acc(N, D, V, chunk, 4, ctypes.byref(out)) == INVALID
+    assert L.lce_workspace_size_opt(N, D, V, chunk, 8, ctypes.byref(out)) == INVALID
     vp = ctypes.c_void_p
     # dH accumulation with only the plain workspace: refused before anything runs
-    assert L.lce_fwd_bwd_acc(vp(FAKE), vp(FAKE), vp(FAKE), None, 128, 64, 1000, -100, 64, 0, 2,
+    assert L.lce_fwd_bwd_opt(vp(FAKE), vp(FAKE), vp(FAKE), None, 128, 64, 1000, -100, 64, 0, 2,
                              vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
                              ws_size(L, 128, 64, 1000, 64)[1], None) == WORKSPACE
-    assert L.lce_backward_acc(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), vp(FAKE), 128,
+    assert L.lce_backward_opt(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), vp(FAKE), 128,
                               64, 1000, -100, 64, 0, 8, vp(FAKE), 1 << 30, None) == INVALID
+    # fp16 inputs with per-row losses: refused
+    UNSUPPORTED = 7
+    assert L.lce_fwd_bwd_opt(vp(FAKE), vp(FAKE), vp(FAKE), None, 128, 64, 1000, -100, 64, 2, 4,
+                             vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 1 << 30,
+                             None) == UNSUPPORTED
+    assert L.lce_forward_opt(vp(FAKE), vp(FAKE), vp(FAKE), 128, 64, 1000, -100, 64, 0, 1, vp(FAKE),
+                             vp(FAKE), vp(FAKE), 1 << 30, None) == INVALID      # no accumulate in fwd
