@@ -55,3 +55,26 @@ def test_reference_arm_is_rank0_only(monkeypatch, capsys):
     args = type("A", (), dict(gpus=2, steps=1, warmup=0))()
     bench.run_reference(args, None, 1024)   # returns at once on rank 1, prints nothing
     assert capsys.readouterr().out == ""
+
+
+def test_bench_defines_every_path_it_dispatches():
+    """bench.py's entry points all exist (a missing one would only surface on a
+    GPU run)."""
+    import ast
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "bench.py")).read()
+    tree = ast.parse(src)
+    defined = set()
+    for n in ast.walk(tree):
+        if isinstance(n, (ast.FunctionDef, ast.ClassDef)):
+            defined.add(n.name)
+        elif isinstance(n, (ast.Import, ast.ImportFrom)):
+            defined.update((a.asname or a.name).split(".")[0] for a in n.names)
+        elif isinstance(n, ast.Name) and isinstance(n.ctx, ast.Store):
+            defined.add(n.id)
+        elif isinstance(n, ast.arg):
+            defined.add(n.arg)
+    called = {n.func.id for n in ast.walk(tree)
+              if isinstance(n, ast.Call) and isinstance(n.func, ast.Name)}
+    builtins = set(dir(__import__("builtins")))
+    missing = {c for c in called if c not in defined and c not in builtins}
+    assert not missing, missing
