@@ -549,26 +549,49 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
             uint32_t sphase = 0;
             int issued = 0;  // loads issued (for the drain on abort)
             bool ok = true;
+            // The leader fetches tiles from the global counter and publishes them to
+            // both CTAs' schedule rings one tile ahead of its own streaming: while it
+            // streams tile i, tile i+1 is already in the rings (so the peer's
+            // producer and the MMA warp never wait for it at the tile boundary) and
+            // the counter fetch for tile i+2 is in flight (its latency is hidden
+            // behind tile i's loads).
+            auto publish = [&](int v) -> bool {
+                if (!mbar_wait_cluster(&sempty_bar[sq], sphase ^ 1, ab)) return false;
+                sched_tile[sq] = v;
+                if constexpr (CL == 2) {
+                    st_cluster_u32(map_to_rank(&sched_tile[sq], 1), v);
+                    mbar_arrive_cluster(map_to_rank(&sfull_bar[sq], 1));
+                }
+                mbar_arrive(&sfull_bar[sq]);
+                if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
+                return true;
+            };
+            int t_lead = -1;      // leader: the tile it streams next
+            int pending_raw = 0;  // leader: counter value fetched for the tile after that
+            if (leader) {
+                const int f = atomicAdd(p.tile_counter, 1);
+                t_lead = f < p.total_tiles ? f : -1;
+                ok = publish(t_lead);
+                if (ok && t_lead >= 0) pending_raw = atomicAdd(p.tile_counter, 1);
+            }
             while (ok) {
                 int t;
                 if (leader) {
-                    // the leader fetches the next tile and publishes it to both CTAs
-                    if (!mbar_wait_cluster(&sempty_bar[sq], sphase ^ 1, ab)) { ok = false; break; }
-                    t = atomicAdd(p.tile_counter, 1);
-                    if (t >= p.total_tiles) t = -1;
-                    sched_tile[sq] = t;
-                    if constexpr (CL == 2) {
-                        st_cluster_u32(map_to_rank(&sched_tile[sq], 1), t);
-                        mbar_arrive_cluster(map_to_rank(&sfull_bar[sq], 1));
-                    }
-                    mbar_arrive(&sfull_bar[sq]);
+                    if (t_lead < 0) break;
+                    // publish the next tile (fetched one tile ago), fetch the one after;
+                    // the fetched value is first needed a tile from now
+                    const int nxt = pending_raw < p.total_tiles ? pending_raw : -1;
+                    if (!publish(nxt)) { ok = false; break; }
+                    if (nxt >= 0) pending_raw = atomicAdd(p.tile_counter, 1);
+                    t = t_lead;
+                    t_lead = nxt;
                 } else {
                     if (!mbar_wait_cluster(&sfull_bar[sq], sphase, ab)) { ok = false; break; }
                     t = sched_tile[sq];
                     release_on_leader(&sempty_bar[sq]);
+                    if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
+                    if (t < 0) break;
                 }
-                if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
-                if (t < 0) break;
                 const Tile tl = decode_tile<CL>(p, t, static_cast<int>(crank));
                 for (int kb = 0; kb < tl.nk; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, ab)) { ok = false; break; }
