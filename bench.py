@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--chunk", type=int, default=0, help="0: the workload's own chunk")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ce-rows", type=int, default=0,
+                    help="ce-logits path: rows of the logits (0: the workload's N)")
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
                     help="H and W dtype of the fused path (the headline is bf16)")
     ap.add_argument("--path", choices=["fused", "ce-logits", "norm"], default="fused",
@@ -457,11 +459,11 @@ def run_ce_logits(args, wl):
     dev = torch.device("cuda", torch.cuda.current_device())
     lce.build()
     peaks, peak_src = load_peaks()
-    N, V = wl.N, wl.V
+    N, V = (args.ce_rows or wl.N), wl.V
     g = torch.Generator(device=dev).manual_seed(wl.seed)
     Z = torch.randn(N, V, device=dev, generator=g).mul_(1.3).to(torch.bfloat16)
     yv = torch.randint(0, V, (N,), device=dev, generator=g)
-    yv[torch.randperm(N, device=dev, generator=g)[:wl.n_ignored]] = -100
+    yv[torch.randperm(N, device=dev, generator=g)[:wl.n_ignored * N // wl.N]] = -100
     ws = torch.empty(1024 + 4 * N + 1024, dtype=torch.uint8, device=dev)
     loss = torch.empty(1, device=dev)
     lse = torch.empty(N, device=dev)
