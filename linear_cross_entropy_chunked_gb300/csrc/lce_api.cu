@@ -100,7 +100,7 @@ bool make_layout(long long N, long long D, long long V, long long chunk, Layout 
     L.nparts = static_cast<int>(cdiv(V, PART_COLS));
     L.ldg = static_cast<int>(align_up(static_cast<size_t>(V), BN));
     if (static_cast<unsigned long long>(L.C) * L.ldg > (1ull << 40)) return false;
-    L.hdr_bytes = align_up(sizeof(int) * (HDR_COUNTERS + 2 * L.nchunks + 2), 1024);
+    L.hdr_bytes = align_up(sizeof(int) * (HDR_COUNTERS + 3 * L.nchunks + 2), 1024);
     size_t off = L.hdr_bytes;
     L.off_loss_rows = off;
     off += align_up(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1), 1024);
@@ -266,6 +266,32 @@ void prof_end(int idx, cudaStream_t s) {
 
 #define LCE_LAUNCH(expr) LCE_LAUNCH_KIND(LCE_KERNEL_OTHER, c.s, expr)
 
+// A second stream per device for the kernel that runs concurrently with the
+// caller's stream inside one call (fork and join through two events). The
+// mutex keeps the record / wait / launch sequence of one call together when
+// several host threads use the same device.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    std::mutex mu;
+};
+SideStream g_side[64];
+std::mutex g_side_mu;
+
+SideStream *side_stream() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream &ss = g_side[dev];
+    if (!ss.s) {
+        if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+    }
+    return &ss;
+}
+
 lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
                  int64_t V, int64_t ign, int64_t chunk, void *ws, size_t ws_bytes,
                  lce_stream_t stream, bool h_chunked = false, bool f16 = false) {
@@ -391,6 +417,40 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     p.dW = dW;
     p.dw_accumulate = accumulate ? 1 : 0;
     const int units = cl == 2 ? c.pairs : c.sms;
+    if (cl == 2) {
+        // CTA pairs: the dH tiles run 512 columns wide (two MMAs share each A
+        // block: a quarter fewer operand bytes per flop) in one kernel, the dW
+        // tiles in a second kernel on a side stream, concurrently; the first
+        // takes as many pairs as it has tiles, the second all that are free
+        // and the rest as the first finishes.
+        GemmParams ph = p;
+        ph.n_blocks0 = static_cast<int>(cdiv(c.D, BN_WIDE));
+        ph.m_blocks1 = ph.n_blocks1 = ph.k_blocks1 = 0;
+        ph.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * ph.n_blocks0;
+        GemmParams pw = p;
+        pw.m_blocks0 = 0;
+        pw.total_tiles = static_cast<int>(cdiv(p.m_blocks1, cl)) * p.n_blocks1;
+        pw.tile_counter = c.hdr + HDR_COUNTERS + 2 * c.L.nchunks + 2 + slot / 2;
+        SideStream *ss = side_stream();
+        if (!ss) return LCE_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(ss->mu);
+        const int gh = cl * (ph.total_tiles < units ? ph.total_tiles : units);
+        const int gw = cl * (pw.total_tiles < units ? pw.total_tiles : units);
+        const int pi = prof_begin(LCE_KERNEL_GRAD, c.s);
+        if (cudaEventRecord(ss->fork, c.s) != cudaSuccess ||
+            cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
+            return LCE_ERR_CUDA;
+        if (ph.total_tiles > 0 && launch_gemm(MODE_DH, cl, ph, gh, c.s) != cudaSuccess)
+            return LCE_ERR_CUDA;
+        if (pw.total_tiles > 0 && launch_gemm(MODE_BWD, cl, pw, gw, ss->s) != cudaSuccess)
+            return LCE_ERR_CUDA;
+        if (cudaEventRecord(ss->join, ss->s) != cudaSuccess ||
+            cudaStreamWaitEvent(c.s, ss->join, 0) != cudaSuccess)
+            return LCE_ERR_CUDA;
+        prof_end(pi, c.s);
+        g_launches += 2;
+        return LCE_OK;
+    }
     const int grid = cl * (p.total_tiles < units ? p.total_tiles : units);
     LCE_LAUNCH_KIND(LCE_KERNEL_GRAD, c.s, launch_gemm(MODE_BWD, cl, p, grid, c.s));
     return LCE_OK;

@@ -150,14 +150,14 @@ enum : int { TILE_MAIN = 0, TILE_DW = 1 };
 // fastest, so the tiles that share one G^T slab run together); the dynamic
 // schedule lets the SMs left over by the dH tiles start on dW at once.
 template <int CL>
-__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int crank) {
+__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int crank, bool wide) {
     Tile tl;
     const int mp0 = (p.m_blocks0 + CL - 1) / CL;
     const int nH = mp0 * p.n_blocks0;
     if (t < nH) {
         tl.type = TILE_MAIN;
         tl.m0 = ((t % mp0) * CL + crank) * BM;
-        tl.n0 = (t / mp0) * BN;
+        tl.n0 = (t / mp0) * (wide ? BN_WIDE : BN);
         tl.nk = p.k_blocks0;
     } else {
         t -= nH;
@@ -457,7 +457,8 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t mask) {
 
 template <int MODE, int CL>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_constant__ GemmParams p) {
-    using P = Pipe<CL>;
+    using P = Pipe<CL, MODE == MODE_DH>;
+    static_assert(MODE != MODE_DH || CL == 2, "wide dH tiles run on CTA pairs only");
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
     __shared__ __align__(8) uint64_t empty_bar[MAX_STAGES];
@@ -592,7 +593,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                     if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
                     if (t < 0) break;
                 }
-                const Tile tl = decode_tile<CL>(p, t, static_cast<int>(crank));
+                const Tile tl = decode_tile<CL>(p, t, static_cast<int>(crank), MODE == MODE_DH);
                 for (int kb = 0; kb < tl.nk; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, ab)) { ok = false; break; }
                     uint8_t *sA = smem + stage * P::kStageBytes;
@@ -621,6 +622,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                         } else {
                             tma_load_2d(sB, mb, fb, kx, tl.n0);
                         }
+                    } else if constexpr (MODE == MODE_DH) {
+                        // A = G rows (K-major); B = W, MN-major, two 256-column halves
+                        // of which this CTA loads 128 columns each
+                        if (leader) mbar_arrive_expect_tx(fb, 2 * P::kStageBytes);
+                        const uint32_t lfb = map_to_rank(fb, 0);
+                        tma_load_2d_pair(sA, &p.tmA0, lfb, kx, tl.m0);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int nb = tl.n0 + h * BN + static_cast<int>(crank) * (BN / 2);
+                            tma_load_2d_pair(sB + h * 16384, &p.tmB0, lfb, nb, kx);
+                            tma_load_2d_pair(sB + h * 16384 + 8192, &p.tmB0, lfb, nb + 64, kx);
+                        }
+                        (void)ma; (void)mb; (void)ya; (void)a_mn; (void)b_mn;
                     } else {
                         // both CTAs' bytes complete on the leader's barrier
                         if (leader) mbar_arrive_expect_tx(fb, 2 * P::kStageBytes);
@@ -674,13 +688,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                 release_on_leader(&sempty_bar[sq]);
                 if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
                 if (t < 0) break;
-                const Tile tl = decode_tile<CL>(p, t, 0);
+                const Tile tl = decode_tile<CL>(p, t, 0, MODE == MODE_DH);
                 if (!mbar_wait_cluster(&tempty_bar[acc], aphase ^ 1, ab)) { ok = false; break; }
+                // a wide dH tile accumulates into both buffers (acc is 0 at its start)
+                if (MODE == MODE_DH && !mbar_wait_cluster(&tempty_bar[1], aphase ^ 1, ab)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 // MN-major operands: W for the dH tiles (B), the chunk buffer for the
                 // dW tiles (A = G^T); everything else is K-major
-                const bool b_mn = (MODE == MODE_BWD) && tl.type != TILE_DW;
+                const bool b_mn = (MODE == MODE_BWD || MODE == MODE_DH) && tl.type != TILE_DW;
                 const bool a_mn = (MODE == MODE_BWD) && tl.type == TILE_DW;
                 const uint32_t idesc = idesc_f16kind(CL * BM, BN, a_mn, b_mn, p.f16 != 0);
                 const uint32_t a_lbo = a_mn ? 8192u : 16u;
@@ -701,6 +720,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                         const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
                         if constexpr (CL == 2) umma_bf16_pair(d_tmem, a, b, idesc, accumulate);
                         else umma_bf16(d_tmem, a, b, idesc, accumulate);
+                        // the second 256-column half: same A, B 16 KB further on
+                        if constexpr (MODE == MODE_DH)
+                            umma_bf16_pair(d_tmem + BN, a, b + static_cast<uint64_t>(16384u >> 4), idesc,
+                                           accumulate);
                     }
                     any_mma = true;
                     if constexpr (CL == 2) umma_commit_pair(&empty_bar[stage], both);
@@ -708,9 +731,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                     if (++stage == P::kStages) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                if constexpr (CL == 2) umma_commit_pair(&tfull_bar[acc], both);
-                else umma_commit(&tfull_bar[acc]);
-                if (++acc == 2) { acc = 0; aphase ^= 1; }
+                if constexpr (MODE == MODE_DH) {
+                    umma_commit_pair(&tfull_bar[0], both);
+                    umma_commit_pair(&tfull_bar[1], both);
+                    aphase ^= 1;
+                } else {
+                    if constexpr (CL == 2) umma_commit_pair(&tfull_bar[acc], both);
+                    else umma_commit(&tfull_bar[acc]);
+                    if (++acc == 2) { acc = 0; aphase ^= 1; }
+                }
             }
             if (any_mma) {
                 // every MMA (and every arrival it sends to the peer) has completed
@@ -733,8 +762,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
         WarpStager wst;
         wst.buf = smem + PIPE_BYTES + warp * (2 * STAGING_BYTES / NUM_EPI_WARPS);
         wst.lane = lane;
-        const float out_scale =
-            MODE == MODE_BWD ? lce_out_scale(p.dloss, p.mean, p.hdr[HDR_NVALID], p.f16) : 1.f;
+        const float out_scale = (MODE == MODE_BWD || MODE == MODE_DH)
+                                    ? lce_out_scale(p.dloss, p.mean, p.hdr[HDR_NVALID], p.f16)
+                                    : 1.f;
         int sq = 0;
         uint32_t sphase = 0;
         int acc = 0;
@@ -747,13 +777,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
             if (lane == 0) release_on_leader(&sempty_bar[sq]);
             if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
             if (t < 0) break;
-            const Tile tl = decode_tile<CL>(p, t, static_cast<int>(crank));
+            const Tile tl = decode_tile<CL>(p, t, static_cast<int>(crank), MODE == MODE_DH);
             ok = mbar_wait_cluster(&tfull_bar[acc], aphase, ab);
             if (!named_bar_and(st.bar_id, 128, ok)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN + half * 128);
-            if (MODE != MODE_BWD) {
+            if constexpr (MODE == MODE_DH) {
+                // both accumulators of the wide tile: columns n0 .. n0 + 255, then + 256
+                epilogue_grad(p, tl, taddr, half, st, out_scale);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) release_on_leader(&tempty_bar[0]);
+                ok = mbar_wait_cluster(&tfull_bar[1], aphase, ab);
+                if (!named_bar_and(st.bar_id, 128, ok)) break;
+                tc_fence_after();
+                Tile tl2 = tl;
+                tl2.n0 += BN;
+                epilogue_grad(p, tl2, taddr + BN, half, st, out_scale);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) release_on_leader(&tempty_bar[1]);
+                aphase ^= 1;
+                continue;
+            }
+            if constexpr (MODE != MODE_BWD && MODE != MODE_DH) {
                 epilogue_logits<MODE>(p, tl, taddr, quarter, half, wst);
             } else {
                 epilogue_grad(p, tl, taddr, half, st, out_scale);
@@ -800,7 +848,8 @@ cudaError_t gemm_set_attributes() {
     if ((e = set_attr<MODE_LSE, 2>()) != cudaSuccess) return e;
     if ((e = set_attr<MODE_LSE_P, 2>()) != cudaSuccess) return e;
     if ((e = set_attr<MODE_G, 2>()) != cudaSuccess) return e;
-    return set_attr<MODE_BWD, 2>();
+    if ((e = set_attr<MODE_BWD, 2>()) != cudaSuccess) return e;
+    return set_attr<MODE_DH, 2>();
 }
 
 template <int MODE, int CL>
@@ -827,6 +876,7 @@ cudaError_t launch_gemm(int mode, int cluster, const GemmParams &p, int grid, cu
             case MODE_LSE: e = launch_one<MODE_LSE, 2>(p, grid, s); break;
             case MODE_LSE_P: e = launch_one<MODE_LSE_P, 2>(p, grid, s); break;
             case MODE_G: e = launch_one<MODE_G, 2>(p, grid, s); break;
+            case MODE_DH: e = launch_one<MODE_DH, 2>(p, grid, s); break;
             default: e = launch_one<MODE_BWD, 2>(p, grid, s); break;
         }
     } else {

@@ -23,10 +23,13 @@ constexpr int B_BYTES = BN * BK * 2;             // 32 KB
 // Pipeline per CTA. One CTA per tile: 4 stages of A (16 KB) + B (32 KB). CTA
 // pair on one 256 x 256 tile (tcgen05 cta_group::2): each CTA holds its own A
 // rows and half of B, 6 stages of 16 + 16 KB.
-template <int CL> struct Pipe {
-    static constexpr int kStages = CL == 2 ? 6 : 4;
-    static constexpr int kBBytes = B_BYTES / CL;
+// Pipeline stages: A (128 rows x 64) plus this CTA's share of B. WIDE: the
+// CTA-pair dH tiles 512 columns wide (two N = 256 MMAs share A), whose stage
+// carries two B halves.
+template <int CL, bool WIDE = false> struct Pipe {
+    static constexpr int kBBytes = (WIDE ? 2 : 1) * B_BYTES / CL;
     static constexpr int kStageBytes = A_BYTES + kBBytes;
+    static constexpr int kStages = (4 * 48 * 1024) / kStageBytes;
 };
 constexpr int MAX_STAGES = 6;
 constexpr int STAGES = 4;                                  // one-CTA pipeline
@@ -40,6 +43,7 @@ constexpr int MMA_WARP = 9;
 constexpr int GEMM_THREADS = 320;
 constexpr int SCHED_DEPTH = 4;
 constexpr int TMEM_COLS = 512;
+constexpr int BN_WIDE = 512;   // MODE_DH tile width: both 256-column TMEM accumulators
 constexpr int PART_COLS = 128;     // columns covered by one (max, sum) partial
 
 // Epilogue / tile-set modes of the GEMM kernel.
@@ -47,7 +51,8 @@ enum GemmMode : int {
     MODE_LSE = 0,     // logits tiles -> per-(row, 128-col) (max, sumexp) partials + target logit
     MODE_LSE_P = 1,   // ... + store P' = exp(z - max_part) as bf16 into the chunk buffer
     MODE_G = 2,       // logits tiles -> G = (exp(z - lse) - onehot) * scale as bf16 (given lse)
-    MODE_BWD = 3      // dH tiles (G W) followed by dW tiles (G^T H) in one persistent launch
+    MODE_BWD = 3,     // dH tiles (G W) followed by dW tiles (G^T H) in one persistent launch
+    MODE_DH = 4       // dH tiles only, 256 rows x 512 columns per CTA pair (CTA pairs only)
 };
 
 // Scale of row i of G: dloss (a scalar, or row i of a per-row vector) divided
