@@ -247,9 +247,12 @@ __global__ void __launch_bounds__(256) lce_dgamma_reduce_kernel(const float *par
     dgamma[j] = s;
 }
 
+// The forward keeps no per-CTA state across rows, so it takes one CTA per row
+// (up to 2048, then rows are strided): a chunk's rows are all in flight at once.
 template <int VPT>
 cudaError_t launch_fwd_vpt(const NormParams &p, cudaStream_t s) {
-    lce_rmsnorm_fwd_kernel<VPT><<<NRM_GRID, NRM_THREADS, 0, s>>>(p);
+    const int grid = p.rows < 2048 ? static_cast<int>(p.rows) : 2048;
+    lce_rmsnorm_fwd_kernel<VPT><<<grid, NRM_THREADS, 0, s>>>(p);
     return cudaGetLastError();
 }
 
