@@ -4,8 +4,10 @@ The compute runs in liblce_gb300.so (tcgen05/TMEM/TMA kernels behind a C ABI,
 include/lce.h); this package is the thin ctypes binding around it.
 """
 from ._binding import (  # noqa: F401
+    ACCUMULATE,
     EXPORTED,
     IGNORE_INDEX,
+    INPUT_FP16,
     KERNEL_KINDS,
     LCEError,
     LinearCrossEntropyFunction,
@@ -29,5 +31,6 @@ from ._binding import (  # noqa: F401
     rmsnorm_forward,
     selftest_wait_timeout,
     workspace_size,
+    workspace_size_opt,
 )
 from .build_lib import LIB_PATH, build  # noqa: F401

@@ -87,9 +87,25 @@ struct Layout {
     int nparts = 0;          // 128-column slabs per row
     int ldg = 0;             // row stride of the chunk buffer (elements)
     int ldt = 0;             // row stride (elements) of H^T: chunk rows rounded up
-    size_t off_loss_rows = 0, off_zy = 0, off_parts = 0, off_G = 0, off_HT = 0, total = 0;
+    int dh_splits = 1;       // vocabulary parts of a full chunk's dH tiles
+    long long ldp = 0;       // rows per fp32 dH partial array: chunk rows rounded up to 128
+    size_t off_loss_rows = 0, off_zy = 0, off_parts = 0, off_G = 0, off_HT = 0, off_dHp = 0;
+    size_t total = 0;
     size_t hdr_bytes = 0;
 };
+
+// Vocabulary parts of the dH tiles of a chunk of `rows` rows (CTA-pair tiles of
+// 256 x 512): enough for DH_SPLIT_TILES tiles, at most DH_MAX_SPLITS and at most
+// one per 64-column k block; one below DH_SPLIT_MIN_V. A function of the shapes
+// alone, so a result does not depend on the device it ran on.
+int dh_splits_for(long long rows, long long D, long long V) {
+    if (V < DH_SPLIT_MIN_V || rows <= 0) return 1;
+    const long long tiles = cdiv(cdiv(rows, BM), 2) * cdiv(D, BN_WIDE);
+    long long sp = cdiv(DH_SPLIT_TILES, tiles);
+    if (sp > DH_MAX_SPLITS) sp = DH_MAX_SPLITS;
+    if (sp > cdiv(V, BK)) sp = cdiv(V, BK);
+    return sp < 1 ? 1 : static_cast<int>(sp);
+}
 
 bool make_layout(long long N, long long D, long long V, long long chunk, Layout &L) {
     if (N < 0 || D <= 0 || V <= 0 || chunk <= 0) return false;
@@ -114,6 +130,13 @@ bool make_layout(long long N, long long D, long long V, long long chunk, Layout 
     L.ldt = static_cast<int>(align_up(static_cast<size_t>(L.C), 64));
     L.off_HT = off;
     off += align_up(2 * static_cast<size_t>(D) * L.ldt, 1024);
+    // fp32 dH partial sums of a split dH contraction, one [ldp][D] array per part
+    // (a single array, past `total`, serves callers that accumulate into dH)
+    L.dh_splits = dh_splits_for(L.C, D, V);
+    L.ldp = static_cast<long long>(align_up(static_cast<size_t>(L.C), BM));
+    L.off_dHp = off;
+    if (L.dh_splits > 1)
+        off += align_up(4 * static_cast<size_t>(L.dh_splits) * L.ldp * static_cast<size_t>(D), 1024);
     L.total = off;
     return true;
 }
@@ -127,20 +150,22 @@ struct NormLayout {
     size_t off_H = 0, off_dH = 0, off_part = 0, total = 0;
 };
 
-// Bytes past the loss path's workspace that accumulating into dH needs: the
-// chunk's dH in fp32, added to the caller's dH once the chunk is done.
+// Bytes past the loss path's workspace that accumulating into dH (and the
+// RMSNorm path) need: one fp32 dH array for the chunk, added to the caller's dH
+// once the chunk is done; none when the layout already holds split partials.
 size_t acc_dh_bytes(const Layout &L, long long D) {
-    return align_up(4 * static_cast<size_t>(L.C) * static_cast<size_t>(D), 1024);
+    if (L.dh_splits > 1) return 0;
+    return align_up(4 * static_cast<size_t>(L.ldp) * static_cast<size_t>(D), 1024);
 }
 
 bool make_norm_layout(long long N, long long D, long long V, long long chunk, NormLayout &NL) {
     if (!make_layout(N, D, V, chunk, NL.L)) return false;
     if (D > NRM_MAX_D) return false;
-    size_t off = NL.L.total;
+    // the chunk's dH (fp32): the layout's partial arrays, or one array past them
+    NL.off_dH = NL.L.off_dHp;
+    size_t off = NL.L.total + acc_dh_bytes(NL.L, D);
     NL.off_H = off;
     off += align_up(2 * static_cast<size_t>(NL.L.C) * D, 1024);
-    NL.off_dH = off;
-    off += align_up(4 * static_cast<size_t>(NL.L.C) * D, 1024);
     NL.off_part = off;
     off += align_up(4 * static_cast<size_t>(NRM_GRID) * D, 1024);
     NL.total = off;
@@ -377,12 +402,39 @@ lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, in
     return LCE_OK;
 }
 
-// dHc: this chunk's dH rows (bf16, or fp32 when dh_fp32).
-lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void *dHc, bool dh_fp32,
-                   float *dW, bool accumulate, const float *dloss) {
+#define LCE_TRY(expr)                         \
+    do {                                      \
+        lce_status _st = (expr);              \
+        if (_st != LCE_OK) return _st;        \
+    } while (0)
+
+// Where a gradient phase leaves dH: the caller's rows (bf16 / fp16, stored by the
+// dH tiles directly), or fp32 partial sums, `parts` arrays of ldp rows x D (one
+// per vocabulary part of the dH tiles), for a combining kernel to add up.
+struct DhOut {
+    void *ptr;
+    bool fp32;
+    int parts;
+    long long ldp;
+};
+
+// Vocabulary parts for a chunk of `rows` rows: one off the CTA-pair path (its
+// 256-column dH tiles are many), else the shapes' split, at most the layout's.
+int dh_parts(const Ctx &c, long long rows) {
+    if (c.pairs <= 0) return 1;
+    const int sp = dh_splits_for(rows, c.D, c.V);
+    return sp < c.L.dh_splits ? sp : c.L.dh_splits;
+}
+
+// *parts_used: the number of non-empty vocabulary parts written (fp32 output).
+lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const DhOut &o,
+                   float *dW, bool accumulate, const float *dloss, int *parts_used = nullptr) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
     base_params(c, p, row0, rows, slot);
+    void *dHc = o.ptr;
+    const bool dh_fp32 = o.fp32;
+    const int want_parts = (o.fp32 && o.parts > 1 && c.pairs > 0) ? o.parts : 1;
     const __nv_bfloat16 *Hc = c.h_chunked ? c.H : c.H + row0 * c.D;
     // the H chunk^T for the K-major B operand of the dW tiles
     TransposeParams tp;
@@ -399,7 +451,8 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     if (!encode_2d(&p.tmA1, c.G, c.V, rows, 2ull * c.L.ldg, 64, BK, c.t16)) return LCE_ERR_CUDA;
     const int cl = c.pairs > 0 ? 2 : 1;
     if (!encode_2d(&p.tmB1, c.HT, rows, c.D, 2ull * c.L.ldt, BK, BN / cl, c.t16)) return LCE_ERR_CUDA;
-    if (!encode_store_2d(&p.tmS0, dHc, c.D, rows, (dh_fp32 ? 4ull : 2ull) * c.D,
+    const uint64_t s0_rows = want_parts > 1 ? static_cast<uint64_t>(want_parts) * o.ldp : rows;
+    if (!encode_store_2d(&p.tmS0, dHc, c.D, s0_rows, (dh_fp32 ? 4ull : 2ull) * c.D,
                          dh_fp32 ? MAP_F32 : c.t16))
         return LCE_ERR_CUDA;
     if (!encode_store_2d(&p.tmS1, dW, c.D, c.V, 4ull * c.D, MAP_F32)) return LCE_ERR_CUDA;
@@ -411,6 +464,14 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     p.k_blocks1 = static_cast<int>(cdiv(rows, BK));
     p.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * p.n_blocks0 +
                     static_cast<int>(cdiv(p.m_blocks1, cl)) * p.n_blocks1;
+    int parts = 1;
+    if (want_parts > 1) {
+        p.kb_per_split = static_cast<int>(cdiv(p.k_blocks0, want_parts));
+        parts = static_cast<int>(cdiv(p.k_blocks0, p.kb_per_split));
+        p.k_splits = parts;
+        p.split_rows = static_cast<int>(o.ldp);
+    }
+    if (parts_used) *parts_used = parts;
     p.dH = static_cast<__nv_bfloat16 *>(dHc);
     p.dh_fp32 = dh_fp32 ? 1 : 0;
     p.dloss = dloss;   // fp16: the epilogues apply the uniform part of the scale
@@ -426,7 +487,7 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
         GemmParams ph = p;
         ph.n_blocks0 = static_cast<int>(cdiv(c.D, BN_WIDE));
         ph.m_blocks1 = ph.n_blocks1 = ph.k_blocks1 = 0;
-        ph.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * ph.n_blocks0;
+        ph.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * ph.n_blocks0 * parts;
         GemmParams pw = p;
         pw.m_blocks0 = 0;
         pw.total_tiles = static_cast<int>(cdiv(p.m_blocks1, cl)) * p.n_blocks1;
@@ -453,6 +514,24 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, void 
     }
     const int grid = cl * (p.total_tiles < units ? p.total_tiles : units);
     LCE_LAUNCH_KIND(LCE_KERNEL_GRAD, c.s, launch_gemm(MODE_BWD, cl, p, grid, c.s));
+    return LCE_OK;
+}
+
+// A chunk's gradient phase on the loss path: dH straight into the caller's rows
+// when there is one vocabulary part and nothing to accumulate, else through the
+// fp32 partial arrays and the combining kernel (which adds into the caller's dH
+// when accumulating).
+lce_status run_grad(const Ctx &c, long long row0, long long rows, int slot, void *dHc,
+                    bool acc_dh, float *dW, bool acc_dw, const float *dloss) {
+    const int want = dh_parts(c, rows);
+    if (want <= 1 && !acc_dh)
+        return run_bwd(c, row0, rows, slot, DhOut{dHc, false, 1, 0}, dW, acc_dw, dloss);
+    float *dHp = reinterpret_cast<float *>(c.ws + c.L.off_dHp);
+    int parts = 1;
+    LCE_TRY(run_bwd(c, row0, rows, slot, DhOut{dHp, true, want, c.L.ldp}, dW, acc_dw, dloss,
+                    &parts));
+    LCE_LAUNCH(launch_combine_dh(dHp, parts, c.L.ldp * c.D, dHc, rows * c.D, c.f16, acc_dh,
+                                 c.sms, c.s));
     return LCE_OK;
 }
 
@@ -500,12 +579,6 @@ lce_status run_fixup(const Ctx &c, long long row0, long long rows, const float *
     LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_fixup(fp, c.s));
     return LCE_OK;
 }
-
-#define LCE_TRY(expr)                         \
-    do {                                      \
-        lce_status _st = (expr);              \
-        if (_st != LCE_OK) return _st;        \
-    } while (0)
 
 }  // namespace
 
@@ -589,7 +662,6 @@ lce_status lce_backward_opt(const void *H, const void *W, const int64_t *y, cons
     Ctx c;
     LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, false, f16));
     c.reduction = reduction;
-    float *dHacc = reinterpret_cast<float *>(c.ws + c.L.total);
     if (c.L.nchunks == 0 && !(flags & LCE_ACCUMULATE_DW)) {
         if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess)
             return LCE_ERR_CUDA;
@@ -599,9 +671,8 @@ lce_status lce_backward_opt(const void *H, const void *W, const int64_t *y, cons
         const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
         __nv_bfloat16 *dHc = static_cast<__nv_bfloat16 *>(dH) + row0 * c.D;
         LCE_TRY(run_logits(c, MODE_G, row0, rows, static_cast<int>(2 * k), lse, dloss));
-        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), acc_dh ? static_cast<void *>(dHacc) : dHc,
-                        acc_dh, dW, k > 0 || (flags & LCE_ACCUMULATE_DW), dloss));
-        if (acc_dh) LCE_LAUNCH(launch_add_dh(dHacc, dHc, rows * c.D, c.f16, c.sms, c.s));
+        LCE_TRY(run_grad(c, row0, rows, static_cast<int>(2 * k + 1), dHc, acc_dh, dW,
+                         k > 0 || (flags & LCE_ACCUMULATE_DW), dloss));
     }
     return LCE_OK;
 }
@@ -644,7 +715,6 @@ lce_status lce_fwd_bwd_opt(const void *H, const void *W, const int64_t *y, const
     LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, false, f16));
     c.reduction = reduction;
     float *rows_out = none ? loss : c.loss_rows;
-    float *dHacc = reinterpret_cast<float *>(c.ws + c.L.total);
     if (c.L.nchunks == 0 && !(flags & LCE_ACCUMULATE_DW)) {
         if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess)
             return LCE_ERR_CUDA;
@@ -656,9 +726,8 @@ lce_status lce_fwd_bwd_opt(const void *H, const void *W, const int64_t *y, const
         LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr));
         LCE_TRY(run_merge(c, true, row0, rows, lse, dloss, rows_out));
         LCE_TRY(run_fixup(c, row0, rows, dloss));
-        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), acc_dh ? static_cast<void *>(dHacc) : dHc,
-                        acc_dh, dW, k > 0 || (flags & LCE_ACCUMULATE_DW), dloss));
-        if (acc_dh) LCE_LAUNCH(launch_add_dh(dHacc, dHc, rows * c.D, c.f16, c.sms, c.s));
+        LCE_TRY(run_grad(c, row0, rows, static_cast<int>(2 * k + 1), dHc, acc_dh, dW,
+                         k > 0 || (flags & LCE_ACCUMULATE_DW), dloss));
     }
     if (!none)
         LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss,
@@ -800,10 +869,14 @@ lce_status lce_norm_fwd_bwd(const void *X, const void *gamma, float eps, const v
         LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr));
         LCE_TRY(run_merge(c, true, row0, rows, lse, dloss, rows_out));
         LCE_TRY(run_fixup(c, row0, rows, dloss));
-        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1), dHbuf, true, dW, k > 0, dloss));
+        int parts = 1;
+        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1),
+                        DhOut{dHbuf, true, dh_parts(c, rows), c.L.ldp}, dW, k > 0, dloss, &parts));
         np.H = nullptr;
         np.dH = dHbuf;
         np.dh_fp32 = 1;
+        np.dh_splits = parts;
+        np.dh_split_stride = c.L.ldp * c.D;
         np.dX = dXb + row0 * c.D;
         np.part = part;
         np.first = k == 0 ? 1 : 0;

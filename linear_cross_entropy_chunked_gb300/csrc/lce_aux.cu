@@ -247,28 +247,41 @@ __global__ void __launch_bounds__(1024) lce_loss_finalize_kernel(const float *__
     }
 }
 
-// ------------------------------------------------------------------ dH accumulation
-// dst[rows][D] (bf16, or fp16 when F16) += src[rows][D] (fp32, a chunk's dH),
-// rounded once.
-template <bool F16>
-__global__ void __launch_bounds__(256) lce_add_dh_kernel(const float *__restrict__ src,
-                                                        void *__restrict__ dst_, long long nvec) {
+// ------------------------------------------------------------------ dH combination
+// dst[rows][D] (bf16, or fp16 when F16) = (ACC ? dst : 0) + the fp32 partial
+// sums src[s][rows][D], s = 0 .. splits-1 added in that order, rounded once. The
+// fixed order keeps dH bit-reproducible whatever the schedule of the tiles that
+// wrote the partials.
+template <bool F16, bool ACC>
+__global__ void __launch_bounds__(256) lce_combine_dh_kernel(const float *__restrict__ src,
+                                                            int splits, long long stride,
+                                                            void *__restrict__ dst_, long long nvec) {
     uint4 *dst = static_cast<uint4 *>(dst_);
     for (long long i = blockIdx.x * 256ll + threadIdx.x; i < nvec; i += 256ll * gridDim.x) {
-        const float4 a = reinterpret_cast<const float4 *>(src)[2 * i];
-        const float4 b = reinterpret_cast<const float4 *>(src)[2 * i + 1];
-        uint4 d = dst[i];
+        float4 a = reinterpret_cast<const float4 *>(src)[2 * i];
+        float4 b = reinterpret_cast<const float4 *>(src)[2 * i + 1];
+        for (int sp = 1; sp < splits; ++sp) {
+            const float4 *q = reinterpret_cast<const float4 *>(src + sp * stride);
+            const float4 c = q[2 * i], e = q[2 * i + 1];
+            a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+            b.x += e.x; b.y += e.y; b.z += e.z; b.w += e.w;
+        }
         const float s[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint4 d = ACC ? dst[i] : make_uint4(0, 0, 0, 0);
         uint32_t *w = &d.x;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             if constexpr (F16) {
-                const float2 x = __half22float2(*reinterpret_cast<__half2 *>(&w[q]));
+                float2 x = make_float2(0.f, 0.f);
+                if constexpr (ACC) x = __half22float2(*reinterpret_cast<__half2 *>(&w[q]));
                 __half2 h = __floats2half2_rn(x.x + s[2 * q], x.y + s[2 * q + 1]);
                 w[q] = *reinterpret_cast<uint32_t *>(&h);
             } else {
-                const float lo = __uint_as_float(w[q] << 16) + s[2 * q];
-                const float hi = __uint_as_float(w[q] & 0xffff0000u) + s[2 * q + 1];
+                float lo = s[2 * q], hi = s[2 * q + 1];
+                if constexpr (ACC) {
+                    lo += __uint_as_float(w[q] << 16);
+                    hi += __uint_as_float(w[q] & 0xffff0000u);
+                }
                 __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
                 w[q] = *reinterpret_cast<uint32_t *>(&h);
             }
@@ -335,14 +348,18 @@ cudaError_t launch_wait_selftest(int *hdr, unsigned long long limit_ns, cudaStre
     return cudaGetLastError();
 }
 
-cudaError_t launch_add_dh(const float *src, void *dst, long long n, bool f16, int sms,
-                          cudaStream_t s) {
+cudaError_t launch_combine_dh(const float *src, int splits, long long stride, void *dst,
+                              long long n, bool f16, bool accumulate, int sms, cudaStream_t s) {
     const long long nvec = n / 8;
     if (nvec <= 0) return cudaSuccess;
     long long blocks = (nvec + 255) / 256;
     if (blocks > 8ll * sms) blocks = 8ll * sms;
-    if (f16) lce_add_dh_kernel<true><<<static_cast<int>(blocks), 256, 0, s>>>(src, dst, nvec);
-    else lce_add_dh_kernel<false><<<static_cast<int>(blocks), 256, 0, s>>>(src, dst, nvec);
+    const int g = static_cast<int>(blocks);
+    if (splits < 1) splits = 1;
+    if (f16 && accumulate) lce_combine_dh_kernel<true, true><<<g, 256, 0, s>>>(src, splits, stride, dst, nvec);
+    else if (f16) lce_combine_dh_kernel<true, false><<<g, 256, 0, s>>>(src, splits, stride, dst, nvec);
+    else if (accumulate) lce_combine_dh_kernel<false, true><<<g, 256, 0, s>>>(src, splits, stride, dst, nvec);
+    else lce_combine_dh_kernel<false, false><<<g, 256, 0, s>>>(src, splits, stride, dst, nvec);
     return cudaGetLastError();
 }
 

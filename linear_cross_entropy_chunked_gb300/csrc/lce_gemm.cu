@@ -138,7 +138,9 @@ constexpr float LOG2E = 1.4426950408889634f;
 struct Tile {
     int type;   // TILE_MAIN: logits tile or dH tile; TILE_DW: dW tile
     int m0, n0; // element offsets of the output tile
+    int kb0;    // first k block
     int nk;     // k blocks
+    int srow;   // row offset of the tile's store (split dH partial sums; else 0)
 };
 enum : int { TILE_MAIN = 0, TILE_DW = 1 };
 
@@ -146,25 +148,39 @@ enum : int { TILE_MAIN = 0, TILE_DW = 1 };
 // or 2 for a CTA pair that shares the B operand); `t` indexes those units and
 // `crank` picks the CTA's own 128 rows. Logits launches: m fastest, so the
 // chunk's row blocks that share one W slab run together. Gradient launches:
-// the few long dH tiles first (m fastest), then the many short dW tiles (n
-// fastest, so the tiles that share one G^T slab run together); the dynamic
-// schedule lets the SMs left over by the dH tiles start on dW at once.
+// the few long dH tiles first (m fastest, then n, then the vocabulary part
+// of a split dH launch), then the many short dW tiles (n fastest, so the tiles
+// that share one G^T slab run together); the dynamic schedule lets the SMs
+// left over by the dH tiles start on dW at once.
 template <int CL>
 __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int crank, bool wide) {
     Tile tl;
     const int mp0 = (p.m_blocks0 + CL - 1) / CL;
-    const int nH = mp0 * p.n_blocks0;
-    if (t < nH) {
+    const int nH1 = mp0 * p.n_blocks0;
+    const int splits = p.k_splits > 1 ? p.k_splits : 1;
+    if (t < nH1 * splits) {
+        const int sp = t / nH1;
+        t -= sp * nH1;
         tl.type = TILE_MAIN;
         tl.m0 = ((t % mp0) * CL + crank) * BM;
         tl.n0 = (t / mp0) * (wide ? BN_WIDE : BN);
-        tl.nk = p.k_blocks0;
+        if (splits > 1) {
+            tl.kb0 = sp * p.kb_per_split;
+            tl.nk = min(p.kb_per_split, p.k_blocks0 - tl.kb0);
+            tl.srow = sp * p.split_rows;
+        } else {
+            tl.kb0 = 0;
+            tl.nk = p.k_blocks0;
+            tl.srow = 0;
+        }
     } else {
-        t -= nH;
+        t -= nH1 * splits;
         tl.type = TILE_DW;
         tl.n0 = (t % p.n_blocks1) * BN;
         tl.m0 = ((t / p.n_blocks1) * CL + crank) * BM;
+        tl.kb0 = 0;
         tl.nk = p.k_blocks1;
+        tl.srow = 0;
     }
     return tl;
 }
@@ -404,7 +420,7 @@ __device__ __forceinline__ void epilogue_grad(const GemmParams &p, const Tile &t
             if (col0 + c * 32 >= p.D) continue;
             st.acquire();
             st.put_f32(v);
-            st.issue(&p.tmS0, ST_STORE, col0 + c * 32, tl.m0);
+            st.issue(&p.tmS0, ST_STORE, col0 + c * 32, tl.m0 + tl.srow);
         } else {
             if (col0 + c * 32 >= p.D) continue;
             st.acquire();
@@ -599,7 +615,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                     uint8_t *sA = smem + stage * P::kStageBytes;
                     uint8_t *sB = sA + A_BYTES;
                     uint64_t *fb = &full_bar[stage];
-                    const int kx = kb * BK;
+                    const int kx = (tl.kb0 + kb) * BK;
                     const CUtensorMap *ma = (MODE == MODE_BWD && tl.type == TILE_DW) ? &p.tmA1 : &p.tmA0;
                     const int ya = (MODE == MODE_BWD) ? tl.m0 : p.a_row0 + tl.m0;
                     const bool b_mn = (MODE == MODE_BWD) && tl.type != TILE_DW;

@@ -44,6 +44,18 @@ constexpr int GEMM_THREADS = 320;
 constexpr int SCHED_DEPTH = 4;
 constexpr int TMEM_COLS = 512;
 constexpr int BN_WIDE = 512;   // MODE_DH tile width: both 256-column TMEM accumulators
+// dH tiles (256 rows x 512 columns on a CTA pair) run over the whole vocabulary
+// while the dW tiles, which are bound by their fp32 read-modify-write of dW in
+// HBM, run concurrently on the other SMs. The phase is shortest when both sets
+// end together: measured on a GB300 that is about 32 dH tiles (a dH tile pair
+// runs ~1.3x the flop rate of a dW one; 74 pairs). A chunk with fewer dH tiles
+// splits them along the vocabulary until there are at least DH_SPLIT_TILES, in
+// at most DH_MAX_SPLITS parts, for vocabularies of at least DH_SPLIT_MIN_V; more
+// dH tiles than that would crowd the dW tiles into the end of the phase, where
+// all of them at once run into the HBM limit.
+constexpr int DH_SPLIT_TILES = 28;
+constexpr int DH_MAX_SPLITS = 4;
+constexpr long long DH_SPLIT_MIN_V = 8192;
 constexpr int PART_COLS = 128;     // columns covered by one (max, sum) partial
 
 // Epilogue / tile-set modes of the GEMM kernel.
@@ -129,6 +141,10 @@ struct GemmParams {
     float *dW;             // [V][D]
     int dw_accumulate;     // 0: store, 1: add to existing dW
     int dh_fp32;           // 1: dH tiles stored as fp32 (tmS0 an fp32 map)
+    // dH launches: the vocabulary (K) range of every dH tile split in k_splits
+    // parts of kb_per_split k blocks; part s stores fp32 partial sums at row
+    // offset s * split_rows of the tmS0 map (k_splits <= 1: one part, no offset)
+    int k_splits, kb_per_split, split_rows;
     int f16;               // 1: fp16 operands (H, W, G) and fp16 P' / G / dH stores
     unsigned long long timeout_ns;
 };
@@ -206,6 +222,8 @@ struct NormParams {
     float *rstd;                 // forward output [rows] or null
     const void *dH;              // backward input [rows][D], bf16 or fp32
     int dh_fp32;
+    int dh_splits;               // fp32 dH: the sum of this many partial arrays,
+    long long dh_split_stride;   // this many elements apart (dh_splits <= 1: one)
     __nv_bfloat16 *dX;           // backward output [rows][D]
     float *part;                 // backward: [NRM_GRID][D] dgamma partials
     int first;                   // 1: the partials start from zero
@@ -232,8 +250,10 @@ cudaError_t gemm_set_attributes();
 cudaError_t aux_set_attributes();
 cudaError_t ce_set_attributes();
 cudaError_t launch_wait_selftest(int *hdr, unsigned long long limit_ns, cudaStream_t s);
-cudaError_t launch_add_dh(const float *src, void *dst, long long n, bool f16, int sms,
-                          cudaStream_t s);
+// dst[i] (bf16 / fp16, n elements) = (accumulate ? dst[i] : 0) + the sum over
+// s = 0 .. splits-1, in that order, of src[s * stride + i] (fp32)
+cudaError_t launch_combine_dh(const float *src, int splits, long long stride, void *dst,
+                              long long n, bool f16, bool accumulate, int sms, cudaStream_t s);
 cudaError_t launch_rmsnorm_fwd(const NormParams &p, cudaStream_t s);
 cudaError_t launch_rmsnorm_bwd(const NormParams &p, cudaStream_t s);
 cudaError_t launch_dgamma_reduce(const float *part, int D, float *dgamma, cudaStream_t s);

@@ -66,18 +66,29 @@ __device__ __forceinline__ void load_row_bf16(const __nv_bfloat16 *base, long lo
     }
 }
 
+// fp32 dH: the sum of `splits` partial arrays `stride` elements apart, added in
+// order (a split dH contraction leaves its vocabulary parts there)
 template <int VPT, bool DH32>
 __device__ __forceinline__ void load_row_dh(const void *base, long long r, int D, int t,
-                                            float (&dh)[VPT][8]) {
+                                            float (&dh)[VPT][8], int splits, long long stride) {
     const int nvec = D / 8;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = t + k * NRM_THREADS;
         const bool in = v < nvec;
         if constexpr (DH32) {
-            const float4 *dr = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + r * D);
-            const float4 a = in ? dr[2 * v] : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 b = in ? dr[2 * v + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float *row = static_cast<const float *>(base) + r * D;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (in) {
+                a = reinterpret_cast<const float4 *>(row)[2 * v];
+                b = reinterpret_cast<const float4 *>(row)[2 * v + 1];
+                for (int sp = 1; sp < splits; ++sp) {
+                    const float4 *q = reinterpret_cast<const float4 *>(row + sp * stride);
+                    const float4 c = q[2 * v], e = q[2 * v + 1];
+                    a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+                    b.x += e.x; b.y += e.y; b.z += e.z; b.w += e.w;
+                }
+            }
             dh[k][0] = a.x; dh[k][1] = a.y; dh[k][2] = a.z; dh[k][3] = a.w;
             dh[k][4] = b.x; dh[k][5] = b.y; dh[k][6] = b.z; dh[k][7] = b.w;
         } else {
@@ -163,14 +174,15 @@ __global__ void __launch_bounds__(NRM_THREADS) lce_rmsnorm_bwd_kernel(const Norm
     float dc[VPT][8];
     if (r < p.rows) {
         load_row_bf16<VPT>(p.X, r, p.D, t, xc);
-        load_row_dh<VPT, DH32>(p.dH, r, p.D, t, dc);
+        load_row_dh<VPT, DH32>(p.dH, r, p.D, t, dc, p.dh_splits, p.dh_split_stride);
     }
     for (; r < p.rows; r += gridDim.x) {
         uint4 xn[VPT];
         float dn[VPT][8];
         if (r + gridDim.x < p.rows) {
             load_row_bf16<VPT>(p.X, r + gridDim.x, p.D, t, xn);
-            load_row_dh<VPT, DH32>(p.dH, r + gridDim.x, p.D, t, dn);
+            load_row_dh<VPT, DH32>(p.dH, r + gridDim.x, p.D, t, dn, p.dh_splits,
+                                        p.dh_split_stride);
         }
         float ss = 0.f, dot = 0.f;
 #pragma unroll

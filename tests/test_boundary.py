@@ -60,9 +60,11 @@ def test_workspace_size_is_order_chunk_times_V(L):
     assert st == OK
     st, b2 = ws_size(L, 16384, 4096, 128256, 2048)
     assert st == OK
-    # the bf16 chunk buffer (P', then G) dominates: ~2 bytes per chunk row per vocab id
-    assert 2 * 1024 * 128256 <= b1 <= 2 * 1024 * 128256 * 1.15
-    assert 1.8 < b2 / b1 < 2.05
+    # the bf16 chunk buffer (P', then G) dominates: ~2 bytes per chunk row per vocab id;
+    # next come the chunk's H^T (bf16) and, at chunk 1024, the two fp32 dH partial
+    # arrays of the vocabulary-split dH tiles (none at chunk 2048: enough tiles)
+    assert 2 * 1024 * 128256 <= b1 <= 2 * 1024 * 128256 * 1.2
+    assert 1.7 < b2 / b1 < 2.05
     # it does not grow with N beyond O(N) bytes
     st, b3 = ws_size(L, 4 * 16384, 4096, 128256, 1024)
     assert b3 - b1 < 64 * 16384 * 4
@@ -162,8 +164,13 @@ def test_norm_workspace_sizes(L):
     base = ws_size(L, N, D, V, chunk)[1]
     out = ctypes.c_size_t(0)
     assert L.lce_norm_workspace_size(N, D, V, chunk, ctypes.byref(out)) == OK
-    # the loss path's workspace + the chunk's H (bf16) and dH (fp32) + 256 dgamma partial rows
-    assert out.value == base + 2 * chunk * D + 4 * chunk * D + 4 * 256 * D
+    # the loss path's workspace + the chunk's dH (fp32) and H (bf16) + 256 dgamma
+    # partial rows
+    assert out.value == base + 4 * chunk * D + 2 * chunk * D + 4 * 256 * D
+    # two vocabulary parts (chunk 512): the loss path's partial arrays hold dH
+    base2 = ws_size(L, N, D, V, 512)[1]
+    assert L.lce_norm_workspace_size(N, D, V, 512, ctypes.byref(out)) == OK
+    assert out.value == base2 + 2 * 512 * D + 4 * 256 * D
     assert L.lce_norm_workspace_size(N, 8200, V, chunk, ctypes.byref(out)) == INVALID  # D > 8192
     assert L.lce_rmsnorm_backward_workspace_size(D, ctypes.byref(out)) == OK
     assert out.value == 4 * 256 * D
@@ -213,7 +220,10 @@ def test_accumulate_workspace_and_flags(L):
     assert L.lce_workspace_size_opt(N, D, V, chunk, 1, ctypes.byref(out)) == OK
     assert out.value == base                                   # dW accumulation needs nothing
     assert L.lce_workspace_size_opt(N, D, V, chunk, 3, ctypes.byref(out)) == OK
-    assert out.value == base + 4 * chunk * D                   # the chunk's dH in fp32
+    assert out.value == base + 4 * chunk * D   # the chunk's dH in fp32
+    base2 = ws_size(L, N, D, V, 512)[1]        # two vocabulary parts: their arrays serve
+    assert L.lce_workspace_size_opt(N, D, V, 512, 2, ctypes.byref(out)) == OK
+    assert out.value == base2
     assert L.lce_workspace_size_opt(N, D, V, chunk, 8, ctypes.byref(out)) == INVALID
     vp = ctypes.c_void_p
     # dH accumulation with only the plain workspace: refused before anything runs
@@ -229,3 +239,53 @@ def test_accumulate_workspace_and_flags(L):
                              None) == UNSUPPORTED
     assert L.lce_forward_opt(vp(FAKE), vp(FAKE), vp(FAKE), 128, 64, 1000, -100, 64, 0, 1, vp(FAKE),
                              vp(FAKE), vp(FAKE), 1 << 30, None) == INVALID      # no accumulate in fwd
+
+
+def test_library_source_allocates_no_device_memory():
+    """The library takes all device memory from its caller (outputs and a workspace
+    sized by the *_workspace_size calls) or from its own static scratch array: no
+    allocation or free call appears in its code, outside comments."""
+    csrc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "linear_cross_entropy_chunked_gb300", "csrc")
+    pat = re.compile(r"\b(cudaMalloc\w*|cudaFree\w*|cuMemAlloc\w*|cuMemFree\w*|cudaHostAlloc|"
+                     r"cuMemCreate|cudaMallocAsync)\s*\(")
+    hits = []
+    for name in sorted(os.listdir(csrc)):
+        if not name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            continue
+        text = open(os.path.join(csrc, name)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for i, line in enumerate(text.splitlines(), 1):
+            code = line.split("//", 1)[0]
+            if pat.search(code):
+                hits.append(f"{name}:{i}: {code.strip()}")
+    assert not hits, hits
+
+
+def test_dh_vocabulary_split_workspace(L):
+    """The dH tiles of a chunk (256 rows x 512 columns each) are split along the
+    vocabulary until there are at least 28 of them, in at most 4 parts, for
+    vocabularies of at least 8192; each part needs one fp32 [chunk rows rounded up
+    to 128] x D array in the workspace."""
+    N, D, chunk = 4096, 1024, 1024
+    small = ws_size(L, N, D, 8191, chunk)[1]
+    big = ws_size(L, N, D, 8192, chunk)[1]     # same G row stride (both round to 8192)
+    # 4 row pairs x 2 column blocks = 8 tiles -> 4 parts
+    assert big - small == 4 * 4 * 1024 * D
+    # 1000 rows round up to 1024 per part; 4 x 2 tiles again
+    assert ws_size(L, N, D, 8192, 1000)[1] - ws_size(L, N, D, 8191, 1000)[1] == 4 * 4 * 1024 * D
+    stats = lambda c, V: 8 * c * (-(-V // 128))     # per-row (max, sum) of each 128-column slab
+    # Llama-3-8B head: at chunk 512, 2 x 8 = 16 tiles -> 2 parts; at chunk 1024,
+    # 4 x 8 = 32 tiles -> one part, no partial arrays
+    b0 = ws_size(L, 16384, 4096, 128256, 512)[1]
+    g0 = 2 * 512 * 128256 + 2 * 4096 * 512          # G (bf16) and H^T (bf16)
+    assert b0 - g0 >= 2 * 4 * 512 * 4096 + stats(512, 128256)
+    assert b0 - g0 < 2 * 4 * 512 * 4096 + stats(512, 128256) + (1 << 20)
+    b1 = ws_size(L, 16384, 4096, 128256, 1024)[1]
+    assert b1 - (2 * 1024 * 128256 + 2 * 4096 * 1024) < stats(1024, 128256) + (1 << 20)
+    # Qwen-2.5-7B head (D 3584: 7 column blocks): chunk 1024 -> 28 tiles, one part;
+    # chunk 512 -> 14 tiles, 2 parts
+    q1 = ws_size(L, 16384, 3584, 152064, 1024)[1]
+    assert q1 - (2 * 1024 * 152064 + 2 * 3584 * 1024) < stats(1024, 152064) + (1 << 20)
+    q0 = ws_size(L, 16384, 3584, 152064, 512)[1]
+    assert q0 - (2 * 512 * 152064 + 2 * 3584 * 512) >= 2 * 4 * 512 * 3584
