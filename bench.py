@@ -435,6 +435,14 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world):
         ev.record(stream)
     run(3)
     torch.cuda.synchronize(dev)
+    # one step's copies alone (outside the timed region): the host link's rate on
+    # this machine, which bounds E when the copies take longer than a step
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(copy_stream)
+    h2d(0)
+    c1.record(copy_stream)
+    torch.cuda.synchronize(dev)
+    copy_ms = c0.elapsed_time(c1)
     steps = max(3, args.steps // 2)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
@@ -447,6 +455,7 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world):
     h2d_bytes = Hh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8
     return {"value": world * N / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "steps": steps, "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": 4,
+            "h2d_ms_per_step_alone": copy_ms, "h2d_gbs": h2d_bytes / copy_ms / 1e6,
             "note": "every step copies H, W and y from pinned host memory (on a copy stream, "
                     "overlapping the previous step's compute) and reads its loss back"}
 
