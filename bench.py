@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ce-rows", type=int, default=0,
                     help="ce-logits path: rows of the logits (0: the workload's N)")
+    ap.add_argument("--frozen-w", action="store_true",
+                    help="fused path with W frozen (LCE_FROZEN_W: no dW, 4NDV per step), the "
+                         "LoRA / QLoRA setting; the headline trains W")
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
                     help="H and W dtype of the fused path (the headline is bf16)")
     ap.add_argument("--path", choices=["fused", "ce-logits", "norm"], default="fused",
@@ -207,11 +210,11 @@ def run_reference(args, wl, chunk):
 
 # ----------------------------------------------------------------- our arm
 
-def workload_config(wl, chunk, l2):
+def workload_config(wl, chunk, l2, **extra):
     return {"workload": f"{wl.name} LM head N={wl.N} D={wl.D} V={wl.V} chunk={chunk}",
             "N": wl.N, "D": wl.D, "V": wl.V, "chunk": chunk,
             "ignored_rows": wl.n_ignored, "labels": wl.labels, "seed": wl.seed,
-            "global_batch_tokens": wl.N, "l2": l2, "parallelism": "replicas"}
+            "global_batch_tokens": wl.N, "l2": l2, "parallelism": "replicas", **extra}
 
 
 def run_ours(args, wl, chunk):
@@ -237,16 +240,17 @@ def run_ours(args, wl, chunk):
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     mem0 = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)
-    ws = lce.alloc_workspace(N, D, V, chunk, dev)
+    frozen = bool(args.frozen_w)
+    ws = lce.alloc_workspace(N, D, V, chunk, dev, lce.FROZEN_W if frozen else 0)
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     dH = torch.empty(N, D, dtype=Hd.dtype, device=dev)
-    dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+    dW = None if frozen else torch.empty(V, D, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk, loss=loss, lse=lse, dH=dH, dW=dW, ws=ws,
-                        stream=stream)
+                        stream=stream, compute_dW=not frozen)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -256,7 +260,7 @@ def run_ours(args, wl, chunk):
         raise RuntimeError(f"device status {st} after warm-up")
     launches_per_step = lce.last_launch_count()
     extra_bytes = torch.cuda.max_memory_allocated(dev) - mem0 - (
-        lse.numel() * 4 + dH.numel() * 2 + dW.numel() * 4 + 4)
+        lse.numel() * 4 + dH.numel() * 2 + (0 if frozen else dW.numel() * 4) + 4)
 
     # ---- timed region: per-step CUDA events, L2 flushed between steps
     lce.profile_reset()
@@ -292,15 +296,16 @@ def run_ours(args, wl, chunk):
 
     ms_per_step = total_ms / args.steps
     tokens_per_s = job_tokens_per_s(world, N, args.steps, total_ms)
-    flops_step = 6.0 * N * D * V
+    flops_step = (4.0 if frozen else 6.0) * N * D * V
     tflops = flops_step / (ms_per_step / 1e3) / 1e12
     peak_burst = peaks.get("bf16_tflops", 1900.0)
     peak_sust = peaks.get("bf16_tflops_sustained", 1700.0)
 
     # dominant kernel: the gradient phase of a chunk (dH and dW GEMMs, two
-    # concurrent kernels timed together from fork to join: 4*C*D*V flops)
+    # concurrent kernels timed together from fork to join: 4*C*D*V flops; with W
+    # frozen the dH GEMM alone, 2*C*D*V)
     nchunks = (N + chunk - 1) // chunk
-    grad_flops_launch = 4.0 * D * V * N / nchunks
+    grad_flops_launch = (2.0 if frozen else 4.0) * D * V * N / nchunks
     grad_avg_ms = grad_ms / max(grad_n, 1)
     grad_tflops = grad_flops_launch / (grad_avg_ms / 1e3) / 1e12
     logit_avg_ms = logit_ms / max(logit_n, 1)
@@ -310,7 +315,7 @@ def run_ours(args, wl, chunk):
     # ---- end to end through the public API from pinned host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, lce, H, W, y, chunk, dev, stream, world)
+        e2e = run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -324,18 +329,22 @@ def run_ours(args, wl, chunk):
             "dtype": args.dtype, "data": "synthetic",
             "config": workload_config(wl, chunk,
                                       l2="L2 flushed between steps (256 MB write); "
-                                         "W 1.05 GB also exceeds L2"),
+                                         "W 1.05 GB also exceeds L2",
+                                      **({"frozen_w": True} if frozen else {})),
             "tflops": tflops,
             "pct_of_bf16_peak": {"vs_burst": tflops / peak_burst, "vs_sustained": tflops / peak_sust,
-                                 "flops": "6NDV algorithmic", "peak_source": peak_src},
+                                 "flops": "4NDV algorithmic (W frozen: no dW)" if frozen
+                                 else "6NDV algorithmic", "peak_source": peak_src},
             "peak_extra_hbm_bytes": int(extra_bytes),
             "workspace_bytes": int(ws.numel()),
-            "roofline": {"kernel": "gradient phase: lce_gemm_kernel<MODE_DH> (dH tiles, 512 wide) "
+            "roofline": {"kernel": "gradient phase, W frozen: lce_gemm_kernel<MODE_DH> (dH tiles, "
+                                   "512 wide, split along the vocabulary) alone" if frozen else
+                                   "gradient phase: lce_gemm_kernel<MODE_DH> (dH tiles, 512 wide) "
                                    "+ lce_gemm_kernel<MODE_BWD> (dW tiles), concurrent",
                          "bound": "tensor", "achieved": grad_tflops, "peak": peak_sust,
                          "peak_kind": f"bf16_tflops_sustained ({peak_src})",
                          "unit": "TFLOP/s", "frac": grad_tflops / peak_sust,
-                         "traffic": traffic.get("grad"),
+                         "traffic": None if frozen else traffic.get("grad"),
                          "launch_ms": grad_avg_ms, "flops_per_launch": grad_flops_launch},
             "kernels": {
                 "grad": {"ms_per_launch": grad_avg_ms, "launches": grad_n,
@@ -385,7 +394,7 @@ def load_traffic():
     return out
 
 
-def run_e2e(args, lce, H, W, y, chunk, dev, stream, world):
+def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False):
     """The same metric through the public API from pinned host buffers: every
     step copies its inputs (H, W, y) host -> device and reads its loss back.
     The copies of step k+1 run on a copy stream while step k computes (two
@@ -397,32 +406,47 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world):
              torch.empty_like(yh, device=dev)) for _ in range(2)]
     N, D = H.shape
     V = W.shape[0]
-    ws = lce.alloc_workspace(N, D, V, chunk, dev)
+    ws = lce.alloc_workspace(N, D, V, chunk, dev, lce.FROZEN_W if frozen else 0)
     loss_h = torch.empty(2, dtype=torch.float32).pin_memory()
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     dH = torch.empty(N, D, dtype=H.dtype, device=dev)
-    dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+    dW = None if frozen else torch.empty(V, D, dtype=torch.float32, device=dev)
     copy_stream = torch.cuda.Stream(dev)
     copied = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
+
+    # (start, end) events of every step's copies and compute: how long each took
+    # under load, and whether the copies stayed hidden behind the compute
+    spans = {"copy": [], "compute": []}
+
+    def timed():
+        return torch.cuda.Event(enable_timing=True)
 
     def h2d(k):
         b = bufs[k % 2]
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(consumed[k % 2])   # the step that last read this buffer
+            e0, e1 = timed(), timed()
+            e0.record(copy_stream)
             b[0].copy_(Hh, non_blocking=True)
             b[1].copy_(Wh, non_blocking=True)
             b[2].copy_(yh, non_blocking=True)
+            e1.record(copy_stream)
             copied[k % 2].record(copy_stream)
+        spans["copy"].append((e0, e1))
 
     def compute(k):
         b = bufs[k % 2]
         stream.wait_event(copied[k % 2])
+        e0, e1 = timed(), timed()
+        e0.record(stream)
         lce.lce_fwd_bwd(b[0], b[1], b[2], chunk=chunk, loss=loss, lse=lse, dH=dH, dW=dW, ws=ws,
-                        stream=stream)
+                        stream=stream, compute_dW=not frozen)
+        e1.record(stream)
         consumed[k % 2].record(stream)
         loss_h[k % 2].copy_(loss[0], non_blocking=True)
+        spans["compute"].append((e0, e1))
 
     def run(steps):
         h2d(0)
@@ -443,6 +467,8 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world):
     c1.record(copy_stream)
     torch.cuda.synchronize(dev)
     copy_ms = c0.elapsed_time(c1)
+    spans["copy"].clear()
+    spans["compute"].clear()
     steps = max(3, args.steps // 2)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
@@ -452,10 +478,13 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world):
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / steps
+    under_load = {k: statistics.mean(e0.elapsed_time(e1) for e0, e1 in v) for k, v in spans.items()}
     h2d_bytes = Hh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8
     return {"value": world * N / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "steps": steps, "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": 4,
             "h2d_ms_per_step_alone": copy_ms, "h2d_gbs": h2d_bytes / copy_ms / 1e6,
+            "h2d_ms_per_step_under_load": under_load["copy"],
+            "compute_ms_per_step_under_load": under_load["compute"],
             "note": "every step copies H, W and y from pinned host memory (on a copy stream, "
                     "overlapping the previous step's compute) and reads its loss back"}
 

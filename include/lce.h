@@ -128,12 +128,27 @@ lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const 
  *                     as (p - onehot) * 2^14 and the gradient GEMMs apply
  *                     dloss / (N_valid * 2^14) to their fp32 accumulators. Reduction
  *                     NONE (a per-row dloss of unknown range inside G) returns
- *                     LCE_ERR_UNSUPPORTED with fp16.
- * With LCE_ACCUMULATE_DH the workspace is lce_workspace_size_opt(..., flags) bytes
- * (the chunk's dH in fp32, 4 * chunk * D bytes more); otherwise it is
- * lce_workspace_size(). lce_forward_opt takes LCE_INPUT_FP16 only. Other arguments
- * and outputs as for the _ex entry points. */
-enum { LCE_ACCUMULATE_DW = 1, LCE_ACCUMULATE_DH = 2, LCE_INPUT_FP16 = 4, LCE_FLAGS_ALL = 7 };
+ *                     LCE_ERR_UNSUPPORTED with fp16;
+ *  LCE_FROZEN_W       W is not trained (a frozen LM head, as in LoRA / QLoRA
+ *                     fine-tuning, the setting of "Unsloth Kernel Architecture:
+ *                     Custom Triton Backpropagation and QLoRA Memory Scaling"; the
+ *                     worked example of "Step 2" computes d_hidden only): dW is not
+ *                     computed and not written, and may be NULL; the gradient phase
+ *                     is the dH contraction alone (4NDV flops per step instead of
+ *                     6NDV). Not with LCE_ACCUMULATE_DW (LCE_ERR_INVALID_ARG).
+ * With LCE_ACCUMULATE_DH or LCE_FROZEN_W the workspace is
+ * lce_workspace_size_opt(..., flags) bytes (the accumulation needs the chunk's dH in
+ * fp32; the frozen-W gradient splits its dH contraction differently); otherwise it
+ * is lce_workspace_size(), which lce_workspace_size_opt(..., 0) equals.
+ * lce_forward_opt takes LCE_INPUT_FP16 only. Other arguments and outputs as for
+ * the _ex entry points. */
+enum {
+    LCE_ACCUMULATE_DW = 1,
+    LCE_ACCUMULATE_DH = 2,
+    LCE_INPUT_FP16 = 4,
+    LCE_FROZEN_W = 8,
+    LCE_FLAGS_ALL = 15
+};
 lce_status lce_workspace_size_opt(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
                                   size_t *bytes);
 lce_status lce_forward_opt(const void *H, const void *W, const int64_t *y,

@@ -6,6 +6,7 @@ include/lce.h); this package is the thin ctypes binding around it.
 from ._binding import (  # noqa: F401
     ACCUMULATE,
     EXPORTED,
+    FROZEN_W,
     IGNORE_INDEX,
     INPUT_FP16,
     KERNEL_KINDS,

@@ -170,9 +170,10 @@ def workspace_size(N: int, D: int, V: int, chunk: int) -> int:
 
 ACCUMULATE = {"dW": 1, "dH": 2}
 INPUT_FP16 = 4
+FROZEN_W = 8
 
 
-def _acc_flags(accumulate, dH, dW) -> int:
+def _acc_flags(accumulate, dH, dW, compute_dW=True) -> int:
     flags = 0
     for name in accumulate:
         if name not in ACCUMULATE:
@@ -180,6 +181,10 @@ def _acc_flags(accumulate, dH, dW) -> int:
         flags |= ACCUMULATE[name]
     if (flags & 1 and dW is None) or (flags & 2 and dH is None):
         raise ValueError("accumulating needs the existing dW / dH tensors passed in")
+    if not compute_dW:
+        if flags & 1:
+            raise ValueError("compute_dW=False (frozen W) cannot accumulate into dW")
+        flags |= FROZEN_W
     return flags
 
 
@@ -191,7 +196,8 @@ def workspace_size_opt(N: int, D: int, V: int, chunk: int, flags: int) -> int:
 
 
 def alloc_workspace(N: int, D: int, V: int, chunk: int, device, flags: int = 0) -> torch.Tensor:
-    n = workspace_size_opt(N, D, V, chunk, flags) if flags & 2 else workspace_size(N, D, V, chunk)
+    n = (workspace_size_opt(N, D, V, chunk, flags) if flags & (ACCUMULATE["dH"] | FROZEN_W)
+         else workspace_size(N, D, V, chunk))
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
@@ -253,17 +259,21 @@ def lce_forward(H, W, y, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
 
 def lce_backward(H, W, y, lse, dloss=None, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
                  dH=None, dW=None, ws=None, stream=None, reduction: str = "mean",
-                 accumulate=()):
+                 accumulate=(), compute_dW: bool = True):
     """dH (bf16) and dW (fp32) from a saved lse. dloss: scalar tensor, or [N] for
     reduction="none"; None means 1. accumulate: a subset of ("dW", "dH") added
-    into the given dW / dH instead of overwriting them."""
+    into the given dW / dH instead of overwriting them. compute_dW=False: W is
+    frozen, dW is neither computed nor returned (None)."""
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
     red = _reduction(reduction)
-    flags = _acc_flags(accumulate, dH, dW) | (INPUT_FP16 if H.dtype == torch.float16 else 0)
+    flags = (_acc_flags(accumulate, dH, dW, compute_dW) |
+             (INPUT_FP16 if H.dtype == torch.float16 else 0))
     if dH is None:
         dH = torch.empty(N, D, dtype=H.dtype, device=dev)
-    if dW is None:
+    if not compute_dW:
+        dW = None
+    elif dW is None:
         dW = torch.empty(V, D, dtype=torch.float32, device=dev)
     if ws is None:
         ws = alloc_workspace(N, D, V, chunk, dev, flags)
@@ -277,19 +287,23 @@ def lce_backward(H, W, y, lse, dloss=None, chunk: int = 1024, ignore_index: int 
 
 def lce_fwd_bwd(H, W, y, dloss=None, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
                 loss=None, lse=None, dH=None, dW=None, ws=None, stream=None,
-                reduction: str = "mean", accumulate=()):
+                reduction: str = "mean", accumulate=(), compute_dW: bool = True):
     """Fused forward + backward: (loss, lse, dH, dW). accumulate: a subset of
-    ("dW", "dH") added into the given dW / dH instead of overwriting them."""
+    ("dW", "dH") added into the given dW / dH instead of overwriting them.
+    compute_dW=False: W is frozen (e.g. a LoRA fine-tune), dW is None."""
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
     red = _reduction(reduction)
-    flags = _acc_flags(accumulate, dH, dW) | (INPUT_FP16 if H.dtype == torch.float16 else 0)
+    flags = (_acc_flags(accumulate, dH, dW, compute_dW) |
+             (INPUT_FP16 if H.dtype == torch.float16 else 0))
     loss = _loss_buffer(loss, N, reduction, dev)
     if lse is None:
         lse = torch.empty(N, dtype=torch.float32, device=dev)
     if dH is None:
         dH = torch.empty(N, D, dtype=H.dtype, device=dev)
-    if dW is None:
+    if not compute_dW:
+        dW = None
+    elif dW is None:
         dW = torch.empty(V, D, dtype=torch.float32, device=dev)
     if ws is None:
         ws = alloc_workspace(N, D, V, chunk, dev, flags)
@@ -474,13 +488,35 @@ def profile_read(kind: str):
 
 
 class LinearCrossEntropyFunction(torch.autograd.Function):
-    """autograd wrapper: forward = lce_forward, backward = lce_backward (recompute)."""
+    """autograd wrapper, two schedules.
+
+    fused (reduction mean or sum, the default): the forward runs lce_fwd_bwd for an
+    upstream gradient of 1 and keeps dH and dW; the backward scales them by the
+    incoming gradient, which the loss is linear in. 6NDV flops per step. The LM
+    head's loss is the first node its backward reaches, so the gradients are
+    held only until then.
+
+    recompute (reduction none, whose per-row incoming gradient is unknown in the
+    forward, or fused=False): forward = lce_forward keeping lse, backward =
+    lce_backward recomputing the logits. 8NDV flops.
+
+    A W that does not require grad is frozen: no dW is computed (LCE_FROZEN_W)."""
 
     @staticmethod
-    def forward(ctx, H, W, y, chunk=1024, ignore_index=IGNORE_INDEX, reduction="mean"):
-        loss, lse = lce_forward(H, W, y, chunk=chunk, ignore_index=ignore_index,
-                                reduction=reduction)
-        ctx.save_for_backward(H, W, y, lse)
+    def forward(ctx, H, W, y, chunk=1024, ignore_index=IGNORE_INDEX, reduction="mean",
+                fused=True):
+        need_dH, need_dW = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        ctx.fused = bool(fused) and reduction != "none" and (need_dH or need_dW)
+        ctx.need_dW = need_dW
+        ctx.w_dtype = W.dtype
+        if ctx.fused:
+            loss, _, dH, dW = lce_fwd_bwd(H, W, y, chunk=chunk, ignore_index=ignore_index,
+                                          reduction=reduction, compute_dW=need_dW)
+            ctx.save_for_backward(dH, dW)
+        else:
+            loss, lse = lce_forward(H, W, y, chunk=chunk, ignore_index=ignore_index,
+                                    reduction=reduction)
+            ctx.save_for_backward(H, W, y, lse)
         ctx.chunk = chunk
         ctx.ignore_index = ignore_index
         ctx.reduction = reduction
@@ -488,15 +524,23 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
 
     @staticmethod
     def backward(ctx, grad_out):
+        if ctx.fused:
+            dH, dW = ctx.saved_tensors
+            g = grad_out.detach().to(torch.float32)
+            gH = (dH.float() * g).to(dH.dtype) if ctx.needs_input_grad[0] else None
+            gW = (dW * g).to(ctx.w_dtype) if dW is not None else None
+            return gH, gW, None, None, None, None, None
         H, W, y, lse = ctx.saved_tensors
         g = grad_out.detach().reshape(-1).to(torch.float32).contiguous()
         dH, dW = lce_backward(H, W, y, lse, dloss=g, chunk=ctx.chunk,
-                              ignore_index=ctx.ignore_index, reduction=ctx.reduction)
-        return dH, dW.to(W.dtype), None, None, None, None
+                              ignore_index=ctx.ignore_index, reduction=ctx.reduction,
+                              compute_dW=ctx.need_dW)
+        return dH, (dW.to(W.dtype) if dW is not None else None), None, None, None, None, None
 
 
 def linear_cross_entropy(H, W, y, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
-                         reduction: str = "mean"):
+                         reduction: str = "mean", fused: bool = True):
     """Cross-entropy of softmax(H W^T) against y (mean, sum or per-row), differentiable
-    in H and W."""
-    return LinearCrossEntropyFunction.apply(H, W, y, chunk, ignore_index, reduction)
+    in H and W (a W with requires_grad False is treated as frozen: no dW work).
+    fused: compute the gradients in the forward pass (reductions mean and sum)."""
+    return LinearCrossEntropyFunction.apply(H, W, y, chunk, ignore_index, reduction, fused)

@@ -87,6 +87,7 @@ struct Layout {
     int nparts = 0;          // 128-column slabs per row
     int ldg = 0;             // row stride of the chunk buffer (elements)
     int ldt = 0;             // row stride (elements) of H^T: chunk rows rounded up
+    bool frozen_w = false;   // no dW contraction (LCE_FROZEN_W)
     int dh_splits = 1;       // vocabulary parts of a full chunk's dH tiles
     long long ldp = 0;       // rows per fp32 dH partial array: chunk rows rounded up to 128
     size_t off_loss_rows = 0, off_zy = 0, off_parts = 0, off_G = 0, off_HT = 0, off_dHp = 0;
@@ -98,16 +99,22 @@ struct Layout {
 // 256 x 512): enough for DH_SPLIT_TILES tiles, at most DH_MAX_SPLITS and at most
 // one per 64-column k block; one below DH_SPLIT_MIN_V. A function of the shapes
 // alone, so a result does not depend on the device it ran on.
-int dh_splits_for(long long rows, long long D, long long V) {
+// With W frozen the dH tiles have the GPU to themselves: they are split into the
+// most parts (at most DH_MAX_SPLITS) that keep them within one wave of the
+// DH_ALONE_PAIRS CTA pairs of a GB300.
+constexpr int DH_ALONE_PAIRS = 74;
+
+int dh_splits_for(long long rows, long long D, long long V, bool frozen_w = false) {
     if (V < DH_SPLIT_MIN_V || rows <= 0) return 1;
     const long long tiles = cdiv(cdiv(rows, BM), 2) * cdiv(D, BN_WIDE);
-    long long sp = cdiv(DH_SPLIT_TILES, tiles);
+    long long sp = frozen_w ? DH_ALONE_PAIRS / tiles : cdiv(DH_SPLIT_TILES, tiles);
     if (sp > DH_MAX_SPLITS) sp = DH_MAX_SPLITS;
     if (sp > cdiv(V, BK)) sp = cdiv(V, BK);
     return sp < 1 ? 1 : static_cast<int>(sp);
 }
 
-bool make_layout(long long N, long long D, long long V, long long chunk, Layout &L) {
+bool make_layout(long long N, long long D, long long V, long long chunk, Layout &L,
+                 bool frozen_w = false) {
     if (N < 0 || D <= 0 || V <= 0 || chunk <= 0) return false;
     if (D % 8 != 0) return false;
     if (N > 0x7fffffffll || D > 0x7fffffffll || V > MAX_V) return false;
@@ -126,13 +133,15 @@ bool make_layout(long long N, long long D, long long V, long long chunk, Layout 
     off += align_up(sizeof(float2) * static_cast<size_t>(L.C) * L.nparts, 1024);
     L.off_G = off;
     off += align_up(2 * static_cast<size_t>(L.C) * L.ldg, 1024);
-    // H chunk^T [D][ldt]: the K-major B operand of the dW contraction
+    // H chunk^T [D][ldt]: the K-major B operand of the dW contraction (none when W
+    // is frozen)
+    L.frozen_w = frozen_w;
     L.ldt = static_cast<int>(align_up(static_cast<size_t>(L.C), 64));
     L.off_HT = off;
-    off += align_up(2 * static_cast<size_t>(D) * L.ldt, 1024);
+    if (!frozen_w) off += align_up(2 * static_cast<size_t>(D) * L.ldt, 1024);
     // fp32 dH partial sums of a split dH contraction, one [ldp][D] array per part
     // (a single array, past `total`, serves callers that accumulate into dH)
-    L.dh_splits = dh_splits_for(L.C, D, V);
+    L.dh_splits = dh_splits_for(L.C, D, V, frozen_w);
     L.ldp = static_cast<long long>(align_up(static_cast<size_t>(L.C), BM));
     L.off_dHp = off;
     if (L.dh_splits > 1)
@@ -319,9 +328,10 @@ SideStream *side_stream() {
 
 lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
                  int64_t V, int64_t ign, int64_t chunk, void *ws, size_t ws_bytes,
-                 lce_stream_t stream, bool h_chunked = false, bool f16 = false) {
+                 lce_stream_t stream, bool h_chunked = false, bool f16 = false,
+                 bool frozen_w = false) {
     g_launches = 0;
-    if (!make_layout(N, D, V, chunk, c.L)) return LCE_ERR_INVALID_ARG;
+    if (!make_layout(N, D, V, chunk, c.L, frozen_w)) return LCE_ERR_INVALID_ARG;
     if (!ws) return LCE_ERR_INVALID_ARG;
     if (N > 0 && (!H || !y)) return LCE_ERR_INVALID_ARG;
     if (!W) return LCE_ERR_INVALID_ARG;
@@ -422,7 +432,7 @@ struct DhOut {
 // 256-column dH tiles are many), else the shapes' split, at most the layout's.
 int dh_parts(const Ctx &c, long long rows) {
     if (c.pairs <= 0) return 1;
-    const int sp = dh_splits_for(rows, c.D, c.V);
+    const int sp = dh_splits_for(rows, c.D, c.V, c.L.frozen_w);
     return sp < c.L.dh_splits ? sp : c.L.dh_splits;
 }
 
@@ -435,33 +445,38 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
     void *dHc = o.ptr;
     const bool dh_fp32 = o.fp32;
     const int want_parts = (o.fp32 && o.parts > 1 && c.pairs > 0) ? o.parts : 1;
-    const __nv_bfloat16 *Hc = c.h_chunked ? c.H : c.H + row0 * c.D;
-    // the H chunk^T for the K-major B operand of the dW tiles
-    TransposeParams tp;
-    tp.src = Hc;
-    tp.ld_src = static_cast<int>(c.D);
-    tp.dst_t = c.HT;
-    tp.ld_t = c.L.ldt;
-    tp.rows = static_cast<int>(rows);
-    tp.cols = static_cast<int>(c.D);
-    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_transpose(tp, c.s));
+    // frozen W: the dH tiles only (no H chunk^T, no dW maps, dW untouched)
+    const bool with_dw = !c.L.frozen_w;
+    const int cl = c.pairs > 0 ? 2 : 1;
+    if (with_dw) {
+        // the H chunk^T for the K-major B operand of the dW tiles
+        const __nv_bfloat16 *Hc = c.h_chunked ? c.H : c.H + row0 * c.D;
+        TransposeParams tp;
+        tp.src = Hc;
+        tp.ld_src = static_cast<int>(c.D);
+        tp.dst_t = c.HT;
+        tp.ld_t = c.L.ldt;
+        tp.rows = static_cast<int>(rows);
+        tp.cols = static_cast<int>(c.D);
+        LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_transpose(tp, c.s));
+        // dW A = G^T read from G itself (MN-major boxes of 64 vocab columns x 64 rows)
+        if (!encode_2d(&p.tmA1, c.G, c.V, rows, 2ull * c.L.ldg, 64, BK, c.t16)) return LCE_ERR_CUDA;
+        if (!encode_2d(&p.tmB1, c.HT, rows, c.D, 2ull * c.L.ldt, BK, BN / cl, c.t16))
+            return LCE_ERR_CUDA;
+        if (!encode_store_2d(&p.tmS1, dW, c.D, c.V, 4ull * c.D, MAP_F32)) return LCE_ERR_CUDA;
+    }
     if (!encode_2d(&p.tmA0, c.G, c.V, rows, 2ull * c.L.ldg, BK, BM, c.t16)) return LCE_ERR_CUDA;
     p.tmB0 = c.tmW_MN;
-    // dW A = G^T read from G itself (MN-major boxes of 64 vocab columns x 64 rows)
-    if (!encode_2d(&p.tmA1, c.G, c.V, rows, 2ull * c.L.ldg, 64, BK, c.t16)) return LCE_ERR_CUDA;
-    const int cl = c.pairs > 0 ? 2 : 1;
-    if (!encode_2d(&p.tmB1, c.HT, rows, c.D, 2ull * c.L.ldt, BK, BN / cl, c.t16)) return LCE_ERR_CUDA;
     const uint64_t s0_rows = want_parts > 1 ? static_cast<uint64_t>(want_parts) * o.ldp : rows;
     if (!encode_store_2d(&p.tmS0, dHc, c.D, s0_rows, (dh_fp32 ? 4ull : 2ull) * c.D,
                          dh_fp32 ? MAP_F32 : c.t16))
         return LCE_ERR_CUDA;
-    if (!encode_store_2d(&p.tmS1, dW, c.D, c.V, 4ull * c.D, MAP_F32)) return LCE_ERR_CUDA;
     p.m_blocks0 = static_cast<int>(cdiv(rows, BM));
     p.n_blocks0 = static_cast<int>(cdiv(c.D, BN));
     p.k_blocks0 = static_cast<int>(cdiv(c.V, BK));
-    p.m_blocks1 = static_cast<int>(cdiv(c.V, BM));
-    p.n_blocks1 = static_cast<int>(cdiv(c.D, BN));
-    p.k_blocks1 = static_cast<int>(cdiv(rows, BK));
+    p.m_blocks1 = with_dw ? static_cast<int>(cdiv(c.V, BM)) : 0;
+    p.n_blocks1 = with_dw ? static_cast<int>(cdiv(c.D, BN)) : 0;
+    p.k_blocks1 = with_dw ? static_cast<int>(cdiv(rows, BK)) : 0;
     p.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * p.n_blocks0 +
                     static_cast<int>(cdiv(p.m_blocks1, cl)) * p.n_blocks1;
     int parts = 1;
@@ -488,6 +503,12 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
         ph.n_blocks0 = static_cast<int>(cdiv(c.D, BN_WIDE));
         ph.m_blocks1 = ph.n_blocks1 = ph.k_blocks1 = 0;
         ph.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * ph.n_blocks0 * parts;
+        if (!with_dw) {
+            const int gh = cl * (ph.total_tiles < units ? ph.total_tiles : units);
+            if (ph.total_tiles > 0)
+                LCE_LAUNCH_KIND(LCE_KERNEL_GRAD, c.s, launch_gemm(MODE_DH, cl, ph, gh, c.s));
+            return LCE_OK;
+        }
         GemmParams pw = p;
         pw.m_blocks0 = 0;
         pw.total_tiles = static_cast<int>(cdiv(p.m_blocks1, cl)) * p.n_blocks1;
@@ -596,7 +617,7 @@ lce_status lce_workspace_size_opt(int64_t N, int64_t D, int64_t V, int64_t chunk
                                   size_t *bytes) {
     if (!bytes || (flags & ~LCE_FLAGS_ALL)) return LCE_ERR_INVALID_ARG;
     Layout L;
-    if (!make_layout(N, D, V, chunk, L)) return LCE_ERR_INVALID_ARG;
+    if (!make_layout(N, D, V, chunk, L, (flags & LCE_FROZEN_W) != 0)) return LCE_ERR_INVALID_ARG;
     *bytes = L.total + ((flags & LCE_ACCUMULATE_DH) ? acc_dh_bytes(L, D) : 0);
     return LCE_OK;
 }
@@ -651,18 +672,22 @@ lce_status lce_backward_opt(const void *H, const void *W, const int64_t *y, cons
     if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
     if (flags & ~LCE_FLAGS_ALL) return LCE_ERR_INVALID_ARG;
     const bool f16 = (flags & LCE_INPUT_FP16) != 0;
+    const bool frozen = (flags & LCE_FROZEN_W) != 0;
+    if (frozen && (flags & LCE_ACCUMULATE_DW)) return LCE_ERR_INVALID_ARG;
     if (f16 && reduction == LCE_REDUCTION_NONE) return LCE_ERR_UNSUPPORTED;
-    if (!dW || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
-    if (!aligned16(dW) || (dH && !aligned16(dH)) || (lse && !aligned16(lse)))
+    if ((!frozen && !dW) || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
+    if ((dW && !aligned16(dW)) || (dH && !aligned16(dH)) || (lse && !aligned16(lse)))
         return LCE_ERR_ALIGNMENT;
     const bool acc_dh = (flags & LCE_ACCUMULATE_DH) != 0;
     Layout L0;
-    if (!make_layout(N, D, V, chunk, L0)) return LCE_ERR_INVALID_ARG;
+    if (!make_layout(N, D, V, chunk, L0, frozen)) return LCE_ERR_INVALID_ARG;
     if (acc_dh && ws_bytes < L0.total + acc_dh_bytes(L0, D)) return LCE_ERR_WORKSPACE;
     Ctx c;
-    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, false, f16));
+    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, false, f16,
+                  frozen));
     c.reduction = reduction;
-    if (c.L.nchunks == 0 && !(flags & LCE_ACCUMULATE_DW)) {
+    if (frozen) dW = nullptr;
+    if (c.L.nchunks == 0 && dW && !(flags & LCE_ACCUMULATE_DW)) {
         if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess)
             return LCE_ERR_CUDA;
     }
@@ -701,21 +726,26 @@ lce_status lce_fwd_bwd_opt(const void *H, const void *W, const int64_t *y, const
     if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
     if (flags & ~LCE_FLAGS_ALL) return LCE_ERR_INVALID_ARG;
     const bool f16 = (flags & LCE_INPUT_FP16) != 0;
+    const bool frozen = (flags & LCE_FROZEN_W) != 0;
     const bool none = reduction == LCE_REDUCTION_NONE;
+    if (frozen && (flags & LCE_ACCUMULATE_DW)) return LCE_ERR_INVALID_ARG;
     if (f16 && none) return LCE_ERR_UNSUPPORTED;
-    if ((!none && !loss) || !dW || (N > 0 && (!lse || !dH || !loss))) return LCE_ERR_INVALID_ARG;
-    if ((loss && !aligned16(loss)) || !aligned16(dW) || (dH && !aligned16(dH)) ||
+    if ((!none && !loss) || (!frozen && !dW) || (N > 0 && (!lse || !dH || !loss)))
+        return LCE_ERR_INVALID_ARG;
+    if ((loss && !aligned16(loss)) || (dW && !aligned16(dW)) || (dH && !aligned16(dH)) ||
         (lse && !aligned16(lse)))
         return LCE_ERR_ALIGNMENT;
     const bool acc_dh = (flags & LCE_ACCUMULATE_DH) != 0;
     Layout L0;
-    if (!make_layout(N, D, V, chunk, L0)) return LCE_ERR_INVALID_ARG;
+    if (!make_layout(N, D, V, chunk, L0, frozen)) return LCE_ERR_INVALID_ARG;
     if (acc_dh && ws_bytes < L0.total + acc_dh_bytes(L0, D)) return LCE_ERR_WORKSPACE;
     Ctx c;
-    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, false, f16));
+    LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, false, f16,
+                  frozen));
     c.reduction = reduction;
+    if (frozen) dW = nullptr;
     float *rows_out = none ? loss : c.loss_rows;
-    if (c.L.nchunks == 0 && !(flags & LCE_ACCUMULATE_DW)) {
+    if (c.L.nchunks == 0 && dW && !(flags & LCE_ACCUMULATE_DW)) {
         if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess)
             return LCE_ERR_CUDA;
     }

@@ -224,14 +224,14 @@ def test_accumulate_workspace_and_flags(L):
     base2 = ws_size(L, N, D, V, 512)[1]        # two vocabulary parts: their arrays serve
     assert L.lce_workspace_size_opt(N, D, V, 512, 2, ctypes.byref(out)) == OK
     assert out.value == base2
-    assert L.lce_workspace_size_opt(N, D, V, chunk, 8, ctypes.byref(out)) == INVALID
+    assert L.lce_workspace_size_opt(N, D, V, chunk, 16, ctypes.byref(out)) == INVALID
     vp = ctypes.c_void_p
     # dH accumulation with only the plain workspace: refused before anything runs
     assert L.lce_fwd_bwd_opt(vp(FAKE), vp(FAKE), vp(FAKE), None, 128, 64, 1000, -100, 64, 0, 2,
                              vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
                              ws_size(L, 128, 64, 1000, 64)[1], None) == WORKSPACE
     assert L.lce_backward_opt(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), vp(FAKE), 128,
-                              64, 1000, -100, 64, 0, 8, vp(FAKE), 1 << 30, None) == INVALID
+                              64, 1000, -100, 64, 0, 16, vp(FAKE), 1 << 30, None) == INVALID
     # fp16 inputs with per-row losses: refused
     UNSUPPORTED = 7
     assert L.lce_fwd_bwd_opt(vp(FAKE), vp(FAKE), vp(FAKE), None, 128, 64, 1000, -100, 64, 2, 4,
@@ -289,3 +289,38 @@ def test_dh_vocabulary_split_workspace(L):
     assert q1 - (2 * 1024 * 152064 + 2 * 3584 * 1024) < stats(1024, 152064) + (1 << 20)
     q0 = ws_size(L, 16384, 3584, 152064, 512)[1]
     assert q0 - (2 * 512 * 152064 + 2 * 3584 * 512) >= 2 * 4 * 512 * 3584
+
+
+def test_frozen_w_flag(L):
+    """LCE_FROZEN_W (8): no dW contraction. Its workspace drops the H chunk^T and
+    splits the dH tiles for the whole GPU (one wave of 74 CTA pairs: 32 tiles of
+    a Llama-3 chunk -> 2 vocabulary parts); dW may be NULL; it does not combine
+    with accumulating into dW."""
+    N, D, V, chunk = 16384, 4096, 128256, 1024
+    base = ws_size(L, N, D, V, chunk)[1]
+    out = ctypes.c_size_t(0)
+    assert L.lce_workspace_size_opt(N, D, V, chunk, 8, ctypes.byref(out)) == OK
+    assert out.value == base - 2 * D * chunk + 2 * 4 * chunk * D
+    assert L.lce_workspace_size_opt(N, D, V, chunk, 8 | 2, ctypes.byref(out)) == OK
+    assert out.value == base - 2 * D * chunk + 2 * 4 * chunk * D   # the parts serve dH += too
+    vp = ctypes.c_void_p
+    n, d, v, c = 128, 64, 1000, 64
+    assert L.lce_workspace_size_opt(n, d, v, c, 8, ctypes.byref(out)) == OK
+    need = out.value
+    # frozen W with accumulation into dW: refused before anything runs
+    assert L.lce_fwd_bwd_opt(vp(FAKE), vp(FAKE), vp(FAKE), None, n, d, v, -100, c, 0, 8 | 1,
+                             vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), need,
+                             None) == INVALID
+    assert L.lce_backward_opt(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), vp(FAKE),
+                              n, d, v, -100, c, 0, 8 | 1, vp(FAKE), need, None) == INVALID
+    # without the flag a NULL dW is an argument error; with it, the argument checks pass
+    assert L.lce_fwd_bwd_opt(vp(FAKE), vp(FAKE), vp(FAKE), None, n, d, v, -100, c, 0, 0,
+                             vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), need,
+                             None) == INVALID
+    assert L.lce_fwd_bwd_opt(vp(FAKE), vp(FAKE), vp(FAKE), None, n, d, v, -100, c, 0, 8,
+                             vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), need,
+                             None) not in (OK, INVALID, ALIGN, WORKSPACE)
+    # a frozen-W call given the plain workspace size may be short of its parts
+    assert L.lce_fwd_bwd_opt(vp(FAKE), vp(FAKE), vp(FAKE), None, N, D, V, -100, chunk, 0, 8,
+                             vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), base,
+                             None) == WORKSPACE
