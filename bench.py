@@ -311,6 +311,14 @@ def run_ours(args, wl, chunk):
     logit_avg_ms = logit_ms / max(logit_n, 1)
     logit_tflops = 2.0 * D * V * N / nchunks / (logit_avg_ms / 1e3) / 1e12
     traffic = load_traffic()
+    # softmax / gather epilogue bytes of the fused path (beyond the GEMM operands):
+    # P' written by the logits epilogue, then read and rewritten in place as G by
+    # the fix-up (3 x N x V x 2 B); the (max, sum) slab partials written, read,
+    # rewritten as factors and read again (4 x N x ceil(V/128) x 8 B); target
+    # logits and lse (N x 12 B)
+    elem = 2
+    epi_bytes = 3.0 * N * V * elem + 4.0 * N * ((V + 127) // 128) * 8 + 12.0 * N
+    merge_ms_step = merge_ms / args.steps
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None
@@ -354,6 +362,12 @@ def run_ours(args, wl, chunk):
                 "merge": {"ms_per_launch": merge_ms / max(merge_n, 1), "launches": merge_n,
                           "share": merge_ms / total_ms},
             },
+            "epilogue": {"bytes_per_step": epi_bytes,
+                         "what": "P' stored by the logits epilogue, read and rewritten as G by the "
+                                 "fix-up; slab (max, sum) partials and factors; target logits, lse",
+                         "aux_kernels_ms_per_step": merge_ms_step,
+                         "aux_kernels": "slab merge, fix-up and H-chunk transpose launches (the P' "
+                                        "store itself runs inside the logits GEMM's epilogue)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "wall_s_timed_region": wall,
