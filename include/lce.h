@@ -225,6 +225,17 @@ lce_status lce_norm_fwd_bwd(const void *X, const void *gamma, float eps, const v
                             int64_t ignore_index, int64_t chunk, int reduction, float *loss,
                             float *lse, void *dX, float *dgamma, float *dW, void *ws,
                             size_t ws_bytes, lce_stream_t stream);
+/* The same with option flags: 0 or LCE_FROZEN_W (a frozen LM head: dW is not
+ * computed and may be NULL; dX and dgamma as above). The workspace is
+ * lce_norm_workspace_size_opt(..., flags) bytes; lce_norm_workspace_size and
+ * lce_norm_fwd_bwd are these with flags = 0. Other flags: LCE_ERR_INVALID_ARG. */
+lce_status lce_norm_workspace_size_opt(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
+                                       size_t *bytes);
+lce_status lce_norm_fwd_bwd_opt(const void *X, const void *gamma, float eps, const void *W,
+                                const int64_t *y, const float *dloss, int64_t N, int64_t D,
+                                int64_t V, int64_t ignore_index, int64_t chunk, int reduction,
+                                int flags, float *loss, float *lse, void *dX, float *dgamma,
+                                float *dW, void *ws, size_t ws_bytes, lce_stream_t stream);
 
 /* Synchronises `stream`, then returns the device-side status recorded in the
  * workspace by the last call that used it (LCE_OK, LCE_ERR_LABEL_RANGE or

@@ -48,6 +48,8 @@ EXPORTED = (
     "lce_rmsnorm_backward",
     "lce_norm_workspace_size",
     "lce_norm_fwd_bwd",
+    "lce_norm_workspace_size_opt",
+    "lce_norm_fwd_bwd_opt",
     "lce_selftest_wait_timeout",
     "lce_read_status",
     "lce_status_string",
@@ -123,6 +125,10 @@ def lib() -> ctypes.CDLL:
     L.lce_norm_workspace_size.argtypes = [_i64, _i64, _i64, _i64, _sz]
     L.lce_norm_fwd_bwd.argtypes = [_vp, _vp, _f, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                    ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    L.lce_norm_workspace_size_opt.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int, _sz]
+    L.lce_norm_fwd_bwd_opt.argtypes = [_vp, _vp, _f, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                       ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp,
+                                       ctypes.c_size_t, _vp]
     L.lce_selftest_wait_timeout.argtypes = [_vp, ctypes.c_size_t, _i64, _vp]
     L.lce_read_status.argtypes = [_vp, _vp]
     L.lce_status_string.argtypes = [ctypes.c_int]
@@ -141,7 +147,8 @@ def lib() -> ctypes.CDLL:
                  "lce_workspace_size_opt", "lce_forward_opt", "lce_backward_opt", "lce_fwd_bwd_opt",
                  "lce_selftest_wait_timeout",
                  "lce_rmsnorm_backward_workspace_size", "lce_rmsnorm_backward",
-                 "lce_norm_workspace_size", "lce_norm_fwd_bwd"):
+                 "lce_norm_workspace_size", "lce_norm_fwd_bwd", "lce_norm_workspace_size_opt",
+                 "lce_norm_fwd_bwd_opt"):
         getattr(L, name).restype = ctypes.c_int
     _LIB = L
     return L
@@ -392,17 +399,19 @@ def rmsnorm_backward(X, gamma, dH, eps: float = 1e-6, ws=None, stream=None):
     return dX, dgamma
 
 
-def norm_workspace_size(N: int, D: int, V: int, chunk: int) -> int:
+def norm_workspace_size(N: int, D: int, V: int, chunk: int, flags: int = 0) -> int:
     out = ctypes.c_size_t(0)
-    _check(lib().lce_norm_workspace_size(N, D, V, chunk, ctypes.byref(out)), "lce_norm_workspace_size")
+    _check(lib().lce_norm_workspace_size_opt(N, D, V, chunk, flags, ctypes.byref(out)),
+           "lce_norm_workspace_size_opt")
     return out.value
 
 
 def norm_fwd_bwd(X, gamma, W, y, eps: float = 1e-6, dloss=None, chunk: int = 1024,
                  ignore_index: int = IGNORE_INDEX, reduction: str = "mean", ws=None, loss=None,
-                 lse=None, stream=None):
+                 lse=None, stream=None, compute_dW: bool = True):
     """RMSNorm + LM head + cross-entropy, forward and backward in one call:
-    (loss, lse, dX bf16, dgamma fp32, dW fp32)."""
+    (loss, lse, dX bf16, dgamma fp32, dW fp32). compute_dW=False: W is frozen and
+    dW is None."""
     _check_norm_inputs(X, gamma)
     _check_inputs(X, W, y)
     N, D = X.shape
@@ -414,26 +423,31 @@ def norm_fwd_bwd(X, gamma, W, y, eps: float = 1e-6, dloss=None, chunk: int = 102
         lse = torch.empty(N, dtype=torch.float32, device=dev)
     dX = torch.empty_like(X)
     dgamma = torch.empty(D, dtype=torch.float32, device=dev)
-    dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+    flags = 0 if compute_dW else FROZEN_W
+    dW = torch.empty(V, D, dtype=torch.float32, device=dev) if compute_dW else None
     if ws is None:
-        ws = torch.empty(norm_workspace_size(N, D, V, chunk), dtype=torch.uint8, device=dev)
+        ws = torch.empty(norm_workspace_size(N, D, V, chunk, flags), dtype=torch.uint8, device=dev)
     _check_dloss(dloss, N, reduction)
-    _check(lib().lce_norm_fwd_bwd(_ptr(X), _ptr(gamma), eps, _ptr(W), _ptr(y), _ptr(dloss), N, D,
-                                  V, ignore_index, chunk, red, _ptr(loss), _ptr(lse), _ptr(dX),
-                                  _ptr(dgamma), _ptr(dW), _ptr(ws), ws.numel(), _stream(stream)),
-           "lce_norm_fwd_bwd")
+    _check(lib().lce_norm_fwd_bwd_opt(_ptr(X), _ptr(gamma), eps, _ptr(W), _ptr(y), _ptr(dloss), N,
+                                      D, V, ignore_index, chunk, red, flags, _ptr(loss), _ptr(lse),
+                                      _ptr(dX), _ptr(dgamma), _ptr(dW), _ptr(ws), ws.numel(),
+                                      _stream(stream)),
+           "lce_norm_fwd_bwd_opt")
     return loss, lse, dX, dgamma, dW
 
 
 class NormLinearCrossEntropyFunction(torch.autograd.Function):
     """loss = CE(RMSNorm(X; gamma) W^T, y) with reduction mean or sum. The forward
     runs lce_norm_fwd_bwd (gradients for an upstream gradient of 1); the backward
-    scales them by the incoming gradient, which the loss is linear in."""
+    scales them by the incoming gradient, which the loss is linear in. A W
+    without requires_grad is frozen (no dW work)."""
 
     @staticmethod
     def forward(ctx, X, gamma, W, y, eps, chunk, ignore_index, reduction):
+        need_dW = ctx.needs_input_grad[2]
         loss, _, dX, dgamma, dW = norm_fwd_bwd(X, gamma, W, y, eps=eps, chunk=chunk,
-                                               ignore_index=ignore_index, reduction=reduction)
+                                               ignore_index=ignore_index, reduction=reduction,
+                                               compute_dW=need_dW)
         ctx.save_for_backward(dX, dgamma, dW)
         ctx.dtypes = (gamma.dtype, W.dtype)
         return loss.reshape(())
@@ -443,7 +457,8 @@ class NormLinearCrossEntropyFunction(torch.autograd.Function):
         dX, dgamma, dW = ctx.saved_tensors
         g = grad_out.to(torch.float32)
         return ((dX.float() * g).to(dX.dtype), (dgamma * g).to(ctx.dtypes[0]),
-                (dW * g).to(ctx.dtypes[1]), None, None, None, None, None)
+                (dW * g).to(ctx.dtypes[1]) if dW is not None else None,
+                None, None, None, None, None)
 
 
 def norm_linear_cross_entropy(X, gamma, W, y, eps: float = 1e-6, chunk: int = 1024,

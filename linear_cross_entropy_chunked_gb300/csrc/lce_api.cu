@@ -167,8 +167,9 @@ size_t acc_dh_bytes(const Layout &L, long long D) {
     return align_up(4 * static_cast<size_t>(L.ldp) * static_cast<size_t>(D), 1024);
 }
 
-bool make_norm_layout(long long N, long long D, long long V, long long chunk, NormLayout &NL) {
-    if (!make_layout(N, D, V, chunk, NL.L)) return false;
+bool make_norm_layout(long long N, long long D, long long V, long long chunk, NormLayout &NL,
+                      bool frozen_w = false) {
+    if (!make_layout(N, D, V, chunk, NL.L, frozen_w)) return false;
     if (D > NRM_MAX_D) return false;
     // the chunk's dH (fp32): the layout's partial arrays, or one array past them
     NL.off_dH = NL.L.off_dHp;
@@ -844,29 +845,38 @@ lce_status lce_rmsnorm_backward(const void *X, const void *gamma, const void *dH
     return LCE_OK;
 }
 
-lce_status lce_norm_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk, size_t *bytes) {
-    if (!bytes) return LCE_ERR_INVALID_ARG;
+lce_status lce_norm_workspace_size_opt(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
+                                       size_t *bytes) {
+    if (!bytes || (flags & ~LCE_FROZEN_W)) return LCE_ERR_INVALID_ARG;
     NormLayout NL;
-    if (!make_norm_layout(N, D, V, chunk, NL)) return LCE_ERR_INVALID_ARG;
+    if (!make_norm_layout(N, D, V, chunk, NL, flags != 0)) return LCE_ERR_INVALID_ARG;
     *bytes = NL.total;
     return LCE_OK;
 }
 
-lce_status lce_norm_fwd_bwd(const void *X, const void *gamma, float eps, const void *W,
-                            const int64_t *y, const float *dloss, int64_t N, int64_t D, int64_t V,
-                            int64_t ignore_index, int64_t chunk, int reduction, float *loss,
-                            float *lse, void *dX, float *dgamma, float *dW, void *ws,
-                            size_t ws_bytes, lce_stream_t stream) {
+lce_status lce_norm_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk, size_t *bytes) {
+    return lce_norm_workspace_size_opt(N, D, V, chunk, 0, bytes);
+}
+
+lce_status lce_norm_fwd_bwd_opt(const void *X, const void *gamma, float eps, const void *W,
+                                const int64_t *y, const float *dloss, int64_t N, int64_t D,
+                                int64_t V, int64_t ignore_index, int64_t chunk, int reduction,
+                                int flags, float *loss, float *lse, void *dX, float *dgamma,
+                                float *dW, void *ws, size_t ws_bytes, lce_stream_t stream) {
     g_launches = 0;
     if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
+    if (flags & ~LCE_FROZEN_W) return LCE_ERR_INVALID_ARG;
+    const bool frozen = flags != 0;
     const bool none = reduction == LCE_REDUCTION_NONE;
     NormLayout NL;
-    if (!make_norm_layout(N, D, V, chunk, NL) || !(eps >= 0.f)) return LCE_ERR_INVALID_ARG;
-    if (!gamma || !dgamma || !dW || (!none && !loss) || (N > 0 && (!X || !lse || !dX || !loss)))
+    if (!make_norm_layout(N, D, V, chunk, NL, frozen) || !(eps >= 0.f)) return LCE_ERR_INVALID_ARG;
+    if (!gamma || !dgamma || (!frozen && !dW) || (!none && !loss) ||
+        (N > 0 && (!X || !lse || !dX || !loss)))
         return LCE_ERR_INVALID_ARG;
-    if ((X && !aligned16(X)) || !aligned16(gamma) || !aligned16(dW) || (dX && !aligned16(dX)) ||
-        (loss && !aligned16(loss)) || (lse && !aligned16(lse)))
+    if ((X && !aligned16(X)) || !aligned16(gamma) || (dW && !aligned16(dW)) ||
+        (dX && !aligned16(dX)) || (loss && !aligned16(loss)) || (lse && !aligned16(lse)))
         return LCE_ERR_ALIGNMENT;
+    if (frozen) dW = nullptr;
     if (!ws) return LCE_ERR_INVALID_ARG;
     if (ws_bytes < NL.total) return LCE_ERR_WORKSPACE;
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -874,11 +884,13 @@ lce_status lce_norm_fwd_bwd(const void *X, const void *gamma, float eps, const v
     float *dHbuf = reinterpret_cast<float *>(w + NL.off_dH);
     float *part = reinterpret_cast<float *>(w + NL.off_part);
     Ctx c;
-    LCE_TRY(setup(c, Hbuf, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, true));
+    LCE_TRY(setup(c, Hbuf, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, true, false,
+                  frozen));
     c.reduction = reduction;
     float *rows_out = none ? loss : c.loss_rows;
     if (c.L.nchunks == 0) {
-        if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess ||
+        if ((dW && cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) !=
+                       cudaSuccess) ||
             cudaMemsetAsync(dgamma, 0, sizeof(float) * static_cast<size_t>(D), c.s) != cudaSuccess)
             return LCE_ERR_CUDA;
     }
@@ -918,6 +930,15 @@ lce_status lce_norm_fwd_bwd(const void *X, const void *gamma, float eps, const v
     if (c.L.nchunks > 0)
         LCE_LAUNCH_KIND(LCE_KERNEL_NORM, c.s, launch_dgamma_reduce(part, static_cast<int>(c.D), dgamma, c.s));
     return LCE_OK;
+}
+
+lce_status lce_norm_fwd_bwd(const void *X, const void *gamma, float eps, const void *W,
+                            const int64_t *y, const float *dloss, int64_t N, int64_t D, int64_t V,
+                            int64_t ignore_index, int64_t chunk, int reduction, float *loss,
+                            float *lse, void *dX, float *dgamma, float *dW, void *ws,
+                            size_t ws_bytes, lce_stream_t stream) {
+    return lce_norm_fwd_bwd_opt(X, gamma, eps, W, y, dloss, N, D, V, ignore_index, chunk, reduction,
+                                0, loss, lse, dX, dgamma, dW, ws, ws_bytes, stream);
 }
 
 lce_status lce_ce_logits_workspace_size(int64_t N, size_t *bytes) {

@@ -324,3 +324,32 @@ def test_frozen_w_flag(L):
     assert L.lce_fwd_bwd_opt(vp(FAKE), vp(FAKE), vp(FAKE), None, N, D, V, -100, chunk, 0, 8,
                              vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), base,
                              None) == WORKSPACE
+
+
+def test_norm_opt_flags(L):
+    """lce_norm_*_opt take 0 or LCE_FROZEN_W; the flag-less calls equal flags = 0."""
+    N, D, V, chunk = 16384, 4096, 128256, 1024
+    out = ctypes.c_size_t(0)
+    plain = ctypes.c_size_t(0)
+    assert L.lce_norm_workspace_size(N, D, V, chunk, ctypes.byref(plain)) == OK
+    assert L.lce_norm_workspace_size_opt(N, D, V, chunk, 0, ctypes.byref(out)) == OK
+    assert out.value == plain.value
+    for bad in (1, 2, 4, 16):
+        assert L.lce_norm_workspace_size_opt(N, D, V, chunk, bad, ctypes.byref(out)) == INVALID
+    assert L.lce_norm_workspace_size_opt(N, D, V, chunk, 8, ctypes.byref(out)) == OK
+    # frozen W: no H chunk^T; the two dH parts of the frozen split hold the chunk's dH
+    assert out.value == (ws_size(L, N, D, V, chunk)[1] - 2 * D * chunk + 2 * 4 * chunk * D
+                         + 2 * chunk * D + 4 * 256 * D)
+    vp = ctypes.c_void_p
+    n, d, v, c = 128, 64, 1000, 64
+    assert L.lce_norm_workspace_size_opt(n, d, v, c, 8, ctypes.byref(out)) == OK
+    need = out.value
+
+    def call(flags, dW):
+        return L.lce_norm_fwd_bwd_opt(vp(FAKE), vp(FAKE), 1e-6, vp(FAKE), vp(FAKE), None, n, d, v,
+                                      -100, c, 0, flags, vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                      dW, vp(FAKE), need, None)
+    assert call(0, None) == INVALID                 # dW needed without the flag
+    assert call(1, vp(FAKE)) == INVALID             # accumulation flags are not taken here
+    assert call(8, vp(FAKE + 4)) == ALIGN           # a given dW is still checked
+    assert call(8, None) not in (OK, INVALID, ALIGN, WORKSPACE)   # argument checks pass

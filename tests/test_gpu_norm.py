@@ -169,3 +169,28 @@ def test_norm_autograd_wrapper(lce):
     check_grad("dX", to64(Xd.grad), ref["dX"])
     check_grad("dgamma", to64(gd.grad), ref["dgamma"])
     check_grad("dW", to64(Wd.grad), ref["dW"])
+
+
+@pytest.mark.parametrize("N,D,V,chunk", [(300, 264, 1000, 128), (1100, 2048, 16411, 512)])
+def test_norm_frozen_w(lce, N, D, V, chunk):
+    """W frozen (LCE_FROZEN_W): loss, lse, dX and dgamma as with W trained, no dW;
+    the second shape splits its dH tiles in vocabulary parts that the RMSNorm
+    backward adds as it reads them."""
+    X, g, W, y = _norm_case(N, D, V, seed=N + 3, n_ign=N // 20)
+    loss, lse, dX, dgamma, dW = lce.norm_fwd_bwd(X.to(DEV), g.to(DEV), W.to(DEV), y.to(DEV),
+                                                 eps=EPS, chunk=chunk, compute_dW=False)
+    torch.cuda.synchronize()
+    assert dW is None
+    ref = O.norm_forward_backward(X, g, EPS, W, y)
+    check_loss(loss.item(), ref["loss"])
+    check_lse(to64(lse), ref["lse"])
+    check_grad("dX", to64(dX), ref["dX"])
+    check_grad("dgamma", to64(dgamma), ref["dgamma"])
+    Xd = X.to(DEV).requires_grad_(True)
+    gd = g.to(DEV).requires_grad_(True)
+    Wd = W.to(DEV)
+    out = lce.norm_linear_cross_entropy(Xd, gd, Wd, y.to(DEV), eps=EPS, chunk=chunk)
+    (out * 0.5).backward()
+    torch.cuda.synchronize()
+    check_grad("dX (autograd, W frozen)", to64(Xd.grad), 0.5 * ref["dX"])
+    check_grad("dgamma (autograd, W frozen)", to64(gd.grad), 0.5 * ref["dgamma"])
