@@ -413,7 +413,9 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False):
     step copies its inputs (H, W, y) host -> device and reads its loss back.
     The copies of step k+1 run on a copy stream while step k computes (two
     device input buffers), as a training loop that prefetches its next batch
-    would; the timed region still contains every step's copies."""
+    would; the loss read-back runs on a third stream from one of two device loss
+    slots, so a read-back queued behind a copy never holds up the next step. The
+    timed region contains every step's copies and read-backs."""
     import torch
     Hh, Wh, yh = H.pin_memory(), W.pin_memory(), y.pin_memory()
     bufs = [(torch.empty_like(Hh, device=dev), torch.empty_like(Wh, device=dev),
@@ -422,13 +424,15 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False):
     V = W.shape[0]
     ws = lce.alloc_workspace(N, D, V, chunk, dev, lce.FROZEN_W if frozen else 0)
     loss_h = torch.empty(2, dtype=torch.float32).pin_memory()
-    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    loss_slots = torch.empty(2, 4, dtype=torch.float32, device=dev)   # 16-byte aligned slots
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     dH = torch.empty(N, D, dtype=H.dtype, device=dev)
     dW = None if frozen else torch.empty(V, D, dtype=torch.float32, device=dev)
     copy_stream = torch.cuda.Stream(dev)
+    d2h_stream = torch.cuda.Stream(dev)
     copied = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
+    read_back = [torch.cuda.Event() for _ in range(2)]
 
     # (start, end) events of every step's copies and compute: how long each took
     # under load, and whether the copies stayed hidden behind the compute
@@ -453,13 +457,17 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False):
     def compute(k):
         b = bufs[k % 2]
         stream.wait_event(copied[k % 2])
+        stream.wait_event(read_back[k % 2])   # this loss slot's last value has been read
         e0, e1 = timed(), timed()
         e0.record(stream)
-        lce.lce_fwd_bwd(b[0], b[1], b[2], chunk=chunk, loss=loss, lse=lse, dH=dH, dW=dW, ws=ws,
-                        stream=stream, compute_dW=not frozen)
+        lce.lce_fwd_bwd(b[0], b[1], b[2], chunk=chunk, loss=loss_slots[k % 2, :1], lse=lse,
+                        dH=dH, dW=dW, ws=ws, stream=stream, compute_dW=not frozen)
         e1.record(stream)
         consumed[k % 2].record(stream)
-        loss_h[k % 2].copy_(loss[0], non_blocking=True)
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(consumed[k % 2])
+            loss_h[k % 2].copy_(loss_slots[k % 2, 0], non_blocking=True)
+            read_back[k % 2].record(d2h_stream)
         spans["compute"].append((e0, e1))
 
     def run(steps):
@@ -469,7 +477,7 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False):
                 h2d(k + 1)
             compute(k)
 
-    for ev in consumed:
+    for ev in consumed + read_back:
         ev.record(stream)
     run(3)
     torch.cuda.synchronize(dev)
@@ -489,6 +497,7 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False):
     a.record(stream)
     copy_stream.wait_event(a)        # the first step's copies start inside the timed region
     run(steps)
+    stream.wait_event(read_back[(steps - 1) % 2])   # ... and the last loss is on the host
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / steps
@@ -500,7 +509,8 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False):
             "h2d_ms_per_step_under_load": under_load["copy"],
             "compute_ms_per_step_under_load": under_load["compute"],
             "note": "every step copies H, W and y from pinned host memory (on a copy stream, "
-                    "overlapping the previous step's compute) and reads its loss back"}
+                    "overlapping the previous step's compute) and reads its loss back (on a "
+                    "third stream, from one of two device loss slots)"}
 
 
 def run_ce_logits(args, wl):
