@@ -24,7 +24,7 @@ in the order the pages state them:
   5. dH = G W and dW = G^T H -- backpropagation into both the hidden states and
      the vocabulary projection (section 3 of the Spanish page).
 
-Readings where the pages are silent (each is listed in the design doc too):
+Readings where the pages are silent:
   * ignore_index rows (y == ignore_index) are dropped from the mean; the
     normaliser is N_valid (the pages divide by the token count, which is the
     same when nothing is ignored).
