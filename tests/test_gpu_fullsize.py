@@ -12,6 +12,8 @@ computes one by one and on properties that hold at any size:
   * sum over the vocabulary of dW is 0 (rows of softmax - onehot sum to 0);
   * dH rows of ignored labels are exactly 0.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -22,6 +24,7 @@ from tests.gpu_util import GRAD_REL, LOSS_REL, LSE_ABS, check_grad, check_lse
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
+W_STD = 0.02      # the workloads' W ~ N(0, 0.02^2)
 
 
 @pytest.fixture(scope="module")
@@ -88,6 +91,12 @@ def test_fullsize_sampled_parity(lce, name, chunk):
     zy_all = np.einsum("ij,ij->i", Hf[idx], Wf[y_np[idx]])
     loss_ref = float(np.sum(lse_g[idx] - zy_all) / n_valid)
     assert abs(loss.item() - loss_ref) <= LOSS_REL * abs(loss_ref)
+    # level at initialisation, independent of any implementation: a row's logits are
+    # Gaussian with variance |h|^2 sigma_w^2 (E = D sigma_w^2), so E[lse] = log V +
+    # D sigma_w^2 / 2 up to O(1/V), and E[z_y] = 0 (W is drawn independently of the
+    # labels); the mean over ~15k rows has a spread of ~0.01
+    expected = math.log(wl.V) + wl.D * W_STD ** 2 / 2
+    assert abs(loss.item() - expected) < 0.05, (loss.item(), expected)
 
     # invariants on the whole GPU output. Rows of softmax - onehot sum to 0, so
     # sum_v dW[v, d] = sum_i H_id * sum_v (G~_iv - G_iv), where G~ is G rounded to
