@@ -58,6 +58,9 @@ def test_tiny_workload(lce):
     (1000, 520, 3000, 384, 40, 2.5),     # chunk not a multiple of the tile
     (77, 128, 100, 1024, 3, 1.0),        # N < chunk, V < one tile
     (256, 8, 513, 256, 0, 1.0),          # tiny D (one partial K block)
+    (5000, 64, 3000, 64, 200, 1.0),      # 79 chunks: one tile counter per launch in the header
+    (1, 64, 1000, 1024, 0, 1.0),         # a single row
+    (2, 72, 9000, 1, 0, 0.5),            # chunk 1: every row its own chunk
 ])
 def test_ragged_shapes(lce, N, D, V, chunk, n_ign, dloss):
     H, W, y = make_inputs(N, D, V, seed=N + D + V, labels="uniform", n_ignored=n_ign, w_std=0.05)
@@ -264,3 +267,14 @@ def test_bounded_wait_times_out_and_context_survives(lce):
     loss, lse = lce.lce_forward(H.to(DEV), W.to(DEV), y.to(DEV), chunk=64)
     torch.cuda.synchronize()
     check_loss(loss.item(), O.forward_backward(H, W, y)["loss"])
+
+
+def test_large_vocabulary(lce):
+    """A vocabulary of a million (ragged: 1,000,003), two chunks, dH tiles in four
+    vocabulary parts; labels at both ends of the vocabulary."""
+    N, D, V, chunk = 160, 64, 1_000_003, 128
+    H, W, y = make_inputs(N, D, V, seed=41, n_ignored=8, w_std=0.3)
+    y[0] = V - 1
+    y[1] = 0
+    r = run_all_paths(lce, H, W, y, chunk=chunk, dloss=1.0)
+    compare(r, O.forward_backward(H, W, y))
