@@ -341,6 +341,9 @@ def run_ours(args, wl, chunk):
                                          "W 1.05 GB also exceeds L2",
                                       **({"frozen_w": True} if frozen else {})),
             "tflops": tflops,
+            "flops_per_step": {"algorithmic": flops_step, "executed": flops_step,
+                               "note": "the fused call recomputes nothing: executed = algorithmic "
+                                       "(lce_forward + lce_backward would execute 8NDV)"},
             "pct_of_bf16_peak": {"vs_burst": tflops / peak_burst, "vs_sustained": tflops / peak_sust,
                                  "flops": "4NDV algorithmic (W frozen: no dW)" if frozen
                                  else "6NDV algorithmic", "peak_source": peak_src},
