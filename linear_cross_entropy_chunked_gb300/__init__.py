@@ -35,3 +35,4 @@ from ._binding import (  # noqa: F401
     workspace_size_opt,
 )
 from .build_lib import LIB_PATH, build  # noqa: F401
+from .sharded import count_valid, sharded_fwd_bwd  # noqa: F401

@@ -4,6 +4,7 @@ and all ranks' tokens. The reference arm runs on rank 0 only."""
 import os
 import socket
 
+import numpy as np
 import pytest
 import torch
 import torch.distributed as dist
@@ -78,3 +79,57 @@ def test_bench_defines_every_path_it_dispatches():
     builtins = set(dir(__import__("builtins")))
     missing = {c for c in called if c not in defined and c not in builtins}
     assert not missing, missing
+
+
+# ---------------------------------------------------------------- token-sharded loss
+
+def _oracle_fwd_bwd(H, W, y, dloss, chunk, ignore_index, reduction, compute_dW):
+    """Stand-in for the library's fused call on the CPU (this test checks the
+    exchange around it; the call itself is parity-tested on the GPU)."""
+    from oracle import lce_oracle as O
+    assert reduction == "sum"
+    r = O.forward_backward(H, W, y, dloss=float(dloss.reshape(-1)[0]), reduction="sum",
+                           ignore_index=ignore_index)
+    dW = torch.from_numpy(r["dW"]).to(torch.float32) if compute_dW else None
+    return (torch.tensor([r["loss"]], dtype=torch.float32), torch.from_numpy(r["lse"]).float(),
+            torch.from_numpy(r["dH"]).float(), dW)
+
+
+def _sharded_worker(rank, world, port, out, cuts, compute_dW):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from lce_synth import make_inputs
+    from linear_cross_entropy_chunked_gb300.sharded import sharded_fwd_bwd
+    H, W, y = make_inputs(96, 16, 40, seed=7, n_ignored=9)
+    y[5] = 40                        # out of range: counts as ignored
+    lo, hi = cuts[rank], cuts[rank + 1]
+    loss, lse, dH, dW = sharded_fwd_bwd(H[lo:hi], W, y[lo:hi], compute_dW=compute_dW,
+                                        fwd_bwd=_oracle_fwd_bwd)
+    out[rank] = (float(loss), dH.numpy(), None if dW is None else dW.numpy())
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("cuts,compute_dW", [((0, 40, 96), True), ((0, 0, 96), True),
+                                             ((0, 70, 96), False)])
+def test_token_sharded_loss_equals_the_whole_batch(cuts, compute_dW):
+    """Two ranks over gloo, each with a slice of the rows (one may be empty):
+    the global loss and dW on every rank, and each rank's dH rows, equal the
+    oracle's on the whole batch."""
+    from lce_synth import make_inputs
+    from oracle import lce_oracle as O
+    world, port = 2, _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_sharded_worker, args=(world, port, out, cuts, compute_dW), nprocs=world, join=True)
+    H, W, y = make_inputs(96, 16, 40, seed=7, n_ignored=9)
+    y[5] = 40
+    ref = O.forward_backward(H, W, y)
+    dH = np.concatenate([out[r][1] for r in range(world)])
+    for r in range(world):
+        assert out[r][0] == pytest.approx(ref["loss"], rel=1e-6)
+        if compute_dW:
+            assert np.allclose(out[r][2], ref["dW"], rtol=1e-5, atol=1e-7)
+        else:
+            assert out[r][2] is None
+    assert np.allclose(dH, ref["dH"], rtol=1e-5, atol=1e-7)
