@@ -324,6 +324,10 @@ def run_ours(args, wl, chunk):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen)
+        w_up = run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen, upload_w=True)
+        e2e["with_weight_upload"] = {k: w_up[k] for k in (
+            "value", "ms_per_step", "h2d_bytes_per_step", "h2d_ms_per_step_alone",
+            "h2d_ms_per_step_under_load", "compute_ms_per_step_under_load")}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -412,17 +416,24 @@ def load_traffic():
     return out
 
 
-def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False):
+def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False, upload_w=False):
     """The same metric through the public API from pinned host buffers: every
-    step copies its inputs (H, W, y) host -> device and reads its loss back.
-    The copies of step k+1 run on a copy stream while step k computes (two
-    device input buffers), as a training loop that prefetches its next batch
-    would; the loss read-back runs on a third stream from one of two device loss
-    slots, so a read-back queued behind a copy never holds up the next step. The
-    timed region contains every step's copies and read-backs."""
+    step copies its inputs host -> device and reads its loss back. The inputs
+    of a loss step are the hidden states H and the labels y; the LM-head weight
+    W is a parameter that stays on the device between steps (uploaded once,
+    before the timed region), unless upload_w, which copies W every step too
+    (the conservative variant). The copies of step k+1 run on a copy stream
+    while step k computes (two device input buffers), as a training loop that
+    prefetches its next batch would; the loss read-back runs on a third stream
+    from one of two device loss slots, so a read-back queued behind a copy never
+    holds up the next step. The timed region contains every step's copies and
+    read-backs."""
     import torch
-    Hh, Wh, yh = H.pin_memory(), W.pin_memory(), y.pin_memory()
-    bufs = [(torch.empty_like(Hh, device=dev), torch.empty_like(Wh, device=dev),
+    Hh, yh = H.pin_memory(), y.pin_memory()
+    Wh = W.pin_memory() if upload_w else None
+    W_dev = None if upload_w else W.to(dev)
+    bufs = [(torch.empty_like(Hh, device=dev),
+             torch.empty_like(Wh, device=dev) if upload_w else W_dev,
              torch.empty_like(yh, device=dev)) for _ in range(2)]
     N, D = H.shape
     V = W.shape[0]
@@ -452,7 +463,8 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False):
             e0, e1 = timed(), timed()
             e0.record(copy_stream)
             b[0].copy_(Hh, non_blocking=True)
-            b[1].copy_(Wh, non_blocking=True)
+            if upload_w:
+                b[1].copy_(Wh, non_blocking=True)
             b[2].copy_(yh, non_blocking=True)
             e1.record(copy_stream)
             copied[k % 2].record(copy_stream)
@@ -506,15 +518,17 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False):
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / steps
     under_load = {k: statistics.mean(e0.elapsed_time(e1) for e0, e1 in v) for k, v in spans.items()}
-    h2d_bytes = Hh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8
+    h2d_bytes = Hh.numel() * 2 + (Wh.numel() * 2 if upload_w else 0) + yh.numel() * 8
     return {"value": world * N / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "steps": steps, "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": 4,
             "h2d_ms_per_step_alone": copy_ms, "h2d_gbs": h2d_bytes / copy_ms / 1e6,
             "h2d_ms_per_step_under_load": under_load["copy"],
             "compute_ms_per_step_under_load": under_load["compute"],
-            "note": "every step copies H, W and y from pinned host memory (on a copy stream, "
-                    "overlapping the previous step's compute) and reads its loss back (on a "
-                    "third stream, from one of two device loss slots)"}
+            "note": ("every step copies H, W and y" if upload_w else
+                     "every step copies H and y (W, a parameter, stays resident)") +
+                    " from pinned host memory (on a copy stream, overlapping the previous step's "
+                    "compute) and reads its loss back (on a third stream, from one of two device "
+                    "loss slots)"}
 
 
 def run_ce_logits(args, wl):

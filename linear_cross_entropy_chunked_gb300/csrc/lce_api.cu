@@ -301,10 +301,10 @@ void prof_end(int idx, cudaStream_t s) {
 
 #define LCE_LAUNCH(expr) LCE_LAUNCH_KIND(LCE_KERNEL_OTHER, c.s, expr)
 
-// A second stream per device for the kernel that runs concurrently with the
-// caller's stream inside one call (fork and join through two events). The
-// mutex keeps the record / wait / launch sequence of one call together when
-// several host threads use the same device.
+// A second stream per device for the dW kernel that runs beside the dH kernel
+// of a gradient phase (forked from and joined back to the caller's stream
+// through two events). The mutex keeps the record / wait / launch sequence of
+// one call together when several host threads use the same device.
 struct SideStream {
     cudaStream_t s = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
@@ -319,10 +319,12 @@ SideStream *side_stream() {
     std::lock_guard<std::mutex> lock(g_side_mu);
     SideStream &ss = g_side[dev];
     if (!ss.s) {
-        if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        cudaStream_t st = nullptr;
+        if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
         if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
             return nullptr;
+        ss.s = st;   // last: marks the set as complete
     }
     return &ss;
 }
@@ -496,10 +498,16 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
     const int units = cl == 2 ? c.pairs : c.sms;
     if (cl == 2) {
         // CTA pairs: the dH tiles run 512 columns wide (two MMAs share each A
-        // block: a quarter fewer operand bytes per flop) in one kernel, the dW
-        // tiles in a second kernel on a side stream, concurrently; the first
-        // takes as many pairs as it has tiles, the second all that are free
-        // and the rest as the first finishes.
+        // block: a quarter fewer operand bytes per flop) in one kernel with one
+        // pair per tile (at most all pairs); the dW tiles run beside it in a
+        // second kernel on the side stream, sized to exactly the pairs the dH
+        // kernel leaves free, so the two grids fit on the GPU together whichever
+        // the hardware dispatches first (nothing orders two ready grids on
+        // separate hardware queues; a dW grid that took every SM would leave the
+        // long dH tiles to run after it). A third launch, a dW grid as large as
+        // the dH one, queued on the caller's stream behind the dH kernel, takes
+        // over the dH kernel's SMs when it ends; both dW grids draw tiles from
+        // the same counter.
         GemmParams ph = p;
         ph.n_blocks0 = static_cast<int>(cdiv(c.D, BN_WIDE));
         ph.m_blocks1 = ph.n_blocks1 = ph.k_blocks1 = 0;
@@ -517,21 +525,32 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
         SideStream *ss = side_stream();
         if (!ss) return LCE_ERR_CUDA;
         std::lock_guard<std::mutex> lock(ss->mu);
-        const int gh = cl * (ph.total_tiles < units ? ph.total_tiles : units);
-        const int gw = cl * (pw.total_tiles < units ? pw.total_tiles : units);
+        const int dh_pairs = ph.total_tiles < units ? ph.total_tiles : units;
+        const int free_pairs = units - dh_pairs;
+        const int w1 = pw.total_tiles < free_pairs ? pw.total_tiles : free_pairs;
+        const int w2 = pw.total_tiles < dh_pairs ? pw.total_tiles : dh_pairs;
         const int pi = prof_begin(LCE_KERNEL_GRAD, c.s);
         if (cudaEventRecord(ss->fork, c.s) != cudaSuccess ||
             cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
             return LCE_ERR_CUDA;
-        if (ph.total_tiles > 0 && launch_gemm(MODE_DH, cl, ph, gh, c.s) != cudaSuccess)
-            return LCE_ERR_CUDA;
-        if (pw.total_tiles > 0 && launch_gemm(MODE_BWD, cl, pw, gw, ss->s) != cudaSuccess)
-            return LCE_ERR_CUDA;
+        int launched = 0;
+        if (dh_pairs > 0) {
+            if (launch_gemm(MODE_DH, cl, ph, cl * dh_pairs, c.s) != cudaSuccess) return LCE_ERR_CUDA;
+            ++launched;
+        }
+        if (w1 > 0) {
+            if (launch_gemm(MODE_BWD, cl, pw, cl * w1, ss->s) != cudaSuccess) return LCE_ERR_CUDA;
+            ++launched;
+        }
+        if (w2 > 0 && (dh_pairs > 0 || w1 == 0)) {
+            if (launch_gemm(MODE_BWD, cl, pw, cl * w2, c.s) != cudaSuccess) return LCE_ERR_CUDA;
+            ++launched;
+        }
         if (cudaEventRecord(ss->join, ss->s) != cudaSuccess ||
             cudaStreamWaitEvent(c.s, ss->join, 0) != cudaSuccess)
             return LCE_ERR_CUDA;
         prof_end(pi, c.s);
-        g_launches += 2;
+        g_launches += launched;
         return LCE_OK;
     }
     const int grid = cl * (p.total_tiles < units ? p.total_tiles : units);
