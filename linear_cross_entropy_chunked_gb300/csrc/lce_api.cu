@@ -101,8 +101,8 @@ struct Layout {
 // alone, so a result does not depend on the device it ran on.
 // With W frozen the dH tiles have the GPU to themselves: they are split into the
 // most parts (at most DH_MAX_SPLITS) that keep them within one wave of the
-// DH_ALONE_PAIRS CTA pairs of a GB300.
-constexpr int DH_ALONE_PAIRS = 74;
+// DH_ALONE_PAIRS CTA pairs a GB300 holds at once (152 SMs).
+constexpr int DH_ALONE_PAIRS = 76;
 
 int dh_splits_for(long long rows, long long D, long long V, bool frozen_w = false) {
     if (V < DH_SPLIT_MIN_V || rows <= 0) return 1;

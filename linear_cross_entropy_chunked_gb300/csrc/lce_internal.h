@@ -48,7 +48,7 @@ constexpr int BN_WIDE = 512;   // MODE_DH tile width: both 256-column TMEM accum
 // while the dW tiles, which are bound by their fp32 read-modify-write of dW in
 // HBM, run concurrently on the other SMs. The phase is shortest when both sets
 // end together: measured on a GB300 that is about 32 dH tiles (a dH tile pair
-// runs ~1.3x the flop rate of a dW one; 74 pairs). A chunk with fewer dH tiles
+// runs ~1.3x the flop rate of a dW one; 76 pairs). A chunk with fewer dH tiles
 // splits them along the vocabulary until there are at least DH_SPLIT_TILES, in
 // at most DH_MAX_SPLITS parts, for vocabularies of at least DH_SPLIT_MIN_V; more
 // dH tiles than that would crowd the dW tiles into the end of the phase, where

@@ -293,7 +293,7 @@ def test_dh_vocabulary_split_workspace(L):
 
 def test_frozen_w_flag(L):
     """LCE_FROZEN_W (8): no dW contraction. Its workspace drops the H chunk^T and
-    splits the dH tiles for the whole GPU (one wave of 74 CTA pairs: 32 tiles of
+    splits the dH tiles for the whole GPU (one wave of 76 CTA pairs: 32 tiles of
     a Llama-3 chunk -> 2 vocabulary parts); dW may be NULL; it does not combine
     with accumulating into dW."""
     N, D, V, chunk = 16384, 4096, 128256, 1024
