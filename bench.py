@@ -6,7 +6,11 @@ Llama-3-8B-shaped LM head: N=16384 tokens, D=4096, V=128256, chunk 1024, 5% of
 rows ignore_index, synthetic seeded inputs (no dataset).
 
 Prints one JSON line (rank 0). With --impl reference the fp64 CPU oracle is
-timed instead on the host cores, one bounded row sample per step.
+timed instead on the host cores, one bounded row sample per step. Other
+measurements: --frozen-w (the LM head frozen: no dW, 4NDV per step),
+--dtype fp16, --workload / --chunk (the other head shapes and chunk sizes),
+--path ce-logits (cross-entropy over given logits), --path norm (final RMSNorm
++ head + cross-entropy).
 
 Multi-GPU (torchrun, --gpus N): every rank runs its own replica of the
 workload (independent problems, weak scaling, no collective on the data path);
@@ -301,9 +305,9 @@ def run_ours(args, wl, chunk):
     peak_burst = peaks.get("bf16_tflops", 1900.0)
     peak_sust = peaks.get("bf16_tflops_sustained", 1700.0)
 
-    # dominant kernel: the gradient phase of a chunk (dH and dW GEMMs, two
-    # concurrent kernels timed together from fork to join: 4*C*D*V flops; with W
-    # frozen the dH GEMM alone, 2*C*D*V)
+    # dominant kernel: the gradient phase of a chunk (the dH GEMM and the two dW
+    # grids beside and behind it, timed together from fork to join: 4*C*D*V
+    # flops; with W frozen the dH GEMM alone, 2*C*D*V)
     nchunks = (N + chunk - 1) // chunk
     grad_flops_launch = (2.0 if frozen else 4.0) * D * V * N / nchunks
     grad_avg_ms = grad_ms / max(grad_n, 1)
@@ -356,7 +360,8 @@ def run_ours(args, wl, chunk):
             "roofline": {"kernel": "gradient phase, W frozen: lce_gemm_kernel<MODE_DH> (dH tiles, "
                                    "512 wide, split along the vocabulary) alone" if frozen else
                                    "gradient phase: lce_gemm_kernel<MODE_DH> (dH tiles, 512 wide) "
-                                   "+ lce_gemm_kernel<MODE_BWD> (dW tiles), concurrent",
+                                   "+ lce_gemm_kernel<MODE_BWD> (dW tiles: one grid beside the "
+                                   "dH kernel, one behind it), concurrent",
                          "bound": "tensor", "achieved": grad_tflops, "peak": peak_sust,
                          "peak_kind": f"bf16_tflops_sustained ({peak_src})",
                          "unit": "TFLOP/s", "frac": grad_tflops / peak_sust,
