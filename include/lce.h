@@ -31,6 +31,11 @@
  *    least lce_workspace_size() bytes. The library allocates no device memory.
  *    The workspace extent is O(chunk * V) plus O(N) bytes.
  *  - All work is enqueued on `stream`; no entry point synchronises the host.
+ *    (The gradient phase runs part of its kernels on a stream the library owns,
+ *    forked from and joined back to `stream` through events, so every call is
+ *    ordered after earlier work on `stream` and before later work on it, and it
+ *    can be captured in a CUDA graph. Several host threads may call the library
+ *    at once, each with its own buffers.)
  *    Argument errors are returned before anything is enqueued. Errors found on
  *    the device (labels outside [0,V) that are not ignore_index, a bounded wait
  *    that ran out) are recorded in the workspace and returned by
