@@ -515,13 +515,16 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False, upload_
     steps = max(3, args.steps // 2)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     a.record(stream)
     copy_stream.wait_event(a)        # the first step's copies start inside the timed region
     run(steps)
     stream.wait_event(read_back[(steps - 1) % 2])   # ... and the last loss is on the host
     b.record(stream)
     torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / steps
+    ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)   # the slowest rank, as for value
     under_load = {k: statistics.mean(e0.elapsed_time(e1) for e0, e1 in v) for k, v in spans.items()}
     h2d_bytes = Hh.numel() * 2 + (Wh.numel() * 2 if upload_w else 0) + yh.numel() * 8
     return {"value": world * N / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
