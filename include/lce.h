@@ -67,7 +67,8 @@ typedef enum lce_status {
     LCE_ERR_LABEL_RANGE = 4,   /* device: some label outside [0,V) and != ignore_index */
     LCE_ERR_TIMEOUT = 5,       /* device: a bounded pipeline wait ran out; outputs invalid */
     LCE_ERR_CUDA = 6,          /* a CUDA runtime call failed */
-    LCE_ERR_UNSUPPORTED = 7    /* current device is not sm_103 */
+    LCE_ERR_UNSUPPORTED = 7    /* current device is not sm_103, or an option combination
+                                  the library does not offer (fp16 with reduction NONE) */
 } lce_status;
 
 /* Same type as cudaStream_t. NULL means the legacy default stream. */
@@ -276,8 +277,8 @@ int lce_last_launch_count(void);
 enum {
     LCE_KERNEL_LOGITS = 0,   /* chunk logits GEMM with the log-sum-exp / G epilogue */
     LCE_KERNEL_GRAD = 1,     /* dH + dW gradient GEMM tiles */
-    LCE_KERNEL_MERGE = 2,    /* slab merge (lse, row loss, G rescale) */
-    LCE_KERNEL_OTHER = 3,    /* label scan, loss finalisation */
+    LCE_KERNEL_MERGE = 2,    /* slab merge (lse, row loss), G rescale, H-chunk transpose */
+    LCE_KERNEL_OTHER = 3,    /* label scan, loss finalisation, dH combination */
     LCE_KERNEL_NORM = 4,     /* RMSNorm forward / backward row kernels, dgamma reduction */
     LCE_KERNEL_KINDS = 5
 };

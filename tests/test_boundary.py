@@ -353,3 +353,23 @@ def test_norm_opt_flags(L):
     assert call(1, vp(FAKE)) == INVALID             # accumulation flags are not taken here
     assert call(8, vp(FAKE + 4)) == ALIGN           # a given dW is still checked
     assert call(8, None) not in (OK, INVALID, ALIGN, WORKSPACE)   # argument checks pass
+
+
+def test_binding_constants_match_the_header():
+    """Status codes, reductions, flags and profiling kinds: the binding's copies
+    equal the values include/lce.h declares."""
+    import linear_cross_entropy_chunked_gb300._binding as B
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    consts = {k: int(v) for k, v in re.findall(r"\b(LCE_[A-Z0-9_]+)\s*=\s*(\d+)", src)}
+    for code, name in B.STATUS_NAMES.items():
+        assert consts[name] == code, name
+    for name, v in B.REDUCTIONS.items():
+        assert consts[f"LCE_REDUCTION_{name.upper()}"] == v
+    assert consts["LCE_ACCUMULATE_DW"] == B.ACCUMULATE["dW"]
+    assert consts["LCE_ACCUMULATE_DH"] == B.ACCUMULATE["dH"]
+    assert consts["LCE_INPUT_FP16"] == B.INPUT_FP16
+    assert consts["LCE_FROZEN_W"] == B.FROZEN_W
+    assert consts["LCE_FLAGS_ALL"] == B.ACCUMULATE["dW"] | B.ACCUMULATE["dH"] | B.INPUT_FP16 | B.FROZEN_W
+    for name, v in B.KERNEL_KINDS.items():
+        assert consts[f"LCE_KERNEL_{name.upper()}"] == v
+    assert consts["LCE_KERNEL_KINDS"] == len(B.KERNEL_KINDS)
