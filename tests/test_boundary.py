@@ -373,3 +373,37 @@ def test_binding_constants_match_the_header():
     for name, v in B.KERNEL_KINDS.items():
         assert consts[f"LCE_KERNEL_{name.upper()}"] == v
     assert consts["LCE_KERNEL_KINDS"] == len(B.KERNEL_KINDS)
+
+
+def test_binding_flag_logic_on_the_host():
+    """The binding's option handling, no device involved: accumulate subsets map
+    to flags, accumulating needs the tensors, frozen W adds its flag and refuses
+    accumulating into dW; unknown reductions raise."""
+    import torch
+    import linear_cross_entropy_chunked_gb300._binding as B
+    t = torch.zeros(1)
+    assert B._acc_flags((), None, None) == 0
+    assert B._acc_flags(("dW",), None, t) == 1
+    assert B._acc_flags(("dH", "dW"), t, t) == 3
+    assert B._acc_flags(("dH",), t, None, compute_dW=False) == 2 | B.FROZEN_W
+    assert B._acc_flags((), None, None, compute_dW=False) == B.FROZEN_W
+    with pytest.raises(ValueError):
+        B._acc_flags(("dW",), None, None)               # nothing to add into
+    with pytest.raises(ValueError):
+        B._acc_flags(("dW",), None, t, compute_dW=False)
+    with pytest.raises(ValueError):
+        B._acc_flags(("dx",), t, t)
+    assert [B._reduction(r) for r in ("mean", "sum", "none")] == [0, 1, 2]
+    with pytest.raises(ValueError):
+        B._reduction("avg")
+
+
+def test_count_valid_matches_the_library_reading():
+    """Rows count as valid when the label lies in [0, V) and is not ignore_index
+    (out-of-range labels are treated as ignored, as the kernels do)."""
+    import torch
+    from linear_cross_entropy_chunked_gb300.sharded import count_valid
+    y = torch.tensor([0, 5, -100, 9, 10, -3, 4])
+    assert count_valid(y, 10).item() == 4
+    assert count_valid(y, 11).item() == 5
+    assert count_valid(torch.zeros(0, dtype=torch.int64), 10).item() == 0
