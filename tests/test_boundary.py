@@ -407,3 +407,24 @@ def test_count_valid_matches_the_library_reading():
     assert count_valid(y, 10).item() == 4
     assert count_valid(y, 11).item() == 5
     assert count_valid(torch.zeros(0, dtype=torch.int64), 10).item() == 0
+
+
+def test_no_library_means_loud_failure(monkeypatch):
+    """Without the built library every call raises (there is no fallback), and
+    every entry point refuses CPU tensors before touching the library."""
+    import torch
+    import linear_cross_entropy_chunked_gb300._binding as B
+    monkeypatch.setattr(B, "_LIB", None)
+    monkeypatch.setattr(B, "LIB_PATH", "/nonexistent/liblce_gb300.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        B.lib()
+    with pytest.raises(RuntimeError):
+        B.workspace_size(8, 64, 100, 64)
+    H = torch.zeros(4, 8, dtype=torch.bfloat16)
+    W = torch.zeros(16, 8, dtype=torch.bfloat16)
+    y = torch.zeros(4, dtype=torch.int64)
+    for call in (lambda: B.lce_fwd_bwd(H, W, y), lambda: B.lce_backward(H, W, y, torch.zeros(4)),
+                 lambda: B.ce_logits(torch.zeros(4, 16), y), lambda: B.rmsnorm_forward(H, H[0]),
+                 lambda: B.norm_fwd_bwd(H, H[0], W, y)):
+        with pytest.raises(ValueError):
+            call()
