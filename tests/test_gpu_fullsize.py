@@ -1,16 +1,20 @@
 """Parity at full size: the Llama-3-8B and Qwen-2.5-7B LM-head workloads, run
 through the C ABI in the launch configuration the benchmark times (fused
-forward + backward, chunk from the workload), checked on outputs the fp64 oracle
-computes one by one and on properties that hold at any size:
+forward + backward, chunk from the workload), and the separate forward +
+backward (the recompute path) on the Llama-3 head. Every expected value comes
+from the fp64 oracle alone; no GPU output enters a reference:
 
-  * lse of sampled rows (oracle: that row's full logit vector);
-  * dH of sampled rows (oracle: that row's softmax - onehot times W);
-  * dW of sampled vocabulary rows (oracle: the column of G over all N rows, with
-    every row's lse taken from the GPU; those lse are checked on the samples);
-  * loss = mean over valid rows of (lse_i - z_{i,y_i}), with z_{i,y_i} = h_i . w_{y_i}
-    from the oracle for every row and lse_i from the GPU;
-  * sum over the vocabulary of dW is 0 (rows of softmax - onehot sum to 0);
-  * dH rows of ignored labels are exactly 0.
+  * lse of all N rows and the loss: the oracle's forward over every row (the
+    logits materialised in row blocks on the host, one run per workload, shared
+    by the cases of that workload);
+  * dH of sampled rows (>= 64: the first and the last row of every chunk, an
+    ignored row, random rows), from that row's softmax - onehot times W;
+  * dW of sampled vocabulary rows (>= 32: ids 0..7, which are the most frequent
+    ids of a Zipf workload, ids of the last 128-column slab, a label that occurs,
+    random ids), from the column of G over all N rows with the oracle's lse;
+  * properties that hold at any size: sum over the vocabulary of dW is 0 (rows of
+    softmax - onehot sum to 0), dH rows of ignored labels are exactly 0, and the
+    loss sits at its level at initialisation.
 """
 import math
 
@@ -20,7 +24,7 @@ import torch
 
 from lce_synth import IGNORE_INDEX, WORKLOADS, workload_inputs
 from oracle import lce_oracle as O
-from tests.gpu_util import GRAD_REL, LOSS_REL, LSE_ABS, check_grad, check_lse
+from tests.gpu_util import GRAD_REL, check_grad, check_loss, check_lse
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -45,6 +49,7 @@ def _cases():
 
 
 _inputs_cache = {}
+_oracle_cache = {}
 
 
 def _inputs(name):
@@ -54,43 +59,67 @@ def _inputs(name):
     return _inputs_cache[name]
 
 
-@pytest.mark.parametrize("name,chunk", _cases())
-def test_fullsize_sampled_parity(lce, name, chunk):
+def _oracle_forward(name):
+    """The oracle's loss and lse over every row of the workload (fp64)."""
+    if name not in _oracle_cache:
+        H, W, y = _inputs(name)
+        loss, lse, n_valid, n_bad = O.forward(H, W, y)
+        assert n_bad == 0
+        _oracle_cache[name] = (loss, lse, n_valid)
+    return _oracle_cache[name]
+
+
+def _sample_rows(wl, chunk, valid, rng):
+    """The first and the last row of every chunk, the first ignored row, and
+    random rows up to at least 64 in all."""
+    rows = set()
+    for r0 in range(0, wl.N, chunk):
+        rows.add(r0)
+        rows.add(min(r0 + chunk, wl.N) - 1)
+    rows.add(int(np.nonzero(~valid)[0][0]))
+    want = max(64, len(rows) + 8)
+    for r in rng.permutation(wl.N):
+        if len(rows) >= want:
+            break
+        rows.add(int(r))
+    return sorted(rows)
+
+
+def _sample_vocab(wl, y_np, valid, rng):
+    """Vocabulary rows of dW to check: ids 0..7 (the most frequent ids of a Zipf
+    workload, where rank k is id k), ids across the last 128-column slab, a label
+    that occurs, and random ids up to at least 32 in all."""
+    last0 = 128 * ((wl.V - 1) // 128)       # first id of the last 128-column slab
+    ids = set(range(8)) | {last0, (last0 + wl.V) // 2, wl.V - 2, wl.V - 1,
+                           int(y_np[valid][0])}
+    for v in rng.permutation(wl.V):
+        if len(ids) >= 34:
+            break
+        ids.add(int(v))
+    return sorted(ids)
+
+
+def _check_against_oracle(name, chunk, H, W, y, loss, lse, dH, dW, rng):
     wl = WORKLOADS[name]
-    H, W, y = _inputs(name)
-    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
-    loss, lse, dH, dW = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk)
-    torch.cuda.synchronize()
-    lse_g = lse.double().cpu().numpy()
+    loss_o, lse_o, n_valid = _oracle_forward(name)
     y_np = y.numpy()
     valid = y_np != IGNORE_INDEX
-    n_valid = int(valid.sum())
     assert n_valid == wl.N - wl.n_ignored
 
-    rng = np.random.default_rng(1234 + chunk)
-    # sampled rows: first / last row of a chunk, ragged positions, an ignored row
-    rows = sorted(set([0, chunk - 1, chunk, wl.N - 1, int(np.nonzero(~valid)[0][0])] +
-                      rng.choice(wl.N, 11, replace=False).tolist()))
-    lse_o, zy_o = O.rows_lse_and_target(H, W, y, rows)
-    check_lse(lse_g[rows], lse_o)
+    # every row's lse, and the loss, against the oracle's forward
+    check_lse(lse.double().cpu().numpy(), lse_o)
+    check_loss(loss.item(), loss_o)
 
+    rows = _sample_rows(wl, chunk, valid, rng)
+    assert len(rows) >= 64
     dH_o = O.rows_dH(H, W, y, rows, n_valid)
-    dH_g = dH[rows].float().double().cpu().numpy()
-    check_grad("dH rows", dH_g, dH_o)
+    check_grad("dH rows", dH[rows].float().double().cpu().numpy(), dH_o)
 
-    vrows = sorted(set([0, wl.V - 1] + rng.choice(wl.V, 6, replace=False).tolist() +
-                       [int(y_np[valid][0])]))
-    dW_o = O.cols_dW(H, W, y, vrows, lse_g, n_valid)
-    dW_g = dW[vrows].double().cpu().numpy()
-    check_grad("dW rows", dW_g, dW_o)
+    vrows = _sample_vocab(wl, y_np, valid, rng)
+    assert len(vrows) >= 32
+    dW_o = O.cols_dW(H, W, y, vrows, lse_o, n_valid)
+    check_grad("dW rows", dW[vrows].double().cpu().numpy(), dW_o)
 
-    # loss against every row's target logit (oracle) and the GPU lse
-    Hf = H.double().numpy()
-    Wf = W.double().numpy()
-    idx = np.nonzero(valid)[0]
-    zy_all = np.einsum("ij,ij->i", Hf[idx], Wf[y_np[idx]])
-    loss_ref = float(np.sum(lse_g[idx] - zy_all) / n_valid)
-    assert abs(loss.item() - loss_ref) <= LOSS_REL * abs(loss_ref)
     # level at initialisation, independent of any implementation: a row's logits are
     # Gaussian with variance |h|^2 sigma_w^2 (E = D sigma_w^2), so E[lse] = log V +
     # D sigma_w^2 / 2 up to O(1/V), and E[z_y] = 0 (W is drawn independently of the
@@ -102,11 +131,37 @@ def test_fullsize_sampled_parity(lce, name, chunk):
     # sum_v dW[v, d] = sum_i H_id * sum_v (G~_iv - G_iv), where G~ is G rounded to
     # bf16 (at most 2 ulp = 2^-8 relative, P' and then G being rounded), and
     # sum_v |G_iv| <= 2 * dloss / N_valid: |sum_v dW[v, d]| <= 2^-7 / N_valid * sum_i |H_id|.
+    Hf = H.double().numpy()
     colsum = dW.sum(dim=0).abs().double().cpu().numpy()
-    bound = 2.0 ** -7 / n_valid * np.abs(Hf[idx]).sum(axis=0)
+    bound = 2.0 ** -7 / n_valid * np.abs(Hf[valid]).sum(axis=0)
     assert np.all(colsum <= bound), float(np.max(colsum / bound))
     ign = torch.from_numpy(~valid).to(DEV)
     assert dH[ign].abs().max().item() == 0.0
+
+
+def test_fullsize_separate_path_matches_oracle(lce):
+    """lce_forward, then lce_backward from the saved lse (the logits recomputed
+    with the gradient epilogue), on the Llama-3 head at the benchmark's chunk."""
+    name = "llama3-8b"
+    chunk = WORKLOADS[name].chunks[0]
+    H, W, y = _inputs(name)
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    loss, lse = lce.lce_forward(Hd, Wd, yd, chunk=chunk)
+    dH, dW = lce.lce_backward(Hd, Wd, yd, lse, chunk=chunk)
+    torch.cuda.synchronize()
+    del Hd, Wd, yd
+    _check_against_oracle(name, chunk, H, W, y, loss, lse, dH, dW, np.random.default_rng(77))
+
+
+@pytest.mark.parametrize("name,chunk", _cases())
+def test_fullsize_fused_matches_oracle(lce, name, chunk):
+    H, W, y = _inputs(name)
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    loss, lse, dH, dW = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk)
+    torch.cuda.synchronize()
+    del Hd, Wd, yd
+    _check_against_oracle(name, chunk, H, W, y, loss, lse, dH, dW,
+                          np.random.default_rng(1234 + chunk))
 
 
 def test_fullsize_chunk_sweep_agrees(lce):
@@ -127,3 +182,4 @@ def test_fullsize_chunk_sweep_agrees(lce):
         assert (cur[3] - ref[3]).abs().max().item() <= GRAD_REL * ref[3].abs().max().item()
         del loss, lse, dH, dW
     _inputs_cache.clear()
+    _oracle_cache.clear()

@@ -151,17 +151,30 @@ def test_autograd_wrapper(lce):
 
 @pytest.mark.parametrize("name", ["llama2-7b", "mistral-7b"])
 def test_workload_full_oracle(lce, name):
-    """Whole-output comparison on the two mid-size workloads (oracle in fp64)."""
+    """Whole-output comparison on the two mid-size workloads (oracle in fp64),
+    for the fused call and for the separate forward + backward (the backward
+    recomputes each chunk's logits from the saved lse)."""
     wl = WORKLOADS[name]
     H, W, y = workload_inputs(wl)
-    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
-    loss, lse, dH, dW = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=wl.chunks[0])
+    r = run_all_paths(lce, H, W, y, chunk=wl.chunks[0])
+    compare(r, O.forward_backward(H, W, y))
+
+
+def test_autograd_per_row_losses_llama2(lce):
+    """The autograd wrapper with reduction "none" (per-row incoming gradients:
+    it keeps lse and runs the separate backward) on the Llama-2 workload."""
+    wl = WORKLOADS["llama2-7b"]
+    H, W, y = workload_inputs(wl)
+    Hd = H.to(DEV).requires_grad_(True)
+    Wd = W.to(DEV).requires_grad_(True)
+    rows = lce.linear_cross_entropy(Hd, Wd, y.to(DEV), chunk=wl.chunks[0], reduction="none")
+    g = torch.from_numpy(np.random.default_rng(5).standard_normal(wl.N)).float().to(DEV)
+    (rows * g).sum().backward()
     torch.cuda.synchronize()
-    ref = O.forward_backward(H, W, y)
-    check_loss(loss.item(), ref["loss"])
-    check_lse(to64(lse), ref["lse"])
-    check_grad("dH", to64(dH), ref["dH"])
-    check_grad("dW", to64(dW), ref["dW"])
+    ref = O.forward_backward(H, W, y, dloss=g.double().cpu().numpy(), reduction="none")
+    assert np.abs(to64(rows) - ref["loss"]).max() <= 1e-3 * np.abs(ref["loss"]).max()
+    check_grad("dH", to64(Hd.grad), ref["dH"])
+    check_grad("dW", to64(Wd.grad), ref["dW"])
 
 
 @pytest.mark.parametrize("N,D,V,chunk", [(300, 264, 1000, 128), (1000, 520, 3000, 384),
