@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--frozen-w", action="store_true",
                     help="fused path with W frozen (LCE_FROZEN_W: no dW, 4NDV per step), the "
                          "LoRA / QLoRA setting; the headline trains W")
+    ap.add_argument("--low-memory", action="store_true",
+                    help="one chunk buffer (LCE_LOW_MEMORY): no overlap of a chunk's logits GEMM "
+                         "with the previous chunk's gradient GEMMs, about half the workspace")
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
                     help="H and W dtype of the fused path (the headline is bf16)")
     ap.add_argument("--path", choices=["fused", "ce-logits", "norm"], default="fused",
@@ -245,7 +248,9 @@ def run_ours(args, wl, chunk):
     mem0 = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)
     frozen = bool(args.frozen_w)
-    ws = lce.alloc_workspace(N, D, V, chunk, dev, lce.FROZEN_W if frozen else 0)
+    low = bool(args.low_memory)
+    ws_flags = (lce.FROZEN_W if frozen else 0) | (lce.LOW_MEMORY if low else 0)
+    ws = lce.alloc_workspace(N, D, V, chunk, dev, ws_flags)
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     dH = torch.empty(N, D, dtype=Hd.dtype, device=dev)
@@ -254,7 +259,7 @@ def run_ours(args, wl, chunk):
 
     def step():
         lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk, loss=loss, lse=lse, dH=dH, dW=dW, ws=ws,
-                        stream=stream, compute_dW=not frozen)
+                        stream=stream, compute_dW=not frozen, low_memory=low)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -291,6 +296,7 @@ def run_ours(args, wl, chunk):
     step_ms = [a.elapsed_time(b) for a, b in evs]
     total_ms = sum(step_ms)
     grad_ms, grad_n = lce.profile_read("grad")
+    phase_ms, phase_n = lce.profile_read("phase")
     logit_ms, logit_n = lce.profile_read("logits")
     merge_ms, merge_n = lce.profile_read("merge")
     st = lce.read_status(ws)
@@ -305,33 +311,66 @@ def run_ours(args, wl, chunk):
     peak_burst = peaks.get("bf16_tflops", 1900.0)
     peak_sust = peaks.get("bf16_tflops_sustained", 1700.0)
 
-    # dominant kernel: the gradient phase of a chunk (the dH GEMM and the two dW
-    # grids beside and behind it, timed together from fork to join: 4*C*D*V
-    # flops; with W frozen the dH GEMM alone, 2*C*D*V)
+    # dominant kernel. With two chunk buffers (the default) it is the overlapped
+    # phase of a chunk: chunk k-1's dH GEMM beside chunk k's logits tiles and chunk
+    # k-1's dW tiles, which share their launches (one grid beside the dH kernel,
+    # one behind it), timed together from fork to join: 6*C*D*V flops (2 each for
+    # the logits, dH and dW contractions of a chunk). With one buffer (or W frozen)
+    # it is the gradient phase alone: the dH GEMM and the dW grids, 4*C*D*V flops
+    # (W frozen: the dH GEMM alone, 2*C*D*V).
     nchunks = (N + chunk - 1) // chunk
-    grad_flops_launch = (2.0 if frozen else 4.0) * D * V * N / nchunks
+    cdv = float(D) * V * N / nchunks
+    overlapped = phase_n > 0
+    if overlapped:
+        dom_ms, dom_n, dom_flops = phase_ms, phase_n, 6.0 * cdv
+        dom_name = ("overlapped phase: lce_gemm_kernel<MODE_DH> (dH tiles of chunk k-1, 512 wide) "
+                    "beside lce_gemm_kernel<MODE_MIX_P> (logits tiles of chunk k interleaved with "
+                    "the dW tiles of chunk k-1: one grid beside the dH kernel, one behind it)")
+    else:
+        dom_ms, dom_n, dom_flops = grad_ms, grad_n, (2.0 if frozen else 4.0) * cdv
+        dom_name = ("gradient phase, W frozen: lce_gemm_kernel<MODE_DH> (dH tiles, 512 wide, split "
+                    "along the vocabulary) alone" if frozen else
+                    "gradient phase: lce_gemm_kernel<MODE_DH> (dH tiles, 512 wide) + "
+                    "lce_gemm_kernel<MODE_BWD> (dW tiles: one grid beside the dH kernel, one "
+                    "behind it), concurrent")
+    dom_avg_ms = dom_ms / max(dom_n, 1)
+    dom_tflops = dom_flops / (dom_avg_ms / 1e3) / 1e12
     grad_avg_ms = grad_ms / max(grad_n, 1)
-    grad_tflops = grad_flops_launch / (grad_avg_ms / 1e3) / 1e12
+    grad_tflops = (2.0 if frozen else 4.0) * cdv / (grad_avg_ms / 1e3) / 1e12 if grad_n else None
     logit_avg_ms = logit_ms / max(logit_n, 1)
-    logit_tflops = 2.0 * D * V * N / nchunks / (logit_avg_ms / 1e3) / 1e12
+    logit_tflops = 2.0 * cdv / (logit_avg_ms / 1e3) / 1e12 if logit_n else None
     traffic = load_traffic()
+    dom_traffic = traffic.get("phase" if overlapped else ("grad_frozen" if frozen else "grad"))
+    # algorithmic bytes of the method (the minimum it must move) per step: read H, W
+    # and y, write lse, dH and dW (fp32); a launch of the dominant kernel is one of the
+    # step's nchunks units (one chunk), so it carries 1/nchunks of them
+    alg_bytes_step = (N * D * 2 + V * D * 2 + N * 8 + N * 4 + N * D * 2 +
+                      (0 if frozen else V * D * 4))
+    alg_bytes_launch = alg_bytes_step / nchunks
     # softmax / gather epilogue bytes of the fused path (beyond the GEMM operands):
-    # P' written by the logits epilogue, then read and rewritten in place as G by
-    # the fix-up (3 x N x V x 2 B); the (max, sum) slab partials written, read,
-    # rewritten as factors and read again (4 x N x ceil(V/128) x 8 B); target
-    # logits and lse (N x 12 B)
+    # P' written by the logits epilogue, then read and rewritten in place as G by the
+    # prep kernel (3 x N x V x 2 B); the (max, sum) slab partials written and read
+    # (2 x N x ceil(V/128) x 8 B, read once per 16384-column segment of a row:
+    # L2-resident); target logits and lse (N x 12 B)
     elem = 2
-    epi_bytes = 3.0 * N * V * elem + 4.0 * N * ((V + 127) // 128) * 8 + 12.0 * N
+    epi_bytes = 3.0 * N * V * elem + 2.0 * N * ((V + 127) // 128) * 8 + 12.0 * N
     merge_ms_step = merge_ms / args.steps
+    sm_peak_clk = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen)
-        w_up = run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen, upload_w=True)
+        e2e = run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen, low=low)
+        w_up = run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen, upload_w=True,
+                       low=low)
         e2e["with_weight_upload"] = {k: w_up[k] for k in (
             "value", "ms_per_step", "h2d_bytes_per_step", "h2d_ms_per_step_alone",
             "h2d_ms_per_step_under_load", "compute_ms_per_step_under_load")}
+        dh_back = run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen, low=low,
+                          read_dh=True)
+        e2e["with_dh_readback"] = {k: dh_back[k] for k in (
+            "value", "ms_per_step", "h2d_bytes_per_step", "d2h_bytes_per_step",
+            "compute_ms_per_step_under_load", "note")}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -347,7 +386,8 @@ def run_ours(args, wl, chunk):
             "config": workload_config(wl, chunk,
                                       l2="L2 flushed between steps (256 MB write); "
                                          "W 1.05 GB also exceeds L2",
-                                      **({"frozen_w": True} if frozen else {})),
+                                      **({"frozen_w": True} if frozen else {}),
+                                      chunk_buffers=1 if (low or frozen or nchunks == 1) else 2),
             "tflops": tflops,
             "flops_per_step": {"algorithmic": flops_step, "executed": flops_step,
                                "note": "the fused call recomputes nothing: executed = algorithmic "
@@ -357,30 +397,41 @@ def run_ours(args, wl, chunk):
                                  else "6NDV algorithmic", "peak_source": peak_src},
             "peak_extra_hbm_bytes": int(extra_bytes),
             "workspace_bytes": int(ws.numel()),
-            "roofline": {"kernel": "gradient phase, W frozen: lce_gemm_kernel<MODE_DH> (dH tiles, "
-                                   "512 wide, split along the vocabulary) alone" if frozen else
-                                   "gradient phase: lce_gemm_kernel<MODE_DH> (dH tiles, 512 wide) "
-                                   "+ lce_gemm_kernel<MODE_BWD> (dW tiles: one grid beside the "
-                                   "dH kernel, one behind it), concurrent",
-                         "bound": "tensor", "achieved": grad_tflops, "peak": peak_sust,
-                         "peak_kind": f"bf16_tflops_sustained ({peak_src})",
-                         "unit": "TFLOP/s", "frac": grad_tflops / peak_sust,
-                         "traffic": None if frozen else traffic.get("grad"),
-                         "launch_ms": grad_avg_ms, "flops_per_launch": grad_flops_launch},
+            "roofline": {"kernel": dom_name, "bound": "tensor", "achieved": dom_tflops,
+                         "peak": peak_burst,
+                         "peak_kind": f"bf16_tflops, burst ({peak_src}; the launch is timed "
+                                      f"inside the step, not alone: see frac_vs_sustained)",
+                         "unit": "TFLOP/s", "frac": dom_tflops / peak_burst,
+                         "peak_sustained": peak_sust, "frac_vs_sustained": dom_tflops / peak_sust,
+                         "sm_mhz_median": {"this_run": clk.get("sm_mhz"),
+                                           "peak_measurement": sm_peak_clk},
+                         "traffic": dom_traffic,
+                         "alg_bytes_per_launch": alg_bytes_launch,
+                         "traffic_over_alg_bytes": (dom_traffic / alg_bytes_launch
+                                                    if dom_traffic else None),
+                         "alg_bytes_note": "the method's algorithmic bytes per step (read H, W, "
+                                           "y; write lse, dH, dW fp32) / chunks per step",
+                         "launch_ms": dom_avg_ms, "launches": dom_n,
+                         "flops_per_launch": dom_flops},
             "kernels": {
+                "phase": {"ms_per_launch": phase_ms / max(phase_n, 1), "launches": phase_n,
+                          "tflops": dom_tflops if overlapped else None,
+                          "share": phase_ms / total_ms},
                 "grad": {"ms_per_launch": grad_avg_ms, "launches": grad_n,
                          "tflops": grad_tflops, "share": grad_ms / total_ms},
                 "logits": {"ms_per_launch": logit_avg_ms, "launches": logit_n,
                            "tflops": logit_tflops, "share": logit_ms / total_ms},
-                "merge": {"ms_per_launch": merge_ms / max(merge_n, 1), "launches": merge_n,
-                          "share": merge_ms / total_ms},
+                "prep": {"ms_per_launch": merge_ms / max(merge_n, 1), "launches": merge_n,
+                         "share": merge_ms / total_ms},
             },
+            "alg_bytes_per_step": alg_bytes_step,
             "epilogue": {"bytes_per_step": epi_bytes,
                          "what": "P' stored by the logits epilogue, read and rewritten as G by the "
                                  "fix-up; slab (max, sum) partials and factors; target logits, lse",
                          "aux_kernels_ms_per_step": merge_ms_step,
-                         "aux_kernels": "slab merge, fix-up and H-chunk transpose launches (the P' "
-                                        "store itself runs inside the logits GEMM's epilogue)"},
+                         "aux_kernels": "one prep launch per chunk: lse and row losses from the "
+                                        "slab partials, P' -> G in place, H chunk transpose (the "
+                                        "P' store itself runs inside the logits GEMM's epilogue)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "wall_s_timed_region": wall,
@@ -421,7 +472,8 @@ def load_traffic():
     return out
 
 
-def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False, upload_w=False):
+def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False, upload_w=False,
+            low=False, read_dh=False):
     """The same metric through the public API from pinned host buffers: every
     step copies its inputs host -> device and reads its loss back. The inputs
     of a loss step are the hidden states H and the labels y; the LM-head weight
@@ -432,7 +484,9 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False, upload_
     prefetches its next batch would; the loss read-back runs on a third stream
     from one of two device loss slots, so a read-back queued behind a copy never
     holds up the next step. The timed region contains every step's copies and
-    read-backs."""
+    read-backs. read_dh: every step also reads its dH (N x D bf16) back to pinned
+    host memory (from one of two device dH slots, on the read-back stream), as a
+    caller whose next layer's backward runs elsewhere would."""
     import torch
     Hh, yh = H.pin_memory(), y.pin_memory()
     Wh = W.pin_memory() if upload_w else None
@@ -442,11 +496,13 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False, upload_
              torch.empty_like(yh, device=dev)) for _ in range(2)]
     N, D = H.shape
     V = W.shape[0]
-    ws = lce.alloc_workspace(N, D, V, chunk, dev, lce.FROZEN_W if frozen else 0)
+    ws = lce.alloc_workspace(N, D, V, chunk, dev, (lce.FROZEN_W if frozen else 0) |
+                             (lce.LOW_MEMORY if low else 0))
     loss_h = torch.empty(2, dtype=torch.float32).pin_memory()
     loss_slots = torch.empty(2, 4, dtype=torch.float32, device=dev)   # 16-byte aligned slots
     lse = torch.empty(N, dtype=torch.float32, device=dev)
-    dH = torch.empty(N, D, dtype=H.dtype, device=dev)
+    dH_slots = [torch.empty(N, D, dtype=H.dtype, device=dev) for _ in range(2 if read_dh else 1)]
+    dH_h = [torch.empty(N, D, dtype=H.dtype).pin_memory() for _ in range(2)] if read_dh else None
     dW = None if frozen else torch.empty(V, D, dtype=torch.float32, device=dev)
     copy_stream = torch.cuda.Stream(dev)
     d2h_stream = torch.cuda.Stream(dev)
@@ -481,13 +537,16 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False, upload_
         stream.wait_event(read_back[k % 2])   # this loss slot's last value has been read
         e0, e1 = timed(), timed()
         e0.record(stream)
+        dH = dH_slots[k % len(dH_slots)]
         lce.lce_fwd_bwd(b[0], b[1], b[2], chunk=chunk, loss=loss_slots[k % 2, :1], lse=lse,
-                        dH=dH, dW=dW, ws=ws, stream=stream, compute_dW=not frozen)
+                        dH=dH, dW=dW, ws=ws, stream=stream, compute_dW=not frozen, low_memory=low)
         e1.record(stream)
         consumed[k % 2].record(stream)
         with torch.cuda.stream(d2h_stream):
             d2h_stream.wait_event(consumed[k % 2])
             loss_h[k % 2].copy_(loss_slots[k % 2, 0], non_blocking=True)
+            if read_dh:
+                dH_h[k % 2].copy_(dH, non_blocking=True)
             read_back[k % 2].record(d2h_stream)
         spans["compute"].append((e0, e1))
 
@@ -527,16 +586,18 @@ def run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen=False, upload_
     ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)   # the slowest rank, as for value
     under_load = {k: statistics.mean(e0.elapsed_time(e1) for e0, e1 in v) for k, v in spans.items()}
     h2d_bytes = Hh.numel() * 2 + (Wh.numel() * 2 if upload_w else 0) + yh.numel() * 8
+    d2h_bytes = 4 + (N * D * H.element_size() if read_dh else 0)
     return {"value": world * N / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
-            "steps": steps, "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": 4,
+            "steps": steps, "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
             "h2d_ms_per_step_alone": copy_ms, "h2d_gbs": h2d_bytes / copy_ms / 1e6,
             "h2d_ms_per_step_under_load": under_load["copy"],
             "compute_ms_per_step_under_load": under_load["compute"],
             "note": ("every step copies H, W and y" if upload_w else
                      "every step copies H and y (W, a parameter, stays resident)") +
                     " from pinned host memory (on a copy stream, overlapping the previous step's "
-                    "compute) and reads its loss back (on a third stream, from one of two device "
-                    "loss slots)"}
+                    "compute) and reads its loss " + ("and its dH (N x D) " if read_dh else "") +
+                    "back (on a third stream, from one of two device slots)" +
+                    ("" if read_dh else "; dH and dW stay on the device, as in a training step")}
 
 
 def run_ce_logits(args, wl):

@@ -74,12 +74,20 @@ typedef enum lce_status {
 /* Same type as cudaStream_t. NULL means the legacy default stream. */
 typedef struct CUstream_st *lce_stream_t;
 
-/* Bytes of workspace the calls below need for these sizes (same for all three
+/* Bytes of workspace the calls below need for these sizes (enough for all three
  * calls). Writes *bytes; returns LCE_ERR_INVALID_ARG for bad sizes. */
 lce_status lce_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk, size_t *bytes);
 
+/* Bytes of workspace lce_forward (and lce_forward_ex / _opt) needs: the header,
+ * the per-row losses (4 N bytes), the chunk's target logits and its (max, sum)
+ * partial per 128-column slab (8 chunk ceil(V/128) bytes); no chunk buffer, since
+ * the forward stores no logits. At most lce_workspace_size(). */
+lce_status lce_forward_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk,
+                                      size_t *bytes);
+
 /* Forward: loss (device scalar, fp32) and lse[N] (device, fp32).
- * Work: 2*N*D*V flops on the tensor cores, chunk rows at a time. */
+ * Work: 2*N*D*V flops on the tensor cores, chunk rows at a time. The workspace
+ * needs lce_forward_workspace_size() bytes. */
 lce_status lce_forward(const void *H, const void *W, const int64_t *y,
                        int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
                        float *loss, float *lse,
@@ -142,18 +150,27 @@ lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const 
  *                     computed and not written, and may be NULL; the gradient phase
  *                     is the dH contraction alone (4NDV flops per step instead of
  *                     6NDV). Not with LCE_ACCUMULATE_DW (LCE_ERR_INVALID_ARG).
- * With LCE_ACCUMULATE_DH or LCE_FROZEN_W the workspace is
+ *  LCE_LOW_MEMORY     one chunk buffer instead of two. By default (more than one
+ *                     chunk, dW computed) the workspace holds two [chunk, V] chunk
+ *                     buffers, so that chunk k's logits GEMM runs in the same
+ *                     launches as chunk k-1's dW tiles (and beside its dH tiles)
+ *                     while chunk k-1's G sits in the other buffer; with this flag
+ *                     the chunks run one after the other (about half the workspace,
+ *                     slower). Results are the same bits either way.
+ * With LCE_ACCUMULATE_DH, LCE_FROZEN_W or LCE_LOW_MEMORY the workspace is
  * lce_workspace_size_opt(..., flags) bytes (the accumulation needs the chunk's dH in
- * fp32; the frozen-W gradient splits its dH contraction differently); otherwise it
- * is lce_workspace_size(), which lce_workspace_size_opt(..., 0) equals.
- * lce_forward_opt takes LCE_INPUT_FP16 only. Other arguments and outputs as for
- * the _ex entry points. */
+ * fp32; the frozen-W gradient splits its dH contraction differently and keeps one
+ * chunk buffer); otherwise it is lce_workspace_size(), which
+ * lce_workspace_size_opt(..., 0) equals. lce_forward_opt takes LCE_INPUT_FP16 (and
+ * ignores LCE_LOW_MEMORY: the forward keeps no chunk buffer). Other arguments and
+ * outputs as for the _ex entry points. */
 enum {
     LCE_ACCUMULATE_DW = 1,
     LCE_ACCUMULATE_DH = 2,
     LCE_INPUT_FP16 = 4,
     LCE_FROZEN_W = 8,
-    LCE_FLAGS_ALL = 15
+    LCE_LOW_MEMORY = 16,
+    LCE_FLAGS_ALL = 31
 };
 lce_status lce_workspace_size_opt(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
                                   size_t *bytes);
@@ -170,6 +187,33 @@ lce_status lce_fwd_bwd_opt(const void *H, const void *W, const int64_t *y, const
                            int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
                            int reduction, int flags, float *loss, float *lse, void *dH, float *dW,
                            void *ws, size_t ws_bytes, lce_stream_t stream);
+
+/* Token-sharded batches (rows split over several calls, e.g. one per GPU, with W
+ * replicated): the mean loss over the valid rows of ALL shards. Rows are
+ * independent except for the normaliser N_valid, so each shard
+ *  1. counts its valid rows with lce_count_valid (labels in [0, V) other than
+ *     ignore_index, the rule every call uses) into a device int64,
+ *  2. sums the counts of all shards (an all-reduce; not part of this library),
+ *  3. calls lce_fwd_bwd_sharded with that total: the call is lce_fwd_bwd_opt
+ *     with reduction MEAN, except that the mean divides by *n_valid_total
+ *     instead of this call's own count. Its loss is then this shard's share
+ *     sum_{valid i here}(lse_i - z_{i,y_i}) / N_total, and G's rows carry
+ *     dloss / N_total;
+ *  4. sums loss and dW over the shards (all-reduces); dH and lse are per row.
+ * The summed loss and dW are those of one call over the whole batch; dH rows are
+ * that call's rows. ("Unsloth Architecture: Manual Triton Backpropagation,
+ * Fused Cross-Entropy, and 80% VRAM Cut", pillar 1, normalises the loss by the
+ * number of counted tokens; the pages run on one GPU and describe no sharding.)
+ * n_valid_total is a device int64 below 2^31; flags as for lce_fwd_bwd_opt;
+ * the workspace is lce_workspace_size_opt(..., flags) bytes. lce_count_valid
+ * needs no workspace; y is 16-byte aligned, n_valid 8-byte aligned. */
+lce_status lce_count_valid(const int64_t *y, int64_t N, int64_t V, int64_t ignore_index,
+                           int64_t *n_valid, lce_stream_t stream);
+lce_status lce_fwd_bwd_sharded(const void *H, const void *W, const int64_t *y, const float *dloss,
+                               const int64_t *n_valid_total, int64_t N, int64_t D, int64_t V,
+                               int64_t ignore_index, int64_t chunk, int flags, float *loss,
+                               float *lse, void *dH, float *dW, void *ws, size_t ws_bytes,
+                               lce_stream_t stream);
 
 /* Cross-entropy over logits the caller already has (no projection): the
  * streaming row kernel of "Unsloth Kernel Architecture: Custom Triton
@@ -280,7 +324,9 @@ enum {
     LCE_KERNEL_MERGE = 2,    /* slab merge (lse, row loss), G rescale, H-chunk transpose */
     LCE_KERNEL_OTHER = 3,    /* label scan, loss finalisation, dH combination */
     LCE_KERNEL_NORM = 4,     /* RMSNorm forward / backward row kernels, dgamma reduction */
-    LCE_KERNEL_KINDS = 5
+    LCE_KERNEL_PHASE = 5,    /* a gradient phase that also runs the next chunk's logits tiles
+                                (two chunk buffers): dH + dW of chunk k-1, logits of chunk k */
+    LCE_KERNEL_KINDS = 6
 };
 lce_status lce_profile_enable(int on);
 lce_status lce_profile_read(int kind, double *total_ms, int64_t *launches);
@@ -294,19 +340,24 @@ void lce_profile_reset(void);
  * This call takes the same arguments as lce_forward minus the workspace and
  * uses a 64 MiB array built into the library instead (held on every GPU that
  * loads the library until the process exits). It allocates nothing.
- *  - Sizes whose lce_workspace_size() exceeds 64 MiB return LCE_ERR_WORKSPACE
- *    before anything is enqueued; a smaller chunk may fit.
+ *  - Sizes whose lce_forward_workspace_size() exceeds 64 MiB return
+ *    LCE_ERR_WORKSPACE before anything is enqueued; a smaller chunk may fit
+ *    (the Llama-3-sized head, N = 16384, V = 128256, needs ~8.3 MB at chunk 1024).
  *  - The first call on a device looks up the array's device address (one
  *    cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *    before any stream capture. A device reset (cudaDeviceReset) invalidates
+ *    that address: do not use this entry point across one in the same process.
  *  - Every call shares the array, which keeps the last call's contents; each
  *    call clears what must start at zero on its stream. Calls that overlap on
  *    the GPU race on the array: order them on one stream.
- *  - Device-side status (out-of-range labels) is recorded in the shared array
- *    and is not reported by this call. */
+ *  - Device-side status (labels out of range, a bounded wait that ran out) is
+ *    recorded in the shared array: lce_noalloc_read_status(stream) synchronises
+ *    the stream and returns (and clears) it, as lce_read_status does for a
+ *    workspace. Read it before the next call on the device overwrites it. */
 lce_status lce_forward_noalloc(const void *H, const void *W, const int64_t *y,
                                int64_t N, int64_t D, int64_t V, int64_t ignore_index,
                                int64_t chunk, float *loss, float *lse, lce_stream_t stream);
+lce_status lce_noalloc_read_status(lce_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -11,10 +11,14 @@ from ._binding import (  # noqa: F401
     INPUT_FP16,
     KERNEL_KINDS,
     LCEError,
+    LOW_MEMORY,
     LinearCrossEntropyFunction,
     NormLinearCrossEntropyFunction,
     alloc_workspace,
     ce_logits,
+    count_valid,
+    forward_noalloc,
+    forward_workspace_size,
     last_launch_count,
     lce_backward,
     lce_forward,
@@ -23,6 +27,7 @@ from ._binding import (  # noqa: F401
     linear_cross_entropy,
     norm_fwd_bwd,
     norm_linear_cross_entropy,
+    noalloc_read_status,
     norm_workspace_size,
     profile_enable,
     profile_read,
@@ -35,4 +40,4 @@ from ._binding import (  # noqa: F401
     workspace_size_opt,
 )
 from .build_lib import LIB_PATH, build  # noqa: F401
-from .sharded import count_valid, sharded_fwd_bwd  # noqa: F401
+from .sharded import sharded_fwd_bwd  # noqa: F401

@@ -41,6 +41,11 @@ EXPORTED = (
     "lce_forward_opt",
     "lce_backward_opt",
     "lce_fwd_bwd_opt",
+    "lce_forward_workspace_size",
+    "lce_count_valid",
+    "lce_fwd_bwd_sharded",
+    "lce_noalloc_read_status",
+    "lce_forward_noalloc",
     "lce_ce_logits_workspace_size",
     "lce_ce_logits",
     "lce_rmsnorm_forward",
@@ -60,7 +65,7 @@ EXPORTED = (
     "lce_profile_reset",
 )
 
-KERNEL_KINDS = {"logits": 0, "grad": 1, "merge": 2, "other": 3, "norm": 4}
+KERNEL_KINDS = {"logits": 0, "grad": 1, "merge": 2, "other": 3, "norm": 4, "phase": 5}
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 
@@ -113,6 +118,13 @@ def lib() -> ctypes.CDLL:
                                    ctypes.c_int, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
     L.lce_fwd_bwd_opt.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
                                   ctypes.c_int, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    L.lce_forward_workspace_size.argtypes = [_i64, _i64, _i64, _i64,
+                                             ctypes.POINTER(ctypes.c_size_t)]
+    L.lce_count_valid.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp]
+    L.lce_fwd_bwd_sharded.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                      ctypes.c_int, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    L.lce_noalloc_read_status.argtypes = [_vp]
+    L.lce_forward_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp]
     L.lce_ce_logits_workspace_size.argtypes = [_i64, ctypes.POINTER(ctypes.c_size_t)]
     L.lce_ce_logits.argtypes = [_vp, ctypes.c_int, _i64, _vp, _i64, _i64, _i64, ctypes.c_int, _vp,
                                 _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
@@ -148,7 +160,8 @@ def lib() -> ctypes.CDLL:
                  "lce_selftest_wait_timeout",
                  "lce_rmsnorm_backward_workspace_size", "lce_rmsnorm_backward",
                  "lce_norm_workspace_size", "lce_norm_fwd_bwd", "lce_norm_workspace_size_opt",
-                 "lce_norm_fwd_bwd_opt"):
+                 "lce_norm_fwd_bwd_opt", "lce_forward_workspace_size", "lce_count_valid",
+                 "lce_fwd_bwd_sharded", "lce_noalloc_read_status", "lce_forward_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _LIB = L
     return L
@@ -178,6 +191,7 @@ def workspace_size(N: int, D: int, V: int, chunk: int) -> int:
 ACCUMULATE = {"dW": 1, "dH": 2}
 INPUT_FP16 = 4
 FROZEN_W = 8
+LOW_MEMORY = 16
 
 
 def _acc_flags(accumulate, dH, dW, compute_dW=True) -> int:
@@ -195,6 +209,14 @@ def _acc_flags(accumulate, dH, dW, compute_dW=True) -> int:
     return flags
 
 
+def forward_workspace_size(N: int, D: int, V: int, chunk: int) -> int:
+    """Workspace bytes of lce_forward (no chunk buffer)."""
+    out = ctypes.c_size_t(0)
+    _check(lib().lce_forward_workspace_size(N, D, V, chunk, ctypes.byref(out)),
+           "lce_forward_workspace_size")
+    return out.value
+
+
 def workspace_size_opt(N: int, D: int, V: int, chunk: int, flags: int) -> int:
     out = ctypes.c_size_t(0)
     _check(lib().lce_workspace_size_opt(N, D, V, chunk, flags, ctypes.byref(out)),
@@ -203,9 +225,7 @@ def workspace_size_opt(N: int, D: int, V: int, chunk: int, flags: int) -> int:
 
 
 def alloc_workspace(N: int, D: int, V: int, chunk: int, device, flags: int = 0) -> torch.Tensor:
-    n = (workspace_size_opt(N, D, V, chunk, flags) if flags & (ACCUMULATE["dH"] | FROZEN_W)
-         else workspace_size(N, D, V, chunk))
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    return torch.empty(workspace_size_opt(N, D, V, chunk, flags), dtype=torch.uint8, device=device)
 
 
 def _check_inputs(H, W, y):
@@ -256,7 +276,7 @@ def lce_forward(H, W, y, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
     if lse is None:
         lse = torch.empty(N, dtype=torch.float32, device=dev)
     if ws is None:
-        ws = alloc_workspace(N, D, V, chunk, dev)
+        ws = torch.empty(forward_workspace_size(N, D, V, chunk), dtype=torch.uint8, device=dev)
     flags = INPUT_FP16 if H.dtype == torch.float16 else 0
     st = lib().lce_forward_opt(_ptr(H), _ptr(W), _ptr(y), N, D, V, ignore_index, chunk, red, flags,
                                _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
@@ -266,16 +286,17 @@ def lce_forward(H, W, y, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
 
 def lce_backward(H, W, y, lse, dloss=None, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
                  dH=None, dW=None, ws=None, stream=None, reduction: str = "mean",
-                 accumulate=(), compute_dW: bool = True):
+                 accumulate=(), compute_dW: bool = True, low_memory: bool = False):
     """dH (bf16) and dW (fp32) from a saved lse. dloss: scalar tensor, or [N] for
     reduction="none"; None means 1. accumulate: a subset of ("dW", "dH") added
     into the given dW / dH instead of overwriting them. compute_dW=False: W is
-    frozen, dW is neither computed nor returned (None)."""
+    frozen, dW is neither computed nor returned (None). low_memory: one chunk
+    buffer (LCE_LOW_MEMORY; the chunks do not overlap; same results)."""
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
     red = _reduction(reduction)
     flags = (_acc_flags(accumulate, dH, dW, compute_dW) |
-             (INPUT_FP16 if H.dtype == torch.float16 else 0))
+             (INPUT_FP16 if H.dtype == torch.float16 else 0) | (LOW_MEMORY if low_memory else 0))
     if dH is None:
         dH = torch.empty(N, D, dtype=H.dtype, device=dev)
     if not compute_dW:
@@ -294,15 +315,21 @@ def lce_backward(H, W, y, lse, dloss=None, chunk: int = 1024, ignore_index: int 
 
 def lce_fwd_bwd(H, W, y, dloss=None, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
                 loss=None, lse=None, dH=None, dW=None, ws=None, stream=None,
-                reduction: str = "mean", accumulate=(), compute_dW: bool = True):
+                reduction: str = "mean", accumulate=(), compute_dW: bool = True,
+                n_valid_total=None, low_memory: bool = False):
     """Fused forward + backward: (loss, lse, dH, dW). accumulate: a subset of
     ("dW", "dH") added into the given dW / dH instead of overwriting them.
-    compute_dW=False: W is frozen (e.g. a LoRA fine-tune), dW is None."""
+    compute_dW=False: W is frozen (e.g. a LoRA fine-tune), dW is None.
+    n_valid_total: a device int64 tensor of one element, the valid rows of every
+    shard of a token-sharded batch (reduction "mean" only): the mean divides by
+    it instead of this call's count (lce_fwd_bwd_sharded). low_memory: one chunk
+    buffer (LCE_LOW_MEMORY: about half the workspace; the chunks do not overlap;
+    same results)."""
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
     red = _reduction(reduction)
     flags = (_acc_flags(accumulate, dH, dW, compute_dW) |
-             (INPUT_FP16 if H.dtype == torch.float16 else 0))
+             (INPUT_FP16 if H.dtype == torch.float16 else 0) | (LOW_MEMORY if low_memory else 0))
     loss = _loss_buffer(loss, N, reduction, dev)
     if lse is None:
         lse = torch.empty(N, dtype=torch.float32, device=dev)
@@ -315,11 +342,36 @@ def lce_fwd_bwd(H, W, y, dloss=None, chunk: int = 1024, ignore_index: int = IGNO
     if ws is None:
         ws = alloc_workspace(N, D, V, chunk, dev, flags)
     _check_dloss(dloss, N, reduction)
+    if n_valid_total is not None:
+        if reduction != "mean":
+            raise ValueError("n_valid_total is the normaliser of the mean: reduction must be 'mean'")
+        if (n_valid_total.dtype != torch.int64 or not n_valid_total.is_cuda
+                or n_valid_total.numel() != 1):
+            raise TypeError("n_valid_total must be a CUDA int64 tensor of one element")
+        st = lib().lce_fwd_bwd_sharded(_ptr(H), _ptr(W), _ptr(y), _ptr(dloss), _ptr(n_valid_total),
+                                       N, D, V, ignore_index, chunk, flags, _ptr(loss), _ptr(lse),
+                                       _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream(stream))
+        _check(st, "lce_fwd_bwd_sharded")
+        return loss, lse, dH, dW
     st = lib().lce_fwd_bwd_opt(_ptr(H), _ptr(W), _ptr(y), _ptr(dloss), N, D, V, ignore_index,
                                chunk, red, flags, _ptr(loss), _ptr(lse), _ptr(dH), _ptr(dW),
                                _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "lce_fwd_bwd")
     return loss, lse, dH, dW
+
+
+def count_valid(y, V: int, ignore_index: int = IGNORE_INDEX, out=None, stream=None):
+    """Rows of y whose label lies in [0, V) and is not ignore_index, counted on the
+    device by the library (lce_count_valid): an int64 CUDA tensor of one element."""
+    if not y.is_cuda:
+        raise ValueError("y must be a CUDA tensor (there is no CPU path)")
+    if y.dtype != torch.int64 or y.dim() != 1 or not y.is_contiguous():
+        raise TypeError("y must be a contiguous int64 vector")
+    if out is None:
+        out = torch.empty(1, dtype=torch.int64, device=y.device)
+    _check(lib().lce_count_valid(_ptr(y), y.shape[0], V, ignore_index, _ptr(out), _stream(stream)),
+           "lce_count_valid")
+    return out
 
 
 _CE_DTYPES = {torch.bfloat16: 0, torch.float32: 1, torch.float16: 2}
@@ -479,6 +531,24 @@ def selftest_wait_timeout(ws: torch.Tensor, limit_us: int = 20000, stream=None):
 def read_status(ws: torch.Tensor, stream=None) -> int:
     """Synchronise the stream and return (and clear) the device-side status."""
     return lib().lce_read_status(_ptr(ws), _stream(stream))
+
+
+def forward_noalloc(H, W, y, loss, lse, chunk: int = 1024, ignore_index: int = IGNORE_INDEX,
+                    stream=None):
+    """lce_forward on the library's built-in scratch array (lce_forward_noalloc):
+    the caller passes the outputs (loss [1] and lse [N], fp32) and no workspace;
+    nothing is allocated, by the library or here."""
+    N, D, V = _check_inputs(H, W, y)
+    _check(lib().lce_forward_noalloc(_ptr(H), _ptr(W), _ptr(y), N, D, V, ignore_index, chunk,
+                                     _ptr(loss), _ptr(lse), _stream(stream)),
+           "lce_forward_noalloc")
+    return loss, lse
+
+
+def noalloc_read_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device-side status of the
+    built-in scratch array used by forward_noalloc."""
+    return lib().lce_noalloc_read_status(_stream(stream))
 
 
 def last_launch_count() -> int:

@@ -87,11 +87,15 @@ struct Layout {
     int nparts = 0;          // 128-column slabs per row
     int ldg = 0;             // row stride of the chunk buffer (elements)
     int ldt = 0;             // row stride (elements) of H^T: chunk rows rounded up
+    int nbuf = 1;            // chunk buffers: with two, a chunk's logits GEMM runs while
+                             // the previous chunk's gradient GEMMs read the other
+    size_t gbuf_bytes = 0;   // bytes of one chunk buffer
     bool frozen_w = false;   // no dW contraction (LCE_FROZEN_W)
     int dh_splits = 1;       // vocabulary parts of a full chunk's dH tiles
     long long ldp = 0;       // rows per fp32 dH partial array: chunk rows rounded up to 128
     size_t off_loss_rows = 0, off_zy = 0, off_parts = 0, off_G = 0, off_HT = 0, off_dHp = 0;
     size_t total = 0;
+    size_t fwd_total = 0;    // the forward's share: header, row losses, target logits, partials
     size_t hdr_bytes = 0;
 };
 
@@ -114,7 +118,7 @@ int dh_splits_for(long long rows, long long D, long long V, bool frozen_w = fals
 }
 
 bool make_layout(long long N, long long D, long long V, long long chunk, Layout &L,
-                 bool frozen_w = false) {
+                 bool frozen_w = false, bool low_mem = false) {
     if (N < 0 || D <= 0 || V <= 0 || chunk <= 0) return false;
     if (D % 8 != 0) return false;
     if (N > 0x7fffffffll || D > 0x7fffffffll || V > MAX_V) return false;
@@ -132,7 +136,13 @@ bool make_layout(long long N, long long D, long long V, long long chunk, Layout 
     L.off_parts = off;
     off += align_up(sizeof(float2) * static_cast<size_t>(L.C) * L.nparts, 1024);
     L.off_G = off;
-    off += align_up(2 * static_cast<size_t>(L.C) * L.ldg, 1024);
+    L.fwd_total = off;
+    // two chunk buffers when there is a dW contraction and more than one chunk:
+    // chunk k's logits (P' or G) go into one while chunk k-1's dH and dW tiles read
+    // the other (LCE_LOW_MEMORY: one buffer, no overlap across chunks)
+    L.nbuf = (!frozen_w && !low_mem && L.nchunks > 1) ? 2 : 1;
+    L.gbuf_bytes = align_up(2 * static_cast<size_t>(L.C) * L.ldg, 1024);
+    off += static_cast<size_t>(L.nbuf) * L.gbuf_bytes;
     // H chunk^T [D][ldt]: the K-major B operand of the dW contraction (none when W
     // is frozen)
     L.frozen_w = frozen_w;
@@ -169,7 +179,7 @@ size_t acc_dh_bytes(const Layout &L, long long D) {
 
 bool make_norm_layout(long long N, long long D, long long V, long long chunk, NormLayout &NL,
                       bool frozen_w = false) {
-    if (!make_layout(N, D, V, chunk, NL.L, frozen_w)) return false;
+    if (!make_layout(N, D, V, chunk, NL.L, frozen_w, true)) return false;
     if (D > NRM_MAX_D) return false;
     // the chunk's dH (fp32): the layout's partial arrays, or one array past them
     NL.off_dH = NL.L.off_dHp;
@@ -239,7 +249,7 @@ struct Ctx {
     int *hdr;
     float *loss_rows, *zy;
     float2 *parts;
-    __nv_bfloat16 *G;
+    __nv_bfloat16 *Gb[2];   // the chunk buffers (Gb[1] == Gb[0] with one)
     __nv_bfloat16 *HT;
     int sms;
     int pairs;   // > 0: GEMMs run as CTA pairs (cluster of 2), at most this many at once
@@ -332,15 +342,15 @@ SideStream *side_stream() {
 lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t N, int64_t D,
                  int64_t V, int64_t ign, int64_t chunk, void *ws, size_t ws_bytes,
                  lce_stream_t stream, bool h_chunked = false, bool f16 = false,
-                 bool frozen_w = false) {
+                 bool frozen_w = false, bool fwd_only = false, bool low_mem = false) {
     g_launches = 0;
-    if (!make_layout(N, D, V, chunk, c.L, frozen_w)) return LCE_ERR_INVALID_ARG;
+    if (!make_layout(N, D, V, chunk, c.L, frozen_w, low_mem)) return LCE_ERR_INVALID_ARG;
     if (!ws) return LCE_ERR_INVALID_ARG;
     if (N > 0 && (!H || !y)) return LCE_ERR_INVALID_ARG;
     if (!W) return LCE_ERR_INVALID_ARG;
     if (!aligned16(ws) || !aligned16(W) || (H && !aligned16(H)) || (y && !aligned16(y)))
         return LCE_ERR_ALIGNMENT;
-    if (ws_bytes < c.L.total) return LCE_ERR_WORKSPACE;
+    if (ws_bytes < (fwd_only ? c.L.fwd_total : c.L.total)) return LCE_ERR_WORKSPACE;
     lce_status st = init_device(&c.sms, &c.pairs);
     if (st != LCE_OK) return st;
     c.H = static_cast<const __nv_bfloat16 *>(H);
@@ -355,14 +365,17 @@ lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t
     c.loss_rows = reinterpret_cast<float *>(c.ws + c.L.off_loss_rows);
     c.zy = reinterpret_cast<float *>(c.ws + c.L.off_zy);
     c.parts = reinterpret_cast<float2 *>(c.ws + c.L.off_parts);
-    c.G = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_G);
+    c.Gb[0] = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_G);
+    c.Gb[1] = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_G +
+                                                (c.L.nbuf > 1 ? c.L.gbuf_bytes : 0));
     c.HT = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_HT);
     c.s = reinterpret_cast<cudaStream_t>(stream);
     c.reduction = LCE_REDUCTION_MEAN;
     c.h_chunked = h_chunked;
     c.f16 = f16;
     c.t16 = f16 ? MAP_F16 : MAP_BF16;
-    // with CTA pairs each CTA loads half of a 256-row W tile (multicast to both)
+    // with CTA pairs each CTA loads its own half (128 rows) of a 256-row W tile; the
+    // pair MMA reads both CTAs' halves from their shared memory
     if (!encode_2d(&c.tmW_K, W, D, V, D * 2, BK, c.pairs > 0 ? BN / 2 : BN, c.t16)) return LCE_ERR_CUDA;
     if (!encode_2d(&c.tmW_MN, W, D, V, D * 2, 64, BK, c.t16)) return LCE_ERR_CUDA;
     if (N > 0 && !encode_2d(&c.tmH_K, H, D, h_chunked ? c.L.C : N, D * 2, BK, BM, c.t16))
@@ -384,7 +397,7 @@ void base_params(const Ctx &c, GemmParams &p, long long row0, long long rows, in
     p.parts = c.parts;
     p.nparts = c.L.nparts;
     p.zy = c.zy;
-    p.G = c.G;
+    p.G = c.Gb[0];
     p.ldg = c.L.ldg;
     p.timeout_ns = kDefaultTimeoutNs;
     p.dloss_per_row = c.reduction == LCE_REDUCTION_NONE ? 1 : 0;
@@ -393,7 +406,7 @@ void base_params(const Ctx &c, GemmParams &p, long long row0, long long rows, in
 }
 
 lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, int slot,
-                      const float *lse, const float *dloss) {
+                      const float *lse, const float *dloss, __nv_bfloat16 *G) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
     base_params(c, p, row0, rows, slot);
@@ -407,7 +420,8 @@ lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, in
     p.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * p.n_blocks0;
     p.lse = lse;
     p.dloss = dloss;
-    if (mode != MODE_LSE && !encode_store_2d(&p.tmS0, c.G, c.V, rows, 2ull * c.L.ldg, c.t16, 32))
+    p.G = G;
+    if (mode != MODE_LSE && !encode_store_2d(&p.tmS0, G, c.V, rows, 2ull * c.L.ldg, c.t16, 32))
         return LCE_ERR_CUDA;
     const int units = cl == 2 ? c.pairs : c.sms;
     const int grid = cl * (p.total_tiles < units ? p.total_tiles : units);
@@ -439,12 +453,41 @@ int dh_parts(const Ctx &c, long long rows) {
     return sp < c.L.dh_splits ? sp : c.L.dh_splits;
 }
 
+// The logits tiles of the next chunk that a gradient phase runs in the same
+// launches as its dW tiles (MODE_MIX_P: P' epilogue of the fused path; MODE_MIX_G:
+// G epilogue of the backward from a saved lse), writing into chunk buffer G.
+struct Mix {
+    int mode;
+    long long row0, rows;
+    int slot;                // tile counter of the launches
+    __nv_bfloat16 *G;
+    const float *lse;        // MODE_MIX_G
+};
+
+lce_status run_transpose(const Ctx &c, long long row0, long long rows) {
+    const __nv_bfloat16 *Hc = c.h_chunked ? c.H : c.H + row0 * c.D;
+    TransposeParams tp;
+    tp.src = Hc;
+    tp.ld_src = static_cast<int>(c.D);
+    tp.dst_t = c.HT;
+    tp.ld_t = c.L.ldt;
+    tp.rows = static_cast<int>(rows);
+    tp.cols = static_cast<int>(c.D);
+    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_transpose(tp, c.s));
+    return LCE_OK;
+}
+
+// The gradient phase of the chunk at row0 (dH and dW from chunk buffer G).
+// transposed: the H chunk^T the dW tiles read is already in place (else it is
+// made first). mix: logits tiles of the next chunk to run in the dW launches.
 // *parts_used: the number of non-empty vocabulary parts written (fp32 output).
 lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const DhOut &o,
-                   float *dW, bool accumulate, const float *dloss, int *parts_used = nullptr) {
+                   float *dW, bool accumulate, const float *dloss, __nv_bfloat16 *G,
+                   bool transposed, const Mix *mix, int *parts_used = nullptr) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
     base_params(c, p, row0, rows, slot);
+    p.G = G;
     void *dHc = o.ptr;
     const bool dh_fp32 = o.fp32;
     const int want_parts = (o.fp32 && o.parts > 1 && c.pairs > 0) ? o.parts : 1;
@@ -453,22 +496,14 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
     const int cl = c.pairs > 0 ? 2 : 1;
     if (with_dw) {
         // the H chunk^T for the K-major B operand of the dW tiles
-        const __nv_bfloat16 *Hc = c.h_chunked ? c.H : c.H + row0 * c.D;
-        TransposeParams tp;
-        tp.src = Hc;
-        tp.ld_src = static_cast<int>(c.D);
-        tp.dst_t = c.HT;
-        tp.ld_t = c.L.ldt;
-        tp.rows = static_cast<int>(rows);
-        tp.cols = static_cast<int>(c.D);
-        LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_transpose(tp, c.s));
+        if (!transposed) LCE_TRY(run_transpose(c, row0, rows));
         // dW A = G^T read from G itself (MN-major boxes of 64 vocab columns x 64 rows)
-        if (!encode_2d(&p.tmA1, c.G, c.V, rows, 2ull * c.L.ldg, 64, BK, c.t16)) return LCE_ERR_CUDA;
+        if (!encode_2d(&p.tmA1, G, c.V, rows, 2ull * c.L.ldg, 64, BK, c.t16)) return LCE_ERR_CUDA;
         if (!encode_2d(&p.tmB1, c.HT, rows, c.D, 2ull * c.L.ldt, BK, BN / cl, c.t16))
             return LCE_ERR_CUDA;
         if (!encode_store_2d(&p.tmS1, dW, c.D, c.V, 4ull * c.D, MAP_F32)) return LCE_ERR_CUDA;
     }
-    if (!encode_2d(&p.tmA0, c.G, c.V, rows, 2ull * c.L.ldg, BK, BM, c.t16)) return LCE_ERR_CUDA;
+    if (!encode_2d(&p.tmA0, G, c.V, rows, 2ull * c.L.ldg, BK, BM, c.t16)) return LCE_ERR_CUDA;
     p.tmB0 = c.tmW_MN;
     const uint64_t s0_rows = want_parts > 1 ? static_cast<uint64_t>(want_parts) * o.ldp : rows;
     if (!encode_store_2d(&p.tmS0, dHc, c.D, s0_rows, (dh_fp32 ? 4ull : 2ull) * c.D,
@@ -507,7 +542,8 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
         // long dH tiles to run after it). A third launch, a dW grid as large as
         // the dH one, queued on the caller's stream behind the dH kernel, takes
         // over the dH kernel's SMs when it ends; both dW grids draw tiles from
-        // the same counter.
+        // the same counter. With `mix`, the dW grids also carry the next chunk's
+        // logits tiles, interleaved with the dW tiles.
         GemmParams ph = p;
         ph.n_blocks0 = static_cast<int>(cdiv(c.D, BN_WIDE));
         ph.m_blocks1 = ph.n_blocks1 = ph.k_blocks1 = 0;
@@ -519,9 +555,31 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
             return LCE_OK;
         }
         GemmParams pw = p;
+        int mode_w = MODE_BWD;
         pw.m_blocks0 = 0;
+        pw.k_splits = 0;
         pw.total_tiles = static_cast<int>(cdiv(p.m_blocks1, cl)) * p.n_blocks1;
         pw.tile_counter = c.hdr + HDR_COUNTERS + 2 * c.L.nchunks + 2 + slot / 2;
+        if (mix) {
+            // the next chunk's logits tiles: A = its H rows, B = W (both K-major),
+            // P' / G stored into mix->G; rows and row0 are that chunk's (the dW
+            // tiles use neither)
+            mode_w = mix->mode;
+            pw.tmA0 = c.tmH_K;
+            pw.tmB0 = c.tmW_K;
+            pw.a_row0 = static_cast<int>(mix->row0);
+            pw.rows = static_cast<int>(mix->rows);
+            pw.row0 = static_cast<int>(mix->row0);
+            pw.lse = mix->lse;
+            pw.G = mix->G;
+            if (!encode_store_2d(&pw.tmS0, mix->G, c.V, mix->rows, 2ull * c.L.ldg, c.t16, 32))
+                return LCE_ERR_CUDA;
+            pw.m_blocks0 = static_cast<int>(cdiv(mix->rows, BM));
+            pw.n_blocks0 = static_cast<int>(cdiv(c.V, BN));
+            pw.k_blocks0 = static_cast<int>(cdiv(c.D, BK));
+            pw.total_tiles += static_cast<int>(cdiv(pw.m_blocks0, cl)) * pw.n_blocks0;
+            pw.tile_counter = c.hdr + HDR_COUNTERS + mix->slot;
+        }
         SideStream *ss = side_stream();
         if (!ss) return LCE_ERR_CUDA;
         std::lock_guard<std::mutex> lock(ss->mu);
@@ -529,7 +587,7 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
         const int free_pairs = units - dh_pairs;
         const int w1 = pw.total_tiles < free_pairs ? pw.total_tiles : free_pairs;
         const int w2 = pw.total_tiles < dh_pairs ? pw.total_tiles : dh_pairs;
-        const int pi = prof_begin(LCE_KERNEL_GRAD, c.s);
+        const int pi = prof_begin(mix ? LCE_KERNEL_PHASE : LCE_KERNEL_GRAD, c.s);
         if (cudaEventRecord(ss->fork, c.s) != cudaSuccess ||
             cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
             return LCE_ERR_CUDA;
@@ -539,11 +597,11 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
             ++launched;
         }
         if (w1 > 0) {
-            if (launch_gemm(MODE_BWD, cl, pw, cl * w1, ss->s) != cudaSuccess) return LCE_ERR_CUDA;
+            if (launch_gemm(mode_w, cl, pw, cl * w1, ss->s) != cudaSuccess) return LCE_ERR_CUDA;
             ++launched;
         }
         if (w2 > 0 && (dh_pairs > 0 || w1 == 0)) {
-            if (launch_gemm(MODE_BWD, cl, pw, cl * w2, c.s) != cudaSuccess) return LCE_ERR_CUDA;
+            if (launch_gemm(mode_w, cl, pw, cl * w2, c.s) != cudaSuccess) return LCE_ERR_CUDA;
             ++launched;
         }
         if (cudaEventRecord(ss->join, ss->s) != cudaSuccess ||
@@ -563,14 +621,16 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
 // fp32 partial arrays and the combining kernel (which adds into the caller's dH
 // when accumulating).
 lce_status run_grad(const Ctx &c, long long row0, long long rows, int slot, void *dHc,
-                    bool acc_dh, float *dW, bool acc_dw, const float *dloss) {
+                    bool acc_dh, float *dW, bool acc_dw, const float *dloss, __nv_bfloat16 *G,
+                    bool transposed, const Mix *mix = nullptr) {
     const int want = dh_parts(c, rows);
     if (want <= 1 && !acc_dh)
-        return run_bwd(c, row0, rows, slot, DhOut{dHc, false, 1, 0}, dW, acc_dw, dloss);
+        return run_bwd(c, row0, rows, slot, DhOut{dHc, false, 1, 0}, dW, acc_dw, dloss, G,
+                       transposed, mix);
     float *dHp = reinterpret_cast<float *>(c.ws + c.L.off_dHp);
     int parts = 1;
-    LCE_TRY(run_bwd(c, row0, rows, slot, DhOut{dHp, true, want, c.L.ldp}, dW, acc_dw, dloss,
-                    &parts));
+    LCE_TRY(run_bwd(c, row0, rows, slot, DhOut{dHp, true, want, c.L.ldp}, dW, acc_dw, dloss, G,
+                    transposed, mix, &parts));
     LCE_LAUNCH(launch_combine_dh(dHp, parts, c.L.ldp * c.D, dHc, rows * c.D, c.f16, acc_dh,
                                  c.sms, c.s));
     return LCE_OK;
@@ -582,7 +642,7 @@ lce_status run_merge(const Ctx &c, bool fused, long long row0, long long rows, f
     m.parts = c.parts;
     m.nparts = c.L.nparts;
     m.zy = c.zy;
-    m.G = c.G;
+    m.G = c.Gb[0];
     m.ldg = c.L.ldg;
     m.rows = static_cast<int>(rows);
     m.row0 = static_cast<int>(row0);
@@ -600,25 +660,56 @@ lce_status run_merge(const Ctx &c, bool fused, long long row0, long long rows, f
     return LCE_OK;
 }
 
-// Fused path: P' -> G in place in the chunk buffer.
-lce_status run_fixup(const Ctx &c, long long row0, long long rows, const float *dloss) {
-    FixupParams fp;
-    fp.G = c.G;
-    fp.ldg = c.L.ldg;
-    fp.rows = static_cast<int>(rows);
-    fp.V = static_cast<int>(c.V);
-    fp.parts = c.parts;
-    fp.nparts = c.L.nparts;
-    fp.y = c.y;
-    fp.row0 = static_cast<int>(row0);
-    fp.ignore_index = c.ign;
-    fp.hdr = c.hdr;
-    fp.dloss = dloss;
-    fp.dloss_per_row = c.reduction == LCE_REDUCTION_NONE ? 1 : 0;
-    fp.mean = c.reduction == LCE_REDUCTION_MEAN ? 1 : 0;
-    fp.f16 = c.f16 ? 1 : 0;
-    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_fixup(fp, c.s));
+// Fused path, between a chunk's logits GEMM and its gradient GEMMs, one launch:
+// lse and the row losses, P' -> G in place in chunk buffer G, and (transpose) the
+// H chunk^T the dW tiles read.
+lce_status run_prep(const Ctx &c, long long row0, long long rows, float *lse,
+                    const float *dloss, float *loss_rows, __nv_bfloat16 *G, bool transpose) {
+    PrepParams pp;
+    memset(&pp, 0, sizeof(pp));
+    MergeParams &m = pp.m;
+    m.parts = c.parts;
+    m.nparts = c.L.nparts;
+    m.zy = c.zy;
+    m.G = G;
+    m.ldg = c.L.ldg;
+    m.rows = static_cast<int>(rows);
+    m.row0 = static_cast<int>(row0);
+    m.V = static_cast<int>(c.V);
+    m.ignore_index = c.ign;
+    m.y = c.y;
+    m.hdr = c.hdr;
+    m.dloss = dloss;
+    m.dloss_per_row = c.reduction == LCE_REDUCTION_NONE ? 1 : 0;
+    m.mean = c.reduction == LCE_REDUCTION_MEAN ? 1 : 0;
+    m.f16 = c.f16 ? 1 : 0;
+    m.lse = lse;
+    m.loss_rows = loss_rows;
+    pp.ldg = c.L.ldg;
+    pp.segs = static_cast<int>(cdiv(cdiv(c.V, 8), PREP_VEC_PER_CTA));
+    if (transpose) {
+        pp.tp.src = c.h_chunked ? c.H : c.H + row0 * c.D;
+        pp.tp.ld_src = static_cast<int>(c.D);
+        pp.tp.dst_t = c.HT;
+        pp.tp.ld_t = c.L.ldt;
+        pp.tp.rows = static_cast<int>(rows);
+        pp.tp.cols = static_cast<int>(c.D);
+        pp.tt_x = static_cast<int>(cdiv(c.D, 64));
+    }
+    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_prep(pp, c.s));
     return LCE_OK;
+}
+
+// Rows of chunk k (the last chunk may be shorter).
+inline long long chunk_rows(const Ctx &c, long long k) {
+    const long long row0 = k * c.L.C;
+    return (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
+}
+
+// Whether the chunks' gradient phases overlap the next chunk's logits GEMM: CTA
+// pairs, a dW contraction, two chunk buffers (so more than one chunk), H in place.
+inline bool overlapped(const Ctx &c) {
+    return c.pairs > 0 && !c.L.frozen_w && c.L.nbuf == 2 && !c.h_chunked;
 }
 
 }  // namespace
@@ -633,11 +724,37 @@ lce_status lce_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk, si
     return LCE_OK;
 }
 
+lce_status lce_forward_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk,
+                                      size_t *bytes) {
+    if (!bytes) return LCE_ERR_INVALID_ARG;
+    Layout L;
+    if (!make_layout(N, D, V, chunk, L)) return LCE_ERR_INVALID_ARG;
+    *bytes = L.fwd_total;
+    return LCE_OK;
+}
+
+lce_status lce_count_valid(const int64_t *y, int64_t N, int64_t V, int64_t ignore_index,
+                           int64_t *n_valid, lce_stream_t stream) {
+    g_launches = 0;
+    if (N < 0 || V <= 0 || !n_valid || (N > 0 && !y)) return LCE_ERR_INVALID_ARG;
+    if ((y && !aligned16(y)) || (reinterpret_cast<uintptr_t>(n_valid) & 7u))
+        return LCE_ERR_ALIGNMENT;
+    int sms = 0, pairs = 0;
+    lce_status st = init_device(&sms, &pairs);
+    if (st != LCE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    LCE_LAUNCH_KIND(LCE_KERNEL_OTHER, s,
+                    launch_count_valid(reinterpret_cast<const long long *>(y), N, V, ignore_index,
+                                       reinterpret_cast<long long *>(n_valid), s));
+    return LCE_OK;
+}
+
 lce_status lce_workspace_size_opt(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
                                   size_t *bytes) {
     if (!bytes || (flags & ~LCE_FLAGS_ALL)) return LCE_ERR_INVALID_ARG;
     Layout L;
-    if (!make_layout(N, D, V, chunk, L, (flags & LCE_FROZEN_W) != 0)) return LCE_ERR_INVALID_ARG;
+    if (!make_layout(N, D, V, chunk, L, (flags & LCE_FROZEN_W) != 0, (flags & LCE_LOW_MEMORY) != 0))
+        return LCE_ERR_INVALID_ARG;
     *bytes = L.total + ((flags & LCE_ACCUMULATE_DH) ? acc_dh_bytes(L, D) : 0);
     return LCE_OK;
 }
@@ -648,19 +765,21 @@ lce_status lce_forward_opt(const void *H, const void *W, const int64_t *y, int64
                            lce_stream_t stream) {
     g_launches = 0;
     if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
-    if (flags & ~LCE_INPUT_FP16) return LCE_ERR_INVALID_ARG;   // nothing to accumulate here
+    // nothing to accumulate here, and no chunk buffer to keep small
+    if (flags & ~(LCE_INPUT_FP16 | LCE_LOW_MEMORY)) return LCE_ERR_INVALID_ARG;
     const bool none = reduction == LCE_REDUCTION_NONE;
     if ((!none && !loss) || (N > 0 && (!lse || !loss))) return LCE_ERR_INVALID_ARG;
     if ((loss && !aligned16(loss)) || (lse && !aligned16(lse))) return LCE_ERR_ALIGNMENT;
     Ctx c;
     LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, false,
-                  (flags & LCE_INPUT_FP16) != 0));
+                  (flags & LCE_INPUT_FP16) != 0, false, true));
     c.reduction = reduction;
     float *rows_out = none ? loss : c.loss_rows;
     for (long long k = 0; k < c.L.nchunks; ++k) {
         const long long row0 = k * c.L.C;
         const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
-        LCE_TRY(run_logits(c, MODE_LSE, row0, rows, static_cast<int>(k), nullptr, nullptr));
+        LCE_TRY(run_logits(c, MODE_LSE, row0, rows, static_cast<int>(k), nullptr, nullptr,
+                           c.Gb[0]));
         LCE_TRY(run_merge(c, false, row0, rows, lse, nullptr, rows_out));
     }
     if (!none)
@@ -699,25 +818,43 @@ lce_status lce_backward_opt(const void *H, const void *W, const int64_t *y, cons
     if ((dW && !aligned16(dW)) || (dH && !aligned16(dH)) || (lse && !aligned16(lse)))
         return LCE_ERR_ALIGNMENT;
     const bool acc_dh = (flags & LCE_ACCUMULATE_DH) != 0;
+    const bool low_mem = (flags & LCE_LOW_MEMORY) != 0;
     Layout L0;
-    if (!make_layout(N, D, V, chunk, L0, frozen)) return LCE_ERR_INVALID_ARG;
+    if (!make_layout(N, D, V, chunk, L0, frozen, low_mem)) return LCE_ERR_INVALID_ARG;
     if (acc_dh && ws_bytes < L0.total + acc_dh_bytes(L0, D)) return LCE_ERR_WORKSPACE;
     Ctx c;
     LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, false, f16,
-                  frozen));
+                  frozen, false, low_mem));
     c.reduction = reduction;
     if (frozen) dW = nullptr;
     if (c.L.nchunks == 0 && dW && !(flags & LCE_ACCUMULATE_DW)) {
         if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess)
             return LCE_ERR_CUDA;
     }
+    const bool acc_dw0 = (flags & LCE_ACCUMULATE_DW) != 0;
+    __nv_bfloat16 *dHb = static_cast<__nv_bfloat16 *>(dH);
+    if (overlapped(c)) {
+        // chunk k's logits (G epilogue, into buffer k % 2) run in the same launches
+        // as chunk k-1's dW tiles, beside chunk k-1's dH tiles; then chunk k's H^T
+        LCE_TRY(run_logits(c, MODE_G, 0, chunk_rows(c, 0), 0, lse, dloss, c.Gb[0]));
+        LCE_TRY(run_transpose(c, 0, chunk_rows(c, 0)));
+        for (long long k = 1; k <= c.L.nchunks; ++k) {
+            const long long p0 = (k - 1) * c.L.C, prow = chunk_rows(c, k - 1);
+            Mix mx{MODE_MIX_G, k * c.L.C, k < c.L.nchunks ? chunk_rows(c, k) : 0,
+                   static_cast<int>(2 * k), c.Gb[k & 1], lse};
+            LCE_TRY(run_grad(c, p0, prow, static_cast<int>(2 * k - 1), dHb + p0 * c.D, acc_dh, dW,
+                             k > 1 || acc_dw0, dloss, c.Gb[(k - 1) & 1], true,
+                             k < c.L.nchunks ? &mx : nullptr));
+            if (k < c.L.nchunks) LCE_TRY(run_transpose(c, k * c.L.C, chunk_rows(c, k)));
+        }
+        return LCE_OK;
+    }
     for (long long k = 0; k < c.L.nchunks; ++k) {
         const long long row0 = k * c.L.C;
-        const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
-        __nv_bfloat16 *dHc = static_cast<__nv_bfloat16 *>(dH) + row0 * c.D;
-        LCE_TRY(run_logits(c, MODE_G, row0, rows, static_cast<int>(2 * k), lse, dloss));
-        LCE_TRY(run_grad(c, row0, rows, static_cast<int>(2 * k + 1), dHc, acc_dh, dW,
-                         k > 0 || (flags & LCE_ACCUMULATE_DW), dloss));
+        const long long rows = chunk_rows(c, k);
+        LCE_TRY(run_logits(c, MODE_G, row0, rows, static_cast<int>(2 * k), lse, dloss, c.Gb[0]));
+        LCE_TRY(run_grad(c, row0, rows, static_cast<int>(2 * k + 1), dHb + row0 * c.D, acc_dh, dW,
+                         k > 0 || acc_dw0, dloss, c.Gb[0], false));
     }
     return LCE_OK;
 }
@@ -738,10 +875,17 @@ lce_status lce_backward(const void *H, const void *W, const int64_t *y, const fl
                            LCE_REDUCTION_MEAN, ws, ws_bytes, stream);
 }
 
-lce_status lce_fwd_bwd_opt(const void *H, const void *W, const int64_t *y, const float *dloss,
-                           int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
-                           int reduction, int flags, float *loss, float *lse, void *dH, float *dW,
-                           void *ws, size_t ws_bytes, lce_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The fused call; n_valid_total (device int64, or null) replaces this call's own
+// count of valid rows as the normaliser of the mean.
+lce_status fwd_bwd_impl(const void *H, const void *W, const int64_t *y, const float *dloss,
+                        int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                        int reduction, int flags, float *loss, float *lse, void *dH, float *dW,
+                        void *ws, size_t ws_bytes, lce_stream_t stream,
+                        const int64_t *n_valid_total) {
     g_launches = 0;
     if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
     if (flags & ~LCE_FLAGS_ALL) return LCE_ERR_INVALID_ARG;
@@ -756,33 +900,81 @@ lce_status lce_fwd_bwd_opt(const void *H, const void *W, const int64_t *y, const
         (lse && !aligned16(lse)))
         return LCE_ERR_ALIGNMENT;
     const bool acc_dh = (flags & LCE_ACCUMULATE_DH) != 0;
+    const bool low_mem = (flags & LCE_LOW_MEMORY) != 0;
     Layout L0;
-    if (!make_layout(N, D, V, chunk, L0, frozen)) return LCE_ERR_INVALID_ARG;
+    if (!make_layout(N, D, V, chunk, L0, frozen, low_mem)) return LCE_ERR_INVALID_ARG;
     if (acc_dh && ws_bytes < L0.total + acc_dh_bytes(L0, D)) return LCE_ERR_WORKSPACE;
     Ctx c;
     LCE_TRY(setup(c, H, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, false, f16,
-                  frozen));
+                  frozen, false, low_mem));
     c.reduction = reduction;
+    if (n_valid_total) LCE_LAUNCH(launch_set_nvalid(reinterpret_cast<const long long *>(n_valid_total),
+                                                    c.hdr, c.s));
     if (frozen) dW = nullptr;
     float *rows_out = none ? loss : c.loss_rows;
     if (c.L.nchunks == 0 && dW && !(flags & LCE_ACCUMULATE_DW)) {
         if (cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V) * D, c.s) != cudaSuccess)
             return LCE_ERR_CUDA;
     }
-    for (long long k = 0; k < c.L.nchunks; ++k) {
-        const long long row0 = k * c.L.C;
-        const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
-        __nv_bfloat16 *dHc = static_cast<__nv_bfloat16 *>(dH) + row0 * c.D;
-        LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr));
-        LCE_TRY(run_merge(c, true, row0, rows, lse, dloss, rows_out));
-        LCE_TRY(run_fixup(c, row0, rows, dloss));
-        LCE_TRY(run_grad(c, row0, rows, static_cast<int>(2 * k + 1), dHc, acc_dh, dW,
-                         k > 0 || (flags & LCE_ACCUMULATE_DW), dloss));
+    const bool acc_dw0 = (flags & LCE_ACCUMULATE_DW) != 0;
+    __nv_bfloat16 *dHb = static_cast<__nv_bfloat16 *>(dH);
+    if (overlapped(c)) {
+        // chunk k's logits (P' epilogue, into buffer k % 2) run in the same launches
+        // as chunk k-1's dW tiles, beside chunk k-1's dH tiles; then chunk k's
+        // prep (lse, row losses, P' -> G, H^T)
+        LCE_TRY(run_logits(c, MODE_LSE_P, 0, chunk_rows(c, 0), 0, nullptr, nullptr, c.Gb[0]));
+        LCE_TRY(run_prep(c, 0, chunk_rows(c, 0), lse, dloss, rows_out, c.Gb[0], true));
+        for (long long k = 1; k <= c.L.nchunks; ++k) {
+            const long long p0 = (k - 1) * c.L.C, prow = chunk_rows(c, k - 1);
+            const bool more = k < c.L.nchunks;
+            Mix mx{MODE_MIX_P, k * c.L.C, more ? chunk_rows(c, k) : 0, static_cast<int>(2 * k),
+                   c.Gb[k & 1], nullptr};
+            LCE_TRY(run_grad(c, p0, prow, static_cast<int>(2 * k - 1), dHb + p0 * c.D, acc_dh, dW,
+                             k > 1 || acc_dw0, dloss, c.Gb[(k - 1) & 1], true,
+                             more ? &mx : nullptr));
+            if (more)
+                LCE_TRY(run_prep(c, k * c.L.C, chunk_rows(c, k), lse, dloss, rows_out, c.Gb[k & 1],
+                                 true));
+        }
+    } else {
+        for (long long k = 0; k < c.L.nchunks; ++k) {
+            const long long row0 = k * c.L.C;
+            const long long rows = chunk_rows(c, k);
+            LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr,
+                               c.Gb[0]));
+            LCE_TRY(run_prep(c, row0, rows, lse, dloss, rows_out, c.Gb[0], !frozen));
+            LCE_TRY(run_grad(c, row0, rows, static_cast<int>(2 * k + 1), dHb + row0 * c.D, acc_dh,
+                             dW, k > 0 || acc_dw0, dloss, c.Gb[0], true));
+        }
     }
     if (!none)
         LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss,
                                         reduction == LCE_REDUCTION_MEAN, c.s));
     return LCE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lce_status lce_fwd_bwd_opt(const void *H, const void *W, const int64_t *y, const float *dloss,
+                           int64_t N, int64_t D, int64_t V, int64_t ignore_index, int64_t chunk,
+                           int reduction, int flags, float *loss, float *lse, void *dH, float *dW,
+                           void *ws, size_t ws_bytes, lce_stream_t stream) {
+    return fwd_bwd_impl(H, W, y, dloss, N, D, V, ignore_index, chunk, reduction, flags, loss, lse,
+                        dH, dW, ws, ws_bytes, stream, nullptr);
+}
+
+lce_status lce_fwd_bwd_sharded(const void *H, const void *W, const int64_t *y, const float *dloss,
+                               const int64_t *n_valid_total, int64_t N, int64_t D, int64_t V,
+                               int64_t ignore_index, int64_t chunk, int flags, float *loss,
+                               float *lse, void *dH, float *dW, void *ws, size_t ws_bytes,
+                               lce_stream_t stream) {
+    g_launches = 0;
+    if (!n_valid_total) return LCE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(n_valid_total) & 7u) return LCE_ERR_ALIGNMENT;
+    return fwd_bwd_impl(H, W, y, dloss, N, D, V, ignore_index, chunk, LCE_REDUCTION_MEAN, flags,
+                        loss, lse, dH, dW, ws, ws_bytes, stream, n_valid_total);
 }
 
 lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const float *dloss,
@@ -903,8 +1095,9 @@ lce_status lce_norm_fwd_bwd_opt(const void *X, const void *gamma, float eps, con
     float *dHbuf = reinterpret_cast<float *>(w + NL.off_dH);
     float *part = reinterpret_cast<float *>(w + NL.off_part);
     Ctx c;
+    // one chunk buffer: the chunks of this path run one after the other
     LCE_TRY(setup(c, Hbuf, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, true, false,
-                  frozen));
+                  frozen, false, true));
     c.reduction = reduction;
     float *rows_out = none ? loss : c.loss_rows;
     if (c.L.nchunks == 0) {
@@ -927,12 +1120,13 @@ lce_status lce_norm_fwd_bwd_opt(const void *X, const void *gamma, float eps, con
         np.D = static_cast<int>(c.D);
         np.eps = eps;
         LCE_LAUNCH_KIND(LCE_KERNEL_NORM, c.s, launch_rmsnorm_fwd(np, c.s));
-        LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr));
-        LCE_TRY(run_merge(c, true, row0, rows, lse, dloss, rows_out));
-        LCE_TRY(run_fixup(c, row0, rows, dloss));
+        LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr,
+                           c.Gb[0]));
+        LCE_TRY(run_prep(c, row0, rows, lse, dloss, rows_out, c.Gb[0], !frozen));
         int parts = 1;
         LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1),
-                        DhOut{dHbuf, true, dh_parts(c, rows), c.L.ldp}, dW, k > 0, dloss, &parts));
+                        DhOut{dHbuf, true, dh_parts(c, rows), c.L.ldp}, dW, k > 0, dloss, c.Gb[0],
+                        true, nullptr, &parts));
         np.H = nullptr;
         np.dH = dHbuf;
         np.dh_fp32 = 1;

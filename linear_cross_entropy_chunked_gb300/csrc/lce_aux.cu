@@ -72,38 +72,64 @@ __global__ void __launch_bounds__(1024) lce_label_scan_kernel(const long long *_
     }
 }
 
+// Count of rows with a label in [0, V) (the same rule as the scan above), written
+// as an int64 to *out. One CTA: no atomics, no zeroing, a fixed summation order.
+__global__ void __launch_bounds__(1024) lce_count_valid_kernel(const long long *__restrict__ y,
+                                                               long long N, long long V,
+                                                               long long ign, long long *out) {
+    __shared__ long long s_cnt[32];
+    long long cnt = 0;
+    for (long long i = threadIdx.x; i < N; i += 1024) {
+        const long long v = y[i];
+        if (v != ign && v >= 0 && v < V) ++cnt;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) s_cnt[w] = cnt;
+    __syncthreads();
+    if (w == 0) {
+        cnt = s_cnt[l];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        if (l == 0) *out = cnt;
+    }
+}
+
+// The normaliser of the mean taken from the caller (the valid rows of every
+// shard of a batch) instead of this call's own count; counts beyond the int32
+// header word are clamped (the caller's API rejects them before this point).
+__global__ void lce_set_nvalid_kernel(const long long *__restrict__ n_total, int *hdr) {
+    const long long n = *n_total;
+    hdr[HDR_NVALID] = n < 0 ? 0 : (n > 0x7fffffffll ? 0x7fffffff : static_cast<int>(n));
+}
+
 // ------------------------------------------------------------------ merge
 
 constexpr int MERGE_THREADS = 256;
 
-// One CTA per chunk row: lse_i from the slab partials, the row's loss, and
-// (FACTORS) each slab's rescale factor exp(m_p - lse_i) * dloss / N_valid,
-// written over the slab max so the fix-up pass reads one float per slab.
-template <bool FACTORS>
-__global__ void __launch_bounds__(MERGE_THREADS) lce_merge_kernel(const MergeParams p) {
-    __shared__ float s_red[MERGE_THREADS / 32];
-    __shared__ float s_bcast;
-    const int r = blockIdx.x;          // row within the chunk
+// lse of one chunk row from its (max, sumexp) slab partials, by a CTA of
+// MERGE_THREADS threads: M = the maximum of the slab maxima, lse = M + log sum_p
+// s_p exp(m_p - M). The order of every sum is fixed, so each CTA that computes a
+// row's lse gets the same bits. Returns it in every thread.
+__device__ __forceinline__ float row_lse(const float2 *parts, int nparts, float *s_red,
+                                         float *s_bcast) {
     const int t = threadIdx.x, w = t >> 5, l = t & 31;
-    float2 *parts = const_cast<float2 *>(p.parts) + static_cast<size_t>(r) * p.nparts;
-
-    // row maximum over the slab maxima
     float m = -INFINITY;
-    for (int i = t; i < p.nparts; i += MERGE_THREADS) m = fmaxf(m, parts[i].x);
+    for (int i = t; i < nparts; i += MERGE_THREADS) m = fmaxf(m, parts[i].x);
     m = warp_max(m);
     if (l == 0) s_red[w] = m;
     __syncthreads();
     if (w == 0) {
         m = (l < MERGE_THREADS / 32) ? s_red[l] : -INFINITY;
         m = warp_max(m);
-        if (l == 0) s_bcast = m;
+        if (l == 0) *s_bcast = m;
     }
     __syncthreads();
-    const float M = s_bcast;
+    const float M = *s_bcast;
     const float M2 = M * LOG2E_F;
-    // rescaled sum of the slab sums
     float s = 0.f;
-    for (int i = t; i < p.nparts; i += MERGE_THREADS) {
+    for (int i = t; i < nparts; i += MERGE_THREADS) {
         const float2 q = parts[i];
         s += q.y * exp2f(fmaf(q.x, LOG2E_F, -M2));
     }
@@ -114,10 +140,23 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_merge_kernel(const MergePar
     if (w == 0) {
         s = (l < MERGE_THREADS / 32) ? s_red[l] : 0.f;
         s = warp_sum(s);
-        if (l == 0) s_bcast = M + logf(s);
+        if (l == 0) *s_bcast = M + logf(s);
     }
     __syncthreads();
-    const float lse = s_bcast;
+    return *s_bcast;
+}
+
+// One CTA per chunk row: lse_i from the slab partials, the row's loss, and
+// (FACTORS) each slab's rescale factor exp(m_p - lse_i) * dloss / N_valid,
+// written over the slab max so the fix-up pass reads one float per slab.
+template <bool FACTORS>
+__global__ void __launch_bounds__(MERGE_THREADS) lce_merge_kernel(const MergeParams p) {
+    __shared__ float s_red[MERGE_THREADS / 32];
+    __shared__ float s_bcast;
+    const int r = blockIdx.x;          // row within the chunk
+    const int t = threadIdx.x;
+    float2 *parts = const_cast<float2 *>(p.parts) + static_cast<size_t>(r) * p.nparts;
+    const float lse = row_lse(parts, p.nparts, s_red, &s_bcast);
 
     const int grow = p.row0 + r;
     const long long yv = p.y[grow];
@@ -224,6 +263,120 @@ __global__ void __launch_bounds__(256) lce_transpose_kernel(const TransposeParam
     }
 }
 
+// ------------------------------------------------------------------ prep
+// Everything between a chunk's logits GEMM and its gradient GEMMs on the fused
+// path in one launch. CTAs [0, rows * segs): row r = b / segs, segment b % segs
+// of PREP_VEC_PER_CTA 8-column vectors: the row's lse from its slab partials
+// (row_lse, the merge's arithmetic), then P' = exp(z - m_p) -> G = P' * exp(m_p -
+// lse) * s - 1[j = y] * s in place, s the stored-G row scale (the fix-up's
+// arithmetic, with the slab factor formed where it is used instead of stored);
+// segment 0 writes lse and the row loss. The CTAs after those transpose 64 x 64
+// tiles of the H chunk (lce_transpose_kernel's arithmetic) for the dW contraction.
+static_assert(PREP_THREADS == MERGE_THREADS, "the prep kernel computes lse as the merge does");
+
+__device__ __forceinline__ void transpose_tile(const TransposeParams &p, int c0, int r0,
+                                               __nv_bfloat16 *tile) {
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int k = tid + 256 * i;
+        const int rr = k >> 3, cb = (k & 7) * 8;
+        const int r = r0 + rr, c = c0 + cb;
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (r < p.rows && c < p.cols)
+            u = *reinterpret_cast<const uint4 *>(p.src + static_cast<size_t>(r) * p.ld_src + c);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(tile + rr * TSTRIDE + cb);
+        dst[0] = u.x;
+        dst[1] = u.y;
+        dst[2] = u.z;
+        dst[3] = u.w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int k = tid + 256 * i;
+        const int cc = k >> 3, rb = (k & 7) * 8;
+        const int c = c0 + cc, r = r0 + rb;
+        if (c < p.cols && r < p.rows) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t lo = reinterpret_cast<const uint16_t &>(tile[(rb + 2 * q) * TSTRIDE + cc]);
+                const uint32_t hi =
+                    reinterpret_cast<const uint16_t &>(tile[(rb + 2 * q + 1) * TSTRIDE + cc]);
+                w[q] = lo | (hi << 16);
+            }
+            *reinterpret_cast<uint4 *>(p.dst_t + static_cast<size_t>(c) * p.ld_t + r) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(MERGE_THREADS) lce_prep_kernel(const PrepParams p) {
+    __shared__ float s_red[MERGE_THREADS / 32];
+    __shared__ float s_bcast;
+    __shared__ __align__(16) __nv_bfloat16 tile[TT * TSTRIDE];
+    const MergeParams &m = p.m;
+    const long long nrow_ctas = static_cast<long long>(m.rows) * p.segs;
+    if (blockIdx.x >= nrow_ctas) {
+        const int b = static_cast<int>(blockIdx.x - nrow_ctas);
+        transpose_tile(p.tp, (b % p.tt_x) * TT, (b / p.tt_x) * TT, tile);
+        return;
+    }
+    const int r = static_cast<int>(blockIdx.x / p.segs);
+    const int seg = static_cast<int>(blockIdx.x % p.segs);
+    const float2 *parts = m.parts + static_cast<size_t>(r) * m.nparts;
+    const float lse = row_lse(parts, m.nparts, s_red, &s_bcast);
+    const int grow = m.row0 + r;
+    const long long yv = m.y[grow];
+    const bool y_ok = yv != m.ignore_index && yv >= 0 && yv < m.V;
+    if (seg == 0 && threadIdx.x == 0) {
+        m.lse[grow] = lse;
+        m.loss_rows[grow] = y_ok ? lse - m.zy[r] : 0.f;
+    }
+    const float scale = lce_store_scale(m.dloss, m.dloss_per_row, m.mean, m.hdr[HDR_NVALID], grow,
+                                        y_ok, m.f16);
+    const float lse2 = lse * LOG2E_F;
+    const int ycol = y_ok ? static_cast<int>(yv) : -1;
+    const int nvec = (m.V + 7) >> 3;
+    const int v0 = seg * PREP_VEC_PER_CTA + threadIdx.x;
+    uint4 *row = reinterpret_cast<uint4 *>(m.G + static_cast<size_t>(r) * p.ldg);
+    uint4 u[PREP_VPT];
+#pragma unroll
+    for (int i = 0; i < PREP_VPT; ++i) {
+        const int v = v0 + i * MERGE_THREADS;
+        if (v < nvec) u[i] = row[v];
+    }
+#pragma unroll
+    for (int i = 0; i < PREP_VPT; ++i) {
+        const int v = v0 + i * MERGE_THREADS;
+        if (v >= nvec) continue;
+        const int c = v * 8;
+        const float f = scale != 0.f
+                            ? exp2f(fmaf(parts[c >> 7].x, LOG2E_F, -lse2)) * scale
+                            : 0.f;
+        uint32_t *wv = reinterpret_cast<uint32_t *>(&u[i]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float2 x;
+            if (m.f16) x = __half22float2(*reinterpret_cast<__half2 *>(&wv[q]));
+            else x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&wv[q]));
+            x.x *= f;
+            x.y *= f;
+            if (c + 2 * q == ycol) x.x -= scale;
+            if (c + 2 * q + 1 == ycol) x.y -= scale;
+            if (m.f16) {
+                __half2 h = __floats2half2_rn(x.x, x.y);
+                wv[q] = *reinterpret_cast<uint32_t *>(&h);
+            } else {
+                __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
+                wv[q] = *reinterpret_cast<uint32_t *>(&h);
+            }
+        }
+        row[v] = u[i];
+    }
+}
+
 // ------------------------------------------------------------------ loss
 
 __global__ void __launch_bounds__(1024) lce_loss_finalize_kernel(const float *__restrict__ loss_rows,
@@ -319,6 +472,17 @@ cudaError_t launch_label_scan(const long long *y, long long N, long long V, long
     return cudaGetLastError();
 }
 
+cudaError_t launch_count_valid(const long long *y, long long N, long long V, long long ign,
+                               long long *out, cudaStream_t s) {
+    lce_count_valid_kernel<<<1, 1024, 0, s>>>(y, N, V, ign, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_set_nvalid(const long long *n_total, int *hdr, cudaStream_t s) {
+    lce_set_nvalid_kernel<<<1, 1, 0, s>>>(n_total, hdr);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_merge(bool factors, const MergeParams &p, cudaStream_t s) {
     if (p.rows <= 0) return cudaSuccess;
     if (factors) lce_merge_kernel<true><<<p.rows, MERGE_THREADS, 0, s>>>(p);
@@ -338,6 +502,17 @@ cudaError_t launch_fixup(const FixupParams &p, cudaStream_t s) {
     const int nvec = (p.V + 7) / 8;
     const dim3 grid((nvec + 255) / 256, p.rows < 65535 ? p.rows : 65535);
     lce_fixup_kernel<<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const PrepParams &p, cudaStream_t s) {
+    const long long row_ctas = static_cast<long long>(p.m.rows) * p.segs;
+    const long long tt = p.tp.rows > 0 ? static_cast<long long>(p.tt_x) * ((p.tp.rows + TT - 1) / TT)
+                                       : 0;
+    const long long grid = row_ctas + tt;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffll) return cudaErrorInvalidValue;
+    lce_prep_kernel<<<static_cast<unsigned>(grid), MERGE_THREADS, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -64,7 +64,13 @@ enum GemmMode : int {
     MODE_LSE_P = 1,   // ... + store P' = exp(z - max_part) as bf16 into the chunk buffer
     MODE_G = 2,       // logits tiles -> G = (exp(z - lse) - onehot) * scale as bf16 (given lse)
     MODE_BWD = 3,     // dH tiles (G W) followed by dW tiles (G^T H) in one persistent launch
-    MODE_DH = 4       // dH tiles only, 256 rows x 512 columns per CTA pair (CTA pairs only)
+    MODE_DH = 4,      // dH tiles only, 256 rows x 512 columns per CTA pair (CTA pairs only)
+    // Two chunks in one launch (CTA pairs only): the logits tiles of chunk k (with
+    // the MODE_LSE_P or the MODE_G epilogue) interleaved with the dW tiles of chunk
+    // k - 1, so that the dW tiles' HBM-bound read-modify-write of dW overlaps the
+    // tensor-bound logits work on the same SMs.
+    MODE_MIX_P = 5,
+    MODE_MIX_G = 6
 };
 
 // Scale of row i of G: dloss (a scalar, or row i of a per-row vector) divided
@@ -191,6 +197,23 @@ struct FixupParams {
     int f16;                    // fp16 P' / G (scale from lce_store_scale)
 };
 
+// The step between a chunk's logits GEMM and its gradient GEMMs on the fused
+// path, one launch: for each row, lse from the slab partials, the row's loss,
+// and P' -> G in place (each of `segs` CTAs of a row recomputes the row's lse
+// from the partials, in the same order, and rescales its own segment of the
+// row); then, in the CTAs after those, the H chunk transposed for the dW
+// contraction (tp.rows == 0: no transpose).
+constexpr int PREP_THREADS = 256;
+constexpr int PREP_VPT = 8;                                  // 8-column vectors per thread
+constexpr int PREP_VEC_PER_CTA = PREP_THREADS * PREP_VPT;    // 2048 vectors = 16384 columns
+struct PrepParams {
+    MergeParams m;              // parts, zy, y, hdr, dloss, scales, lse, loss_rows
+    int ldg;
+    int segs;                   // CTAs per row
+    TransposeParams tp;
+    int tt_x;                   // transpose tiles along D (64 columns each)
+};
+
 // Cross-entropy over precomputed logits Z [N][ld] (bf16 or fp32), one row at a time.
 enum : int { CE_BF16 = 0, CE_FP32 = 1, CE_FP16 = 2 };   // logits dtype codes of lce_ce_logits
 
@@ -240,9 +263,15 @@ cudaError_t launch_gemm(int mode, int cluster, const GemmParams &p, int grid, cu
 cudaError_t gemm_max_pairs(int *pairs);
 cudaError_t launch_label_scan(const long long *y, long long N, long long V, long long ign,
                               int *hdr, cudaStream_t s);
+// *out (device int64) = number of labels in [0, V) that are not ign
+cudaError_t launch_count_valid(const long long *y, long long N, long long V, long long ign,
+                               long long *out, cudaStream_t s);
+// hdr[HDR_NVALID] = *n_total (device int64), for a mean over several shards' rows
+cudaError_t launch_set_nvalid(const long long *n_total, int *hdr, cudaStream_t s);
 cudaError_t launch_merge(bool factors, const MergeParams &p, cudaStream_t s);
 cudaError_t launch_transpose(const TransposeParams &p, cudaStream_t s);
 cudaError_t launch_fixup(const FixupParams &p, cudaStream_t s);
+cudaError_t launch_prep(const PrepParams &p, cudaStream_t s);
 cudaError_t launch_loss_finalize(const float *loss_rows, long long N, const int *hdr,
                                  float *loss, int mean, cudaStream_t s);
 cudaError_t launch_ce_logits(const CELogitsParams &p, int sms, cudaStream_t s);

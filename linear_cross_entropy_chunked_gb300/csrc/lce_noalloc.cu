@@ -11,14 +11,21 @@
 // Cost and limits:
 //  * the array is kNoAllocScratchBytes (64 MiB) and is held on every GPU that
 //    loads this library until the process exits;
-//  * problems whose lce_workspace_size() exceeds it are rejected with
-//    LCE_ERR_WORKSPACE before anything is enqueued;
+//  * problems whose forward workspace (lce_forward_workspace_size(): the header,
+//    the per-row losses, the chunk's target logits and its (max, sum) slab
+//    partials) exceeds it are rejected with LCE_ERR_WORKSPACE before anything is
+//    enqueued;
 //  * all calls share the array, and it keeps the last call's contents. The
 //    forward clears what must start at zero (the header with the tile counters
 //    and the valid-row count) on the stream before its kernels run, so stale
 //    contents do no harm to calls that are ordered one after the other. Calls
 //    that overlap on the GPU (on different streams or devices sharing nothing
-//    but this array on one device) race on it and give wrong results.
+//    but this array on one device) race on it and give wrong results;
+//  * the array's device address is looked up once per device; a reset of the
+//    device (cudaDeviceReset) unloads the library's module and invalidates it,
+//    so the entry point is not for use across such a reset in one process;
+//  * device-side status (labels out of range, a bounded wait that ran out) is
+//    recorded in the array's header and read by lce_noalloc_read_status().
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -58,7 +65,7 @@ extern "C" lce_status lce_forward_noalloc(const void *H, const void *W, const in
                                           int64_t chunk, float *loss, float *lse,
                                           lce_stream_t stream) {
     size_t need = 0;
-    lce_status st = lce_workspace_size(N, D, V, chunk, &need);
+    lce_status st = lce_forward_workspace_size(N, D, V, chunk, &need);
     if (st != LCE_OK) return st;
     if (need > kNoAllocScratchBytes) return LCE_ERR_WORKSPACE;
     void *ws = nullptr;
@@ -66,4 +73,11 @@ extern "C" lce_status lce_forward_noalloc(const void *H, const void *W, const in
     if (st != LCE_OK) return st;
     return lce_forward(H, W, y, N, D, V, ignore_index, chunk, loss, lse, ws, kNoAllocScratchBytes,
                        stream);
+}
+
+extern "C" lce_status lce_noalloc_read_status(lce_stream_t stream) {
+    void *ws = nullptr;
+    lce_status st = scratch_address(&ws);
+    if (st != LCE_OK) return st;
+    return lce_read_status(ws, stream);
 }

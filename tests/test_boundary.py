@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_binding_lists_every_declared_symbol():
     import linear_cross_entropy_chunked_gb300 as pkg
-    names = set(declared_functions()) - {"lce_forward_noalloc"}
+    names = set(declared_functions())
     assert names <= set(pkg.EXPORTED), names - set(pkg.EXPORTED)
 
 
@@ -60,17 +60,22 @@ def test_workspace_size_is_order_chunk_times_V(L):
     assert st == OK
     st, b2 = ws_size(L, 16384, 4096, 128256, 2048)
     assert st == OK
-    # the bf16 chunk buffer (P', then G) dominates: ~2 bytes per chunk row per vocab id;
-    # next come the chunk's H^T (bf16) and, at chunk 1024, the two fp32 dH partial
-    # arrays of the vocabulary-split dH tiles (none at chunk 2048: enough tiles)
-    assert 2 * 1024 * 128256 <= b1 <= 2 * 1024 * 128256 * 1.2
+    # the two bf16 chunk buffers (P', then G; the next chunk's logits fill one while
+    # the previous chunk's gradients read the other) dominate: ~4 bytes per chunk row
+    # per vocab id; next come the chunk's H^T (bf16) and the (max, sum) partials
+    assert 2 * 2 * 1024 * 128256 <= b1 <= 2 * 2 * 1024 * 128256 * 1.1
     assert 1.7 < b2 / b1 < 2.05
+    # LCE_LOW_MEMORY keeps one chunk buffer: about half
+    low = ctypes.c_size_t(0)
+    assert L.lce_workspace_size_opt(16384, 4096, 128256, 1024, 16, ctypes.byref(low)) == OK
+    assert 2 * 1024 * 128256 <= low.value <= 2 * 1024 * 128256 * 1.2
+    assert b1 - low.value == 2 * 1024 * (-(-128256 // 256) * 256)   # one [chunk][ldg] bf16 buffer
     # it does not grow with N beyond O(N) bytes
     st, b3 = ws_size(L, 4 * 16384, 4096, 128256, 1024)
     assert b3 - b1 < 64 * 16384 * 4
     # far below the full logit tensor the fused loss avoids (N*V*2 bytes in bf16):
-    # the chunk buffer is chunk/N of it
-    assert b1 < 0.075 * 16384 * 128256 * 2
+    # each chunk buffer is chunk/N of it
+    assert b1 < 0.14 * 16384 * 128256 * 2
 
 
 @pytest.mark.parametrize("N,D,V,chunk", [(-1, 64, 100, 64), (8, 0, 100, 64), (8, 12, 100, 64),
@@ -105,8 +110,10 @@ def test_forward_argument_errors_return_before_launch(L):
     assert fwd(L, H=FAKE + 2) == ALIGN
     assert fwd(L, ws=FAKE + 8) == ALIGN
     assert fwd(L, lse=FAKE + 4) == ALIGN
-    need = ws_size(L, 128, 64, 1000, 64)[1]
-    assert fwd(L, ws_bytes=need - 1) == WORKSPACE
+    # the forward needs only its own share of the workspace (no chunk buffer)
+    need = ctypes.c_size_t(0)
+    assert L.lce_forward_workspace_size(128, 64, 1000, 64, ctypes.byref(need)) == OK
+    assert fwd(L, ws_bytes=need.value - 1) == WORKSPACE
 
 
 def test_backward_and_fused_argument_errors(L):
@@ -159,16 +166,23 @@ def test_binding_refuses_cpu_tensors():
 
 # ---------------------------------------------------------------- final RMSNorm
 
+def ws_size_low(L, N, D, V, chunk):
+    out = ctypes.c_size_t(0)
+    assert L.lce_workspace_size_opt(N, D, V, chunk, 16, ctypes.byref(out)) == OK   # LCE_LOW_MEMORY
+    return out.value
+
+
 def test_norm_workspace_sizes(L):
+    # the RMSNorm path runs its chunks one after the other: one chunk buffer
     N, D, V, chunk = 16384, 4096, 128256, 1024
-    base = ws_size(L, N, D, V, chunk)[1]
+    base = ws_size_low(L, N, D, V, chunk)
     out = ctypes.c_size_t(0)
     assert L.lce_norm_workspace_size(N, D, V, chunk, ctypes.byref(out)) == OK
     # the loss path's workspace + the chunk's dH (fp32) and H (bf16) + 256 dgamma
     # partial rows
     assert out.value == base + 4 * chunk * D + 2 * chunk * D + 4 * 256 * D
     # two vocabulary parts (chunk 512): the loss path's partial arrays hold dH
-    base2 = ws_size(L, N, D, V, 512)[1]
+    base2 = ws_size_low(L, N, D, V, 512)
     assert L.lce_norm_workspace_size(N, D, V, 512, ctypes.byref(out)) == OK
     assert out.value == base2 + 2 * 512 * D + 4 * 256 * D
     assert L.lce_norm_workspace_size(N, 8200, V, chunk, ctypes.byref(out)) == INVALID  # D > 8192
@@ -224,14 +238,14 @@ def test_accumulate_workspace_and_flags(L):
     base2 = ws_size(L, N, D, V, 512)[1]        # two vocabulary parts: their arrays serve
     assert L.lce_workspace_size_opt(N, D, V, 512, 2, ctypes.byref(out)) == OK
     assert out.value == base2
-    assert L.lce_workspace_size_opt(N, D, V, chunk, 16, ctypes.byref(out)) == INVALID
+    assert L.lce_workspace_size_opt(N, D, V, chunk, 32, ctypes.byref(out)) == INVALID   # unknown flag
     vp = ctypes.c_void_p
     # dH accumulation with only the plain workspace: refused before anything runs
     assert L.lce_fwd_bwd_opt(vp(FAKE), vp(FAKE), vp(FAKE), None, 128, 64, 1000, -100, 64, 0, 2,
                              vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
                              ws_size(L, 128, 64, 1000, 64)[1], None) == WORKSPACE
     assert L.lce_backward_opt(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), vp(FAKE), 128,
-                              64, 1000, -100, 64, 0, 16, vp(FAKE), 1 << 30, None) == INVALID
+                              64, 1000, -100, 64, 0, 32, vp(FAKE), 1 << 30, None) == INVALID
     # fp16 inputs with per-row losses: refused
     UNSUPPORTED = 7
     assert L.lce_fwd_bwd_opt(vp(FAKE), vp(FAKE), vp(FAKE), None, 128, 64, 1000, -100, 64, 2, 4,
@@ -266,28 +280,29 @@ def test_dh_vocabulary_split_workspace(L):
     """The dH tiles of a chunk (256 rows x 512 columns each) are split along the
     vocabulary until there are at least 28 of them, in at most 4 parts, for
     vocabularies of at least 8192; each part needs one fp32 [chunk rows rounded up
-    to 128] x D array in the workspace."""
+    to 128] x D array in the workspace. (Sizes with one chunk buffer,
+    LCE_LOW_MEMORY: the parts are the same either way.)"""
     N, D, chunk = 4096, 1024, 1024
-    small = ws_size(L, N, D, 8191, chunk)[1]
-    big = ws_size(L, N, D, 8192, chunk)[1]     # same G row stride (both round to 8192)
+    small = ws_size_low(L, N, D, 8191, chunk)
+    big = ws_size_low(L, N, D, 8192, chunk)     # same G row stride (both round to 8192)
     # 4 row pairs x 2 column blocks = 8 tiles -> 4 parts
     assert big - small == 4 * 4 * 1024 * D
     # 1000 rows round up to 1024 per part; 4 x 2 tiles again
-    assert ws_size(L, N, D, 8192, 1000)[1] - ws_size(L, N, D, 8191, 1000)[1] == 4 * 4 * 1024 * D
+    assert ws_size_low(L, N, D, 8192, 1000) - ws_size_low(L, N, D, 8191, 1000) == 4 * 4 * 1024 * D
     stats = lambda c, V: 8 * c * (-(-V // 128))     # per-row (max, sum) of each 128-column slab
     # Llama-3-8B head: at chunk 512, 2 x 8 = 16 tiles -> 2 parts; at chunk 1024,
     # 4 x 8 = 32 tiles -> one part, no partial arrays
-    b0 = ws_size(L, 16384, 4096, 128256, 512)[1]
+    b0 = ws_size_low(L, 16384, 4096, 128256, 512)
     g0 = 2 * 512 * 128256 + 2 * 4096 * 512          # G (bf16) and H^T (bf16)
     assert b0 - g0 >= 2 * 4 * 512 * 4096 + stats(512, 128256)
     assert b0 - g0 < 2 * 4 * 512 * 4096 + stats(512, 128256) + (1 << 20)
-    b1 = ws_size(L, 16384, 4096, 128256, 1024)[1]
+    b1 = ws_size_low(L, 16384, 4096, 128256, 1024)
     assert b1 - (2 * 1024 * 128256 + 2 * 4096 * 1024) < stats(1024, 128256) + (1 << 20)
     # Qwen-2.5-7B head (D 3584: 7 column blocks): chunk 1024 -> 28 tiles, one part;
     # chunk 512 -> 14 tiles, 2 parts
-    q1 = ws_size(L, 16384, 3584, 152064, 1024)[1]
+    q1 = ws_size_low(L, 16384, 3584, 152064, 1024)
     assert q1 - (2 * 1024 * 152064 + 2 * 3584 * 1024) < stats(1024, 152064) + (1 << 20)
-    q0 = ws_size(L, 16384, 3584, 152064, 512)[1]
+    q0 = ws_size_low(L, 16384, 3584, 152064, 512)
     assert q0 - (2 * 512 * 152064 + 2 * 3584 * 512) >= 2 * 4 * 512 * 3584
 
 
@@ -297,7 +312,7 @@ def test_frozen_w_flag(L):
     a Llama-3 chunk -> 2 vocabulary parts); dW may be NULL; it does not combine
     with accumulating into dW."""
     N, D, V, chunk = 16384, 4096, 128256, 1024
-    base = ws_size(L, N, D, V, chunk)[1]
+    base = ws_size_low(L, N, D, V, chunk)    # frozen W keeps one chunk buffer
     out = ctypes.c_size_t(0)
     assert L.lce_workspace_size_opt(N, D, V, chunk, 8, ctypes.byref(out)) == OK
     assert out.value == base - 2 * D * chunk + 2 * 4 * chunk * D
@@ -338,7 +353,7 @@ def test_norm_opt_flags(L):
         assert L.lce_norm_workspace_size_opt(N, D, V, chunk, bad, ctypes.byref(out)) == INVALID
     assert L.lce_norm_workspace_size_opt(N, D, V, chunk, 8, ctypes.byref(out)) == OK
     # frozen W: no H chunk^T; the two dH parts of the frozen split hold the chunk's dH
-    assert out.value == (ws_size(L, N, D, V, chunk)[1] - 2 * D * chunk + 2 * 4 * chunk * D
+    assert out.value == (ws_size_low(L, N, D, V, chunk) - 2 * D * chunk + 2 * 4 * chunk * D
                          + 2 * chunk * D + 4 * 256 * D)
     vp = ctypes.c_void_p
     n, d, v, c = 128, 64, 1000, 64
@@ -353,6 +368,11 @@ def test_norm_opt_flags(L):
     assert call(1, vp(FAKE)) == INVALID             # accumulation flags are not taken here
     assert call(8, vp(FAKE + 4)) == ALIGN           # a given dW is still checked
     assert call(8, None) not in (OK, INVALID, ALIGN, WORKSPACE)   # argument checks pass
+    # without flags, the size lce_norm_workspace_size gives passes the checks too
+    assert L.lce_norm_workspace_size(n, d, v, c, ctypes.byref(out)) == OK
+    assert L.lce_norm_fwd_bwd_opt(vp(FAKE), vp(FAKE), 1e-6, vp(FAKE), vp(FAKE), None, n, d, v,
+                                  -100, c, 0, 0, vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                  vp(FAKE), out.value, None) not in (OK, INVALID, ALIGN, WORKSPACE)
 
 
 def test_binding_constants_match_the_header():
@@ -369,7 +389,9 @@ def test_binding_constants_match_the_header():
     assert consts["LCE_ACCUMULATE_DH"] == B.ACCUMULATE["dH"]
     assert consts["LCE_INPUT_FP16"] == B.INPUT_FP16
     assert consts["LCE_FROZEN_W"] == B.FROZEN_W
-    assert consts["LCE_FLAGS_ALL"] == B.ACCUMULATE["dW"] | B.ACCUMULATE["dH"] | B.INPUT_FP16 | B.FROZEN_W
+    assert consts["LCE_LOW_MEMORY"] == B.LOW_MEMORY
+    assert consts["LCE_FLAGS_ALL"] == (B.ACCUMULATE["dW"] | B.ACCUMULATE["dH"] | B.INPUT_FP16 |
+                                       B.FROZEN_W | B.LOW_MEMORY)
     for name, v in B.KERNEL_KINDS.items():
         assert consts[f"LCE_KERNEL_{name.upper()}"] == v
     assert consts["LCE_KERNEL_KINDS"] == len(B.KERNEL_KINDS)
@@ -398,15 +420,55 @@ def test_binding_flag_logic_on_the_host():
         B._reduction("avg")
 
 
-def test_count_valid_matches_the_library_reading():
-    """Rows count as valid when the label lies in [0, V) and is not ignore_index
-    (out-of-range labels are treated as ignored, as the kernels do)."""
+def test_count_valid_refuses_host_tensors():
+    """The valid-row count runs in the library (lce_count_valid): a host tensor is
+    refused before the library is touched."""
     import torch
-    from linear_cross_entropy_chunked_gb300.sharded import count_valid
-    y = torch.tensor([0, 5, -100, 9, 10, -3, 4])
-    assert count_valid(y, 10).item() == 4
-    assert count_valid(y, 11).item() == 5
-    assert count_valid(torch.zeros(0, dtype=torch.int64), 10).item() == 0
+    from linear_cross_entropy_chunked_gb300 import count_valid
+    with pytest.raises(ValueError):
+        count_valid(torch.tensor([0, 5, -100]), 10)
+
+
+def test_count_and_sharded_argument_errors(L):
+    """lce_count_valid and lce_fwd_bwd_sharded reject bad arguments before any
+    launch (fake device pointers, never dereferenced)."""
+    fake = ctypes.c_void_p(1 << 20)
+    out = ctypes.c_void_p(1 << 21)
+    assert L.lce_count_valid(fake, -1, 10, -100, out, None) == INVALID
+    assert L.lce_count_valid(fake, 4, 0, -100, out, None) == INVALID
+    assert L.lce_count_valid(fake, 4, 10, -100, None, None) == INVALID
+    assert L.lce_count_valid(ctypes.c_void_p((1 << 20) + 8), 4, 10, -100, out, None) == ALIGN
+    assert L.lce_count_valid(fake, 4, 10, -100, ctypes.c_void_p((1 << 21) + 4), None) == ALIGN
+    p = [ctypes.c_void_p((1 << 20) + 4096 * i) for i in range(10)]
+    # no n_valid_total
+    assert L.lce_fwd_bwd_sharded(p[0], p[1], p[2], None, None, 8, 64, 100, -100, 64, 0, p[3], p[4],
+                                 p[5], p[6], p[7], 1 << 30, None) == INVALID
+    # n_valid_total not 8-byte aligned
+    assert L.lce_fwd_bwd_sharded(p[0], p[1], p[2], None, ctypes.c_void_p((1 << 20) + 3), 8, 64,
+                                 100, -100, 64, 0, p[3], p[4], p[5], p[6], p[7], 1 << 30,
+                                 None) == ALIGN
+    # workspace too small
+    assert L.lce_fwd_bwd_sharded(p[0], p[1], p[2], None, p[8], 8, 64, 100, -100, 64, 0, p[3], p[4],
+                                 p[5], p[6], p[7], 16, None) == WORKSPACE
+
+
+def test_forward_workspace_is_the_forward_share(L):
+    """lce_forward needs no chunk buffer: its workspace is the header, the row
+    losses, the chunk's target logits and slab partials, far below the full size."""
+    for N, D, V, chunk in ((16384, 4096, 128256, 1024), (4096, 4096, 32000, 1024),
+                           (77, 128, 100, 1024), (0, 64, 300, 128)):
+        full = ctypes.c_size_t(0)
+        fwd = ctypes.c_size_t(0)
+        assert L.lce_workspace_size(N, D, V, chunk, ctypes.byref(full)) == OK
+        assert L.lce_forward_workspace_size(N, D, V, chunk, ctypes.byref(fwd)) == OK
+        C = min(chunk, max(N, 1))
+        parts = C * ((V + 127) // 128) * 8
+        assert parts + 4 * max(N, 1) <= fwd.value <= parts + 4 * max(N, 1) + 4 * C + 16 * 1024
+        assert fwd.value < full.value
+    assert L.lce_forward_workspace_size(8, 7, 100, 64, ctypes.byref(fwd)) == INVALID
+    # 16384 x 128256 at chunk 1024: ~8.3 MB, within the no-alloc entry point's 64 MiB
+    assert L.lce_forward_workspace_size(16384, 4096, 128256, 1024, ctypes.byref(fwd)) == OK
+    assert fwd.value < 9 << 20
 
 
 def test_no_library_means_loud_failure(monkeypatch):

@@ -1,0 +1,104 @@
+"""The cross-chunk overlap (two chunk buffers: chunk k's logits tiles run in the
+same launches as chunk k-1's dW tiles, beside chunk k-1's dH tiles) against the
+one-buffer schedule (LCE_LOW_MEMORY, chunks one after the other) and the fp64
+oracle. Every reduction keeps its order in both schedules, so the results must be
+the same bits; the oracle pins both."""
+import numpy as np
+import pytest
+import torch
+
+from lce_synth import make_inputs
+from oracle import lce_oracle as O
+from tests.gpu_util import check_grad, check_loss, check_lse, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def lce():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import linear_cross_entropy_chunked_gb300 as pkg
+    pkg.build()
+    return pkg
+
+
+CASES = [
+    # N, D, V, chunk, ignored
+    (1000, 520, 3000, 384, 40),      # ragged last chunk, D not a multiple of 256
+    (300, 264, 1000, 128, 17),       # three chunks, odd row-block counts
+    (2500, 1024, 9000, 512, 60),     # vocabulary-split dH tiles
+    (1536, 256, 40000, 256, 30),     # six chunks, wide vocabulary
+    (129, 64, 257, 64, 5),           # three chunks of 64, 1 row in the last
+]
+
+
+@pytest.mark.parametrize("N,D,V,chunk,n_ign", CASES)
+def test_fused_overlap_equals_one_buffer_and_oracle(lce, N, D, V, chunk, n_ign):
+    H, W, y = make_inputs(N, D, V, seed=N + V, n_ignored=n_ign, w_std=0.05)
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    dl = torch.tensor([0.8], dtype=torch.float32, device=DEV)
+    a = lce.lce_fwd_bwd(Hd, Wd, yd, dloss=dl, chunk=chunk)
+    b = lce.lce_fwd_bwd(Hd, Wd, yd, dloss=dl, chunk=chunk, low_memory=True)
+    torch.cuda.synchronize()
+    for x, z, name in zip(a, b, ("loss", "lse", "dH", "dW")):
+        assert torch.equal(x, z), name
+    ref = O.forward_backward(H, W, y, dloss=0.8)
+    check_loss(a[0].item(), ref["loss"])
+    check_lse(to64(a[1]), ref["lse"])
+    check_grad("dH", to64(a[2]), ref["dH"])
+    check_grad("dW", to64(a[3]), ref["dW"])
+
+
+@pytest.mark.parametrize("N,D,V,chunk,n_ign", CASES[:3])
+def test_backward_overlap_equals_one_buffer_and_oracle(lce, N, D, V, chunk, n_ign):
+    H, W, y = make_inputs(N, D, V, seed=N + V + 1, n_ignored=n_ign, w_std=0.05)
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    loss, lse = lce.lce_forward(Hd, Wd, yd, chunk=chunk)
+    a = lce.lce_backward(Hd, Wd, yd, lse, chunk=chunk)
+    b = lce.lce_backward(Hd, Wd, yd, lse, chunk=chunk, low_memory=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    ref = O.forward_backward(H, W, y)
+    check_grad("dH", to64(a[0]), ref["dH"])
+    check_grad("dW", to64(a[1]), ref["dW"])
+
+
+@pytest.mark.parametrize("reduction", ["sum", "none"])
+def test_overlap_reductions_and_accumulation(lce, reduction):
+    N, D, V, chunk = 1100, 392, 5000, 256
+    H, W, y = make_inputs(N, D, V, seed=77, n_ignored=25, w_std=0.05)
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    rng = np.random.default_rng(3)
+    dl_host = rng.standard_normal(N) if reduction == "none" else 0.6
+    dl = torch.tensor(np.atleast_1d(dl_host), dtype=torch.float32, device=DEV)
+    gen = torch.Generator().manual_seed(9)
+    dH0 = (torch.randn(N, D, generator=gen) * 1e-4).to(torch.bfloat16).to(DEV)
+    dW0 = (torch.randn(V, D, generator=gen) * 1e-4).to(DEV)
+    outs = []
+    for low in (False, True):
+        dH, dW = dH0.clone(), dW0.clone()
+        outs.append(lce.lce_fwd_bwd(Hd, Wd, yd, dloss=dl, chunk=chunk, dH=dH, dW=dW,
+                                    reduction=reduction, accumulate=("dW", "dH"), low_memory=low))
+    torch.cuda.synchronize()
+    for x, z in zip(*outs):
+        assert torch.equal(x, z)
+    ref = O.forward_backward(H, W, y, dloss=dl_host, reduction=reduction)
+    check_grad("dH", to64(outs[0][2]), ref["dH"] + to64(dH0))
+    check_grad("dW", to64(outs[0][3]), ref["dW"] + to64(dW0))
+
+
+def test_overlap_fp16(lce):
+    N, D, V, chunk = 900, 264, 4000, 256
+    H, W, y = make_inputs(N, D, V, seed=78, n_ignored=20, w_std=0.05, dtype="fp16")
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    a = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk)
+    b = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk, low_memory=True)
+    torch.cuda.synchronize()
+    for x, z in zip(a, b):
+        assert torch.equal(x, z)
+    ref = O.forward_backward(H, W, y)
+    check_loss(a[0].item(), ref["loss"])
+    check_grad("dH", to64(a[2]), ref["dH"])
+    check_grad("dW", to64(a[3]), ref["dW"])

@@ -1,16 +1,17 @@
 """The token-sharded call on the GPU through a one-rank NCCL group (the
 exchange logic with two ranks is tested over gloo on the CPU): with every row
-on one rank it must give the single-GPU fused call's loss, lse, dH and dW (up to
-the rounding of 1 / N_valid, formed on the host side of the call here and inside
-the kernels there)."""
+on one rank it must match the fp64 oracle on the whole batch, and give the
+single-GPU fused call's loss, lse, dH and dW."""
 import os
 import socket
 
+import numpy as np
 import pytest
 import torch
 
 from lce_synth import make_inputs
-from tests.gpu_util import check_grad, to64
+from oracle import lce_oracle as O
+from tests.gpu_util import check_grad, check_loss, check_lse, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -45,6 +46,12 @@ def test_one_rank_sharded_equals_fused(group, compute_dW):
                                             compute_dW=compute_dW)
     rl, rlse, rdH, rdW = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=512, compute_dW=compute_dW)
     torch.cuda.synchronize()
+    ref = O.forward_backward(H, W, y)
+    check_loss(loss.item(), ref["loss"])
+    check_lse(to64(lse), ref["lse"])
+    check_grad("dH vs oracle", to64(dH), ref["dH"])
+    if compute_dW:
+        check_grad("dW vs oracle", to64(dW), ref["dW"])
     assert abs(loss.item() - rl.item()) <= 1e-6 * abs(rl.item())
     assert torch.equal(lse, rlse)
     check_grad("dH", to64(dH), to64(rdH))
@@ -52,3 +59,44 @@ def test_one_rank_sharded_equals_fused(group, compute_dW):
         check_grad("dW", to64(dW), to64(rdW))
     else:
         assert dW is None
+
+
+def test_count_valid_matches_the_oracle():
+    """lce_count_valid counts the labels in [0, V) other than ignore_index (the
+    oracle's reading: out-of-range labels count as ignored)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import linear_cross_entropy_chunked_gb300 as lce
+    lce.build()
+    for N, V, seed in ((7, 10, 1), (5000, 300, 2), (70000, 32000, 3), (0, 10, 4)):
+        rng = np.random.default_rng(seed)
+        y = rng.integers(-5, V + 5, size=N).astype(np.int64)
+        y[rng.random(N) < 0.1] = -100
+        yt = torch.from_numpy(y)
+        got = lce.count_valid(yt.to(DEV), V).item()
+        valid, _ = O.valid_rows(y, V)
+        assert got == int(valid.sum())
+
+
+@pytest.mark.parametrize("factor", [1, 3])
+def test_sharded_normaliser_matches_the_oracle(factor):
+    """lce_fwd_bwd_sharded with a given total count N_total: the loss is this
+    call's loss sum / N_total and G carries 1 / N_total (oracle: reduction sum with
+    dloss = 1 / N_total)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import linear_cross_entropy_chunked_gb300 as lce
+    lce.build()
+    H, W, y = make_inputs(900, 264, 3000, seed=13, n_ignored=31, w_std=0.05)
+    y[4] = 3000                            # out of range: ignored, as in every call
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    n_local = lce.count_valid(yd, 3000)
+    n_total = n_local * factor
+    loss, lse, dH, dW = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=256, n_valid_total=n_total)
+    torch.cuda.synchronize()
+    nt = int(n_total.item())
+    ref = O.forward_backward(H, W, y, dloss=1.0 / nt, reduction="sum")
+    check_loss(loss.item(), ref["loss"] / nt)
+    check_lse(to64(lse), ref["lse"])
+    check_grad("dH", to64(dH), ref["dH"])
+    check_grad("dW", to64(dW), ref["dW"])

@@ -83,16 +83,25 @@ def test_bench_defines_every_path_it_dispatches():
 
 # ---------------------------------------------------------------- token-sharded loss
 
-def _oracle_fwd_bwd(H, W, y, dloss, chunk, ignore_index, reduction, compute_dW):
-    """Stand-in for the library's fused call on the CPU (this test checks the
-    exchange around it; the call itself is parity-tested on the GPU)."""
+def _oracle_fwd_bwd(H, W, y, chunk, ignore_index, compute_dW, n_valid_total):
+    """Stand-in for the library's fused call with a given normaliser on the CPU
+    (this test checks the exchange around it; the call itself is parity-tested on
+    the GPU): the rank's loss sum and G scaled by 1 / n_valid_total."""
     from oracle import lce_oracle as O
-    assert reduction == "sum"
-    r = O.forward_backward(H, W, y, dloss=float(dloss.reshape(-1)[0]), reduction="sum",
+    n = int(n_valid_total.reshape(-1)[0])
+    r = O.forward_backward(H, W, y, dloss=1.0 / n if n else 0.0, reduction="sum",
                            ignore_index=ignore_index)
     dW = torch.from_numpy(r["dW"]).to(torch.float32) if compute_dW else None
-    return (torch.tensor([r["loss"]], dtype=torch.float32), torch.from_numpy(r["lse"]).float(),
+    loss = r["loss"] / n if n else 0.0
+    return (torch.tensor([loss], dtype=torch.float32), torch.from_numpy(r["lse"]).float(),
             torch.from_numpy(r["dH"]).float(), dW)
+
+
+def _oracle_count(y, V, ignore_index):
+    """Stand-in for the library's valid-row count (the oracle's reading)."""
+    from oracle import lce_oracle as O
+    valid, _ = O.valid_rows(y, V, ignore_index)
+    return torch.tensor([int(valid.sum())], dtype=torch.int64)
 
 
 def _sharded_worker(rank, world, port, out, cuts, compute_dW):
@@ -104,7 +113,7 @@ def _sharded_worker(rank, world, port, out, cuts, compute_dW):
     y[5] = 40                        # out of range: counts as ignored
     lo, hi = cuts[rank], cuts[rank + 1]
     loss, lse, dH, dW = sharded_fwd_bwd(H[lo:hi], W, y[lo:hi], compute_dW=compute_dW,
-                                        fwd_bwd=_oracle_fwd_bwd)
+                                        fwd_bwd=_oracle_fwd_bwd, count=_oracle_count)
     out[rank] = (float(loss), dH.numpy(), None if dW is None else dW.numpy())
     dist.barrier()
     dist.destroy_process_group()
