@@ -297,6 +297,7 @@ def run_ours(args, wl, chunk):
     total_ms = sum(step_ms)
     grad_ms, grad_n = lce.profile_read("grad")
     phase_ms, phase_n = lce.profile_read("phase")
+    dh_ms, dh_n = lce.profile_read("dh")
     logit_ms, logit_n = lce.profile_read("logits")
     merge_ms, merge_n = lce.profile_read("merge")
     st = lce.read_status(ws)
@@ -311,21 +312,23 @@ def run_ours(args, wl, chunk):
     peak_burst = peaks.get("bf16_tflops", 1900.0)
     peak_sust = peaks.get("bf16_tflops_sustained", 1700.0)
 
-    # dominant kernel. With two chunk buffers (the default) it is the overlapped
-    # phase of a chunk: chunk k-1's dH GEMM beside chunk k's logits tiles and chunk
-    # k-1's dW tiles, which share their launches (one grid beside the dH kernel,
-    # one behind it), timed together from fork to join: 6*C*D*V flops (2 each for
-    # the logits, dH and dW contractions of a chunk). With one buffer (or W frozen)
-    # it is the gradient phase alone: the dH GEMM and the dW grids, 4*C*D*V flops
-    # (W frozen: the dH GEMM alone, 2*C*D*V).
+    # dominant kernel. With two chunk buffers (the default) the chunks go in pairs
+    # and it is the second chunk's gradient phase: its dH GEMM beside one dW
+    # contraction over both chunks of the pair (one dW grid beside the dH kernel,
+    # one behind it), timed together from fork to join: 6*C*D*V flops (2 for the
+    # dH, 4 for the dW over 2C rows). The first chunk's dH GEMM runs beside the
+    # second chunk's logits GEMM (kind "dh", 4*C*D*V), the first chunk's logits GEMM
+    # alone (kind "logits"). With one buffer (or W frozen) it is a chunk's gradient phase:
+    # the dH GEMM and the dW grids, 4*C*D*V flops (W frozen: the dH GEMM alone,
+    # 2*C*D*V).
     nchunks = (N + chunk - 1) // chunk
     cdv = float(D) * V * N / nchunks
     overlapped = phase_n > 0
     if overlapped:
         dom_ms, dom_n, dom_flops = phase_ms, phase_n, 6.0 * cdv
-        dom_name = ("overlapped phase: lce_gemm_kernel<MODE_DH> (dH tiles of chunk k-1, 512 wide) "
-                    "beside lce_gemm_kernel<MODE_MIX_P> (logits tiles of chunk k interleaved with "
-                    "the dW tiles of chunk k-1: one grid beside the dH kernel, one behind it)")
+        dom_name = ("gradient phase of the second chunk of a pair: lce_gemm_kernel<MODE_DH> (its "
+                    "dH tiles, 512 wide) beside lce_gemm_kernel<MODE_BWD> (the dW tiles of both "
+                    "chunks, K = 2 chunks: one grid beside the dH kernel, one behind it)")
     else:
         dom_ms, dom_n, dom_flops = grad_ms, grad_n, (2.0 if frozen else 4.0) * cdv
         dom_name = ("gradient phase, W frozen: lce_gemm_kernel<MODE_DH> (dH tiles, 512 wide, split "
@@ -419,6 +422,10 @@ def run_ours(args, wl, chunk):
                           "share": phase_ms / total_ms},
                 "grad": {"ms_per_launch": grad_avg_ms, "launches": grad_n,
                          "tflops": grad_tflops, "share": grad_ms / total_ms},
+                "dh_with_next_logits": {"ms_per_launch": dh_ms / max(dh_n, 1), "launches": dh_n,
+                                        "tflops": (4.0 * cdv / (dh_ms / max(dh_n, 1) / 1e3) / 1e12
+                                                   if dh_n else None),
+                                        "share": dh_ms / total_ms},
                 "logits": {"ms_per_launch": logit_avg_ms, "launches": logit_n,
                            "tflops": logit_tflops, "share": logit_ms / total_ms},
                 "prep": {"ms_per_launch": merge_ms / max(merge_n, 1), "launches": merge_n,

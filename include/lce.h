@@ -151,12 +151,16 @@ lce_status lce_fwd_bwd_ex(const void *H, const void *W, const int64_t *y, const 
  *                     is the dH contraction alone (4NDV flops per step instead of
  *                     6NDV). Not with LCE_ACCUMULATE_DW (LCE_ERR_INVALID_ARG).
  *  LCE_LOW_MEMORY     one chunk buffer instead of two. By default (more than one
- *                     chunk, dW computed) the workspace holds two [chunk, V] chunk
- *                     buffers, so that chunk k's logits GEMM runs in the same
- *                     launches as chunk k-1's dW tiles (and beside its dH tiles)
- *                     while chunk k-1's G sits in the other buffer; with this flag
- *                     the chunks run one after the other (about half the workspace,
- *                     slower). Results are the same bits either way.
+ *                     chunk, chunk a multiple of 8, dW computed) the workspace
+ *                     holds two [chunk, V] chunk buffers and the chunks go in pairs:
+ *                     both chunks' G stay in the buffers and one dW contraction
+ *                     runs over the pair (K = two chunks' rows), which halves the
+ *                     fp32 read-modify-write of dW; the logits and dH are still
+ *                     computed one chunk at a time. With this flag every chunk has
+ *                     its own dW contraction (about half the workspace, slower).
+ *                     Either way the results meet the same tolerances and are
+ *                     deterministic; the two schedules differ in the rounding
+ *                     order of dW and of split dH contractions.
  * With LCE_ACCUMULATE_DH, LCE_FROZEN_W or LCE_LOW_MEMORY the workspace is
  * lce_workspace_size_opt(..., flags) bytes (the accumulation needs the chunk's dH in
  * fp32; the frozen-W gradient splits its dH contraction differently and keeps one
@@ -324,9 +328,11 @@ enum {
     LCE_KERNEL_MERGE = 2,    /* slab merge (lse, row loss), G rescale, H-chunk transpose */
     LCE_KERNEL_OTHER = 3,    /* label scan, loss finalisation, dH combination */
     LCE_KERNEL_NORM = 4,     /* RMSNorm forward / backward row kernels, dgamma reduction */
-    LCE_KERNEL_PHASE = 5,    /* a gradient phase that also runs the next chunk's logits tiles
-                                (two chunk buffers): dH + dW of chunk k-1, logits of chunk k */
-    LCE_KERNEL_KINDS = 6
+    LCE_KERNEL_PHASE = 5,    /* the second chunk of a pair (two chunk buffers): its dH tiles
+                                beside one dW contraction over both chunks of the pair */
+    LCE_KERNEL_DH = 6,       /* the first chunk of a pair: its dH tiles, with the second
+                                chunk's logits tiles on the CTA pairs they leave free */
+    LCE_KERNEL_KINDS = 7
 };
 lce_status lce_profile_enable(int on);
 lce_status lce_profile_read(int kind, double *total_ms, int64_t *launches);

@@ -65,7 +65,7 @@ EXPORTED = (
     "lce_profile_reset",
 )
 
-KERNEL_KINDS = {"logits": 0, "grad": 1, "merge": 2, "other": 3, "norm": 4, "phase": 5}
+KERNEL_KINDS = {"logits": 0, "grad": 1, "merge": 2, "other": 3, "norm": 4, "phase": 5, "dh": 6}
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 
@@ -291,7 +291,7 @@ def lce_backward(H, W, y, lse, dloss=None, chunk: int = 1024, ignore_index: int 
     reduction="none"; None means 1. accumulate: a subset of ("dW", "dH") added
     into the given dW / dH instead of overwriting them. compute_dW=False: W is
     frozen, dW is neither computed nor returned (None). low_memory: one chunk
-    buffer (LCE_LOW_MEMORY; the chunks do not overlap; same results)."""
+    buffer (LCE_LOW_MEMORY: one dW contraction per chunk)."""
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
     red = _reduction(reduction)
@@ -323,8 +323,8 @@ def lce_fwd_bwd(H, W, y, dloss=None, chunk: int = 1024, ignore_index: int = IGNO
     n_valid_total: a device int64 tensor of one element, the valid rows of every
     shard of a token-sharded batch (reduction "mean" only): the mean divides by
     it instead of this call's count (lce_fwd_bwd_sharded). low_memory: one chunk
-    buffer (LCE_LOW_MEMORY: about half the workspace; the chunks do not overlap;
-    same results)."""
+    buffer (LCE_LOW_MEMORY: about half the workspace, one dW contraction per chunk
+    instead of one per pair of chunks)."""
     N, D, V = _check_inputs(H, W, y)
     dev = H.device
     red = _reduction(reduction)

@@ -86,10 +86,11 @@ struct Layout {
     long long nchunks = 0;
     int nparts = 0;          // 128-column slabs per row
     int ldg = 0;             // row stride of the chunk buffer (elements)
-    int ldt = 0;             // row stride (elements) of H^T: chunk rows rounded up
-    int nbuf = 1;            // chunk buffers: with two, a chunk's logits GEMM runs while
-                             // the previous chunk's gradient GEMMs read the other
-    size_t gbuf_bytes = 0;   // bytes of one chunk buffer
+    int ldt = 0;             // row stride (elements) of H^T: rows of one chunk (or of a
+                             // pair of chunks) rounded up to 64
+    int nbuf = 1;            // chunk buffers: with two, the dW contraction of a pair of
+                             // chunks runs once, over both chunks' G (K = 2 chunks)
+    size_t gbuf_bytes = 0;   // bytes of one chunk buffer (the two are contiguous)
     bool frozen_w = false;   // no dW contraction (LCE_FROZEN_W)
     int dh_splits = 1;       // vocabulary parts of a full chunk's dH tiles
     long long ldp = 0;       // rows per fp32 dH partial array: chunk rows rounded up to 128
@@ -138,20 +139,28 @@ bool make_layout(long long N, long long D, long long V, long long chunk, Layout 
     L.off_G = off;
     L.fwd_total = off;
     // two chunk buffers when there is a dW contraction and more than one chunk:
-    // chunk k's logits (P' or G) go into one while chunk k-1's dH and dW tiles read
-    // the other (LCE_LOW_MEMORY: one buffer, no overlap across chunks)
-    L.nbuf = (!frozen_w && !low_mem && L.nchunks > 1) ? 2 : 1;
-    L.gbuf_bytes = align_up(2 * static_cast<size_t>(L.C) * L.ldg, 1024);
-    off += static_cast<size_t>(L.nbuf) * L.gbuf_bytes;
+    // chunks are taken in pairs, the second chunk's G goes into the buffer after the
+    // first's, and one dW contraction runs over both (K = the pair's rows), which
+    // halves the fp32 read-modify-write of dW (LCE_LOW_MEMORY: one buffer, one dW
+    // contraction per chunk). The buffers are contiguous rows of one [2C][ldg]
+    // array (2 * C * ldg bytes each, a multiple of 512), and the second chunk's
+    // columns of H^T start at column C, which the transpose's 16-byte stores need to
+    // be a multiple of 8.
+    L.nbuf = (!frozen_w && !low_mem && L.nchunks > 1 && L.C % 8 == 0) ? 2 : 1;
+    L.gbuf_bytes = 2 * static_cast<size_t>(L.C) * L.ldg;
+    off += align_up(static_cast<size_t>(L.nbuf) * L.gbuf_bytes, 1024);
     // H chunk^T [D][ldt]: the K-major B operand of the dW contraction (none when W
     // is frozen)
     L.frozen_w = frozen_w;
-    L.ldt = static_cast<int>(align_up(static_cast<size_t>(L.C), 64));
+    L.ldt = static_cast<int>(align_up(static_cast<size_t>(L.nbuf) * L.C, 64));
     L.off_HT = off;
     if (!frozen_w) off += align_up(2 * static_cast<size_t>(D) * L.ldt, 1024);
     // fp32 dH partial sums of a split dH contraction, one [ldp][D] array per part
     // (a single array, past `total`, serves callers that accumulate into dH)
     L.dh_splits = dh_splits_for(L.C, D, V, frozen_w);
+    // the first chunk of a pair runs its dH tiles alone (split for all pairs)
+    if (L.nbuf == 2 && dh_splits_for(L.C, D, V, true) > L.dh_splits)
+        L.dh_splits = dh_splits_for(L.C, D, V, true);
     L.ldp = static_cast<long long>(align_up(static_cast<size_t>(L.C), BM));
     L.off_dHp = off;
     if (L.dh_splits > 1)
@@ -368,6 +377,7 @@ lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t
     c.Gb[0] = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_G);
     c.Gb[1] = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_G +
                                                 (c.L.nbuf > 1 ? c.L.gbuf_bytes : 0));
+    // (with two buffers Gb[1] is row C of one [2C][ldg] array starting at Gb[0])
     c.HT = reinterpret_cast<__nv_bfloat16 *>(c.ws + c.L.off_HT);
     c.s = reinterpret_cast<cudaStream_t>(stream);
     c.reduction = LCE_REDUCTION_MEAN;
@@ -405,24 +415,43 @@ void base_params(const Ctx &c, GemmParams &p, long long row0, long long rows, in
     p.f16 = c.f16 ? 1 : 0;
 }
 
-lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, int slot,
-                      const float *lse, const float *dloss, __nv_bfloat16 *G) {
-    GemmParams p;
+// The logits launches of the chunk at row0 (MODE_LSE / _LSE_P / _G epilogue, P' or G
+// into chunk buffer G).
+struct LogitsSpec {
+    int mode;
+    long long row0, rows;
+    int slot;
+    const float *lse;       // MODE_G
+    const float *dloss;
+    __nv_bfloat16 *G;
+};
+
+lce_status logits_params(const Ctx &c, const LogitsSpec &l, GemmParams &p) {
     memset(&p, 0, sizeof(p));
-    base_params(c, p, row0, rows, slot);
+    base_params(c, p, l.row0, l.rows, l.slot);
     p.tmA0 = c.tmH_K;
-    p.a_row0 = c.h_chunked ? 0 : static_cast<int>(row0);
+    p.a_row0 = c.h_chunked ? 0 : static_cast<int>(l.row0);
     p.tmB0 = c.tmW_K;
-    p.m_blocks0 = static_cast<int>(cdiv(rows, BM));
+    p.m_blocks0 = static_cast<int>(cdiv(l.rows, BM));
     p.n_blocks0 = static_cast<int>(cdiv(c.V, BN));
     p.k_blocks0 = static_cast<int>(cdiv(c.D, BK));
     const int cl = c.pairs > 0 ? 2 : 1;
     p.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * p.n_blocks0;
-    p.lse = lse;
-    p.dloss = dloss;
-    p.G = G;
-    if (mode != MODE_LSE && !encode_store_2d(&p.tmS0, G, c.V, rows, 2ull * c.L.ldg, c.t16, 32))
+    p.lse = l.lse;
+    p.dloss = l.dloss;
+    p.G = l.G;
+    if (l.mode != MODE_LSE &&
+        !encode_store_2d(&p.tmS0, l.G, c.V, l.rows, 2ull * c.L.ldg, c.t16, 32))
         return LCE_ERR_CUDA;
+    return LCE_OK;
+}
+
+lce_status run_logits(const Ctx &c, int mode, long long row0, long long rows, int slot,
+                      const float *lse, const float *dloss, __nv_bfloat16 *G) {
+    GemmParams p;
+    const lce_status st = logits_params(c, LogitsSpec{mode, row0, rows, slot, lse, dloss, G}, p);
+    if (st != LCE_OK) return st;
+    const int cl = c.pairs > 0 ? 2 : 1;
     const int units = cl == 2 ? c.pairs : c.sms;
     const int grid = cl * (p.total_tiles < units ? p.total_tiles : units);
     LCE_LAUNCH_KIND(LCE_KERNEL_LOGITS, c.s, launch_gemm(mode, cl, p, grid, c.s));
@@ -447,29 +476,21 @@ struct DhOut {
 
 // Vocabulary parts for a chunk of `rows` rows: one off the CTA-pair path (its
 // 256-column dH tiles are many), else the shapes' split, at most the layout's.
-int dh_parts(const Ctx &c, long long rows) {
+// alone: the dH tiles have the GPU to themselves (no dW tiles beside them).
+int dh_parts(const Ctx &c, long long rows, bool alone) {
     if (c.pairs <= 0) return 1;
-    const int sp = dh_splits_for(rows, c.D, c.V, c.L.frozen_w);
+    const int sp = dh_splits_for(rows, c.D, c.V, c.L.frozen_w || alone);
     return sp < c.L.dh_splits ? sp : c.L.dh_splits;
 }
 
-// The logits tiles of the next chunk that a gradient phase runs in the same
-// launches as its dW tiles (MODE_MIX_P: P' epilogue of the fused path; MODE_MIX_G:
-// G epilogue of the backward from a saved lse), writing into chunk buffer G.
-struct Mix {
-    int mode;
-    long long row0, rows;
-    int slot;                // tile counter of the launches
-    __nv_bfloat16 *G;
-    const float *lse;        // MODE_MIX_G
-};
-
-lce_status run_transpose(const Ctx &c, long long row0, long long rows) {
+// H chunk^T into columns col0 .. col0 + rows - 1 of H^T (the K-major B operand of
+// the dW tiles; col0 = C for the second chunk of a pair).
+lce_status run_transpose(const Ctx &c, long long row0, long long rows, long long col0) {
     const __nv_bfloat16 *Hc = c.h_chunked ? c.H : c.H + row0 * c.D;
     TransposeParams tp;
     tp.src = Hc;
     tp.ld_src = static_cast<int>(c.D);
-    tp.dst_t = c.HT;
+    tp.dst_t = c.HT + col0;
     tp.ld_t = c.L.ldt;
     tp.rows = static_cast<int>(rows);
     tp.cols = static_cast<int>(c.D);
@@ -477,33 +498,53 @@ lce_status run_transpose(const Ctx &c, long long row0, long long rows) {
     return LCE_OK;
 }
 
-// The gradient phase of the chunk at row0 (dH and dW from chunk buffer G).
-// transposed: the H chunk^T the dW tiles read is already in place (else it is
-// made first). mix: logits tiles of the next chunk to run in the dW launches.
+// What one gradient launch set computes. The dH tiles of the chunk at row0 read
+// its G (buffer G); the dW tiles, when there are any (dw_rows > 0), contract over
+// dw_rows rows of G starting at Gdw (the chunk's own rows, or the rows of a pair of
+// chunks) against as many columns of H^T.
+struct GradSpec {
+    __nv_bfloat16 *G;
+    __nv_bfloat16 *Gdw;
+    long long dw_rows;      // K of the dW tiles (0: no dW tiles)
+    bool transposed;        // H^T is in place (else it is made first, for this chunk)
+    bool dh_alone;          // no dW tiles beside the dH tiles: split for all CTA pairs
+    bool dw_only;           // the dW tiles alone (the chunk's dH is computed elsewhere)
+    const LogitsSpec *beside = nullptr;   // with dh_alone: another chunk's logits tiles on
+                                          // the pairs the dH tiles leave free, then on all
+};
+
 // *parts_used: the number of non-empty vocabulary parts written (fp32 output).
 lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const DhOut &o,
-                   float *dW, bool accumulate, const float *dloss, __nv_bfloat16 *G,
-                   bool transposed, const Mix *mix, int *parts_used = nullptr) {
+                   float *dW, bool accumulate, const float *dloss, const GradSpec &g,
+                   int *parts_used = nullptr) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
     base_params(c, p, row0, rows, slot);
-    p.G = G;
+    p.G = g.G;
     void *dHc = o.ptr;
     const bool dh_fp32 = o.fp32;
     const int want_parts = (o.fp32 && o.parts > 1 && c.pairs > 0) ? o.parts : 1;
-    // frozen W: the dH tiles only (no H chunk^T, no dW maps, dW untouched)
-    const bool with_dw = !c.L.frozen_w;
+    // frozen W or the first chunk of a pair: the dH tiles only (no dW maps, dW untouched)
+    const bool with_dw = !c.L.frozen_w && g.dw_rows > 0;
     const int cl = c.pairs > 0 ? 2 : 1;
     if (with_dw) {
         // the H chunk^T for the K-major B operand of the dW tiles
-        if (!transposed) LCE_TRY(run_transpose(c, row0, rows));
-        // dW A = G^T read from G itself (MN-major boxes of 64 vocab columns x 64 rows)
-        if (!encode_2d(&p.tmA1, G, c.V, rows, 2ull * c.L.ldg, 64, BK, c.t16)) return LCE_ERR_CUDA;
-        if (!encode_2d(&p.tmB1, c.HT, rows, c.D, 2ull * c.L.ldt, BK, BN / cl, c.t16))
+        if (!g.transposed) LCE_TRY(run_transpose(c, row0, rows, 0));
+        // dW A = G^T read from G itself, MN-major: per k block a CTA's 128 vocabulary
+        // columns x 64 rows as two 64-column blocks, fetched by one 3-D box {64
+        // columns, 64 rows, 2 blocks} (x: the column within a block, y: the row, z: the
+        // 64-column block, 128 bytes apart). The columns of the last block past V read
+        // the buffer's padding; they meet only dW rows past V, which the store clips.
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(g.dw_rows),
+                                  static_cast<uint64_t>(cdiv(c.V, 64))};
+        const uint64_t strides[2] = {2ull * c.L.ldg, 128};
+        const uint32_t box[3] = {64, BK, 2};
+        if (!encode_map(&p.tmA1, g.Gdw, 3, dims, strides, box, c.t16)) return LCE_ERR_CUDA;
+        if (!encode_2d(&p.tmB1, c.HT, g.dw_rows, c.D, 2ull * c.L.ldt, BK, BN / cl, c.t16))
             return LCE_ERR_CUDA;
         if (!encode_store_2d(&p.tmS1, dW, c.D, c.V, 4ull * c.D, MAP_F32)) return LCE_ERR_CUDA;
     }
-    if (!encode_2d(&p.tmA0, G, c.V, rows, 2ull * c.L.ldg, BK, BM, c.t16)) return LCE_ERR_CUDA;
+    if (!encode_2d(&p.tmA0, g.G, c.V, rows, 2ull * c.L.ldg, BK, BM, c.t16)) return LCE_ERR_CUDA;
     p.tmB0 = c.tmW_MN;
     const uint64_t s0_rows = want_parts > 1 ? static_cast<uint64_t>(want_parts) * o.ldp : rows;
     if (!encode_store_2d(&p.tmS0, dHc, c.D, s0_rows, (dh_fp32 ? 4ull : 2ull) * c.D,
@@ -514,7 +555,7 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
     p.k_blocks0 = static_cast<int>(cdiv(c.V, BK));
     p.m_blocks1 = with_dw ? static_cast<int>(cdiv(c.V, BM)) : 0;
     p.n_blocks1 = with_dw ? static_cast<int>(cdiv(c.D, BN)) : 0;
-    p.k_blocks1 = with_dw ? static_cast<int>(cdiv(rows, BK)) : 0;
+    p.k_blocks1 = with_dw ? static_cast<int>(cdiv(g.dw_rows, BK)) : 0;
     p.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * p.n_blocks0 +
                     static_cast<int>(cdiv(p.m_blocks1, cl)) * p.n_blocks1;
     int parts = 1;
@@ -531,6 +572,11 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
     p.dW = dW;
     p.dw_accumulate = accumulate ? 1 : 0;
     const int units = cl == 2 ? c.pairs : c.sms;
+    // profiling kind: a pair's second chunk (its dH with both chunks' dW), a pair's
+    // first chunk (its dH alone), or a chunk's whole gradient phase
+    const int kind = (with_dw && g.dw_rows > rows) ? LCE_KERNEL_PHASE
+                     : (!with_dw && !c.L.frozen_w) ? LCE_KERNEL_DH
+                                                   : LCE_KERNEL_GRAD;
     if (cl == 2) {
         // CTA pairs: the dH tiles run 512 columns wide (two MMAs share each A
         // block: a quarter fewer operand bytes per flop) in one kernel with one
@@ -542,44 +588,61 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
         // long dH tiles to run after it). A third launch, a dW grid as large as
         // the dH one, queued on the caller's stream behind the dH kernel, takes
         // over the dH kernel's SMs when it ends; both dW grids draw tiles from
-        // the same counter. With `mix`, the dW grids also carry the next chunk's
-        // logits tiles, interleaved with the dW tiles.
+        // the same counter.
         GemmParams ph = p;
         ph.n_blocks0 = static_cast<int>(cdiv(c.D, BN_WIDE));
         ph.m_blocks1 = ph.n_blocks1 = ph.k_blocks1 = 0;
-        ph.total_tiles = static_cast<int>(cdiv(p.m_blocks0, cl)) * ph.n_blocks0 * parts;
-        if (!with_dw) {
+        ph.total_tiles = g.dw_only ? 0 : static_cast<int>(cdiv(p.m_blocks0, cl)) * ph.n_blocks0 * parts;
+        if (!with_dw && !g.beside) {
             const int gh = cl * (ph.total_tiles < units ? ph.total_tiles : units);
             if (ph.total_tiles > 0)
-                LCE_LAUNCH_KIND(LCE_KERNEL_GRAD, c.s, launch_gemm(MODE_DH, cl, ph, gh, c.s));
+                LCE_LAUNCH_KIND(kind, c.s, launch_gemm(MODE_DH, cl, ph, gh, c.s));
+            return LCE_OK;
+        }
+        if (!with_dw) {
+            // the dH tiles beside another chunk's logits tiles: as with the dW grids
+            // below, one logits grid on the side stream sized to the pairs the dH grid
+            // leaves free and one behind the dH kernel, drawing from one counter
+            GemmParams pl;
+            LCE_TRY(logits_params(c, *g.beside, pl));
+            SideStream *ss = side_stream();
+            if (!ss) return LCE_ERR_CUDA;
+            std::lock_guard<std::mutex> lock(ss->mu);
+            const int dh_pairs = ph.total_tiles < units ? ph.total_tiles : units;
+            const int free_pairs = units - dh_pairs;
+            const int l1 = pl.total_tiles < free_pairs ? pl.total_tiles : free_pairs;
+            const int l2 = pl.total_tiles < dh_pairs ? pl.total_tiles : dh_pairs;
+            const int pi = prof_begin(kind, c.s);
+            if (cudaEventRecord(ss->fork, c.s) != cudaSuccess ||
+                cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
+                return LCE_ERR_CUDA;
+            int launched = 0;
+            if (dh_pairs > 0) {
+                if (launch_gemm(MODE_DH, cl, ph, cl * dh_pairs, c.s) != cudaSuccess) return LCE_ERR_CUDA;
+                ++launched;
+            }
+            if (l1 > 0) {
+                if (launch_gemm(g.beside->mode, cl, pl, cl * l1, ss->s) != cudaSuccess)
+                    return LCE_ERR_CUDA;
+                ++launched;
+            }
+            if (l2 > 0 && (dh_pairs > 0 || l1 == 0)) {
+                if (launch_gemm(g.beside->mode, cl, pl, cl * l2, c.s) != cudaSuccess)
+                    return LCE_ERR_CUDA;
+                ++launched;
+            }
+            if (cudaEventRecord(ss->join, ss->s) != cudaSuccess ||
+                cudaStreamWaitEvent(c.s, ss->join, 0) != cudaSuccess)
+                return LCE_ERR_CUDA;
+            prof_end(pi, c.s);
+            g_launches += launched;
             return LCE_OK;
         }
         GemmParams pw = p;
-        int mode_w = MODE_BWD;
         pw.m_blocks0 = 0;
         pw.k_splits = 0;
         pw.total_tiles = static_cast<int>(cdiv(p.m_blocks1, cl)) * p.n_blocks1;
         pw.tile_counter = c.hdr + HDR_COUNTERS + 2 * c.L.nchunks + 2 + slot / 2;
-        if (mix) {
-            // the next chunk's logits tiles: A = its H rows, B = W (both K-major),
-            // P' / G stored into mix->G; rows and row0 are that chunk's (the dW
-            // tiles use neither)
-            mode_w = mix->mode;
-            pw.tmA0 = c.tmH_K;
-            pw.tmB0 = c.tmW_K;
-            pw.a_row0 = static_cast<int>(mix->row0);
-            pw.rows = static_cast<int>(mix->rows);
-            pw.row0 = static_cast<int>(mix->row0);
-            pw.lse = mix->lse;
-            pw.G = mix->G;
-            if (!encode_store_2d(&pw.tmS0, mix->G, c.V, mix->rows, 2ull * c.L.ldg, c.t16, 32))
-                return LCE_ERR_CUDA;
-            pw.m_blocks0 = static_cast<int>(cdiv(mix->rows, BM));
-            pw.n_blocks0 = static_cast<int>(cdiv(c.V, BN));
-            pw.k_blocks0 = static_cast<int>(cdiv(c.D, BK));
-            pw.total_tiles += static_cast<int>(cdiv(pw.m_blocks0, cl)) * pw.n_blocks0;
-            pw.tile_counter = c.hdr + HDR_COUNTERS + mix->slot;
-        }
         SideStream *ss = side_stream();
         if (!ss) return LCE_ERR_CUDA;
         std::lock_guard<std::mutex> lock(ss->mu);
@@ -587,7 +650,7 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
         const int free_pairs = units - dh_pairs;
         const int w1 = pw.total_tiles < free_pairs ? pw.total_tiles : free_pairs;
         const int w2 = pw.total_tiles < dh_pairs ? pw.total_tiles : dh_pairs;
-        const int pi = prof_begin(mix ? LCE_KERNEL_PHASE : LCE_KERNEL_GRAD, c.s);
+        const int pi = prof_begin(kind, c.s);
         if (cudaEventRecord(ss->fork, c.s) != cudaSuccess ||
             cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
             return LCE_ERR_CUDA;
@@ -597,11 +660,11 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
             ++launched;
         }
         if (w1 > 0) {
-            if (launch_gemm(mode_w, cl, pw, cl * w1, ss->s) != cudaSuccess) return LCE_ERR_CUDA;
+            if (launch_gemm(MODE_BWD, cl, pw, cl * w1, ss->s) != cudaSuccess) return LCE_ERR_CUDA;
             ++launched;
         }
         if (w2 > 0 && (dh_pairs > 0 || w1 == 0)) {
-            if (launch_gemm(mode_w, cl, pw, cl * w2, c.s) != cudaSuccess) return LCE_ERR_CUDA;
+            if (launch_gemm(MODE_BWD, cl, pw, cl * w2, c.s) != cudaSuccess) return LCE_ERR_CUDA;
             ++launched;
         }
         if (cudaEventRecord(ss->join, ss->s) != cudaSuccess ||
@@ -612,25 +675,24 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
         return LCE_OK;
     }
     const int grid = cl * (p.total_tiles < units ? p.total_tiles : units);
-    LCE_LAUNCH_KIND(LCE_KERNEL_GRAD, c.s, launch_gemm(MODE_BWD, cl, p, grid, c.s));
+    LCE_LAUNCH_KIND(kind, c.s, launch_gemm(MODE_BWD, cl, p, grid, c.s));
     return LCE_OK;
 }
 
-// A chunk's gradient phase on the loss path: dH straight into the caller's rows
-// when there is one vocabulary part and nothing to accumulate, else through the
-// fp32 partial arrays and the combining kernel (which adds into the caller's dH
-// when accumulating).
+// A chunk's gradient launches on the loss path: dH straight into the caller's
+// rows when there is one vocabulary part and nothing to accumulate, else through
+// the fp32 partial arrays and the combining kernel (which adds into the caller's
+// dH when accumulating).
 lce_status run_grad(const Ctx &c, long long row0, long long rows, int slot, void *dHc,
-                    bool acc_dh, float *dW, bool acc_dw, const float *dloss, __nv_bfloat16 *G,
-                    bool transposed, const Mix *mix = nullptr) {
-    const int want = dh_parts(c, rows);
+                    bool acc_dh, float *dW, bool acc_dw, const float *dloss, const GradSpec &g) {
+    if (g.dw_only) return run_bwd(c, row0, rows, slot, DhOut{dHc, false, 1, 0}, dW, acc_dw, dloss, g);
+    const int want = dh_parts(c, rows, g.dh_alone);
     if (want <= 1 && !acc_dh)
-        return run_bwd(c, row0, rows, slot, DhOut{dHc, false, 1, 0}, dW, acc_dw, dloss, G,
-                       transposed, mix);
+        return run_bwd(c, row0, rows, slot, DhOut{dHc, false, 1, 0}, dW, acc_dw, dloss, g);
     float *dHp = reinterpret_cast<float *>(c.ws + c.L.off_dHp);
     int parts = 1;
-    LCE_TRY(run_bwd(c, row0, rows, slot, DhOut{dHp, true, want, c.L.ldp}, dW, acc_dw, dloss, G,
-                    transposed, mix, &parts));
+    LCE_TRY(run_bwd(c, row0, rows, slot, DhOut{dHp, true, want, c.L.ldp}, dW, acc_dw, dloss, g,
+                    &parts));
     LCE_LAUNCH(launch_combine_dh(dHp, parts, c.L.ldp * c.D, dHc, rows * c.D, c.f16, acc_dh,
                                  c.sms, c.s));
     return LCE_OK;
@@ -662,9 +724,10 @@ lce_status run_merge(const Ctx &c, bool fused, long long row0, long long rows, f
 
 // Fused path, between a chunk's logits GEMM and its gradient GEMMs, one launch:
 // lse and the row losses, P' -> G in place in chunk buffer G, and (transpose) the
-// H chunk^T the dW tiles read.
+// H chunk^T the dW tiles read, into columns ht_col0 .. of H^T.
 lce_status run_prep(const Ctx &c, long long row0, long long rows, float *lse,
-                    const float *dloss, float *loss_rows, __nv_bfloat16 *G, bool transpose) {
+                    const float *dloss, float *loss_rows, __nv_bfloat16 *G, bool transpose,
+                    long long ht_col0 = 0) {
     PrepParams pp;
     memset(&pp, 0, sizeof(pp));
     MergeParams &m = pp.m;
@@ -690,7 +753,7 @@ lce_status run_prep(const Ctx &c, long long row0, long long rows, float *lse,
     if (transpose) {
         pp.tp.src = c.h_chunked ? c.H : c.H + row0 * c.D;
         pp.tp.ld_src = static_cast<int>(c.D);
-        pp.tp.dst_t = c.HT;
+        pp.tp.dst_t = c.HT + ht_col0;
         pp.tp.ld_t = c.L.ldt;
         pp.tp.rows = static_cast<int>(rows);
         pp.tp.cols = static_cast<int>(c.D);
@@ -706,9 +769,9 @@ inline long long chunk_rows(const Ctx &c, long long k) {
     return (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
 }
 
-// Whether the chunks' gradient phases overlap the next chunk's logits GEMM: CTA
-// pairs, a dW contraction, two chunk buffers (so more than one chunk), H in place.
-inline bool overlapped(const Ctx &c) {
+// Whether chunks are taken in pairs with one dW contraction per pair: CTA pairs,
+// a dW contraction, two chunk buffers (so more than one chunk), H in place.
+inline bool paired(const Ctx &c) {
     return c.pairs > 0 && !c.L.frozen_w && c.L.nbuf == 2 && !c.h_chunked;
 }
 
@@ -833,19 +896,32 @@ lce_status lce_backward_opt(const void *H, const void *W, const int64_t *y, cons
     }
     const bool acc_dw0 = (flags & LCE_ACCUMULATE_DW) != 0;
     __nv_bfloat16 *dHb = static_cast<__nv_bfloat16 *>(dH);
-    if (overlapped(c)) {
-        // chunk k's logits (G epilogue, into buffer k % 2) run in the same launches
-        // as chunk k-1's dW tiles, beside chunk k-1's dH tiles; then chunk k's H^T
-        LCE_TRY(run_logits(c, MODE_G, 0, chunk_rows(c, 0), 0, lse, dloss, c.Gb[0]));
-        LCE_TRY(run_transpose(c, 0, chunk_rows(c, 0)));
-        for (long long k = 1; k <= c.L.nchunks; ++k) {
-            const long long p0 = (k - 1) * c.L.C, prow = chunk_rows(c, k - 1);
-            Mix mx{MODE_MIX_G, k * c.L.C, k < c.L.nchunks ? chunk_rows(c, k) : 0,
-                   static_cast<int>(2 * k), c.Gb[k & 1], lse};
-            LCE_TRY(run_grad(c, p0, prow, static_cast<int>(2 * k - 1), dHb + p0 * c.D, acc_dh, dW,
-                             k > 1 || acc_dw0, dloss, c.Gb[(k - 1) & 1], true,
-                             k < c.L.nchunks ? &mx : nullptr));
-            if (k < c.L.nchunks) LCE_TRY(run_transpose(c, k * c.L.C, chunk_rows(c, k)));
+    if (paired(c)) {
+        // chunks in pairs (a, b): a's G (G epilogue) into buffer 0, its H^T into
+        // columns 0..C-1; a's dH tiles, with b's logits (G into buffer 1) on the pairs
+        // they leave free; b's H^T into columns C.., then b's dH beside one dW
+        // contraction over both chunks (K = C + rows_b). An odd last chunk runs by itself.
+        for (long long a = 0; a < c.L.nchunks; a += 2) {
+            const long long ra = a * c.L.C, na = chunk_rows(c, a);
+            const bool has_b = a + 1 < c.L.nchunks;
+            const bool acc = a > 0 || acc_dw0;
+            LCE_TRY(run_logits(c, MODE_G, ra, na, static_cast<int>(2 * a), lse, dloss, c.Gb[0]));
+            LCE_TRY(run_transpose(c, ra, na, 0));
+            if (!has_b) {
+                LCE_TRY(run_grad(c, ra, na, static_cast<int>(2 * a + 1), dHb + ra * c.D, acc_dh, dW,
+                                 acc, dloss, GradSpec{c.Gb[0], c.Gb[0], na, true, false}));
+                break;
+            }
+            const long long b = a + 1, rb = b * c.L.C, nb = chunk_rows(c, b);
+            // a's dH tiles, with b's logits tiles on the pairs they leave free
+            const LogitsSpec lb{MODE_G, rb, nb, static_cast<int>(2 * b), lse, dloss, c.Gb[1]};
+            GradSpec ga{c.Gb[0], c.Gb[0], 0, true, true};
+            ga.beside = &lb;
+            LCE_TRY(run_grad(c, ra, na, static_cast<int>(2 * a + 1), dHb + ra * c.D, acc_dh, dW,
+                             acc, dloss, ga));
+            LCE_TRY(run_transpose(c, rb, nb, c.L.C));
+            LCE_TRY(run_grad(c, rb, nb, static_cast<int>(2 * b + 1), dHb + rb * c.D, acc_dh, dW,
+                             acc, dloss, GradSpec{c.Gb[1], c.Gb[0], c.L.C + nb, true, false}));
         }
         return LCE_OK;
     }
@@ -854,7 +930,7 @@ lce_status lce_backward_opt(const void *H, const void *W, const int64_t *y, cons
         const long long rows = chunk_rows(c, k);
         LCE_TRY(run_logits(c, MODE_G, row0, rows, static_cast<int>(2 * k), lse, dloss, c.Gb[0]));
         LCE_TRY(run_grad(c, row0, rows, static_cast<int>(2 * k + 1), dHb + row0 * c.D, acc_dh, dW,
-                         k > 0 || acc_dw0, dloss, c.Gb[0], false));
+                         k > 0 || acc_dw0, dloss, GradSpec{c.Gb[0], c.Gb[0], rows, false, false}));
     }
     return LCE_OK;
 }
@@ -918,23 +994,35 @@ lce_status fwd_bwd_impl(const void *H, const void *W, const int64_t *y, const fl
     }
     const bool acc_dw0 = (flags & LCE_ACCUMULATE_DW) != 0;
     __nv_bfloat16 *dHb = static_cast<__nv_bfloat16 *>(dH);
-    if (overlapped(c)) {
-        // chunk k's logits (P' epilogue, into buffer k % 2) run in the same launches
-        // as chunk k-1's dW tiles, beside chunk k-1's dH tiles; then chunk k's
-        // prep (lse, row losses, P' -> G, H^T)
-        LCE_TRY(run_logits(c, MODE_LSE_P, 0, chunk_rows(c, 0), 0, nullptr, nullptr, c.Gb[0]));
-        LCE_TRY(run_prep(c, 0, chunk_rows(c, 0), lse, dloss, rows_out, c.Gb[0], true));
-        for (long long k = 1; k <= c.L.nchunks; ++k) {
-            const long long p0 = (k - 1) * c.L.C, prow = chunk_rows(c, k - 1);
-            const bool more = k < c.L.nchunks;
-            Mix mx{MODE_MIX_P, k * c.L.C, more ? chunk_rows(c, k) : 0, static_cast<int>(2 * k),
-                   c.Gb[k & 1], nullptr};
-            LCE_TRY(run_grad(c, p0, prow, static_cast<int>(2 * k - 1), dHb + p0 * c.D, acc_dh, dW,
-                             k > 1 || acc_dw0, dloss, c.Gb[(k - 1) & 1], true,
-                             more ? &mx : nullptr));
-            if (more)
-                LCE_TRY(run_prep(c, k * c.L.C, chunk_rows(c, k), lse, dloss, rows_out, c.Gb[k & 1],
-                                 true));
+    if (paired(c)) {
+        // chunks in pairs (a, b): a's P' into buffer 0, its prep (lse, row losses,
+        // P' -> G, H^T into columns 0..C-1); a's dH tiles, with b's logits (P' into
+        // buffer 1) on the pairs they leave free; b's prep (H^T into columns C..), then
+        // b's dH beside one dW contraction over both chunks (K = C + rows_b). An odd
+        // last chunk runs by itself.
+        for (long long a = 0; a < c.L.nchunks; a += 2) {
+            const long long ra = a * c.L.C, na = chunk_rows(c, a);
+            const bool has_b = a + 1 < c.L.nchunks;
+            const bool acc = a > 0 || acc_dw0;
+            LCE_TRY(run_logits(c, MODE_LSE_P, ra, na, static_cast<int>(2 * a), nullptr, nullptr,
+                               c.Gb[0]));
+            LCE_TRY(run_prep(c, ra, na, lse, dloss, rows_out, c.Gb[0], true, 0));
+            if (!has_b) {
+                LCE_TRY(run_grad(c, ra, na, static_cast<int>(2 * a + 1), dHb + ra * c.D, acc_dh, dW,
+                                 acc, dloss, GradSpec{c.Gb[0], c.Gb[0], na, true, false}));
+                break;
+            }
+            const long long b = a + 1, rb = b * c.L.C, nb = chunk_rows(c, b);
+            // a's dH tiles, with b's logits tiles on the pairs they leave free
+            const LogitsSpec lb{MODE_LSE_P, rb, nb, static_cast<int>(2 * b), nullptr, nullptr,
+                                c.Gb[1]};
+            GradSpec ga{c.Gb[0], c.Gb[0], 0, true, true};
+            ga.beside = &lb;
+            LCE_TRY(run_grad(c, ra, na, static_cast<int>(2 * a + 1), dHb + ra * c.D, acc_dh, dW,
+                             acc, dloss, ga));
+            LCE_TRY(run_prep(c, rb, nb, lse, dloss, rows_out, c.Gb[1], true, c.L.C));
+            LCE_TRY(run_grad(c, rb, nb, static_cast<int>(2 * b + 1), dHb + rb * c.D, acc_dh, dW,
+                             acc, dloss, GradSpec{c.Gb[1], c.Gb[0], c.L.C + nb, true, false}));
         }
     } else {
         for (long long k = 0; k < c.L.nchunks; ++k) {
@@ -944,7 +1032,8 @@ lce_status fwd_bwd_impl(const void *H, const void *W, const int64_t *y, const fl
                                c.Gb[0]));
             LCE_TRY(run_prep(c, row0, rows, lse, dloss, rows_out, c.Gb[0], !frozen));
             LCE_TRY(run_grad(c, row0, rows, static_cast<int>(2 * k + 1), dHb + row0 * c.D, acc_dh,
-                             dW, k > 0 || acc_dw0, dloss, c.Gb[0], true));
+                             dW, k > 0 || acc_dw0, dloss,
+                             GradSpec{c.Gb[0], c.Gb[0], frozen ? 0 : rows, true, false}));
         }
     }
     if (!none)
@@ -1125,8 +1214,8 @@ lce_status lce_norm_fwd_bwd_opt(const void *X, const void *gamma, float eps, con
         LCE_TRY(run_prep(c, row0, rows, lse, dloss, rows_out, c.Gb[0], !frozen));
         int parts = 1;
         LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1),
-                        DhOut{dHbuf, true, dh_parts(c, rows), c.L.ldp}, dW, k > 0, dloss, c.Gb[0],
-                        true, nullptr, &parts));
+                        DhOut{dHbuf, true, dh_parts(c, rows, false), c.L.ldp}, dW, k > 0, dloss,
+                        GradSpec{c.Gb[0], c.Gb[0], frozen ? 0 : rows, true, false}, &parts));
         np.H = nullptr;
         np.dH = dHbuf;
         np.dh_fp32 = 1;

@@ -37,6 +37,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// 3-D box (x, y, z): the dW tiles' A operand, two 64-column blocks of G^T per load.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -152,24 +162,12 @@ enum : int { TILE_MAIN = 0, TILE_DW = 1 };
 // of a split dH launch), then the many short dW tiles (n fastest, so the tiles
 // that share one G^T slab run together); the dynamic schedule lets the SMs
 // left over by the dH tiles start on dW at once.
-// MIX launches interleave the two tile sets in proportion: among the first t
-// units, floor(t * nL / (nL + nW)) are logits units, so unit t is a logits unit
-// when that count steps up at t, and the logits and dW units each keep their own
-// order (logits: m fastest; dW: n fastest) and their share of every stretch of
-// the schedule.
-template <int CL, bool MIX = false>
+template <int CL>
 __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, int crank, bool wide) {
     Tile tl;
     const int mp0 = (p.m_blocks0 + CL - 1) / CL;
     const int nH1 = mp0 * p.n_blocks0;
     const int splits = p.k_splits > 1 ? p.k_splits : 1;
-    if constexpr (MIX) {
-        const long long nL = nH1;
-        const long long T = p.total_tiles;
-        const int before = static_cast<int>(static_cast<long long>(t) * nL / T);
-        const int upto = static_cast<int>(static_cast<long long>(t + 1) * nL / T);
-        t = upto > before ? before : nH1 + (t - before);
-    }
     if (t < nH1 * splits) {
         const int sp = t / nH1;
         t -= sp * nH1;
@@ -454,6 +452,14 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map, uint32_t bar,
+                                                 int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
 __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
                                                uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -487,11 +493,6 @@ template <int MODE, int CL>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_constant__ GemmParams p) {
     using P = Pipe<CL, MODE == MODE_DH>;
     static_assert(MODE != MODE_DH || CL == 2, "wide dH tiles run on CTA pairs only");
-    // MIX: logits tiles of one chunk interleaved with the dW tiles of the previous one
-    constexpr bool kMix = MODE == MODE_MIX_P || MODE == MODE_MIX_G;
-    static_assert(!kMix || CL == 2, "two-chunk launches run on CTA pairs only");
-    constexpr bool kHasDW = MODE == MODE_BWD || kMix;
-    constexpr int kLogitsEpi = MODE == MODE_MIX_P ? MODE_LSE_P : (MODE == MODE_MIX_G ? MODE_G : MODE);
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
     __shared__ __align__(8) uint64_t empty_bar[MAX_STAGES];
@@ -535,7 +536,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
         prefetch_tmap(&p.tmA0);
         prefetch_tmap(&p.tmB0);
         if (MODE != MODE_LSE) prefetch_tmap(&p.tmS0);
-        if (kHasDW) {
+        if (MODE == MODE_BWD) {
             prefetch_tmap(&p.tmA1);
             prefetch_tmap(&p.tmB1);
             prefetch_tmap(&p.tmS1);
@@ -626,28 +627,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                     if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
                     if (t < 0) break;
                 }
-                const Tile tl = decode_tile<CL, kMix>(p, t, static_cast<int>(crank), MODE == MODE_DH);
-                const bool is_dw = kHasDW && tl.type == TILE_DW;
+                const Tile tl = decode_tile<CL>(p, t, static_cast<int>(crank), MODE == MODE_DH);
                 for (int kb = 0; kb < tl.nk; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, ab)) { ok = false; break; }
                     uint8_t *sA = smem + stage * P::kStageBytes;
                     uint8_t *sB = sA + A_BYTES;
                     uint64_t *fb = &full_bar[stage];
                     const int kx = (tl.kb0 + kb) * BK;
-                    // logits tiles: A = H rows, B = W rows (both K-major); dH tiles: A =
-                    // G rows (K-major), B = W (MN-major); dW tiles: A = G^T, B = H chunk^T
-                    const CUtensorMap *ma = is_dw ? &p.tmA1 : &p.tmA0;
+                    const CUtensorMap *ma = (MODE == MODE_BWD && tl.type == TILE_DW) ? &p.tmA1 : &p.tmA0;
                     const int ya = (MODE == MODE_BWD) ? tl.m0 : p.a_row0 + tl.m0;
-                    const bool b_mn = (MODE == MODE_BWD) && !is_dw;
-                    const CUtensorMap *mb = is_dw ? &p.tmB1 : &p.tmB0;
+                    const bool b_mn = (MODE == MODE_BWD) && tl.type != TILE_DW;
+                    const CUtensorMap *mb = (MODE == MODE_BWD && !b_mn) ? &p.tmB1 : &p.tmB0;
                     // dW tiles read A = G^T straight from the row-major chunk buffer
                     // (MN-major: two 64-wide vocabulary boxes per 64 chunk rows)
-                    const bool a_mn = is_dw;
+                    const bool a_mn = (MODE == MODE_BWD) && tl.type == TILE_DW;
                     if constexpr (CL == 1) {
                         mbar_arrive_expect_tx(fb, P::kStageBytes);
                         if (a_mn) {
-                            tma_load_2d(sA, ma, fb, tl.m0, kx);
-                            tma_load_2d(sA + 8192, ma, fb, tl.m0 + 64, kx);
+                            // two 64-column blocks of G^T (z = tl.m0 / 64 and the next)
+                            tma_load_3d(sA, ma, fb, 0, kx, tl.m0 >> 6);
                         } else {
                             tma_load_2d(sA, ma, fb, kx, ya);
                         }
@@ -677,8 +675,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                         const uint32_t lfb = map_to_rank(fb, 0);
                         const int nb = tl.n0 + static_cast<int>(crank) * (BN / 2);
                         if (a_mn) {
-                            tma_load_2d_pair(sA, ma, lfb, tl.m0, kx);
-                            tma_load_2d_pair(sA + 8192, ma, lfb, tl.m0 + 64, kx);
+                            // two 64-column blocks of G^T (z = tl.m0 / 64 and the next)
+                            tma_load_3d_pair(sA, ma, lfb, 0, kx, tl.m0 >> 6);
                         } else {
                             tma_load_2d_pair(sA, ma, lfb, kx, ya);
                         }
@@ -724,7 +722,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                 release_on_leader(&sempty_bar[sq]);
                 if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
                 if (t < 0) break;
-                const Tile tl = decode_tile<CL, kMix>(p, t, 0, MODE == MODE_DH);
+                const Tile tl = decode_tile<CL>(p, t, 0, MODE == MODE_DH);
                 if (!mbar_wait_cluster(&tempty_bar[acc], aphase ^ 1, ab)) { ok = false; break; }
                 // a wide dH tile accumulates into both buffers (acc is 0 at its start)
                 if (MODE == MODE_DH && !mbar_wait_cluster(&tempty_bar[1], aphase ^ 1, ab)) {
@@ -736,7 +734,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                 // MN-major operands: W for the dH tiles (B), the chunk buffer for the
                 // dW tiles (A = G^T); everything else is K-major
                 const bool b_mn = (MODE == MODE_BWD || MODE == MODE_DH) && tl.type != TILE_DW;
-                const bool a_mn = kHasDW && tl.type == TILE_DW;
+                const bool a_mn = (MODE == MODE_BWD) && tl.type == TILE_DW;
                 const uint32_t idesc = idesc_f16kind(CL * BM, BN, a_mn, b_mn, p.f16 != 0);
                 const uint32_t a_lbo = a_mn ? 8192u : 16u;
                 const uint32_t b_lbo = b_mn ? 8192u : 16u;
@@ -798,10 +796,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
         WarpStager wst;
         wst.buf = smem + PIPE_BYTES + warp * (2 * STAGING_BYTES / NUM_EPI_WARPS);
         wst.lane = lane;
-        const float out_scale = (kHasDW || MODE == MODE_DH)
+        const float out_scale = (MODE == MODE_BWD || MODE == MODE_DH)
                                     ? lce_out_scale(p.dloss, p.mean, p.hdr[HDR_NVALID], p.f16)
                                     : 1.f;
-        int prev_type = -1;   // MIX: the tile type of the previous epilogue
         int sq = 0;
         uint32_t sphase = 0;
         int acc = 0;
@@ -814,7 +811,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
             if (lane == 0) release_on_leader(&sempty_bar[sq]);
             if (++sq == SCHED_DEPTH) { sq = 0; sphase ^= 1; }
             if (t < 0) break;
-            const Tile tl = decode_tile<CL, kMix>(p, t, static_cast<int>(crank), MODE == MODE_DH);
+            const Tile tl = decode_tile<CL>(p, t, static_cast<int>(crank), MODE == MODE_DH);
             ok = mbar_wait_cluster(&tfull_bar[acc], aphase, ab);
             if (!named_bar_and(st.bar_id, 128, ok)) break;
             tc_fence_after();
@@ -838,20 +835,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) lce_gemm_kernel(const __grid_
                 aphase ^= 1;
                 continue;
             }
-            if constexpr (kMix) {
-                // The logits epilogue stages through per-warp 4 KB boxes, the dW
-                // epilogue through the half's 16 KB box over the same shared memory.
-                // When the tile type changes, every store still reading the boxes
-                // is waited for (each issuing lane waits for its own) before any
-                // warp of the half writes them again.
-                if (tl.type != prev_type) {
-                    if (lane == 0) bulk_wait_read0();
-                    named_bar_sync(st.bar_id, 128);
-                    prev_type = tl.type;
-                }
-                if (tl.type == TILE_DW) epilogue_grad(p, tl, taddr, half, st, out_scale);
-                else epilogue_logits<kLogitsEpi>(p, tl, taddr, quarter, half, wst);
-            } else if constexpr (MODE != MODE_BWD && MODE != MODE_DH) {
+            if constexpr (MODE != MODE_BWD && MODE != MODE_DH) {
                 epilogue_logits<MODE>(p, tl, taddr, quarter, half, wst);
             } else {
                 epilogue_grad(p, tl, taddr, half, st, out_scale);
@@ -899,8 +883,6 @@ cudaError_t gemm_set_attributes() {
     if ((e = set_attr<MODE_LSE_P, 2>()) != cudaSuccess) return e;
     if ((e = set_attr<MODE_G, 2>()) != cudaSuccess) return e;
     if ((e = set_attr<MODE_BWD, 2>()) != cudaSuccess) return e;
-    if ((e = set_attr<MODE_MIX_P, 2>()) != cudaSuccess) return e;
-    if ((e = set_attr<MODE_MIX_G, 2>()) != cudaSuccess) return e;
     return set_attr<MODE_DH, 2>();
 }
 
@@ -929,8 +911,6 @@ cudaError_t launch_gemm(int mode, int cluster, const GemmParams &p, int grid, cu
             case MODE_LSE_P: e = launch_one<MODE_LSE_P, 2>(p, grid, s); break;
             case MODE_G: e = launch_one<MODE_G, 2>(p, grid, s); break;
             case MODE_DH: e = launch_one<MODE_DH, 2>(p, grid, s); break;
-            case MODE_MIX_P: e = launch_one<MODE_MIX_P, 2>(p, grid, s); break;
-            case MODE_MIX_G: e = launch_one<MODE_MIX_G, 2>(p, grid, s); break;
             default: e = launch_one<MODE_BWD, 2>(p, grid, s); break;
         }
     } else {
@@ -939,7 +919,7 @@ cudaError_t launch_gemm(int mode, int cluster, const GemmParams &p, int grid, cu
             case MODE_LSE_P: e = launch_one<MODE_LSE_P, 1>(p, grid, s); break;
             case MODE_G: e = launch_one<MODE_G, 1>(p, grid, s); break;
             case MODE_BWD: e = launch_one<MODE_BWD, 1>(p, grid, s); break;
-            default: return cudaErrorInvalidValue;   // wide dH and two-chunk tiles need pairs
+            default: return cudaErrorInvalidValue;   // the wide dH tiles need CTA pairs
         }
     }
     if (e != cudaSuccess) return e;

@@ -64,13 +64,7 @@ enum GemmMode : int {
     MODE_LSE_P = 1,   // ... + store P' = exp(z - max_part) as bf16 into the chunk buffer
     MODE_G = 2,       // logits tiles -> G = (exp(z - lse) - onehot) * scale as bf16 (given lse)
     MODE_BWD = 3,     // dH tiles (G W) followed by dW tiles (G^T H) in one persistent launch
-    MODE_DH = 4,      // dH tiles only, 256 rows x 512 columns per CTA pair (CTA pairs only)
-    // Two chunks in one launch (CTA pairs only): the logits tiles of chunk k (with
-    // the MODE_LSE_P or the MODE_G epilogue) interleaved with the dW tiles of chunk
-    // k - 1, so that the dW tiles' HBM-bound read-modify-write of dW overlaps the
-    // tensor-bound logits work on the same SMs.
-    MODE_MIX_P = 5,
-    MODE_MIX_G = 6
+    MODE_DH = 4       // dH tiles only, 256 rows x 512 columns per CTA pair (CTA pairs only)
 };
 
 // Scale of row i of G: dloss (a scalar, or row i of a per-row vector) divided
@@ -117,7 +111,8 @@ constexpr int FLAG_TIMEOUT = 2;
 struct GemmParams {
     CUtensorMap tmA0;      // logits A = H (K-major) | dH A = G (K-major)
     CUtensorMap tmB0;      // logits B = W (K-major) | dH B = W (MN-major)
-    CUtensorMap tmA1;      // dW A = G^T, read from the chunk buffer G [C][ldg] (MN-major)
+    CUtensorMap tmA1;      // dW A = G^T, read from the chunk buffer G [C][ldg] (MN-major;
+                           // 3-D: {64 columns, rows, 64-column blocks})
     CUtensorMap tmB1;      // dW B = H chunk^T [D][C] (K-major)
     CUtensorMap tmS0;      // output store: P' / G chunk buffer (bf16) | dH chunk (bf16)
     CUtensorMap tmS1;      // dW output store / reduce-add (fp32)

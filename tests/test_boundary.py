@@ -60,16 +60,19 @@ def test_workspace_size_is_order_chunk_times_V(L):
     assert st == OK
     st, b2 = ws_size(L, 16384, 4096, 128256, 2048)
     assert st == OK
-    # the two bf16 chunk buffers (P', then G; the next chunk's logits fill one while
-    # the previous chunk's gradients read the other) dominate: ~4 bytes per chunk row
-    # per vocab id; next come the chunk's H^T (bf16) and the (max, sum) partials
-    assert 2 * 2 * 1024 * 128256 <= b1 <= 2 * 2 * 1024 * 128256 * 1.1
+    # the two bf16 chunk buffers (P', then G, of the two chunks of a pair) dominate:
+    # ~4 bytes per chunk row per vocab id; next come the pair's H^T (bf16), the fp32
+    # dH parts of the first chunk's dH tiles (split in two when they run alone) and
+    # the (max, sum) partials
+    assert 2 * 2 * 1024 * 128256 <= b1 <= 2 * 2 * 1024 * 128256 * 1.15
     assert 1.7 < b2 / b1 < 2.05
-    # LCE_LOW_MEMORY keeps one chunk buffer: about half
+    # LCE_LOW_MEMORY keeps one chunk buffer and one chunk's H^T, and no dH parts at
+    # chunk 1024 (32 dH tiles beside the dW tiles): about half
     low = ctypes.c_size_t(0)
     assert L.lce_workspace_size_opt(16384, 4096, 128256, 1024, 16, ctypes.byref(low)) == OK
     assert 2 * 1024 * 128256 <= low.value <= 2 * 1024 * 128256 * 1.2
-    assert b1 - low.value == 2 * 1024 * (-(-128256 // 256) * 256)   # one [chunk][ldg] bf16 buffer
+    ldg = -(-128256 // 256) * 256
+    assert b1 - low.value == 2 * 1024 * ldg + 2 * 4096 * 1024 + 2 * 4 * 1024 * 4096
     # it does not grow with N beyond O(N) bytes
     st, b3 = ws_size(L, 4 * 16384, 4096, 128256, 1024)
     assert b3 - b1 < 64 * 16384 * 4
@@ -234,7 +237,10 @@ def test_accumulate_workspace_and_flags(L):
     assert L.lce_workspace_size_opt(N, D, V, chunk, 1, ctypes.byref(out)) == OK
     assert out.value == base                                   # dW accumulation needs nothing
     assert L.lce_workspace_size_opt(N, D, V, chunk, 3, ctypes.byref(out)) == OK
-    assert out.value == base + 4 * chunk * D   # the chunk's dH in fp32
+    assert out.value == base   # the dH parts of a pair's first chunk serve
+    low = ws_size_low(L, N, D, V, chunk)
+    assert L.lce_workspace_size_opt(N, D, V, chunk, 3 | 16, ctypes.byref(out)) == OK
+    assert out.value == low + 4 * chunk * D    # one buffer: the chunk's dH in fp32
     base2 = ws_size(L, N, D, V, 512)[1]        # two vocabulary parts: their arrays serve
     assert L.lce_workspace_size_opt(N, D, V, 512, 2, ctypes.byref(out)) == OK
     assert out.value == base2

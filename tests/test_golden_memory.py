@@ -62,8 +62,8 @@ def test_library_workspace_within_the_pages_chunked_budgets(L):
     (LCE_LOW_MEMORY): below the exercise's chunked peak (chunks of 128 tokens, D
     4096 assumed: the exercise gives none), below the worked example's chunked
     figure, and a small fraction of the Llama-3 logits. The default workspace holds
-    a second chunk buffer (the next chunk's logits overlap the previous chunk's
-    gradients): at most twice that, still O(chunk * V)."""
+    a second chunk buffer (chunks go in pairs with one dW contraction per pair) and
+    the pair's H^T and dH parts: a little over twice that, still O(chunk * V)."""
     ex = _fig("exercise_fp16_batch4_seq2048")
     assert _ws(L, ex["rows"], 4096, ex["V"], ex["chunk"], LOW_MEMORY) < \
         ex["chunked_peak_below_mb"] * 1e6
@@ -74,5 +74,5 @@ def test_library_workspace_within_the_pages_chunked_budgets(L):
     low = _ws(L, l3["rows"], 4096, l3["V"], 1024, LOW_MEMORY)
     assert low < 0.07 * l3["printed"] * 1e9
     default = _ws(L, l3["rows"], 4096, l3["V"], 1024)
-    assert low < default <= 2 * low
-    assert default < 0.14 * l3["printed"] * 1e9
+    assert low < default <= 2.2 * low
+    assert default < 0.15 * l3["printed"] * 1e9

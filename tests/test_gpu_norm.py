@@ -119,14 +119,16 @@ def test_norm_fwd_bwd_llama2_shape(lce):
 
 def test_norm_fused_equals_composed_calls(lce):
     """lce_norm_fwd_bwd against rmsnorm_forward -> lce_fwd_bwd -> rmsnorm_backward
-    on the GPU: the same H, so loss, lse and dW are bit-identical; dX differs only
-    by the bf16 rounding of dH in the composed path."""
+    on the GPU: the same H and the same one-dW-contraction-per-chunk schedule (the
+    RMSNorm path keeps one chunk buffer, so the composed call takes low_memory), so
+    loss, lse and dW are bit-identical; dX differs only by the bf16 rounding of dH
+    in the composed path."""
     N, D, V, chunk = 1500, 1024, 5000, 512
     X, g, W, y = _norm_case(N, D, V, seed=17, n_ign=40)
     Xd, gd, Wd, yd = X.to(DEV), g.to(DEV), W.to(DEV), y.to(DEV)
     loss, lse, dX, dgamma, dW = lce.norm_fwd_bwd(Xd, gd, Wd, yd, eps=EPS, chunk=chunk)
     H = lce.rmsnorm_forward(Xd, gd, eps=EPS)
-    loss2, lse2, dH2, dW2 = lce.lce_fwd_bwd(H, Wd, yd, chunk=chunk)
+    loss2, lse2, dH2, dW2 = lce.lce_fwd_bwd(H, Wd, yd, chunk=chunk, low_memory=True)
     dX2, dgamma2 = lce.rmsnorm_backward(Xd, gd, dH2, eps=EPS)
     torch.cuda.synchronize()
     assert torch.equal(loss, loss2) and torch.equal(lse, lse2) and torch.equal(dW, dW2)
