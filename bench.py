@@ -345,11 +345,12 @@ def run_ours(args, wl, chunk):
     traffic = load_traffic()
     dom_traffic = traffic.get("phase" if overlapped else ("grad_frozen" if frozen else "grad"))
     # algorithmic bytes of the method (the minimum it must move) per step: read H, W
-    # and y, write lse, dH and dW (fp32); a launch of the dominant kernel is one of the
-    # step's nchunks units (one chunk), so it carries 1/nchunks of them
+    # and y, write lse, dH and dW (fp32); a launch of the dominant kernel carries the
+    # share of them that its flops are of the step's (a pair's phase: 6 of a chunk
+    # pair's 12 C*D*V; a chunk's gradient phase: 4 of its 6)
     alg_bytes_step = (N * D * 2 + V * D * 2 + N * 8 + N * 4 + N * D * 2 +
                       (0 if frozen else V * D * 4))
-    alg_bytes_launch = alg_bytes_step / nchunks
+    alg_bytes_launch = alg_bytes_step * dom_flops / flops_step
     # softmax / gather epilogue bytes of the fused path (beyond the GEMM operands):
     # P' written by the logits epilogue, then read and rewritten in place as G by the
     # prep kernel (3 x N x V x 2 B); the (max, sum) slab partials written and read
@@ -413,7 +414,8 @@ def run_ours(args, wl, chunk):
                          "traffic_over_alg_bytes": (dom_traffic / alg_bytes_launch
                                                     if dom_traffic else None),
                          "alg_bytes_note": "the method's algorithmic bytes per step (read H, W, "
-                                           "y; write lse, dH, dW fp32) / chunks per step",
+                                           "y; write lse, dH, dW fp32) x the launch's share of "
+                                           "the step's flops",
                          "launch_ms": dom_avg_ms, "launches": dom_n,
                          "flops_per_launch": dom_flops},
             "kernels": {

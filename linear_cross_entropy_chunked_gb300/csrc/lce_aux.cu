@@ -325,6 +325,16 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_prep_kernel(const PrepParam
     }
     const int r = static_cast<int>(blockIdx.x / p.segs);
     const int seg = static_cast<int>(blockIdx.x % p.segs);
+    // the segment's P' first: its loads are in flight while the row's lse is formed
+    const int nvec = (m.V + 7) >> 3;
+    const int v0 = seg * PREP_VEC_PER_CTA + threadIdx.x;
+    uint4 *row = reinterpret_cast<uint4 *>(m.G + static_cast<size_t>(r) * p.ldg);
+    uint4 u[PREP_VPT];
+#pragma unroll
+    for (int i = 0; i < PREP_VPT; ++i) {
+        const int v = v0 + i * MERGE_THREADS;
+        if (v < nvec) u[i] = row[v];
+    }
     const float2 *parts = m.parts + static_cast<size_t>(r) * m.nparts;
     const float lse = row_lse(parts, m.nparts, s_red, &s_bcast);
     const int grow = m.row0 + r;
@@ -338,15 +348,6 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_prep_kernel(const PrepParam
                                         y_ok, m.f16);
     const float lse2 = lse * LOG2E_F;
     const int ycol = y_ok ? static_cast<int>(yv) : -1;
-    const int nvec = (m.V + 7) >> 3;
-    const int v0 = seg * PREP_VEC_PER_CTA + threadIdx.x;
-    uint4 *row = reinterpret_cast<uint4 *>(m.G + static_cast<size_t>(r) * p.ldg);
-    uint4 u[PREP_VPT];
-#pragma unroll
-    for (int i = 0; i < PREP_VPT; ++i) {
-        const int v = v0 + i * MERGE_THREADS;
-        if (v < nvec) u[i] = row[v];
-    }
 #pragma unroll
     for (int i = 0; i < PREP_VPT; ++i) {
         const int v = v0 + i * MERGE_THREADS;
