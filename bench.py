@@ -54,8 +54,10 @@ def parse():
                          "with the previous chunk's gradient GEMMs, about half the workspace")
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
                     help="H and W dtype of the fused path (the headline is bf16)")
-    ap.add_argument("--path", choices=["fused", "ce-logits", "norm"], default="fused",
+    ap.add_argument("--path", choices=["fused", "separate", "ce-logits", "norm"], default="fused",
                     help="fused: the LM-head linear + CE forward+backward (the headline); "
+                         "separate: lce_forward, then lce_backward recomputing the logits from the "
+                         "saved lse (8NDV executed); "
                          "ce-logits: the CE over precomputed bf16 logits of the same workload "
                          "(gradient in place); norm: final RMSNorm + LM head + CE forward and "
                          "backward into the pre-norm hidden state (lce_norm_fwd_bwd)")
@@ -257,9 +259,16 @@ def run_ours(args, wl, chunk):
     dW = None if frozen else torch.empty(V, D, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    separate = args.path == "separate"
+
     def step():
-        lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk, loss=loss, lse=lse, dH=dH, dW=dW, ws=ws,
-                        stream=stream, compute_dW=not frozen, low_memory=low)
+        if separate:
+            lce.lce_forward(Hd, Wd, yd, chunk=chunk, loss=loss, lse=lse, ws=ws, stream=stream)
+            lce.lce_backward(Hd, Wd, yd, lse, chunk=chunk, dH=dH, dW=dW, ws=ws, stream=stream,
+                             compute_dW=not frozen, low_memory=low)
+        else:
+            lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk, loss=loss, lse=lse, dH=dH, dW=dW, ws=ws,
+                            stream=stream, compute_dW=not frozen, low_memory=low)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -342,7 +351,10 @@ def run_ours(args, wl, chunk):
     grad_tflops = (2.0 if frozen else 4.0) * cdv / (grad_avg_ms / 1e3) / 1e12 if grad_n else None
     logit_avg_ms = logit_ms / max(logit_n, 1)
     logit_tflops = 2.0 * cdv / (logit_avg_ms / 1e3) / 1e12 if logit_n else None
-    traffic = load_traffic()
+    variant = "+".join(x for x in (("fp16" if args.dtype == "fp16" else ""),
+                                   ("frozen_w" if frozen else ""), ("low_memory" if low else ""),
+                                   ("separate" if separate else "")) if x)
+    traffic = load_traffic(wl.name, chunk, variant)
     dom_traffic = traffic.get("phase" if overlapped else ("grad_frozen" if frozen else "grad"))
     # algorithmic bytes of the method (the minimum it must move) per step: read H, W
     # and y, write lse, dH and dW (fp32); a launch of the dominant kernel carries the
@@ -363,7 +375,7 @@ def run_ours(args, wl, chunk):
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not separate:
         e2e = run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen, low=low)
         w_up = run_e2e(args, lce, H, W, y, chunk, dev, stream, world, frozen, upload_w=True,
                        low=low)
@@ -391,10 +403,16 @@ def run_ours(args, wl, chunk):
                                       l2="L2 flushed between steps (256 MB write); "
                                          "W 1.05 GB also exceeds L2",
                                       **({"frozen_w": True} if frozen else {}),
+                                      **({"path": "lce_forward + lce_backward"} if separate
+                                         else {}),
                                       chunk_buffers=1 if (low or frozen or nchunks == 1) else 2),
             "tflops": tflops,
-            "flops_per_step": {"algorithmic": flops_step, "executed": flops_step,
-                               "note": "the fused call recomputes nothing: executed = algorithmic "
+            "flops_per_step": {"algorithmic": flops_step,
+                               "executed": flops_step * (8.0 / 6.0 if separate and not frozen else
+                                                         (6.0 / 4.0 if separate else 1.0)),
+                               "note": ("lce_forward + lce_backward: the backward recomputes the "
+                                        "logits (2NDV more)") if separate else
+                                       "the fused call recomputes nothing: executed = algorithmic "
                                        "(lce_forward + lce_backward would execute 8NDV)"},
             "pct_of_bf16_peak": {"vs_burst": tflops / peak_burst, "vs_sustained": tflops / peak_sust,
                                  "flops": "4NDV algorithmic (W frozen: no dW)" if frozen
@@ -465,10 +483,10 @@ def kernel_source_hash(files) -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic():
-    """DRAM bytes per launch (scaled to the bench workload) from the committed ncu
-    summary, per kernel; a kernel is left out when its sources changed since the
-    capture (or the file is absent)."""
+def load_traffic(workload: str = "", chunk: int = 0, variant: str = ""):
+    """DRAM bytes per launch from the committed ncu summary, per kernel; a kernel is
+    left out when its sources changed since the capture, when the capture was of
+    another workload, chunk or variant of the path, or when the file is absent."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return {}
@@ -476,8 +494,15 @@ def load_traffic():
         d = json.load(f)
     out = {}
     for k, v in d.get("kernels", {}).items():
-        if v.get("sha256_16") == kernel_source_hash(v.get("sources", [])):
-            out[k] = v.get("dram_bytes_per_launch_bench")
+        if v.get("sha256_16") != kernel_source_hash(v.get("sources", [])):
+            continue
+        if workload and v.get("workload", workload) != workload:
+            continue
+        if chunk and v.get("chunk", chunk) != chunk:
+            continue
+        if v.get("variant", "") != variant:
+            continue
+        out[k] = v.get("dram_bytes_per_launch_bench")
     return out
 
 
@@ -657,7 +682,8 @@ def run_ce_logits(args, wl):
         "roofline": {"kernel": "lce_ce_logits_cluster_kernel<bf16>", "bound": "hbm", "achieved": gbs,
                      "peak": peaks.get("hbm_gbs", 6800.0), "unit": "GB/s",
                      "frac": gbs / peaks.get("hbm_gbs", 6800.0),
-                     "traffic": load_traffic().get("ce_logits"),
+                     "traffic": load_traffic(wl.name).get("ce_logits")
+                                if N == wl.N else None,
                      "alg_bytes_per_launch": alg_bytes, "launch_ms": kernel_ms,
                      "peak_source": peak_src},
         "gpu_launches": 3 * args.steps,
