@@ -274,6 +274,15 @@ __global__ void __launch_bounds__(256) lce_transpose_kernel(const TransposeParam
 // tiles of the H chunk (lce_transpose_kernel's arithmetic) for the dW contraction.
 static_assert(PREP_THREADS == MERGE_THREADS, "the prep kernel computes lse as the merge does");
 
+__device__ __forceinline__ void bulk_copy_to_smem(uint32_t dst, const void *src, uint32_t bytes,
+                                                  uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void transpose_tile(const TransposeParams &p, int c0, int r0,
                                                __nv_bfloat16 *tile) {
     const int tid = threadIdx.x;
@@ -312,29 +321,41 @@ __device__ __forceinline__ void transpose_tile(const TransposeParams &p, int c0,
     }
 }
 
+constexpr uint32_t PREP_SEG_BYTES = PREP_VEC_PER_CTA * 16;       // 32 KB of P' per CTA
+constexpr unsigned long long PREP_WAIT_NS = 2000000000ull;       // bound of the copy wait
+
+// The segment of P' comes into shared memory by one bulk copy, issued first, so
+// it is in flight while the row's lse is formed; shared memory rather than
+// registers holds it, which lets 7 CTAs (224 KB of copies) share an SM.
 __global__ void __launch_bounds__(MERGE_THREADS) lce_prep_kernel(const PrepParams p) {
+    extern __shared__ __align__(128) uint8_t prep_smem[];   // the segment, or a transpose tile
     __shared__ float s_red[MERGE_THREADS / 32];
     __shared__ float s_bcast;
-    __shared__ __align__(16) __nv_bfloat16 tile[TT * TSTRIDE];
+    __shared__ __align__(8) uint64_t seg_bar;
+    __shared__ volatile int s_abort;
     const MergeParams &m = p.m;
     const long long nrow_ctas = static_cast<long long>(m.rows) * p.segs;
     if (blockIdx.x >= nrow_ctas) {
         const int b = static_cast<int>(blockIdx.x - nrow_ctas);
-        transpose_tile(p.tp, (b % p.tt_x) * TT, (b / p.tt_x) * TT, tile);
+        transpose_tile(p.tp, (b % p.tt_x) * TT, (b / p.tt_x) * TT,
+                       reinterpret_cast<__nv_bfloat16 *>(prep_smem));
         return;
     }
     const int r = static_cast<int>(blockIdx.x / p.segs);
     const int seg = static_cast<int>(blockIdx.x % p.segs);
-    // the segment's P' first: its loads are in flight while the row's lse is formed
     const int nvec = (m.V + 7) >> 3;
-    const int v0 = seg * PREP_VEC_PER_CTA + threadIdx.x;
+    const int v0 = seg * PREP_VEC_PER_CTA;
+    const int nv = min(PREP_VEC_PER_CTA, nvec - v0);      // > 0: segs covers nvec exactly
     uint4 *row = reinterpret_cast<uint4 *>(m.G + static_cast<size_t>(r) * p.ldg);
-    uint4 u[PREP_VPT];
-#pragma unroll
-    for (int i = 0; i < PREP_VPT; ++i) {
-        const int v = v0 + i * MERGE_THREADS;
-        if (v < nvec) u[i] = row[v];
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        mbar_init(&seg_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive_expect_tx(&seg_bar, static_cast<uint32_t>(nv) * 16u);
+        bulk_copy_to_smem(smem_u32(prep_smem), row + v0, static_cast<uint32_t>(nv) * 16u,
+                          smem_u32(&seg_bar));
     }
+    // (row_lse's block barriers also order the barrier's initialisation before the waits)
     const float2 *parts = m.parts + static_cast<size_t>(r) * m.nparts;
     const float lse = row_lse(parts, m.nparts, s_red, &s_bcast);
     const int grow = m.row0 + r;
@@ -348,15 +369,22 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_prep_kernel(const PrepParam
                                         y_ok, m.f16);
     const float lse2 = lse * LOG2E_F;
     const int ycol = y_ok ? static_cast<int>(yv) : -1;
-#pragma unroll
-    for (int i = 0; i < PREP_VPT; ++i) {
-        const int v = v0 + i * MERGE_THREADS;
-        if (v >= nvec) continue;
-        const int c = v * 8;
+    const Abort ab{&s_abort, const_cast<int *>(m.hdr), PREP_WAIT_NS};
+    if (!mbar_wait(&seg_bar, 0, ab)) {
+        // the copy did not complete in time (recorded as a timeout): let it finish
+        // (bounded) before the CTA's shared memory is released
+        mbar_wait_drain(&seg_bar, 0, PREP_WAIT_NS);
+        return;
+    }
+    const uint4 *sv = reinterpret_cast<const uint4 *>(prep_smem);
+#pragma unroll 4
+    for (int v = threadIdx.x; v < nv; v += MERGE_THREADS) {
+        uint4 u = sv[v];
+        const int c = (v0 + v) * 8;
         const float f = scale != 0.f
                             ? exp2f(fmaf(parts[c >> 7].x, LOG2E_F, -lse2)) * scale
                             : 0.f;
-        uint32_t *wv = reinterpret_cast<uint32_t *>(&u[i]);
+        uint32_t *wv = reinterpret_cast<uint32_t *>(&u);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             float2 x;
@@ -374,7 +402,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_prep_kernel(const PrepParam
                 wv[q] = *reinterpret_cast<uint32_t *>(&h);
             }
         }
-        row[v] = u[i];
+        row[v0 + v] = u;
     }
 }
 
@@ -513,7 +541,7 @@ cudaError_t launch_prep(const PrepParams &p, cudaStream_t s) {
     const long long grid = row_ctas + tt;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffll) return cudaErrorInvalidValue;
-    lce_prep_kernel<<<static_cast<unsigned>(grid), MERGE_THREADS, 0, s>>>(p);
+    lce_prep_kernel<<<static_cast<unsigned>(grid), MERGE_THREADS, PREP_SEG_BYTES, s>>>(p);
     return cudaGetLastError();
 }
 
