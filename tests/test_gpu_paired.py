@@ -34,6 +34,9 @@ CASES = [
     (1536, 256, 40000, 256, 30),     # three full pairs, wide vocabulary
     (129, 64, 257, 64, 5),           # a pair and a last chunk of one row
     (500, 64, 1000, 100, 9),         # chunk not a multiple of 8: one buffer, no pairs
+    (40, 8, 300, 8, 3),              # chunks of 8 rows (the second chunk's H^T from column 8), D = 8
+    (100, 64, 513, 16, 5),           # chunks of 16: a pair's dW contraction in one k block
+    (4096, 1024, 32000, 1024, 100),  # four full chunks, two pairs, no ignored-row edge
 ]
 
 
