@@ -333,7 +333,14 @@ def run_ours(args, wl, chunk):
     nchunks = (N + chunk - 1) // chunk
     cdv = float(D) * V * N / nchunks
     overlapped = phase_n > 0
-    if overlapped:
+    if frozen and dh_n > 0:
+        # W frozen, two chunk buffers: chunk k's dH GEMM with chunk k+1's logits GEMM
+        # on the pairs it leaves free (4*C*D*V: 2 each)
+        dom_ms, dom_n, dom_flops = dh_ms, dh_n, 4.0 * cdv
+        dom_name = ("W frozen: lce_gemm_kernel<MODE_DH> (dH tiles of chunk k, 512 wide, split along "
+                    "the vocabulary) beside lce_gemm_kernel<MODE_LSE_P> (logits tiles of chunk k+1: "
+                    "one grid on the pairs the dH kernel leaves free, one behind it)")
+    elif overlapped:
         dom_ms, dom_n, dom_flops = phase_ms, phase_n, 6.0 * cdv
         dom_name = ("gradient phase of the second chunk of a pair: lce_gemm_kernel<MODE_DH> (its "
                     "dH tiles, 512 wide) beside lce_gemm_kernel<MODE_BWD> (the dW tiles of both "

@@ -146,7 +146,9 @@ bool make_layout(long long N, long long D, long long V, long long chunk, Layout 
     // array (2 * C * ldg bytes each, a multiple of 512), and the second chunk's
     // columns of H^T start at column C, which the transpose's 16-byte stores need to
     // be a multiple of 8.
-    L.nbuf = (!frozen_w && !low_mem && L.nchunks > 1 && L.C % 8 == 0) ? 2 : 1;
+    // With W frozen there is no dW contraction; two buffers then let a chunk's
+    // logits GEMM run on the CTA pairs its predecessor's dH GEMM leaves free.
+    L.nbuf = (!low_mem && L.nchunks > 1 && (frozen_w || L.C % 8 == 0)) ? 2 : 1;
     L.gbuf_bytes = 2 * static_cast<size_t>(L.C) * L.ldg;
     off += align_up(static_cast<size_t>(L.nbuf) * L.gbuf_bytes, 1024);
     // H chunk^T [D][ldt]: the K-major B operand of the dW contraction (none when W
@@ -575,8 +577,8 @@ lce_status run_bwd(const Ctx &c, long long row0, long long rows, int slot, const
     // profiling kind: a pair's second chunk (its dH with both chunks' dW), a pair's
     // first chunk (its dH alone), or a chunk's whole gradient phase
     const int kind = (with_dw && g.dw_rows > rows) ? LCE_KERNEL_PHASE
-                     : (!with_dw && !c.L.frozen_w) ? LCE_KERNEL_DH
-                                                   : LCE_KERNEL_GRAD;
+                     : (!with_dw && (!c.L.frozen_w || g.beside)) ? LCE_KERNEL_DH
+                                                                 : LCE_KERNEL_GRAD;
     if (cl == 2) {
         // CTA pairs: the dH tiles run 512 columns wide (two MMAs share each A
         // block: a quarter fewer operand bytes per flop) in one kernel with one
@@ -775,6 +777,12 @@ inline bool paired(const Ctx &c) {
     return c.pairs > 0 && !c.L.frozen_w && c.L.nbuf == 2 && !c.h_chunked;
 }
 
+// W frozen with two chunk buffers: chunk k+1's logits tiles run on the CTA pairs
+// chunk k's dH tiles leave free (chunk k in buffer k % 2).
+inline bool frozen_overlapped(const Ctx &c) {
+    return c.pairs > 0 && c.L.frozen_w && c.L.nbuf == 2 && !c.h_chunked;
+}
+
 }  // namespace
 
 extern "C" {
@@ -896,6 +904,22 @@ lce_status lce_backward_opt(const void *H, const void *W, const int64_t *y, cons
     }
     const bool acc_dw0 = (flags & LCE_ACCUMULATE_DW) != 0;
     __nv_bfloat16 *dHb = static_cast<__nv_bfloat16 *>(dH);
+    if (frozen_overlapped(c)) {
+        LCE_TRY(run_logits(c, MODE_G, 0, chunk_rows(c, 0), 0, lse, dloss, c.Gb[0]));
+        for (long long k = 0; k < c.L.nchunks; ++k) {
+            const long long r0 = k * c.L.C, n0 = chunk_rows(c, k);
+            GradSpec g{c.Gb[k & 1], c.Gb[k & 1], 0, true, true};
+            LogitsSpec next{};
+            if (k + 1 < c.L.nchunks) {
+                next = LogitsSpec{MODE_G, r0 + c.L.C, chunk_rows(c, k + 1),
+                                  static_cast<int>(2 * k + 2), lse, dloss, c.Gb[(k + 1) & 1]};
+                g.beside = &next;
+            }
+            LCE_TRY(run_grad(c, r0, n0, static_cast<int>(2 * k + 1), dHb + r0 * c.D, acc_dh, dW,
+                             false, dloss, g));
+        }
+        return LCE_OK;
+    }
     if (paired(c)) {
         // chunks in pairs (a, b): a's G (G epilogue) into buffer 0, its H^T into
         // columns 0..C-1; a's dH tiles, with b's logits (G into buffer 1) on the pairs
@@ -994,7 +1018,27 @@ lce_status fwd_bwd_impl(const void *H, const void *W, const int64_t *y, const fl
     }
     const bool acc_dw0 = (flags & LCE_ACCUMULATE_DW) != 0;
     __nv_bfloat16 *dHb = static_cast<__nv_bfloat16 *>(dH);
-    if (paired(c)) {
+    if (frozen_overlapped(c)) {
+        // chunk k's dH tiles, with chunk k+1's logits (P' into buffer (k+1) % 2) on
+        // the pairs they leave free; then chunk k+1's prep (no H^T: no dW)
+        LCE_TRY(run_logits(c, MODE_LSE_P, 0, chunk_rows(c, 0), 0, nullptr, nullptr, c.Gb[0]));
+        LCE_TRY(run_prep(c, 0, chunk_rows(c, 0), lse, dloss, rows_out, c.Gb[0], false));
+        for (long long k = 0; k < c.L.nchunks; ++k) {
+            const long long r0 = k * c.L.C, n0 = chunk_rows(c, k);
+            GradSpec g{c.Gb[k & 1], c.Gb[k & 1], 0, true, true};
+            LogitsSpec next{};
+            if (k + 1 < c.L.nchunks) {
+                next = LogitsSpec{MODE_LSE_P, r0 + c.L.C, chunk_rows(c, k + 1),
+                                  static_cast<int>(2 * k + 2), nullptr, nullptr, c.Gb[(k + 1) & 1]};
+                g.beside = &next;
+            }
+            LCE_TRY(run_grad(c, r0, n0, static_cast<int>(2 * k + 1), dHb + r0 * c.D, acc_dh, dW,
+                             false, dloss, g));
+            if (k + 1 < c.L.nchunks)
+                LCE_TRY(run_prep(c, r0 + c.L.C, chunk_rows(c, k + 1), lse, dloss, rows_out,
+                                 c.Gb[(k + 1) & 1], false));
+        }
+    } else if (paired(c)) {
         // chunks in pairs (a, b): a's P' into buffer 0, its prep (lse, row losses,
         // P' -> G, H^T into columns 0..C-1); a's dH tiles, with b's logits (P' into
         // buffer 1) on the pairs they leave free; b's prep (H^T into columns C..), then

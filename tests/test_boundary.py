@@ -315,15 +315,19 @@ def test_dh_vocabulary_split_workspace(L):
 def test_frozen_w_flag(L):
     """LCE_FROZEN_W (8): no dW contraction. Its workspace drops the H chunk^T and
     splits the dH tiles for the whole GPU (one wave of 76 CTA pairs: 32 tiles of
-    a Llama-3 chunk -> 2 vocabulary parts); dW may be NULL; it does not combine
-    with accumulating into dW."""
+    a Llama-3 chunk -> 2 vocabulary parts), and keeps two chunk buffers (the next
+    chunk's logits beside a chunk's dH; one with LCE_LOW_MEMORY); dW may be NULL;
+    it does not combine with accumulating into dW."""
     N, D, V, chunk = 16384, 4096, 128256, 1024
-    base = ws_size_low(L, N, D, V, chunk)    # frozen W keeps one chunk buffer
+    base = ws_size_low(L, N, D, V, chunk)    # one chunk buffer, H^T, no dH parts
+    gbuf = 2 * chunk * (-(-V // 256) * 256)
     out = ctypes.c_size_t(0)
     assert L.lce_workspace_size_opt(N, D, V, chunk, 8, ctypes.byref(out)) == OK
-    assert out.value == base - 2 * D * chunk + 2 * 4 * chunk * D
+    assert out.value == base - 2 * D * chunk + 2 * 4 * chunk * D + gbuf
     assert L.lce_workspace_size_opt(N, D, V, chunk, 8 | 2, ctypes.byref(out)) == OK
-    assert out.value == base - 2 * D * chunk + 2 * 4 * chunk * D   # the parts serve dH += too
+    assert out.value == base - 2 * D * chunk + 2 * 4 * chunk * D + gbuf   # the parts serve dH += too
+    assert L.lce_workspace_size_opt(N, D, V, chunk, 8 | 16, ctypes.byref(out)) == OK
+    assert out.value == base - 2 * D * chunk + 2 * 4 * chunk * D
     vp = ctypes.c_void_p
     n, d, v, c = 128, 64, 1000, 64
     assert L.lce_workspace_size_opt(n, d, v, c, 8, ctypes.byref(out)) == OK
