@@ -266,22 +266,25 @@ lce_status lce_rmsnorm_backward(const void *X, const void *gamma, const void *dH
 /* RMSNorm + LM head + cross-entropy, forward and backward in one call: the
  * chunked path of lce_fwd_bwd_ex applied to H = RMSNorm(X), returning the
  * gradients of the pre-norm X and of gamma instead of dH. Per chunk the rows
- * are normalised into a chunk-sized buffer, the chunk's dH is kept in fp32 and
- * fed to the RMSNorm backward at once, so neither H nor dH exists for all N
- * rows. Outputs: loss and lse as for lce_fwd_bwd_ex (reduction MEAN / SUM /
- * NONE), dX [N][D] bf16, dgamma [D] fp32, dW [V][D] fp32 (overwritten). The
- * workspace is lce_norm_workspace_size(N, D, V, chunk) bytes: that of
- * lce_workspace_size plus the chunk's H (bf16) and dH (fp32) and the dgamma
- * partials. Device status as for lce_fwd_bwd. */
+ * are normalised into a buffer of one chunk's rows (of a pair's, when the chunks
+ * go in pairs as on the loss path), the chunk's dH is kept in fp32 and fed to the
+ * RMSNorm backward at once, so neither H nor dH exists for all N rows. Outputs:
+ * loss and lse as for lce_fwd_bwd_ex (reduction MEAN / SUM / NONE), dX [N][D]
+ * bf16, dgamma [D] fp32, dW [V][D] fp32 (overwritten). The workspace is
+ * lce_norm_workspace_size(N, D, V, chunk) bytes: that of lce_workspace_size plus
+ * the normalised rows (bf16), the chunk's fp32 dH where the loss path's
+ * workspace holds none, and the dgamma partials. Device status as for
+ * lce_fwd_bwd. */
 lce_status lce_norm_workspace_size(int64_t N, int64_t D, int64_t V, int64_t chunk, size_t *bytes);
 lce_status lce_norm_fwd_bwd(const void *X, const void *gamma, float eps, const void *W,
                             const int64_t *y, const float *dloss, int64_t N, int64_t D, int64_t V,
                             int64_t ignore_index, int64_t chunk, int reduction, float *loss,
                             float *lse, void *dX, float *dgamma, float *dW, void *ws,
                             size_t ws_bytes, lce_stream_t stream);
-/* The same with option flags: 0 or LCE_FROZEN_W (a frozen LM head: dW is not
- * computed and may be NULL; dX and dgamma as above). The workspace is
- * lce_norm_workspace_size_opt(..., flags) bytes; lce_norm_workspace_size and
+/* The same with option flags: LCE_FROZEN_W (a frozen LM head: dW is not
+ * computed and may be NULL; dX and dgamma as above; one chunk buffer) and
+ * LCE_LOW_MEMORY (one chunk buffer, one dW contraction per chunk). The workspace
+ * is lce_norm_workspace_size_opt(..., flags) bytes; lce_norm_workspace_size and
  * lce_norm_fwd_bwd are these with flags = 0. Other flags: LCE_ERR_INVALID_ARG. */
 lce_status lce_norm_workspace_size_opt(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
                                        size_t *bytes);

@@ -460,10 +460,10 @@ def norm_workspace_size(N: int, D: int, V: int, chunk: int, flags: int = 0) -> i
 
 def norm_fwd_bwd(X, gamma, W, y, eps: float = 1e-6, dloss=None, chunk: int = 1024,
                  ignore_index: int = IGNORE_INDEX, reduction: str = "mean", ws=None, loss=None,
-                 lse=None, stream=None, compute_dW: bool = True):
+                 lse=None, stream=None, compute_dW: bool = True, low_memory: bool = False):
     """RMSNorm + LM head + cross-entropy, forward and backward in one call:
     (loss, lse, dX bf16, dgamma fp32, dW fp32). compute_dW=False: W is frozen and
-    dW is None."""
+    dW is None. low_memory: one chunk buffer (LCE_LOW_MEMORY)."""
     _check_norm_inputs(X, gamma)
     _check_inputs(X, W, y)
     N, D = X.shape
@@ -475,7 +475,7 @@ def norm_fwd_bwd(X, gamma, W, y, eps: float = 1e-6, dloss=None, chunk: int = 102
         lse = torch.empty(N, dtype=torch.float32, device=dev)
     dX = torch.empty_like(X)
     dgamma = torch.empty(D, dtype=torch.float32, device=dev)
-    flags = 0 if compute_dW else FROZEN_W
+    flags = (0 if compute_dW else FROZEN_W) | (LOW_MEMORY if low_memory else 0)
     dW = torch.empty(V, D, dtype=torch.float32, device=dev) if compute_dW else None
     if ws is None:
         ws = torch.empty(norm_workspace_size(N, D, V, chunk, flags), dtype=torch.uint8, device=dev)

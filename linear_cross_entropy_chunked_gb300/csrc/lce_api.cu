@@ -189,14 +189,16 @@ size_t acc_dh_bytes(const Layout &L, long long D) {
 }
 
 bool make_norm_layout(long long N, long long D, long long V, long long chunk, NormLayout &NL,
-                      bool frozen_w = false) {
-    if (!make_layout(N, D, V, chunk, NL.L, frozen_w, true)) return false;
+                      bool frozen_w = false, bool low_mem = false) {
+    // W trained: chunk pairs with one dW contraction each, as on the loss path; W
+    // frozen: one chunk buffer
+    if (!make_layout(N, D, V, chunk, NL.L, frozen_w, low_mem || frozen_w)) return false;
     if (D > NRM_MAX_D) return false;
     // the chunk's dH (fp32): the layout's partial arrays, or one array past them
     NL.off_dH = NL.L.off_dHp;
     size_t off = NL.L.total + acc_dh_bytes(NL.L, D);
-    NL.off_H = off;
-    off += align_up(2 * static_cast<size_t>(NL.L.C) * D, 1024);
+    NL.off_H = off;   // the normalised rows of a chunk (of a pair of chunks with two buffers)
+    off += align_up(2 * static_cast<size_t>(NL.L.nbuf) * NL.L.C * D, 1024);
     NL.off_part = off;
     off += align_up(4 * static_cast<size_t>(NRM_GRID) * D, 1024);
     NL.total = off;
@@ -265,12 +267,18 @@ struct Ctx {
     int sms;
     int pairs;   // > 0: GEMMs run as CTA pairs (cluster of 2), at most this many at once
     int reduction;       // LCE_REDUCTION_*
-    bool h_chunked;      // H is a chunk-sized buffer (rows 0..C-1), refilled per chunk
+    bool h_chunked;      // H is a buffer of one chunk's rows (of a pair's with two chunk
+                         // buffers: chunk k at rows (k mod 2) * C), refilled per chunk
     bool f16;            // H, W, G and dH are fp16 (bf16 otherwise)
     MapType t16;         // the 16-bit map type of this call
     cudaStream_t s;
     CUtensorMap tmH_K, tmW_K, tmW_MN;
 };
+
+// Row of H (c.H) where the chunk starting at row0 begins.
+inline long long h_row(const Ctx &c, long long row0) {
+    return c.h_chunked ? ((row0 / c.L.C) % c.L.nbuf) * c.L.C : row0;
+}
 
 // ---- optional per-kernel event timing (lce_profile_*)
 struct ProfPair {
@@ -390,7 +398,7 @@ lce_status setup(Ctx &c, const void *H, const void *W, const int64_t *y, int64_t
     // pair MMA reads both CTAs' halves from their shared memory
     if (!encode_2d(&c.tmW_K, W, D, V, D * 2, BK, c.pairs > 0 ? BN / 2 : BN, c.t16)) return LCE_ERR_CUDA;
     if (!encode_2d(&c.tmW_MN, W, D, V, D * 2, 64, BK, c.t16)) return LCE_ERR_CUDA;
-    if (N > 0 && !encode_2d(&c.tmH_K, H, D, h_chunked ? c.L.C : N, D * 2, BK, BM, c.t16))
+    if (N > 0 && !encode_2d(&c.tmH_K, H, D, h_chunked ? c.L.C * c.L.nbuf : N, D * 2, BK, BM, c.t16))
         return LCE_ERR_CUDA;
     if (cudaMemsetAsync(c.ws, 0, c.L.hdr_bytes, c.s) != cudaSuccess) return LCE_ERR_CUDA;
     LCE_LAUNCH(launch_label_scan(c.y, N, V, ign, c.hdr, c.s));
@@ -432,7 +440,7 @@ lce_status logits_params(const Ctx &c, const LogitsSpec &l, GemmParams &p) {
     memset(&p, 0, sizeof(p));
     base_params(c, p, l.row0, l.rows, l.slot);
     p.tmA0 = c.tmH_K;
-    p.a_row0 = c.h_chunked ? 0 : static_cast<int>(l.row0);
+    p.a_row0 = static_cast<int>(h_row(c, l.row0));
     p.tmB0 = c.tmW_K;
     p.m_blocks0 = static_cast<int>(cdiv(l.rows, BM));
     p.n_blocks0 = static_cast<int>(cdiv(c.V, BN));
@@ -488,7 +496,7 @@ int dh_parts(const Ctx &c, long long rows, bool alone) {
 // H chunk^T into columns col0 .. col0 + rows - 1 of H^T (the K-major B operand of
 // the dW tiles; col0 = C for the second chunk of a pair).
 lce_status run_transpose(const Ctx &c, long long row0, long long rows, long long col0) {
-    const __nv_bfloat16 *Hc = c.h_chunked ? c.H : c.H + row0 * c.D;
+    const __nv_bfloat16 *Hc = c.H + h_row(c, row0) * c.D;
     TransposeParams tp;
     tp.src = Hc;
     tp.ld_src = static_cast<int>(c.D);
@@ -753,7 +761,7 @@ lce_status run_prep(const Ctx &c, long long row0, long long rows, float *lse,
     pp.ldg = c.L.ldg;
     pp.segs = static_cast<int>(cdiv(cdiv(c.V, 8), PREP_VEC_PER_CTA));
     if (transpose) {
-        pp.tp.src = c.h_chunked ? c.H : c.H + row0 * c.D;
+        pp.tp.src = c.H + h_row(c, row0) * c.D;
         pp.tp.ld_src = static_cast<int>(c.D);
         pp.tp.dst_t = c.HT + ht_col0;
         pp.tp.ld_t = c.L.ldt;
@@ -773,8 +781,8 @@ inline long long chunk_rows(const Ctx &c, long long k) {
 
 // Whether chunks are taken in pairs with one dW contraction per pair: CTA pairs,
 // a dW contraction, two chunk buffers (so more than one chunk), H in place.
-inline bool paired(const Ctx &c) {
-    return c.pairs > 0 && !c.L.frozen_w && c.L.nbuf == 2 && !c.h_chunked;
+inline bool paired(const Ctx &c, bool h_chunked_ok = false) {
+    return c.pairs > 0 && !c.L.frozen_w && c.L.nbuf == 2 && (h_chunked_ok || !c.h_chunked);
 }
 
 // W frozen with two chunk buffers: chunk k+1's logits tiles run on the CTA pairs
@@ -1191,9 +1199,11 @@ lce_status lce_rmsnorm_backward(const void *X, const void *gamma, const void *dH
 
 lce_status lce_norm_workspace_size_opt(int64_t N, int64_t D, int64_t V, int64_t chunk, int flags,
                                        size_t *bytes) {
-    if (!bytes || (flags & ~LCE_FROZEN_W)) return LCE_ERR_INVALID_ARG;
+    if (!bytes || (flags & ~(LCE_FROZEN_W | LCE_LOW_MEMORY))) return LCE_ERR_INVALID_ARG;
     NormLayout NL;
-    if (!make_norm_layout(N, D, V, chunk, NL, flags != 0)) return LCE_ERR_INVALID_ARG;
+    if (!make_norm_layout(N, D, V, chunk, NL, (flags & LCE_FROZEN_W) != 0,
+                          (flags & LCE_LOW_MEMORY) != 0))
+        return LCE_ERR_INVALID_ARG;
     *bytes = NL.total;
     return LCE_OK;
 }
@@ -1209,11 +1219,13 @@ lce_status lce_norm_fwd_bwd_opt(const void *X, const void *gamma, float eps, con
                                 float *dW, void *ws, size_t ws_bytes, lce_stream_t stream) {
     g_launches = 0;
     if (reduction < LCE_REDUCTION_MEAN || reduction > LCE_REDUCTION_NONE) return LCE_ERR_INVALID_ARG;
-    if (flags & ~LCE_FROZEN_W) return LCE_ERR_INVALID_ARG;
-    const bool frozen = flags != 0;
+    if (flags & ~(LCE_FROZEN_W | LCE_LOW_MEMORY)) return LCE_ERR_INVALID_ARG;
+    const bool frozen = (flags & LCE_FROZEN_W) != 0;
+    const bool low_mem = (flags & LCE_LOW_MEMORY) != 0;
     const bool none = reduction == LCE_REDUCTION_NONE;
     NormLayout NL;
-    if (!make_norm_layout(N, D, V, chunk, NL, frozen) || !(eps >= 0.f)) return LCE_ERR_INVALID_ARG;
+    if (!make_norm_layout(N, D, V, chunk, NL, frozen, low_mem) || !(eps >= 0.f))
+        return LCE_ERR_INVALID_ARG;
     if (!gamma || !dgamma || (!frozen && !dW) || (!none && !loss) ||
         (N > 0 && (!X || !lse || !dX || !loss)))
         return LCE_ERR_INVALID_ARG;
@@ -1228,9 +1240,8 @@ lce_status lce_norm_fwd_bwd_opt(const void *X, const void *gamma, float eps, con
     float *dHbuf = reinterpret_cast<float *>(w + NL.off_dH);
     float *part = reinterpret_cast<float *>(w + NL.off_part);
     Ctx c;
-    // one chunk buffer: the chunks of this path run one after the other
     LCE_TRY(setup(c, Hbuf, W, y, N, D, V, ignore_index, chunk, ws, ws_bytes, stream, true, false,
-                  frozen, false, true));
+                  frozen, false, low_mem || frozen));
     c.reduction = reduction;
     float *rows_out = none ? loss : c.loss_rows;
     if (c.L.nchunks == 0) {
@@ -1241,34 +1252,89 @@ lce_status lce_norm_fwd_bwd_opt(const void *X, const void *gamma, float eps, con
     }
     const __nv_bfloat16 *Xb = static_cast<const __nv_bfloat16 *>(X);
     __nv_bfloat16 *dXb = static_cast<__nv_bfloat16 *>(dX);
-    for (long long k = 0; k < c.L.nchunks; ++k) {
-        const long long row0 = k * c.L.C;
-        const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
+    const __nv_bfloat16 *gam = static_cast<const __nv_bfloat16 *>(gamma);
+    // RMSNorm forward of rows [row0, row0 + rows) into their place in the H buffer
+    auto norm_fwd = [&](long long row0, long long rows) -> lce_status {
         NormParams np;
         memset(&np, 0, sizeof(np));
         np.X = Xb + row0 * c.D;
-        np.gamma = static_cast<const __nv_bfloat16 *>(gamma);
-        np.H = Hbuf;
+        np.gamma = gam;
+        np.H = Hbuf + h_row(c, row0) * c.D;
         np.rows = rows;
         np.D = static_cast<int>(c.D);
         np.eps = eps;
         LCE_LAUNCH_KIND(LCE_KERNEL_NORM, c.s, launch_rmsnorm_fwd(np, c.s));
-        LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr,
-                           c.Gb[0]));
-        LCE_TRY(run_prep(c, row0, rows, lse, dloss, rows_out, c.Gb[0], !frozen));
-        int parts = 1;
-        LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1),
-                        DhOut{dHbuf, true, dh_parts(c, rows, false), c.L.ldp}, dW, k > 0, dloss,
-                        GradSpec{c.Gb[0], c.Gb[0], frozen ? 0 : rows, true, false}, &parts));
-        np.H = nullptr;
+        return LCE_OK;
+    };
+    // RMSNorm backward of a chunk from its fp32 dH (the sum of `parts` arrays)
+    auto norm_bwd = [&](long long row0, long long rows, int parts) -> lce_status {
+        NormParams np;
+        memset(&np, 0, sizeof(np));
+        np.X = Xb + row0 * c.D;
+        np.gamma = gam;
+        np.rows = rows;
+        np.D = static_cast<int>(c.D);
+        np.eps = eps;
         np.dH = dHbuf;
         np.dh_fp32 = 1;
         np.dh_splits = parts;
         np.dh_split_stride = c.L.ldp * c.D;
         np.dX = dXb + row0 * c.D;
         np.part = part;
-        np.first = k == 0 ? 1 : 0;
+        np.first = row0 == 0 ? 1 : 0;
         LCE_LAUNCH_KIND(LCE_KERNEL_NORM, c.s, launch_rmsnorm_bwd(np, c.s));
+        return LCE_OK;
+    };
+    if (paired(c, true)) {
+        // chunks in pairs (a, b), as on the loss path: the normalised rows of both
+        // in the H buffer; a's logits, prep, a's dH tiles (fp32, in parts) with b's
+        // logits beside them, a's RMSNorm backward; b's prep, b's dH beside one dW
+        // contraction over both chunks, b's RMSNorm backward
+        for (long long a = 0; a < c.L.nchunks; a += 2) {
+            const long long ra = a * c.L.C, na = chunk_rows(c, a);
+            const bool has_b = a + 1 < c.L.nchunks;
+            const long long b = a + 1, rb = b * c.L.C, nb = has_b ? chunk_rows(c, b) : 0;
+            LCE_TRY(norm_fwd(ra, na + nb));
+            LCE_TRY(run_logits(c, MODE_LSE_P, ra, na, static_cast<int>(2 * a), nullptr, nullptr,
+                               c.Gb[0]));
+            LCE_TRY(run_prep(c, ra, na, lse, dloss, rows_out, c.Gb[0], true, 0));
+            int parts = 1;
+            if (!has_b) {
+                LCE_TRY(run_bwd(c, ra, na, static_cast<int>(2 * a + 1),
+                                DhOut{dHbuf, true, dh_parts(c, na, false), c.L.ldp}, dW, a > 0,
+                                dloss, GradSpec{c.Gb[0], c.Gb[0], na, true, false}, &parts));
+                LCE_TRY(norm_bwd(ra, na, parts));
+                break;
+            }
+            const LogitsSpec lb{MODE_LSE_P, rb, nb, static_cast<int>(2 * b), nullptr, nullptr,
+                                c.Gb[1]};
+            GradSpec ga{c.Gb[0], c.Gb[0], 0, true, true};
+            ga.beside = &lb;
+            LCE_TRY(run_bwd(c, ra, na, static_cast<int>(2 * a + 1),
+                            DhOut{dHbuf, true, dh_parts(c, na, true), c.L.ldp}, dW, false, dloss,
+                            ga, &parts));
+            LCE_TRY(norm_bwd(ra, na, parts));
+            LCE_TRY(run_prep(c, rb, nb, lse, dloss, rows_out, c.Gb[1], true, c.L.C));
+            LCE_TRY(run_bwd(c, rb, nb, static_cast<int>(2 * b + 1),
+                            DhOut{dHbuf, true, dh_parts(c, nb, false), c.L.ldp}, dW, a > 0, dloss,
+                            GradSpec{c.Gb[1], c.Gb[0], c.L.C + nb, true, false}, &parts));
+            LCE_TRY(norm_bwd(rb, nb, parts));
+        }
+    } else {
+        for (long long k = 0; k < c.L.nchunks; ++k) {
+            const long long row0 = k * c.L.C;
+            const long long rows = chunk_rows(c, k);
+            LCE_TRY(norm_fwd(row0, rows));
+            LCE_TRY(run_logits(c, MODE_LSE_P, row0, rows, static_cast<int>(2 * k), nullptr, nullptr,
+                               c.Gb[0]));
+            LCE_TRY(run_prep(c, row0, rows, lse, dloss, rows_out, c.Gb[0], !frozen));
+            int parts = 1;
+            LCE_TRY(run_bwd(c, row0, rows, static_cast<int>(2 * k + 1),
+                            DhOut{dHbuf, true, dh_parts(c, rows, false), c.L.ldp}, dW, k > 0,
+                            dloss, GradSpec{c.Gb[0], c.Gb[0], frozen ? 0 : rows, true, false},
+                            &parts));
+            LCE_TRY(norm_bwd(row0, rows, parts));
+        }
     }
     if (!none)
         LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss,

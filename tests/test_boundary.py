@@ -176,17 +176,20 @@ def ws_size_low(L, N, D, V, chunk):
 
 
 def test_norm_workspace_sizes(L):
-    # the RMSNorm path runs its chunks one after the other: one chunk buffer
     N, D, V, chunk = 16384, 4096, 128256, 1024
-    base = ws_size_low(L, N, D, V, chunk)
     out = ctypes.c_size_t(0)
+    # two chunk buffers (chunk pairs, as on the loss path): the loss path's workspace
+    # (whose dH parts hold the chunk's fp32 dH) + the pair's normalised rows H (bf16)
+    # + 256 dgamma partial rows
     assert L.lce_norm_workspace_size(N, D, V, chunk, ctypes.byref(out)) == OK
-    # the loss path's workspace + the chunk's dH (fp32) and H (bf16) + 256 dgamma
-    # partial rows
+    assert out.value == ws_size(L, N, D, V, chunk)[1] + 2 * 2 * chunk * D + 4 * 256 * D
+    # one chunk buffer (LCE_LOW_MEMORY): the loss path's + the chunk's dH (fp32) and H
+    base = ws_size_low(L, N, D, V, chunk)
+    assert L.lce_norm_workspace_size_opt(N, D, V, chunk, 16, ctypes.byref(out)) == OK
     assert out.value == base + 4 * chunk * D + 2 * chunk * D + 4 * 256 * D
     # two vocabulary parts (chunk 512): the loss path's partial arrays hold dH
     base2 = ws_size_low(L, N, D, V, 512)
-    assert L.lce_norm_workspace_size(N, D, V, 512, ctypes.byref(out)) == OK
+    assert L.lce_norm_workspace_size_opt(N, D, V, 512, 16, ctypes.byref(out)) == OK
     assert out.value == base2 + 2 * 512 * D + 4 * 256 * D
     assert L.lce_norm_workspace_size(N, 8200, V, chunk, ctypes.byref(out)) == INVALID  # D > 8192
     assert L.lce_rmsnorm_backward_workspace_size(D, ctypes.byref(out)) == OK
@@ -359,7 +362,7 @@ def test_norm_opt_flags(L):
     assert L.lce_norm_workspace_size(N, D, V, chunk, ctypes.byref(plain)) == OK
     assert L.lce_norm_workspace_size_opt(N, D, V, chunk, 0, ctypes.byref(out)) == OK
     assert out.value == plain.value
-    for bad in (1, 2, 4, 16):
+    for bad in (1, 2, 4, 32):
         assert L.lce_norm_workspace_size_opt(N, D, V, chunk, bad, ctypes.byref(out)) == INVALID
     assert L.lce_norm_workspace_size_opt(N, D, V, chunk, 8, ctypes.byref(out)) == OK
     # frozen W: no H chunk^T; the two dH parts of the frozen split hold the chunk's dH

@@ -117,23 +117,40 @@ def test_norm_fwd_bwd_llama2_shape(lce):
     check_grad("dW", to64(dW), ref["dW"])
 
 
-def test_norm_fused_equals_composed_calls(lce):
+@pytest.mark.parametrize("low_memory", [False, True])
+def test_norm_fused_equals_composed_calls(lce, low_memory):
     """lce_norm_fwd_bwd against rmsnorm_forward -> lce_fwd_bwd -> rmsnorm_backward
-    on the GPU: the same H and the same one-dW-contraction-per-chunk schedule (the
-    RMSNorm path keeps one chunk buffer, so the composed call takes low_memory), so
-    loss, lse and dW are bit-identical; dX differs only by the bf16 rounding of dH
-    in the composed path."""
+    on the GPU, both with the same schedule (chunk pairs with one dW contraction
+    each, or with low_memory one buffer and one dW contraction per chunk): the same
+    H, so loss, lse and dW are bit-identical; dX differs only by the bf16 rounding
+    of dH in the composed path."""
     N, D, V, chunk = 1500, 1024, 5000, 512
     X, g, W, y = _norm_case(N, D, V, seed=17, n_ign=40)
     Xd, gd, Wd, yd = X.to(DEV), g.to(DEV), W.to(DEV), y.to(DEV)
-    loss, lse, dX, dgamma, dW = lce.norm_fwd_bwd(Xd, gd, Wd, yd, eps=EPS, chunk=chunk)
+    loss, lse, dX, dgamma, dW = lce.norm_fwd_bwd(Xd, gd, Wd, yd, eps=EPS, chunk=chunk,
+                                                 low_memory=low_memory)
     H = lce.rmsnorm_forward(Xd, gd, eps=EPS)
-    loss2, lse2, dH2, dW2 = lce.lce_fwd_bwd(H, Wd, yd, chunk=chunk, low_memory=True)
+    loss2, lse2, dH2, dW2 = lce.lce_fwd_bwd(H, Wd, yd, chunk=chunk, low_memory=low_memory)
     dX2, dgamma2 = lce.rmsnorm_backward(Xd, gd, dH2, eps=EPS)
     torch.cuda.synchronize()
     assert torch.equal(loss, loss2) and torch.equal(lse, lse2) and torch.equal(dW, dW2)
     check_grad("dX (composed)", to64(dX2), to64(dX))
     check_grad("dgamma (composed)", to64(dgamma2), to64(dgamma))
+
+
+@pytest.mark.parametrize("N,D,V,chunk", [(1000, 520, 3000, 384), (1024, 4096, 8000, 256)])
+def test_norm_one_buffer_matches_oracle(lce, N, D, V, chunk):
+    """The RMSNorm path with one chunk buffer (LCE_LOW_MEMORY) against the oracle."""
+    X, g, W, y = _norm_case(N, D, V, seed=N + V + 3, n_ign=N // 20)
+    loss, lse, dX, dgamma, dW = lce.norm_fwd_bwd(X.to(DEV), g.to(DEV), W.to(DEV), y.to(DEV),
+                                                 eps=EPS, chunk=chunk, low_memory=True)
+    torch.cuda.synchronize()
+    ref = O.norm_forward_backward(X, g, EPS, W, y)
+    check_loss(loss.item(), ref["loss"])
+    check_lse(to64(lse), ref["lse"])
+    check_grad("dX", to64(dX), ref["dX"])
+    check_grad("dgamma", to64(dgamma), ref["dgamma"])
+    check_grad("dW", to64(dW), ref["dW"])
 
 
 def test_norm_fwd_bwd_deterministic(lce):
