@@ -708,7 +708,7 @@ lce_status run_grad(const Ctx &c, long long row0, long long rows, int slot, void
     return LCE_OK;
 }
 
-lce_status run_merge(const Ctx &c, bool fused, long long row0, long long rows, float *lse,
+lce_status run_merge(const Ctx &c, long long row0, long long rows, float *lse,
                      const float *dloss, float *loss_rows) {
     MergeParams m;
     m.parts = c.parts;
@@ -728,7 +728,7 @@ lce_status run_merge(const Ctx &c, bool fused, long long row0, long long rows, f
     m.f16 = c.f16 ? 1 : 0;
     m.lse = lse;
     m.loss_rows = loss_rows;
-    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_merge(fused, m, c.s));
+    LCE_LAUNCH_KIND(LCE_KERNEL_MERGE, c.s, launch_merge(m, c.s));
     return LCE_OK;
 }
 
@@ -859,7 +859,7 @@ lce_status lce_forward_opt(const void *H, const void *W, const int64_t *y, int64
         const long long rows = (c.N - row0) < c.L.C ? (c.N - row0) : c.L.C;
         LCE_TRY(run_logits(c, MODE_LSE, row0, rows, static_cast<int>(k), nullptr, nullptr,
                            c.Gb[0]));
-        LCE_TRY(run_merge(c, false, row0, rows, lse, nullptr, rows_out));
+        LCE_TRY(run_merge(c, row0, rows, lse, nullptr, rows_out));
     }
     if (!none)
         LCE_LAUNCH(launch_loss_finalize(c.loss_rows, c.N, c.hdr, loss,

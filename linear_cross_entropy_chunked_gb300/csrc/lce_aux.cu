@@ -1,15 +1,19 @@
 // Bandwidth-bound kernels around the tensor-core GEMMs:
-//   * label scan: N_valid and the out-of-range check;
-//   * slab merge: per row, combine the (max, sumexp) partials of the 128-column
-//     slabs into lse_i = M + log sum_p s_p exp(m_p - M), write the row's loss
-//     lse_i - z_{i,y_i} and (fused path) each slab's factor exp(m_p - lse_i) * scale;
-//   * fix-up (fused path): turn the stored P' = exp(z - m_p) into
-//     G = (P' exp(m_p - lse_i) - 1[j = y_i]) * dloss / N_valid in place;
-//   * transpose of the H chunk (the K-major B operand of the dW contraction)
+//   * label scan: N_valid and the out-of-range check; the valid-row count alone
+//     (for sharded batches) and a given total count put in as the normaliser;
+//   * slab merge (forward): per row, combine the (max, sumexp) partials of the
+//     128-column slabs into lse_i = M + log sum_p s_p exp(m_p - M) and write the
+//     row's loss lse_i - z_{i,y_i};
+//   * prep (fused path, one launch per chunk): the merge's lse and row loss, then
+//     the stored P' = exp(z - m_p) turned into
+//     G = (P' exp(m_p - lse_i) - 1[j = y_i]) * dloss / N_valid in place, and the H
+//     chunk transposed for the dW contraction
 //     ("Unsloth Architecture: Manual Triton Backpropagation, Fused Cross-Entropy,
 //     and 80% VRAM Cut", pillar 1: the loss -z_{i,y_i} + log sum_j e^{z_ij} and
 //     the gradient p_ij - 1[j = y_i]);
-//   * loss finalisation: fixed-order fp64 sum of the per-row losses / N_valid.
+//   * transpose of the H chunk alone (the separate backward);
+//   * loss finalisation: fixed-order fp64 sum of the per-row losses / N_valid;
+//   * dH combination: the fp32 parts of split dH contractions added in order.
 // Every reduction has a fixed order, so results are bit-reproducible.
 // Reductions of the loss: mean (sum / N_valid), sum, or none (the per-row losses
 // are the output; G's rows are then scaled by a per-row dloss).
@@ -146,16 +150,13 @@ __device__ __forceinline__ float row_lse(const float2 *parts, int nparts, float 
     return *s_bcast;
 }
 
-// One CTA per chunk row: lse_i from the slab partials, the row's loss, and
-// (FACTORS) each slab's rescale factor exp(m_p - lse_i) * dloss / N_valid,
-// written over the slab max so the fix-up pass reads one float per slab.
-template <bool FACTORS>
+// Forward: one CTA per chunk row, lse_i from the slab partials and the row's loss.
 __global__ void __launch_bounds__(MERGE_THREADS) lce_merge_kernel(const MergeParams p) {
     __shared__ float s_red[MERGE_THREADS / 32];
     __shared__ float s_bcast;
     const int r = blockIdx.x;          // row within the chunk
     const int t = threadIdx.x;
-    float2 *parts = const_cast<float2 *>(p.parts) + static_cast<size_t>(r) * p.nparts;
+    const float2 *parts = p.parts + static_cast<size_t>(r) * p.nparts;
     const float lse = row_lse(parts, p.nparts, s_red, &s_bcast);
 
     const int grow = p.row0 + r;
@@ -164,55 +165,6 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_merge_kernel(const MergePar
     if (t == 0) {
         p.lse[grow] = lse;
         p.loss_rows[grow] = y_ok ? lse - p.zy[r] : 0.f;
-    }
-    if constexpr (FACTORS) {
-        const float scale = lce_store_scale(p.dloss, p.dloss_per_row, p.mean, p.hdr[HDR_NVALID],
-                                            grow, y_ok, p.f16);
-        const float lse2 = lse * LOG2E_F;
-        for (int i = t; i < p.nparts; i += MERGE_THREADS)
-            parts[i].x = scale != 0.f ? exp2f(fmaf(parts[i].x, LOG2E_F, -lse2)) * scale : 0.f;
-    }
-}
-
-// ------------------------------------------------------------------ fix-up
-// The chunk buffer holds P' = exp(z - m_p) (bf16, or fp16 for fp16 inputs). In
-// place it becomes G = P' * factor_p - 1[j = y_i] * s_i, rounded to the same
-// dtype, with s_i the stored-G row scale (dloss / N_valid for bf16; see
-// lce_store_scale for fp16). Grid: x over 8-column vectors of a row, y over rows.
-
-__global__ void __launch_bounds__(256) lce_fixup_kernel(const FixupParams p) {
-    const int nvec = (p.V + 7) >> 3;
-    const int i = blockIdx.x * 256 + threadIdx.x;
-    if (i >= nvec) return;
-    for (int r = blockIdx.y; r < p.rows; r += gridDim.y) {
-    const long long yv = p.y[p.row0 + r];
-    const bool y_ok = yv != p.ignore_index && yv >= 0 && yv < p.V;
-    const float scale = lce_store_scale(p.dloss, p.dloss_per_row, p.mean, p.hdr[HDR_NVALID],
-                                        p.row0 + r, y_ok, p.f16);
-    const int ycol = y_ok ? static_cast<int>(yv) : -1;
-    const int c = i * 8;
-    const float f = p.parts[static_cast<size_t>(r) * p.nparts + (c >> 7)].x;
-    uint4 *ptr = reinterpret_cast<uint4 *>(p.G + static_cast<size_t>(r) * p.ldg + c);
-    uint4 u = *ptr;
-    uint32_t *wv = reinterpret_cast<uint32_t *>(&u);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        float2 x;
-        if (p.f16) x = __half22float2(*reinterpret_cast<__half2 *>(&wv[q]));
-        else x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&wv[q]));
-        x.x *= f;
-        x.y *= f;
-        if (c + 2 * q == ycol) x.x -= scale;
-        if (c + 2 * q + 1 == ycol) x.y -= scale;
-        if (p.f16) {
-            __half2 h = __floats2half2_rn(x.x, x.y);
-            wv[q] = *reinterpret_cast<uint32_t *>(&h);
-        } else {
-            __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
-            wv[q] = *reinterpret_cast<uint32_t *>(&h);
-        }
-    }
-    *ptr = u;
     }
 }
 
@@ -512,10 +464,9 @@ cudaError_t launch_set_nvalid(const long long *n_total, int *hdr, cudaStream_t s
     return cudaGetLastError();
 }
 
-cudaError_t launch_merge(bool factors, const MergeParams &p, cudaStream_t s) {
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t s) {
     if (p.rows <= 0) return cudaSuccess;
-    if (factors) lce_merge_kernel<true><<<p.rows, MERGE_THREADS, 0, s>>>(p);
-    else lce_merge_kernel<false><<<p.rows, MERGE_THREADS, 0, s>>>(p);
+    lce_merge_kernel<<<p.rows, MERGE_THREADS, 0, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -526,13 +477,6 @@ cudaError_t launch_transpose(const TransposeParams &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_fixup(const FixupParams &p, cudaStream_t s) {
-    if (p.rows <= 0) return cudaSuccess;
-    const int nvec = (p.V + 7) / 8;
-    const dim3 grid((nvec + 255) / 256, p.rows < 65535 ? p.rows : 65535);
-    lce_fixup_kernel<<<grid, 256, 0, s>>>(p);
-    return cudaGetLastError();
-}
 
 cudaError_t launch_prep(const PrepParams &p, cudaStream_t s) {
     const long long row_ctas = static_cast<long long>(p.m.rows) * p.segs;

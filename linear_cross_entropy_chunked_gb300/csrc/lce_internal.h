@@ -151,7 +151,7 @@ struct GemmParams {
 };
 
 struct MergeParams {
-    const float2 *parts;   // written in place (slab factors) by the FACTORS variant
+    const float2 *parts;   // [rows][nparts] (max, sumexp) per 128-column slab
     int nparts;
     const float *zy;
     __nv_bfloat16 *G;
@@ -176,21 +176,6 @@ struct TransposeParams {
     int rows, cols;
 };
 
-struct FixupParams {
-    __nv_bfloat16 *G;           // [rows][ldg]: P' in, G out (in place)
-    int ldg;
-    int rows, V;
-    const float2 *parts;        // .x = slab factor exp(m_p - lse) * dloss / N_valid
-    int nparts;
-    const long long *y;
-    int row0;
-    long long ignore_index;
-    const int *hdr;
-    const float *dloss;
-    int dloss_per_row;
-    int mean;
-    int f16;                    // fp16 P' / G (scale from lce_store_scale)
-};
 
 // The step between a chunk's logits GEMM and its gradient GEMMs on the fused
 // path, one launch: for each row, lse from the slab partials, the row's loss,
@@ -263,9 +248,8 @@ cudaError_t launch_count_valid(const long long *y, long long N, long long V, lon
                                long long *out, cudaStream_t s);
 // hdr[HDR_NVALID] = *n_total (device int64), for a mean over several shards' rows
 cudaError_t launch_set_nvalid(const long long *n_total, int *hdr, cudaStream_t s);
-cudaError_t launch_merge(bool factors, const MergeParams &p, cudaStream_t s);
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t s);
 cudaError_t launch_transpose(const TransposeParams &p, cudaStream_t s);
-cudaError_t launch_fixup(const FixupParams &p, cudaStream_t s);
 cudaError_t launch_prep(const PrepParams &p, cudaStream_t s);
 cudaError_t launch_loss_finalize(const float *loss_rows, long long N, const int *hdr,
                                  float *loss, int mean, cudaStream_t s);
