@@ -460,8 +460,9 @@ def run_ours(args, wl, chunk):
             },
             "alg_bytes_per_step": alg_bytes_step,
             "epilogue": {"bytes_per_step": epi_bytes,
-                         "what": "P' stored by the logits epilogue, read and rewritten as G by the "
-                                 "fix-up; slab (max, sum) partials and factors; target logits, lse",
+                         "what": "P' stored by the logits epilogue, read and rewritten in place "
+                                 "as G by the prep kernel; slab (max, sum) partials written and "
+                                 "read; target logits, lse, row losses",
                          "aux_kernels_ms_per_step": merge_ms_step,
                          "aux_kernels": "one prep launch per chunk: lse and row losses from the "
                                         "slab partials, P' -> G in place, H chunk transpose (the "
