@@ -352,10 +352,10 @@ void lce_profile_reset(void);
  *  - Sizes whose lce_forward_workspace_size() exceeds 64 MiB return
  *    LCE_ERR_WORKSPACE before anything is enqueued; a smaller chunk may fit
  *    (the Llama-3-sized head, N = 16384, V = 128256, needs ~8.3 MB at chunk 1024).
- *  - The first call on a device looks up the array's device address (one
- *    cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture. A device reset (cudaDeviceReset) invalidates
- *    that address: do not use this entry point across one in the same process.
+ *  - Every call looks up the array's address on the current device (one
+ *    cudaGetSymbolAddress, a host-side lookup), so a device reset leaves no
+ *    stale address behind. The first lookup on a device may load the library's
+ *    device code: make the first call before any stream capture.
  *  - Every call shares the array, which keeps the last call's contents; each
  *    call clears what must start at zero on its stream. Calls that overlap on
  *    the GPU race on the array: order them on one stream.

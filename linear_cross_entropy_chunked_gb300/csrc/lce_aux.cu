@@ -220,9 +220,9 @@ __global__ void __launch_bounds__(256) lce_transpose_kernel(const TransposeParam
 // path in one launch. CTAs [0, rows * segs): row r = b / segs, segment b % segs
 // of PREP_VEC_PER_CTA 8-column vectors: the row's lse from its slab partials
 // (row_lse, the merge's arithmetic), then P' = exp(z - m_p) -> G = P' * exp(m_p -
-// lse) * s - 1[j = y] * s in place, s the stored-G row scale (the fix-up's
-// arithmetic, with the slab factor formed where it is used instead of stored);
-// segment 0 writes lse and the row loss. The CTAs after those transpose 64 x 64
+// lse) * s - 1[j = y] * s in place, s the stored-G row scale, each slab's factor
+// exp(m_p - lse) * s formed where it is used; segment 0 writes lse and the row
+// loss. The CTAs after those transpose 64 x 64
 // tiles of the H chunk (lce_transpose_kernel's arithmetic) for the dW contraction.
 static_assert(PREP_THREADS == MERGE_THREADS, "the prep kernel computes lse as the merge does");
 

@@ -21,13 +21,11 @@
 //    contents do no harm to calls that are ordered one after the other. Calls
 //    that overlap on the GPU (on different streams or devices sharing nothing
 //    but this array on one device) race on it and give wrong results;
-//  * the array's device address is looked up once per device; a reset of the
-//    device (cudaDeviceReset) unloads the library's module and invalidates it,
-//    so the entry point is not for use across such a reset in one process;
+//  * the array's device address is looked up on every call (a host-side
+//    lookup that allocates nothing), so a reset of the device, after which the
+//    module may load at another address, leaves no stale pointer behind;
 //  * device-side status (labels out of range, a bounded wait that ran out) is
 //    recorded in the array's header and read by lce_noalloc_read_status().
-#include <mutex>
-
 #include <cuda_runtime.h>
 
 #include "../../include/lce.h"
@@ -38,23 +36,12 @@ constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(64) << 20;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-
 // The host-side name g_noalloc_scratch is only a stand-in for the device array;
-// its device address is looked up once per device, with that device current.
+// its address on the current device is looked up each time.
 lce_status scratch_address(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return LCE_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return LCE_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return LCE_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return LCE_ERR_CUDA;
+    *out = p;
     return LCE_OK;
 }
 
