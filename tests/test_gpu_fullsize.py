@@ -1,7 +1,8 @@
 """Parity at full size: the Llama-3-8B and Qwen-2.5-7B LM-head workloads, run
 through the C ABI in the launch configuration the benchmark times (fused
-forward + backward, chunk from the workload), and the separate forward +
-backward (the recompute path) on the Llama-3 head. Every expected value comes
+forward + backward, chunk from the workload), and on the Llama-3 head the
+separate forward + backward (the recompute path) and the fused call's other
+schedules (one chunk buffer; W frozen). Every expected value comes
 from the fp64 oracle alone; no GPU output enters a reference:
 
   * lse of all N rows and the loss: the oracle's forward over every row (the
@@ -115,10 +116,8 @@ def _check_against_oracle(name, chunk, H, W, y, loss, lse, dH, dW, rng):
     dH_o = O.rows_dH(H, W, y, rows, n_valid)
     check_grad("dH rows", dH[rows].float().double().cpu().numpy(), dH_o)
 
-    vrows = _sample_vocab(wl, y_np, valid, rng)
-    assert len(vrows) >= 32
-    dW_o = O.cols_dW(H, W, y, vrows, lse_o, n_valid)
-    check_grad("dW rows", dW[vrows].double().cpu().numpy(), dW_o)
+    ign = torch.from_numpy(~valid).to(DEV)
+    assert dH[ign].abs().max().item() == 0.0
 
     # level at initialisation, independent of any implementation: a row's logits are
     # Gaussian with variance |h|^2 sigma_w^2 (E = D sigma_w^2), so E[lse] = log V +
@@ -126,6 +125,13 @@ def _check_against_oracle(name, chunk, H, W, y, loss, lse, dH, dW, rng):
     # labels); the mean over ~15k rows has a spread of ~0.01
     expected = math.log(wl.V) + wl.D * W_STD ** 2 / 2
     assert abs(loss.item() - expected) < 0.05, (loss.item(), expected)
+
+    if dW is None:      # W frozen: no dW computed
+        return
+    vrows = _sample_vocab(wl, y_np, valid, rng)
+    assert len(vrows) >= 32
+    dW_o = O.cols_dW(H, W, y, vrows, lse_o, n_valid)
+    check_grad("dW rows", dW[vrows].double().cpu().numpy(), dW_o)
 
     # invariants on the whole GPU output. Rows of softmax - onehot sum to 0, so
     # sum_v dW[v, d] = sum_i H_id * sum_v (G~_iv - G_iv), where G~ is G rounded to
@@ -135,8 +141,6 @@ def _check_against_oracle(name, chunk, H, W, y, loss, lse, dH, dW, rng):
     colsum = dW.sum(dim=0).abs().double().cpu().numpy()
     bound = 2.0 ** -7 / n_valid * np.abs(Hf[valid]).sum(axis=0)
     assert np.all(colsum <= bound), float(np.max(colsum / bound))
-    ign = torch.from_numpy(~valid).to(DEV)
-    assert dH[ign].abs().max().item() == 0.0
 
 
 def test_fullsize_separate_path_matches_oracle(lce):
@@ -151,6 +155,26 @@ def test_fullsize_separate_path_matches_oracle(lce):
     torch.cuda.synchronize()
     del Hd, Wd, yd
     _check_against_oracle(name, chunk, H, W, y, loss, lse, dH, dW, np.random.default_rng(77))
+
+
+@pytest.mark.parametrize("variant", ["low_memory", "frozen_w"])
+def test_fullsize_other_schedules_match_oracle(lce, variant):
+    """The fused call's other schedules on the Llama-3 head at the benchmark's
+    chunk: one chunk buffer (LCE_LOW_MEMORY: one dW contraction per chunk), and W
+    frozen (no dW; each chunk's dH with the next chunk's logits beside it)."""
+    name = "llama3-8b"
+    chunk = WORKLOADS[name].chunks[0]
+    H, W, y = _inputs(name)
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    if variant == "low_memory":
+        loss, lse, dH, dW = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk, low_memory=True)
+    else:
+        loss, lse, dH, dW = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk, compute_dW=False)
+        assert dW is None
+    torch.cuda.synchronize()
+    del Hd, Wd, yd
+    _check_against_oracle(name, chunk, H, W, y, loss, lse, dH, dW,
+                          np.random.default_rng(4321 if variant == "low_memory" else 8765))
 
 
 @pytest.mark.parametrize("name,chunk", _cases())
@@ -183,3 +207,41 @@ def test_fullsize_chunk_sweep_agrees(lce):
         del loss, lse, dH, dW
     _inputs_cache.clear()
     _oracle_cache.clear()
+
+
+def test_fullsize_norm_path_matches_oracle(lce):
+    """Final RMSNorm + LM head + cross-entropy (lce_norm_fwd_bwd) on the Llama-3
+    head at the benchmark's chunk, with the inputs the benchmark's norm path
+    draws. Expected values from the oracle alone: H = RMSNorm(X) rounded to bf16,
+    then the oracle's forward over every row (lse, loss), dX of sampled rows
+    (that row's dH through the RMSNorm backward), dW of sampled vocabulary rows.
+    dgamma sums over every row's dH and is checked against the full oracle at
+    the Llama-2 shape (tests/test_gpu_norm.py)."""
+    from lce_synth import workload_norm_inputs
+    name = "llama3-8b"
+    wl = WORKLOADS[name]
+    chunk = wl.chunks[0]
+    eps = 1e-6
+    X, g, W, y = workload_norm_inputs(name)
+    out = lce.norm_fwd_bwd(X.to(DEV), g.to(DEV), W.to(DEV), y.to(DEV), eps=eps, chunk=chunk)
+    torch.cuda.synchronize()
+    loss, lse, dX, dgamma, dW = out
+    assert torch.isfinite(dgamma).all()
+
+    H_o = O.round_bf16(O.rmsnorm_forward(X, g, eps)[0])
+    loss_o, lse_o, n_valid, n_bad = O.forward(H_o, W, y)
+    assert n_bad == 0 and n_valid == wl.N - wl.n_ignored
+    check_lse(lse.double().cpu().numpy(), lse_o)
+    check_loss(loss.item(), loss_o)
+
+    y_np = y.numpy()
+    valid = y_np != IGNORE_INDEX
+    rng = np.random.default_rng(2468)
+    rows = _sample_rows(wl, chunk, valid, rng)
+    dH_rows = O.rows_dH(H_o, W, y, rows, n_valid)
+    dX_o, _ = O.rmsnorm_backward(X[rows], g, eps, dH_rows)
+    check_grad("dX rows", dX[rows].double().cpu().numpy(), dX_o)
+
+    vrows = _sample_vocab(wl, y_np, valid, rng)
+    dW_o = O.cols_dW(H_o, W, y, vrows, lse_o, n_valid)
+    check_grad("dW rows", dW[vrows].double().cpu().numpy(), dW_o)
