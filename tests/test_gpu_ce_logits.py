@@ -177,3 +177,39 @@ def test_ce_logits_cluster_deterministic(lce):
     torch.cuda.synchronize()
     for x, z in zip(a, b):
         assert torch.equal(x, z)
+
+
+def test_ce_logits_bench_workload(lce):
+    """The benchmark's CE-over-logits workload in its launch configuration: the
+    Llama-3 logits N = 16384 x V = 128256 bf16 (4.2 GB), drawn as bench.py draws
+    them, 5 % of the rows ignored, forward and the gradient written in place.
+    The oracle, on a copy of the logits taken before the call, 512 rows at a
+    time: every row's lse, the loss over all rows, dZ of sampled rows (the first
+    and the last rows, an ignored row, random rows)."""
+    N, V, n_ign = 16384, 128256, 819
+    g = torch.Generator(device=DEV).manual_seed(3)
+    Z = torch.randn(N, V, device=DEV, generator=g).mul_(1.3).to(torch.bfloat16)
+    y = torch.randint(0, V, (N,), device=DEV, generator=g)
+    y[torch.randperm(N, device=DEV, generator=g)[:n_ign]] = -100
+    Z0 = Z.clone()
+    loss, lse, dZ = lce.ce_logits(Z, y, inplace=True)
+    torch.cuda.synchronize()
+    assert dZ.data_ptr() == Z.data_ptr()
+    y_h = y.cpu()
+    valid = (y_h != -100).numpy()
+    n_valid = int(valid.sum())
+    assert n_valid == N - n_ign
+    lse_o = np.empty(N)
+    loss_sum = 0.0
+    for r in range(0, N, 512):
+        ref = O.ce_from_logits(Z0[r:r + 512].cpu(), y_h[r:r + 512], reduction="sum")
+        lse_o[r:r + 512] = ref["lse"]
+        loss_sum += ref["loss"]
+    check_lse(to64(lse), lse_o)
+    check_loss(loss.item(), loss_sum / n_valid)
+    rng = np.random.default_rng(16384)
+    rows = sorted({0, 1, N - 2, N - 1, int(np.nonzero(~valid)[0][0])} |
+                  {int(r) for r in rng.choice(N, 59, replace=False)})
+    ref = O.ce_from_logits(Z0[rows].cpu(), y_h[rows], dloss=1.0 / n_valid, reduction="sum")
+    check_grad("dZ rows", to64(dZ[rows]), ref["dZ"])
+    assert dZ[torch.from_numpy(~valid).to(DEV)].abs().max().item() == 0.0

@@ -1,8 +1,8 @@
 """Parity at full size: the Llama-3-8B and Qwen-2.5-7B LM-head workloads, run
 through the C ABI in the launch configuration the benchmark times (fused
 forward + backward, chunk from the workload), and on the Llama-3 head the
-separate forward + backward (the recompute path) and the fused call's other
-schedules (one chunk buffer; W frozen). Every expected value comes
+separate forward + backward (the recompute path), the fused call's other
+schedules (one chunk buffer; W frozen), fp16 inputs and the RMSNorm path. Every expected value comes
 from the fp64 oracle alone; no GPU output enters a reference:
 
   * lse of all N rows and the loss: the oracle's forward over every row (the
@@ -100,9 +100,9 @@ def _sample_vocab(wl, y_np, valid, rng):
     return sorted(ids)
 
 
-def _check_against_oracle(name, chunk, H, W, y, loss, lse, dH, dW, rng):
+def _check_against_oracle(name, chunk, H, W, y, loss, lse, dH, dW, rng, oracle=None):
     wl = WORKLOADS[name]
-    loss_o, lse_o, n_valid = _oracle_forward(name)
+    loss_o, lse_o, n_valid = oracle if oracle is not None else _oracle_forward(name)
     y_np = y.numpy()
     valid = y_np != IGNORE_INDEX
     assert n_valid == wl.N - wl.n_ignored
@@ -175,6 +175,27 @@ def test_fullsize_other_schedules_match_oracle(lce, variant):
     del Hd, Wd, yd
     _check_against_oracle(name, chunk, H, W, y, loss, lse, dH, dW,
                           np.random.default_rng(4321 if variant == "low_memory" else 8765))
+
+
+def test_fullsize_fp16_matches_oracle(lce):
+    """fp16 H and W (LCE_INPUT_FP16: fp16 MMAs, G stored as (p - onehot) * 2^14)
+    on the Llama-3 head at the benchmark's chunk, drawn as the benchmark's fp16
+    run draws them; the oracle on the same fp16 values."""
+    from lce_synth import make_inputs
+    name = "llama3-8b"
+    wl = WORKLOADS[name]
+    chunk = wl.chunks[0]
+    H, W, y = make_inputs(wl.N, wl.D, wl.V, wl.seed, wl.labels, wl.n_ignored, dtype="fp16")
+    assert H.dtype == torch.float16 and W.dtype == torch.float16
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    loss, lse, dH, dW = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk)
+    torch.cuda.synchronize()
+    del Hd, Wd, yd
+    assert dH.dtype == torch.float16
+    loss_o, lse_o, n_valid, n_bad = O.forward(H, W, y)
+    assert n_bad == 0
+    _check_against_oracle(name, chunk, H, W, y, loss, lse, dH, dW, np.random.default_rng(1616),
+                          oracle=(loss_o, lse_o, n_valid))
 
 
 @pytest.mark.parametrize("name,chunk", _cases())
