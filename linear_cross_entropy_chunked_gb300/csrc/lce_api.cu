@@ -10,6 +10,7 @@
 // one bf16 [chunk, V] buffer that holds exp(z - slab max), then G.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 #include <vector>
@@ -286,7 +287,7 @@ struct ProfPair {
     cudaEvent_t a, b;
 };
 std::mutex g_prof_mu;
-bool g_prof_on = false;
+std::atomic<bool> g_prof_on{false};   // read without the mutex on every launch
 std::vector<ProfPair> g_prof_pending;
 std::vector<cudaEvent_t> g_prof_pool;
 double g_prof_ms[LCE_KERNEL_KINDS] = {};
