@@ -68,6 +68,46 @@ def test_ragged_shapes(lce, N, D, V, chunk, n_ign, dloss):
     compare(r, O.forward_backward(H, W, y, dloss=dloss))
 
 
+@pytest.mark.parametrize("N,D,V,chunk", [
+    (600, 8192, 20000, 256),     # a 70B-class hidden size: 128 k blocks per logits tile,
+                                 # 16 wide dH column tiles, 32 dW column tiles
+    (300, 16384, 5000, 128),     # 256 k blocks, 32 dH / 64 dW column tiles, 256 transpose columns
+    (520, 12288, 9000, 192),     # D a multiple of 512 but not of 1024; chunk not of 128
+    (257, 6152, 4099, 128),      # D a multiple of 8 only: ragged last k block and column tile
+])
+def test_large_hidden_sizes(lce, N, D, V, chunk):
+    """Hidden sizes beyond the workloads' (up to 16384) through every path, against
+    the full oracle."""
+    H, W, y = make_inputs(N, D, V, seed=D + N, labels="uniform", n_ignored=N // 25, w_std=0.01)
+    r = run_all_paths(lce, H, W, y, chunk=chunk, dloss=0.8)
+    compare(r, O.forward_backward(H, W, y, dloss=0.8))
+
+
+def test_two_word_vocabulary(lce):
+    """V = 2: the loss is the logistic loss of the logit difference (pinned in the
+    oracle's tests); every path against the full oracle."""
+    H, W, y = make_inputs(300, 72, 2, seed=2, labels="uniform", n_ignored=9, w_std=0.1)
+    r = run_all_paths(lce, H, W, y, chunk=128, dloss=1.0)
+    compare(r, O.forward_backward(H, W, y))
+
+
+def test_one_word_vocabulary(lce):
+    """V = 1: softmax of one logit is 1 and the label is that word, so the loss and
+    both gradients are 0 and lse is the logit itself. On the GPU lse - z and G come
+    out as rounding residues of the log2(e) scaling (|.| ~ 1e-7 relative), so they
+    are checked against bounds rather than for exact zeros."""
+    H, W, y = make_inputs(200, 64, 1, seed=1, labels="uniform", n_ignored=7, w_std=0.1)
+    r = run_all_paths(lce, H, W, y, chunk=64, dloss=1.0)
+    ref = O.forward_backward(H, W, y)
+    assert ref["loss"] == 0.0 and np.all(ref["dH"] == 0.0) and np.all(ref["dW"] == 0.0)
+    for k in ("lse", "flse"):
+        check_lse(r[k], ref["lse"])
+    for k in ("loss", "floss"):
+        assert abs(r[k]) <= 1e-6, (k, r[k])
+    for k in ("dH", "dW", "bdH", "bdW"):
+        assert np.abs(r[k]).max() <= 1e-6, (k, float(np.abs(r[k]).max()))
+
+
 def test_labels_at_vocab_ends(lce):
     N, D, V = 200, 128, 777
     H, W, y = make_inputs(N, D, V, seed=3)
