@@ -154,6 +154,40 @@ def test_label_out_of_range_reports_status(lce):
     check_grad("dW", to64(dW), ref["dW"])
 
 
+@pytest.mark.parametrize("ign", [7, 0, -1])
+def test_custom_ignore_index(lce, ign):
+    """An ignore_index other than -100: a vocabulary id (7, or 0, the first column;
+    rows whose label is that id take no part even though it is in range) or -1.
+    A label of -100 is then out of range: flagged, and its row counts as ignored.
+    Fused, forward and backward paths and CE over the same logits, against the
+    oracle called with the same ignore_index."""
+    N, D, V, chunk = 400, 136, 3000, 128
+    H, W, y = make_inputs(N, D, V, seed=40 + ign, w_std=0.05)
+    y[::9] = ign
+    y[5] = -100
+    Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
+    ws = lce.alloc_workspace(N, D, V, chunk, DEV)
+    ref = O.forward_backward(H, W, y, ignore_index=ign)
+    assert ref["n_bad"] == 1 and ref["n_valid"] == N - int((y == ign).sum()) - 1
+    loss, lse, dH, dW = lce.lce_fwd_bwd(Hd, Wd, yd, chunk=chunk, ignore_index=ign, ws=ws)
+    assert lce.read_status(ws) == 4          # LCE_ERR_LABEL_RANGE: the -100 label
+    floss, flse = lce.lce_forward(Hd, Wd, yd, chunk=chunk, ignore_index=ign, ws=ws)
+    bdH, bdW = lce.lce_backward(Hd, Wd, yd, flse, chunk=chunk, ignore_index=ign, ws=ws)
+    lce.read_status(ws)
+    for got_loss, got_lse in ((loss, lse), (floss, flse)):
+        check_loss(got_loss.item(), ref["loss"])
+        check_lse(to64(got_lse), ref["lse"])
+    for name, got, exp in (("dH", dH, ref["dH"]), ("dW", dW, ref["dW"]),
+                           ("dH (backward)", bdH, ref["dH"]), ("dW (backward)", bdW, ref["dW"])):
+        check_grad(name, to64(got), exp)
+    Z = (H.double() @ W.double().T).float()
+    cl, clse, cdZ = lce.ce_logits(Z.to(DEV), yd, ignore_index=ign)
+    cref = O.ce_from_logits(Z.double().numpy(), y.numpy(), ignore_index=ign)
+    check_loss(cl.item(), cref["loss"])
+    check_lse(to64(clse), cref["lse"])
+    check_grad("dZ", to64(cdZ), cref["dZ"])
+
+
 def test_deterministic_bits(lce):
     H, W, y = make_inputs(520, 256, 4000, seed=6, n_ignored=20)
     Hd, Wd, yd = H.to(DEV), W.to(DEV), y.to(DEV)
