@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--chunk", type=int, default=0, help="0: the workload's own chunk")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cublas", action="store_true",
+                    help="skip the cuBLAS timing of the same GEMM shapes (after the timed region)")
     ap.add_argument("--ce-rows", type=int, default=0,
                     help="ce-logits path: rows of the logits (0: the workload's N)")
     ap.add_argument("--frozen-w", action="store_true",
@@ -398,6 +400,9 @@ def run_ours(args, wl, chunk):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
+    cublas = None
+    if world == 1 and not args.no_cublas and not separate and not frozen:
+        cublas = cublas_same_shapes(Hd, Wd, chunk, stream)
 
     if rank == 0:
         line = {
@@ -475,6 +480,8 @@ def run_ours(args, wl, chunk):
             line["e2e"] = e2e
         if cpu:
             line["cpu_baseline"] = cpu
+        if cublas:
+            line["cublas_same_shapes"] = cublas
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -489,6 +496,66 @@ def kernel_source_hash(files) -> str:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def cublas_same_shapes(Hd, Wd, chunk, stream, reps: int = 10):
+    """cuBLAS (torch.matmul: bf16 or fp16 in and out) on the three GEMM shapes of a
+    chunk pair, each timed alone with CUDA events after the timed region: the
+    logits Z_c = H_c W^T (C x V, K = D), dH_c = G_c W (C x D, K = V) and dW = G^T H
+    over a pair of chunks (V x D, K = 2C). A yardstick for the library's kernels,
+    which do more on the same shapes (the logits kernel's slab LSE, target gather
+    and P' store; the dW tiles' fp32 read-modify-write of dW) and run beside one
+    another inside the step rather than alone."""
+    import torch
+    N, D = Hd.shape
+    V = Wd.shape[0]
+    C = min(chunk, N)
+    C2 = min(2 * C, N)
+    dev = Hd.device
+    g = torch.Generator(device=dev).manual_seed(0)
+    G = (torch.randn(C2, V, device=dev, generator=g) * 1e-4).to(Hd.dtype)
+    Hc, H2 = Hd[:C], Hd[:C2]
+    Z = torch.empty(C, V, dtype=Hd.dtype, device=dev)
+    dHc = torch.empty(C, D, dtype=Hd.dtype, device=dev)
+    dWb = torch.empty(V, D, dtype=Hd.dtype, device=dev)
+    cases = {
+        "logits": (lambda: torch.matmul(Hc, Wd.t(), out=Z), 2.0 * C * D * V,
+                   f"[{C} x {D}] @ [{D} x {V}]"),
+        "dH": (lambda: torch.matmul(G[:C], Wd, out=dHc), 2.0 * C * D * V,
+               f"[{C} x {V}] @ [{V} x {D}]"),
+        "dW": (lambda: torch.matmul(G.t(), H2, out=dWb), 2.0 * C2 * D * V,
+               f"[{V} x {C2}] @ [{C2} x {D}]"),
+    }
+    # the library's dW output: fp32, added to the dW already there (beta = 1)
+    dW32 = torch.zeros(V, D, dtype=torch.float32, device=dev)
+    try:
+        torch.addmm(dW32[:256], G.t()[:256], H2, out_dtype=torch.float32)
+        cases["dW_fp32_accumulate"] = (
+            lambda: torch.addmm(dW32, G.t(), H2, out_dtype=torch.float32), 2.0 * C2 * D * V,
+            f"fp32 [{V} x {D}] + [{V} x {C2}] @ [{C2} x {D}]")
+    except (TypeError, RuntimeError):
+        pass
+    out = {}
+    with torch.cuda.stream(stream):
+        for name, (fn, flops, shape) in cases.items():
+            for _ in range(3):
+                fn()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            for a, b in evs:
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+            out[name] = {"shape": shape, "ms": ms, "tflops": flops / (ms / 1e3) / 1e12}
+    del G, Z, dHc, dWb, dW32
+    out["note"] = ("torch.matmul / addmm (cuBLAS) alone on each shape, bf16/fp16 output (the "
+                   "dW_fp32_accumulate case: fp32 output added to an fp32 dW, as the library "
+                   f"does), median of {reps}; the library's kernels on these shapes also run "
+                   "their epilogues and share the GPU with each other inside the step (see "
+                   "kernels)")
+    return out
 
 
 def load_traffic(workload: str = "", chunk: int = 0, variant: str = ""):
