@@ -101,6 +101,10 @@ def load_peaks():
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
+    """nvidia-smi sampling of the SM clock, power and throttle reasons (every 100 ms)
+    around the timed region. start() returns once the first sample has arrived, so
+    the timed region is covered; the reported SM clock is the median over the
+    samples taken under load (power at least 60 % of the highest sample)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -108,16 +112,22 @@ class ClockSampler:
     def __init__(self, device_index: int = 0):
         self.proc = None
         self.lines = []
+        self.reader = None
         self.dev = device_index
 
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line)
+
     def start(self):
+        import threading
         import torch
         try:
             uuid = "GPU-" + str(torch.cuda.get_device_properties(self.dev).uuid)
         except Exception:
             uuid = None
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "200"]
+               "-lms", "100"]
         if uuid:
             cmd += ["-i", uuid]
         try:
@@ -125,34 +135,45 @@ class ClockSampler:
                                          text=True)
         except Exception:
             self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5.0 and self.proc.poll() is None:
+            time.sleep(0.01)
 
     def stop(self):
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, smax, power, reasons = [], None, [], set()
+            self.proc.wait()
+        if self.reader:
+            self.reader.join(timeout=5)
+        rows = []
+        smax = None
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in out.strip().splitlines():
+        for line in self.lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax = float(parts[1])
-                power.append(float(parts[2]))
+                sm, smax, pw = float(parts[0]), float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "power_w_max": max(power) if power else None, "samples": len(sm),
-                "reasons": sorted(reasons)}
+            rows.append((sm, pw, [nm for nm, v in zip(names, parts[4:8])
+                                  if v.lower().startswith("active")]))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "samples": 0, "reasons": []}
+        pmax = max(r[1] for r in rows)
+        load = [r for r in rows if r[1] >= 0.6 * pmax]
+        reasons = sorted({nm for r in load for nm in r[2]})
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": smax,
+                "power_w_max": pmax, "samples": len(rows), "samples_under_load": len(load),
+                "reasons": reasons}
 
 
 # ----------------------------------------------------------------- reference arm
