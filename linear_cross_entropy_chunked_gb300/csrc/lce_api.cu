@@ -5,9 +5,11 @@
 // The token axis is cut into chunks of `chunk` rows ("Arquitectura interna de
 // Unsloth y optimizacion en Triton", section 3: token blocks; "Unsloth
 // Architecture: Manual Triton Backpropagation, Fused Cross-Entropy, and 80% VRAM
-// Cut", pillar 1: chunks of tokens, logits discarded after each chunk). Per
-// chunk the only HBM state is O(chunk * V): the (max, sumexp) slab partials and
-// one bf16 [chunk, V] buffer that holds exp(z - slab max), then G.
+// Cut", pillar 1: chunks of tokens, logits discarded after each chunk). The
+// only HBM state beyond the outputs is O(chunk * V): the (max, sumexp) slab
+// partials of a chunk and bf16 [chunk, V] buffers that hold exp(z - slab max),
+// then G: two by default (chunks go in pairs that share one dW contraction),
+// one with LCE_LOW_MEMORY.
 #include <cudaTypedefs.h>
 
 #include <atomic>

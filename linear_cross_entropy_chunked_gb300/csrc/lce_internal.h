@@ -45,14 +45,15 @@ constexpr int SCHED_DEPTH = 4;
 constexpr int TMEM_COLS = 512;
 constexpr int BN_WIDE = 512;   // MODE_DH tile width: both 256-column TMEM accumulators
 // dH tiles (256 rows x 512 columns on a CTA pair) run over the whole vocabulary
-// while the dW tiles, which are bound by their fp32 read-modify-write of dW in
-// HBM, run concurrently on the other SMs. The phase is shortest when both sets
-// end together: measured on a GB300 that is about 32 dH tiles (a dH tile pair
-// runs ~1.3x the flop rate of a dW one; 76 pairs). A chunk with fewer dH tiles
-// splits them along the vocabulary until there are at least DH_SPLIT_TILES, in
-// at most DH_MAX_SPLITS parts, for vocabularies of at least DH_SPLIT_MIN_V; more
-// dH tiles than that would crowd the dW tiles into the end of the phase, where
-// all of them at once run into the HBM limit.
+// while the dW tiles, whose 256 x 256 shape needs more operand bytes per flop
+// and which also stage and reduce-add their fp32 output, run concurrently on the
+// other SMs. The phase is shortest when both sets end together: measured on a
+// GB300 that is about 32 dH tiles (a dH tile pair runs ~1.3x the flop rate of a
+// dW one; 76 pairs). A chunk with fewer dH tiles splits them along the
+// vocabulary until there are at least DH_SPLIT_TILES, in at most DH_MAX_SPLITS
+// parts, for vocabularies of at least DH_SPLIT_MIN_V; more dH tiles than that
+// leave the dW tiles to the end of the phase (measured slower, both with one dW
+// contraction per chunk and per pair of chunks).
 constexpr int DH_SPLIT_TILES = 28;
 constexpr int DH_MAX_SPLITS = 4;
 constexpr long long DH_SPLIT_MIN_V = 8192;
