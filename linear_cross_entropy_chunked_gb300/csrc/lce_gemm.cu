@@ -9,9 +9,10 @@
 //     logit, and optionally stores exp(z - slab max) or the final gradient G;
 //   * the two gradient contractions dH_c = G_c W and dW += G_c^T H_c of the
 //     backward ("Arquitectura interna de Unsloth y optimizacion en Triton",
-//     section 3 "Fused Cross Entropy": backpropagation into X and W_vocab),
-//     issued as one tile list so that the few long dH tiles and the many short
-//     dW tiles share the SMs.
+//     section 3 "Fused Cross Entropy": backpropagation into X and W_vocab): on
+//     CTA pairs the dH tiles (512 columns wide) in one launch and the dW tiles
+//     in launches beside and behind it; with one CTA per tile, one tile list in
+//     which the few long dH tiles and the many short dW tiles share the SMs.
 //
 // Roles (320 threads): warps 0-7 epilogue (TMEM lane quarter = warp % 4, column
 // half = warp / 4), warp 8 TMA producer, warp 9 TMEM owner + MMA issuer.
@@ -403,8 +404,8 @@ __device__ __forceinline__ void epilogue_logits(const GemmParams &p, const Tile 
     }
 }
 
-// Gradient tiles: dH (bf16 / fp16, or fp32 when dh_fp32) or dW (fp32, stored
-// for the first chunk, reduce-added into dW afterwards). out_scale: the factor
+// Gradient tiles: dH (bf16 / fp16, or fp32 when dh_fp32) or dW (fp32, stored by
+// a call's first dW contraction, reduce-added into dW by the later ones). out_scale: the factor
 // fp16 calls apply here instead of in G (1 for bf16).
 __device__ __forceinline__ void epilogue_grad(const GemmParams &p, const Tile &tl, uint32_t taddr,
                                               int half, const HalfStager &st, float out_scale) {
