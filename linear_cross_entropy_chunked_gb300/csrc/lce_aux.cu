@@ -221,10 +221,12 @@ __global__ void __launch_bounds__(256) lce_transpose_kernel(const TransposeParam
 // of PREP_VEC_PER_CTA 8-column vectors: the row's lse from its slab partials
 // (row_lse, the merge's arithmetic), then P' = exp(z - m_p) -> G = P' * exp(m_p -
 // lse) * s - 1[j = y] * s in place, s the stored-G row scale, each slab's factor
-// exp(m_p - lse) * s formed where it is used; segment 0 writes lse and the row
-// loss. The CTAs after those transpose 64 x 64
+// exp(m_p - lse) * s formed once per CTA into shared memory; segment 0 writes lse
+// and the row loss. The CTAs after those transpose 64 x 64
 // tiles of the H chunk (lce_transpose_kernel's arithmetic) for the dW contraction.
 static_assert(PREP_THREADS == MERGE_THREADS, "the prep kernel computes lse as the merge does");
+static_assert((PREP_VEC_PER_CTA * 8) % PART_COLS == 0 && PREP_VEC_PER_CTA * 8 / PART_COLS <= PREP_THREADS,
+              "a prep segment starts on a slab boundary and each thread forms at most one factor");
 
 __device__ __forceinline__ void bulk_copy_to_smem(uint32_t dst, const void *src, uint32_t bytes,
                                                   uint32_t bar) {
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_prep_kernel(const PrepParam
     extern __shared__ __align__(128) uint8_t prep_smem[];   // the segment, or a transpose tile
     __shared__ float s_red[MERGE_THREADS / 32];
     __shared__ float s_bcast;
+    __shared__ float s_fac[PREP_VEC_PER_CTA * 8 / PART_COLS];   // the segment's slab factors
     __shared__ __align__(8) uint64_t seg_bar;
     __shared__ volatile int s_abort;
     const MergeParams &m = p.m;
@@ -321,6 +324,15 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_prep_kernel(const PrepParam
                                         y_ok, m.f16);
     const float lse2 = lse * LOG2E_F;
     const int ycol = y_ok ? static_cast<int>(yv) : -1;
+    // the factor exp(m_p - lse) * s of each 128-column slab of the segment, once (a
+    // segment starts on a slab boundary: PREP_VEC_PER_CTA * 8 is a multiple of 128)
+    const int slab0 = (v0 * 8) / PART_COLS;
+    const int nslab = (nv * 8 + PART_COLS - 1) / PART_COLS;
+    if (threadIdx.x < nslab)
+        s_fac[threadIdx.x] = scale != 0.f
+                                 ? exp2f(fmaf(parts[slab0 + threadIdx.x].x, LOG2E_F, -lse2)) * scale
+                                 : 0.f;
+    __syncthreads();
     const Abort ab{&s_abort, const_cast<int *>(m.hdr), PREP_WAIT_NS};
     if (!mbar_wait(&seg_bar, 0, ab)) {
         // the copy did not complete in time (recorded as a timeout): let it finish
@@ -333,9 +345,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) lce_prep_kernel(const PrepParam
     for (int v = threadIdx.x; v < nv; v += MERGE_THREADS) {
         uint4 u = sv[v];
         const int c = (v0 + v) * 8;
-        const float f = scale != 0.f
-                            ? exp2f(fmaf(parts[c >> 7].x, LOG2E_F, -lse2)) * scale
-                            : 0.f;
+        const float f = s_fac[(v * 8) / PART_COLS];
         uint32_t *wv = reinterpret_cast<uint32_t *>(&u);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
